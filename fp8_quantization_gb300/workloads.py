@@ -1,0 +1,95 @@
+"""Seeded synthetic inputs for the cast kernels.
+
+This module only draws random numbers and rounds them to BF16; it holds none
+of the quantisation arithmetic, so both the CUDA path's tests/bench and the
+CPU oracle's tests can use it.  Each generator states the value distribution
+and shape of the workload it stands in for:
+
+* ``pr1``            256x512 N(0,1), 0.1% of entries scaled by 100 (outliers).
+* ``moe_dispatch``   MoE dispatch activations of a 671B-class model
+                     (hidden 7168): N(0,1) rows times a per-row log-normal(0,1)
+                     magnitude.
+* ``ragged_experts`` routed rows of width 2048 over 32 local experts, expert
+                     sizes drawn Zipf(s=1.1) (group offsets, no padding).
+* ``nvfp4_act``      Student-t(nu=4) activations (MLP width 14336).
+* ``nvfp4_weight``   N(0, 0.02) weights 14336x4096.
+* ``sweep``          Student-t(nu=3) rows x 7168 for the bandwidth sweep.
+
+All arrays are returned as BF16 bit patterns (``numpy.uint16``), row-major.
+BF16 rounding is round-to-nearest-even, done by ``torch`` on the host.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+
+def bf16_bits(a: np.ndarray) -> np.ndarray:
+    """float32 array -> BF16 bit patterns (round to nearest even)."""
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_to_float(bits: np.ndarray) -> np.ndarray:
+    """BF16 bit patterns -> float32 values (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def pr1(M: int = 256, K: int = 512, seed: int = 0) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((M, K))
+    mask = rng.random((M, K)) < 1e-3
+    x[mask] *= 100.0
+    return bf16_bits(x.astype(np.float32))
+
+
+def moe_dispatch(M: int = 16384, K: int = 7168, seed: int = 0) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((M, K), dtype=np.float32)
+    x *= rng.lognormal(0.0, 1.0, (M, 1)).astype(np.float32)
+    return bf16_bits(x)
+
+
+def zipf_group_offsets(M: int, G: int = 32, s: float = 1.1, seed: int = 0) -> np.ndarray:
+    """Exclusive prefix sum of per-expert token counts; expert e has Zipf rank
+    e+1, i.e. probability proportional to (e+1)^-s.  Returns int64 [G+1]."""
+    rng = np.random.default_rng(seed + 1)
+    p = np.arange(1, G + 1, dtype=np.float64) ** (-s)
+    p /= p.sum()
+    ids = rng.choice(G, size=M, p=p)
+    counts = np.bincount(ids, minlength=G).astype(np.int64)
+    return np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+
+
+def ragged_experts(M: int = 65536, K: int = 2048, G: int = 32, seed: int = 0):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((M, K), dtype=np.float32)
+    return bf16_bits(x), zipf_group_offsets(M, G, 1.1, seed)
+
+
+def nvfp4_act(M: int = 16384, K: int = 14336, seed: int = 0) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    return bf16_bits(rng.standard_t(4, (M, K)).astype(np.float32))
+
+
+def nvfp4_weight(N: int = 14336, K: int = 4096, seed: int = 0) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    return bf16_bits(rng.normal(0.0, 0.02, (N, K)).astype(np.float32))
+
+
+def sweep(M: int, K: int = 7168, seed: int = 0) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    return bf16_bits(rng.standard_t(3, (M, K)).astype(np.float32))
+
+
+def random_group_offsets(M: int, G: int, seed: int = 0, empty_frac: float = 0.2) -> np.ndarray:
+    """Arbitrary ragged split of M rows into G groups (some empty), for edge
+    cases: sizes are unrelated to 128 so group starts are misaligned."""
+    rng = np.random.default_rng(seed)
+    w = rng.random(G)
+    w[rng.random(G) < empty_frac] = 0.0
+    if w.sum() == 0:
+        w[0] = 1.0
+    counts = np.floor(w / w.sum() * M).astype(np.int64)
+    counts[int(np.argmax(w))] += M - counts.sum()
+    return np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)

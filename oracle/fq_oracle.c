@@ -1,0 +1,568 @@
+/*
+ * Plain CPU oracle for the block-scaled FP4 / FP8 casts.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path links, loads or calls
+ * this file: only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline
+ * and reference legs use it.  It shares no code, header, table or constant
+ * generator with the CUDA library.
+ *
+ * Every routine is written element by element, in the order the formats are
+ * described, with no blocking or fusion.  Floating point follows the rules
+ * below:
+ *   - MXFP4 and FP4->FP8 arithmetic is exact (powers of two) and is done in
+ *     double.
+ *   - The NVFP4 scale arithmetic is done in IEEE binary32 (the per-tensor
+ *     scale is an FP32 number on the page that defines NVFP4), one rounding
+ *     per operation, no contraction (build with -ffp-contract=off).
+ *
+ * Sources, cited by page title and section:
+ *   [MoE-FP4]  "Practical FP4 Training for Large-Scale MoE Models on Hopper
+ *               GPUs", technical overview, section 2 (Methodology):
+ *               1. MXFP4 spec (32-element blocks, UE8M0 scale, E2M1),
+ *               direct bitwise FP4->FP8 conversion, hierarchical scale
+ *               alignment of four 32-element blocks onto one 128-element
+ *               E4M3 block; 3. layout-aware kernels BF16ToFP4Row,
+ *               FP4RowToFP8Row, FP4RowToFP8Col, ragged tensors.
+ *   [NVFP4]    "Train models faster with JAX and MaxText using NVFP4 on
+ *               NVIDIA Blackwell" (Spanish copy), section "Receta de
+ *               pre-entrenamiento NVFP4": 16-element micro-blocks, E4M3 block
+ *               scales under one FP32 per-tensor scale, 16x16 2D weight
+ *               scaling, stochastic rounding.
+ *   [Philox]   Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy
+ *               as 1, 2, 3", SC'11 (Philox4x32-10).
+ *
+ * Readings where the pages are silent are marked READING and are the same
+ * readings the library documents.
+ */
+#include <stdint.h>
+#include <string.h>
+#include <math.h>
+#include <float.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_EARG 1
+
+/* ------------------------------------------------------------------ */
+/* Scalar formats                                                      */
+/* ------------------------------------------------------------------ */
+
+static float bf16_bits_to_float(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+static int bf16_is_nonfinite(uint16_t h) { return ((h >> 7) & 0xFF) == 0xFF; }
+static int bf16_sign(uint16_t h) { return (h >> 15) & 1; }
+
+/* E2M1 ([MoE-FP4] 2.1: 1 sign bit, 2 exponent bits, 1 mantissa bit).
+ * Exponent bias 1; exponent field 0 is the subnormal binade (m * 0.5).
+ * Magnitude of the 3-bit code c = (e1 e0 m). */
+double oracle_e2m1_magnitude(int c)
+{
+    int E = (c >> 1) & 3;
+    int m = c & 1;
+    if (E == 0)
+        return 0.5 * m;
+    return ldexp(1.0 + 0.5 * m, E - 1);
+}
+
+/* E4M3 "fn" (the FP8 type of the Hopper FP8 pipeline named in [MoE-FP4]
+ * 2.1 and of the NVFP4 block scales in [NVFP4]): bias 7, 3 mantissa bits,
+ * exponent field 0 is subnormal (m * 2^-9), code 0x7F is NaN, no infinity,
+ * largest finite magnitude 448 (code 0x7E). */
+double oracle_e4m3_magnitude(int c)
+{
+    int E = (c >> 3) & 15;
+    int m = c & 7;
+    if (E == 0)
+        return ldexp((double)m, -9);
+    return ldexp(1.0 + m / 8.0, E - 7);
+}
+
+/* READING (round to nearest, ties to even, saturate): the magnitude y >= 0
+ * goes to the nearest E2M1 magnitude; an exact tie goes to the code whose
+ * last bit is 0; y >= 6 (or NaN) saturates to 6. */
+static int e2m1_rne_sat(double y)
+{
+    if (!(y < 6.0))
+        return 7;
+    int c = 0;
+    while (c < 6 && oracle_e2m1_magnitude(c + 1) <= y)
+        c++;
+    double lo = oracle_e2m1_magnitude(c), hi = oracle_e2m1_magnitude(c + 1);
+    double dlo = y - lo, dhi = hi - y;
+    if (dlo < dhi)
+        return c;
+    if (dhi < dlo)
+        return c + 1;
+    return (c & 1) ? c + 1 : c;
+}
+
+/* READING (round to nearest even, saturate to the largest finite value):
+ * t >= 0 goes to the nearest E4M3 magnitude, ties to the even code; values
+ * at or above 448 give 448; NaN gives 0x7F. */
+static int e4m3_rne_satfinite(double t)
+{
+    if (t != t)
+        return 0x7F;
+    if (t >= 448.0)
+        return 0x7E;
+    int lo = 0, hi = 126; /* largest code whose magnitude is <= t */
+    while (lo < hi) {
+        int mid = (lo + hi + 1) / 2;
+        if (oracle_e4m3_magnitude(mid) <= t)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    int c = lo;
+    double a = oracle_e4m3_magnitude(c), b = oracle_e4m3_magnitude(c + 1);
+    double da = t - a, db = b - t;
+    if (da < db)
+        return c;
+    if (db < da)
+        return c + 1;
+    return (c & 1) ? c + 1 : c;
+}
+
+/* READING (stochastic rounding, [NVFP4] "Redondeo estocastico"): y >= 0 with
+ * lo <= y < hi on the E2M1 grid rounds up to hi iff R < floor(frac * 2^16),
+ * frac = (y - lo) / (hi - lo), R a uniform 16-bit integer.  P(up) is frac
+ * truncated to 16 bits; a value on the grid never moves; y >= 6 gives 6. */
+static int e2m1_sr_sat(double y, uint32_t R)
+{
+    if (!(y < 6.0))
+        return 7;
+    int c = 0;
+    while (c < 6 && oracle_e2m1_magnitude(c + 1) <= y)
+        c++;
+    double lo = oracle_e2m1_magnitude(c), hi = oracle_e2m1_magnitude(c + 1);
+    double frac = (y - lo) / (hi - lo);
+    uint32_t F = (uint32_t)floor(frac * 65536.0);
+    return (R < F) ? c + 1 : c;
+}
+
+/* UE8M0 shared scale of one MX block ([MoE-FP4] 2.1).
+ * READING (OCP MX rule): e = floor(log2(amax)) - emax + 127 with emax = 2,
+ * the exponent of the largest power of two in E2M1 (4); clamped to
+ * [0, 254]; an all-zero block takes e = 0. */
+int oracle_mx_scale_exponent(double amax)
+{
+    if (amax == 0.0)
+        return 0;
+    int p;
+    frexp(amax, &p); /* amax = f * 2^p, f in [0.5, 1) */
+    int e = (p - 1) - 2 + 127;
+    if (e < 0)
+        e = 0;
+    if (e > 254)
+        e = 254;
+    return e;
+}
+
+/* Philox4x32-10 [Philox]: ten rounds of two 32x32->64 multiplies with
+ * multipliers 0xD2511F53 and 0xCD9E8D57; the key is bumped by the Weyl
+ * constants 0x9E3779B9 and 0xBB67AE85 between rounds. */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; round++) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        uint32_t n0 = hi1 ^ c1 ^ k0;
+        uint32_t n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+/* READING (random stream of the stochastic rounding): element with linear
+ * index i (row-major, counted from `offset`) draws 16 bits from
+ * Philox4x32-10 with key (seed low word, seed high word) and counter
+ * (c low word, c high word, 0, 0), c = i / 8; output word (i mod 8) / 2,
+ * low half for even i, high half for odd i. */
+static uint32_t sr_random16(uint64_t seed, uint64_t i)
+{
+    uint64_t c = i >> 3;
+    uint32_t ctr[4] = {(uint32_t)c, (uint32_t)(c >> 32), 0u, 0u};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    oracle_philox4x32_10(ctr, key, out);
+    uint32_t w = out[(i & 7) >> 1];
+    return (i & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
+
+/* Nibble packing (READING): element 2i goes to the low nibble of byte i,
+ * element 2i+1 to the high nibble ([MoE-FP4] 2.2: two FP4 values per
+ * uint8 container). */
+static void put_nibble(uint8_t *q, int64_t idx, int code)
+{
+    uint8_t *b = q + (idx >> 1);
+    if (idx & 1)
+        *b = (uint8_t)((*b & 0x0F) | ((code & 0xF) << 4));
+    else
+        *b = (uint8_t)((*b & 0xF0) | (code & 0xF));
+}
+
+static int get_nibble(const uint8_t *q, int64_t idx)
+{
+    uint8_t b = q[idx >> 1];
+    return (idx & 1) ? (b >> 4) : (b & 0xF);
+}
+
+static float float_from_bits(uint32_t u)
+{
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* ------------------------------------------------------------------ */
+/* Array helpers for the tests' exhaustive checks                      */
+/* ------------------------------------------------------------------ */
+
+/* Signed y: magnitude by round-to-nearest-even with saturation, sign bit
+ * copied from y (so -0.1 gives code 0x8). */
+void oracle_e2m1_rne_array(const double *y, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = (uint8_t)(e2m1_rne_sat(fabs(y[i])) | (signbit(y[i]) ? 8 : 0));
+}
+
+void oracle_e2m1_sr_array(const double *y, const uint32_t *R, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = (uint8_t)(e2m1_sr_sat(fabs(y[i]), R[i] & 0xFFFFu) | (signbit(y[i]) ? 8 : 0));
+}
+
+void oracle_e4m3_rne_array(const double *t, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; i++) {
+        int c = e4m3_rne_satfinite(fabs(t[i]));
+        if (c != 0x7F && signbit(t[i]))
+            c |= 0x80;
+        out[i] = (uint8_t)c;
+    }
+}
+
+/* FP4 -> FP8 element map: code (4 bits) of an MX block whose exponent is
+ * d below the aligned block exponent, with exponent offset k. */
+static uint8_t fp4_to_fp8_element(int code, int d, int k)
+{
+    double v = oracle_e2m1_magnitude(code & 7);
+    int c8 = e4m3_rne_satfinite(ldexp(v, k - d));
+    return (uint8_t)(c8 | ((code & 8) ? 0x80 : 0));
+}
+
+void oracle_fp4_to_fp8_element_array(const uint8_t *codes, const int32_t *d, int k, int64_t n,
+                                     uint8_t *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = fp4_to_fp8_element(codes[i], d[i], k);
+}
+
+void oracle_philox4x32_10_array(const uint32_t *ctr, const uint32_t *key, int64_t n, uint32_t *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        oracle_philox4x32_10(ctr + 4 * i, key + 2 * i, out + 4 * i);
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------ */
+/* a1: MXFP4 row quantization (BF16ToFP4Row, [MoE-FP4] 2.1 and 2.3)     */
+/* ------------------------------------------------------------------ */
+
+/* x: bf16 bits [M, K]; q: [M, K/2] packed codes; s: [M, K/32] UE8M0.
+ * READING: a block holding NaN or +-Inf gets s = 0xFF (the UE8M0 NaN) and
+ * all its codes 0. */
+int oracle_mxfp4_quantize_rows(const uint16_t *x, int64_t M, int64_t K, uint8_t *q, uint8_t *s)
+{
+    if (M < 0 || K <= 0 || K % 32 != 0)
+        return ORACLE_EARG;
+    int64_t nb = K / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < M; r++) {
+        for (int64_t j = 0; j < nb; j++) {
+            const uint16_t *xb = x + r * K + 32 * j;
+            int64_t base = r * K + 32 * j;
+            int special = 0;
+            double amax = 0.0;
+            for (int i = 0; i < 32; i++) {
+                if (bf16_is_nonfinite(xb[i]))
+                    special = 1;
+                else
+                    amax = fmax(amax, fabs((double)bf16_bits_to_float(xb[i])));
+            }
+            if (special) {
+                s[r * nb + j] = 0xFF;
+                for (int i = 0; i < 32; i++)
+                    put_nibble(q, base + i, 0);
+                continue;
+            }
+            int e = oracle_mx_scale_exponent(amax);
+            s[r * nb + j] = (uint8_t)e;
+            for (int i = 0; i < 32; i++) {
+                double v = fabs((double)bf16_bits_to_float(xb[i]));
+                double y = ldexp(v, 127 - e); /* x / 2^(e-127), exact */
+                int c = e2m1_rne_sat(y) | (bf16_sign(xb[i]) ? 8 : 0);
+                put_nibble(q, base + i, c);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* a2: direct FP4 -> FP8 row conversion (FP4RowToFP8Row)               */
+/* ------------------------------------------------------------------ */
+
+/* q, s: MXFP4 [M, K/2], [M, K/32]; y: E4M3 [M, K]; ys: FP32 [M, K/128].
+ * The four MX exponents e0..e3 of one 128-element block are aligned to
+ * S = max(e_i) ([MoE-FP4] 2.1, hierarchical scale alignment).  An element
+ * of MX block i becomes E4M3(v * 2^(k - (S - e_i))); the block scale is
+ * 2^(S - 127 - k) as FP32.
+ * READING: k (0..6) is an exponent offset; k = 0 is the literal alignment.
+ * READING: if any e_i is 0xFF the block scale is NaN (0x7FC00000) and all
+ * 128 codes are 0x7F. */
+int oracle_fp4_to_fp8_rows(const uint8_t *q, const uint8_t *s, int64_t M, int64_t K, int k,
+                           uint8_t *y, float *ys)
+{
+    if (M < 0 || K <= 0 || K % 128 != 0 || k < 0 || k > 6)
+        return ORACLE_EARG;
+    int64_t nmx = K / 32, nfp8 = K / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < M; r++) {
+        for (int64_t J = 0; J < nfp8; J++) {
+            const uint8_t *e = s + r * nmx + 4 * J;
+            int special = 0, S = 0;
+            for (int i = 0; i < 4; i++) {
+                if (e[i] == 0xFF)
+                    special = 1;
+                if (e[i] > S)
+                    S = e[i];
+            }
+            int64_t base = r * K + 128 * J;
+            if (special) {
+                ys[r * nfp8 + J] = float_from_bits(0x7FC00000u);
+                for (int i = 0; i < 128; i++)
+                    y[base + i] = 0x7F;
+                continue;
+            }
+            ys[r * nfp8 + J] = ldexpf(1.0f, S - 127 - k);
+            for (int i = 0; i < 128; i++) {
+                int d = S - e[i / 32];
+                y[base + i] = fp4_to_fp8_element(get_nibble(q, base + i), d, k);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* a3: FP4 -> FP8 transposed, ragged groups (FP4RowToFP8Col)           */
+/* ------------------------------------------------------------------ */
+
+int64_t oracle_fp4_to_fp8_cols_scale_capacity(int64_t M, int32_t G)
+{
+    return (M + 127) / 128 + G;
+}
+
+/* Groups g = 0..G-1 own token rows offs[g] .. offs[g+1]-1 (no padding,
+ * [MoE-FP4] 2.3 ragged tensors).
+ * READING: a group is cut into 128-token blocks starting at its first token;
+ * the last block of a group may be short; blocks never straddle groups.
+ * READING: element (feature k, token t) goes to yT[k*M + t] (the transpose of
+ * the whole token matrix); block b of group g stores its scale at
+ * yTs[k*cap + base_g + b], base_g = sum over h < g of ceil(count_h / 128).
+ * For one block and one 32-feature MX column, S is the max of the tokens'
+ * exponents and each element is converted as in the row case. */
+int oracle_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t M, int64_t K,
+                           const int64_t *offs, int32_t G, int k, uint8_t *yT, float *yTs,
+                           int64_t cap)
+{
+    if (M < 0 || K <= 0 || K % 128 != 0 || k < 0 || k > 6 || G < 1)
+        return ORACLE_EARG;
+    if (cap < oracle_fp4_to_fp8_cols_scale_capacity(M, G))
+        return ORACLE_EARG;
+    if (offs[0] != 0 || offs[G] != M)
+        return ORACLE_EARG;
+    for (int32_t g = 0; g < G; g++)
+        if (offs[g + 1] < offs[g])
+            return ORACLE_EARG;
+    int64_t nmx = K / 32;
+    int64_t base = 0;
+    for (int32_t g = 0; g < G; g++) {
+        int64_t count = offs[g + 1] - offs[g];
+        int64_t nblk = (count + 127) / 128;
+        for (int64_t b = 0; b < nblk; b++) {
+            int64_t t0 = offs[g] + 128 * b;
+            int64_t t1 = t0 + 128 < offs[g + 1] ? t0 + 128 : offs[g + 1];
+#pragma omp parallel for schedule(static)
+            for (int64_t j = 0; j < nmx; j++) {
+                int special = 0, S = 0;
+                for (int64_t t = t0; t < t1; t++) {
+                    int e = s[t * nmx + j];
+                    if (e == 0xFF)
+                        special = 1;
+                    if (e > S)
+                        S = e;
+                }
+                for (int64_t kk = 32 * j; kk < 32 * j + 32; kk++) {
+                    yTs[kk * cap + base + b] =
+                        special ? float_from_bits(0x7FC00000u) : ldexpf(1.0f, S - 127 - k);
+                    for (int64_t t = t0; t < t1; t++) {
+                        if (special) {
+                            yT[kk * M + t] = 0x7F;
+                            continue;
+                        }
+                        int d = S - s[t * nmx + j];
+                        yT[kk * M + t] = fp4_to_fp8_element(get_nibble(q, t * K + kk), d, k);
+                    }
+                }
+            }
+        }
+        base += nblk;
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* a4-a6: NVFP4 ([NVFP4] recipe)                                       */
+/* ------------------------------------------------------------------ */
+
+/* Per-tensor amax: max |x| over the tensor (current scaling); NaN if any
+ * element is NaN. */
+float oracle_nvfp4_amax(const uint16_t *x, int64_t n)
+{
+    float a = 0.0f;
+    int nan = 0;
+    for (int64_t i = 0; i < n; i++) {
+        uint16_t h = x[i];
+        if ((h & 0x7FFF) > 0x7F80)
+            nan = 1;
+        float v = fabsf(bf16_bits_to_float(h));
+        if (v > a)
+            a = v;
+    }
+    return nan ? float_from_bits(0x7FC00000u) : a;
+}
+
+/* READING (two-level NVFP4 scaling, all binary32, one rounding per op):
+ *   g  = A / 2688   (2688 = 448 * 6: E4M3 max times E2M1 max); g = 1 if A == 0
+ *   t  = amax_blk / (6 * g)          block scale before rounding
+ *   b  = E4M3(t), round to nearest even, saturating
+ *   r  = min(1 / (b * g), FLT_MAX)   (r = 0 if b == 0)
+ *   y  = |x| * r  -> E2M1 (RNE, or stochastic rounding), sign of x kept. */
+static float nvfp4_tensor_scale(float A) { return (A > 0.0f) ? A / 2688.0f : 1.0f; }
+
+static void nvfp4_block_scales(float amax_blk, float g, int *b_out, float *r_out)
+{
+    float six_g = 6.0f * g;
+    float t = amax_blk / six_g;
+    int b = e4m3_rne_satfinite((double)t);
+    float r = 0.0f;
+    if (b != 0) {
+        float den = (float)oracle_e4m3_magnitude(b) * g;
+        r = 1.0f / den;
+        if (r > FLT_MAX)
+            r = FLT_MAX;
+    }
+    *b_out = b;
+    *r_out = r;
+}
+
+int oracle_nvfp4_quantize(const uint16_t *x, int64_t M, int64_t K, float A, int use_sr,
+                          uint64_t seed, uint64_t offset, uint8_t *q, uint8_t *sb, float *g_out)
+{
+    if (M < 0 || K <= 0 || K % 16 != 0 || offset % 16 != 0)
+        return ORACLE_EARG;
+    float g = nvfp4_tensor_scale(A);
+    *g_out = g;
+    int64_t nb = K / 16;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < M; r++) {
+        for (int64_t j = 0; j < nb; j++) {
+            int64_t base = r * K + 16 * j;
+            float amax = 0.0f;
+            for (int i = 0; i < 16; i++) {
+                float v = fabsf(bf16_bits_to_float(x[base + i]));
+                if (v > amax)
+                    amax = v;
+            }
+            int b;
+            float rs;
+            nvfp4_block_scales(amax, g, &b, &rs);
+            sb[r * nb + j] = (uint8_t)b;
+            for (int i = 0; i < 16; i++) {
+                float yv = fabsf(bf16_bits_to_float(x[base + i])) * rs;
+                int c = use_sr ? e2m1_sr_sat((double)yv, sr_random16(seed, offset + base + i))
+                               : e2m1_rne_sat((double)yv);
+                put_nibble(q, base + i, c | (bf16_sign(x[base + i]) ? 8 : 0));
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* 16x16 2D weight scaling ([NVFP4] "Escalado de pesos 2D"): one E4M3 scale
+ * per 16x16 tile, sb[N/16, K/16]; elements round to nearest even. */
+int oracle_nvfp4_quantize_2d(const uint16_t *w, int64_t N, int64_t K, float A, uint8_t *q,
+                             uint8_t *sb, float *g_out)
+{
+    if (N < 0 || K <= 0 || N % 16 != 0 || K % 16 != 0)
+        return ORACLE_EARG;
+    float g = nvfp4_tensor_scale(A);
+    *g_out = g;
+    int64_t tn = N / 16, tk = K / 16;
+#pragma omp parallel for schedule(static)
+    for (int64_t tr = 0; tr < tn; tr++) {
+        for (int64_t tc = 0; tc < tk; tc++) {
+            float amax = 0.0f;
+            for (int i = 0; i < 16; i++)
+                for (int j = 0; j < 16; j++) {
+                    float v = fabsf(bf16_bits_to_float(w[(16 * tr + i) * K + 16 * tc + j]));
+                    if (v > amax)
+                        amax = v;
+                }
+            int b;
+            float rs;
+            nvfp4_block_scales(amax, g, &b, &rs);
+            sb[tr * tk + tc] = (uint8_t)b;
+            for (int i = 0; i < 16; i++)
+                for (int j = 0; j < 16; j++) {
+                    int64_t idx = (16 * tr + i) * K + 16 * tc + j;
+                    float yv = fabsf(bf16_bits_to_float(w[idx])) * rs;
+                    int c = e2m1_rne_sat((double)yv) | (bf16_sign(w[idx]) ? 8 : 0);
+                    put_nibble(q, idx, c);
+                }
+        }
+    }
+    return ORACLE_OK;
+}

@@ -1,0 +1,451 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-scaled cast path on one GB300 (or N replicas).
+
+One step = every cast of the path over one batch of the MoE-dispatch
+activations workload (BF16 16384 x 7168, N(0,1) rows times a per-row
+log-normal(0,1) magnitude, seed 0; the tokens are split over 32 experts with
+Zipf(1.1) counts for the transposed ragged conversion):
+
+  1. mxfp4_quantize_rows   BF16 -> MXFP4 (packed E2M1 + UE8M0)
+  2. fp4_to_fp8_rows       MXFP4 -> E4M3, 128-element blocks, k = 0
+  3. fp4_to_fp8_cols       MXFP4 -> E4M3 transposed, 32 ragged expert groups
+  4. nvfp4_amax            per-tensor amax
+  5. nvfp4_quantize        NVFP4 1x16, stochastic rounding (seed = step)
+  6. nvfp4_quantize_2d     NVFP4 16x16 on the same tensor
+
+The metric is effective bandwidth: algorithmic bytes read + written by the
+kernels over their device time (CUDA events on the launching stream), as GB/s
+and as a fraction of the measured HBM copy bandwidth.  L2 is flushed (256 MB
+write) between steps, outside the timed events.
+
+--impl reference times the CPU oracle (the plain C implementation the tests
+compare against) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective GB/s (bytes read+written) per quantize/convert kernel; % of HBM peak"
+M_ROWS, K_COLS, EXPERTS = 16384, 7168, 32
+WORKLOAD = ("moe_dispatch bf16 16384x7168 (N(0,1) x row lognormal(0,1), seed 0), "
+            "32 experts Zipf(1.1): mxfp4_quantize_rows -> fp4_to_fp8_rows(k=0) -> "
+            "fp4_to_fp8_cols(ragged) ; nvfp4_amax -> nvfp4_quantize(SR) ; nvfp4_quantize_2d")
+KERNELS = ["mxfp4_quantize_rows", "fp4_to_fp8_rows", "fp4_to_fp8_cols", "nvfp4_amax",
+           "nvfp4_quantize", "nvfp4_quantize_2d"]
+# source file of each kernel (for the ncu traffic record's staleness check)
+KERNEL_SRC = {
+    "mxfp4_quantize_rows": "fq_mxfp4.cu", "fp4_to_fp8_rows": "fq_mxfp4.cu",
+    "fp4_to_fp8_cols": "fq_cols.cu", "nvfp4_amax": "fq_nvfp4.cu",
+    "nvfp4_quantize": "fq_nvfp4.cu", "nvfp4_quantize_2d": "fq_nvfp4.cu",
+}
+FALLBACK_HBM_GBS = 6800.0
+
+
+def algorithmic_bytes(M: int, K: int, nblocks_cols: int, G: int) -> dict:
+    """Bytes each kernel must read + write (inputs once, outputs once)."""
+    E = M * K
+    return {
+        "mxfp4_quantize_rows": 2 * E + E // 2 + E // 32,
+        "fp4_to_fp8_rows": E // 2 + E // 32 + E + 4 * (E // 128),
+        "fp4_to_fp8_cols": E // 2 + E // 32 + E + 4 * K * nblocks_cols + 8 * (G + 1),
+        "nvfp4_amax": 2 * E + 4,
+        "nvfp4_quantize": 2 * E + E // 2 + E // 16 + 8,
+        "nvfp4_quantize_2d": 2 * E + E // 2 + E // 256 + 8,
+    }
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def file_sha(name: str) -> str:
+    p = os.path.join(ROOT, "fp8_quantization_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel's source changed since it was captured."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        for line in f:
+            parts = line.split("#", 1)[0].split()
+            if len(parts) >= 3 and parts[0] == kernel:
+                if parts[2] != file_sha(KERNEL_SRC[kernel]):
+                    return None
+                return float(parts[1])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        rows = [l for (ts, l) in self.lines if t0 - 0.06 <= ts <= t1 + 0.06]
+        window = "timed"
+        if not rows:
+            rows = [l for _, l in self.lines]
+            window = "around timed region (none inside)"
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm), "window": window}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, backend_device=None) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=backend_device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample_pass(bits, offs_rows, K):
+    """One pass of every cast through the CPU oracle on a row sample; returns
+    (seconds, algorithmic bytes)."""
+    import oracle
+    M = bits.shape[0]
+    G = offs_rows.size - 1
+    t0 = time.perf_counter()
+    q, s = oracle.mxfp4_quantize_rows(bits)
+    oracle.fp4_to_fp8_rows(q, s, 0)
+    oracle.fp4_to_fp8_cols(q, s, offs_rows, 0)
+    A = oracle.nvfp4_amax(bits)
+    oracle.nvfp4_quantize(bits, A, use_sr=True, seed=1)
+    oracle.nvfp4_quantize_2d(bits, A)
+    dt = time.perf_counter() - t0
+    import numpy as np
+    nb = int(((np.diff(offs_rows) + 127) // 128).sum())
+    return dt, sum(algorithmic_bytes(M, K, nb, G).values())
+
+
+def oracle_sample_inputs(rows: int):
+    from fp8_quantization_gb300 import workloads
+    bits = workloads.moe_dispatch(rows, K_COLS, seed=0)
+    offs = workloads.zipf_group_offsets(rows, EXPERTS, 1.1, 0)
+    return bits, offs
+
+
+def cpu_baseline(target_s: float = 12.0) -> dict:
+    import oracle
+    rows = 64
+    bits, offs = oracle_sample_inputs(rows)
+    dt, nbytes = oracle_sample_pass(bits, offs, K_COLS)
+    rows = int(min(M_ROWS, max(16, rows * target_s / max(dt, 1e-3))))
+    rows = max(16, rows // 16 * 16)
+    bits, offs = oracle_sample_inputs(rows)
+    dt, nbytes = oracle_sample_pass(bits, offs, K_COLS)
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"first {rows} of {M_ROWS} rows of the workload (same recipe), all six casts "
+                      f"once, {dt:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    # size the per-step sample so that warmup + steps take about two minutes
+    probe_rows = 64
+    bits, offs = oracle_sample_inputs(probe_rows)
+    dt, _ = oracle_sample_pass(bits, offs, K_COLS)
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(min(M_ROWS, max(16, probe_rows * per_step / max(dt, 1e-3))))
+    rows = max(16, rows // 16 * 16)
+    bits, offs = oracle_sample_inputs(rows)
+    for _ in range(args.warmup):
+        oracle_sample_pass(bits, offs, K_COLS)
+    tot_t, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, nb = oracle_sample_pass(bits, offs, K_COLS)
+        tot_t += dt
+        tot_b += nb
+    value = tot_b / tot_t / 1e9
+    sample = f"first {rows} of {M_ROWS} rows of the workload per step, all six casts"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot_t / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M_ROWS, "K": K_COLS, "experts": EXPERTS,
+                   "sample_rows": rows},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import fp8_quantization_gb300 as fq
+    from fp8_quantization_gb300 import workloads
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    fq.abi()  # fail loudly if the library is missing
+
+    M, K, G = M_ROWS, K_COLS, EXPERTS
+    bits = workloads.moe_dispatch(M, K, seed=0)
+    offs_np = workloads.zipf_group_offsets(M, G, 1.1, 0)
+    nb_cols = int(((np.diff(offs_np) + 127) // 128).sum())
+    nbytes = algorithmic_bytes(M, K, nb_cols, G)
+    step_bytes = sum(nbytes.values())
+
+    x = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    offs = torch.from_numpy(offs_np).to(dev)
+    cap = fq.fp4_to_fp8_cols_scale_capacity(M, G)
+    u8 = dict(dtype=torch.uint8, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = {
+        "q": torch.empty((M, K // 2), **u8), "s": torch.empty((M, K // 32), **u8),
+        "y": torch.empty((M, K), **u8), "ys": torch.empty((M, K // 128), **f32),
+        "yT": torch.empty((K, M), **u8), "yTs": torch.empty((K, cap), **f32),
+        "amax": torch.empty((1,), **f32),
+        "q4": torch.empty((M, K // 2), **u8), "sb4": torch.empty((M, K // 16), **u8),
+        "g4": torch.empty((1,), **f32),
+        "q2": torch.empty((M, K // 2), **u8), "sb2": torch.empty((M // 16, K // 16), **u8),
+        "g2": torch.empty((1,), **f32),
+    }
+    flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, xin, ev=None):
+        o = out
+        if ev:
+            ev[0].record(stream)
+        fq.mxfp4_quantize_rows(xin, o["q"], o["s"])
+        if ev:
+            ev[1].record(stream)
+        fq.fp4_to_fp8_rows(o["q"], o["s"], 0, o["y"], o["ys"])
+        if ev:
+            ev[2].record(stream)
+        fq.fp4_to_fp8_cols(o["q"], o["s"], offs, 0, o["yT"], o["yTs"])
+        if ev:
+            ev[3].record(stream)
+        fq.nvfp4_amax(xin, o["amax"])
+        if ev:
+            ev[4].record(stream)
+        fq.nvfp4_quantize(xin, o["amax"], use_sr=True, seed=1000 + i, offset=0, q=o["q4"],
+                          sb=o["sb4"], g=o["g4"])
+        if ev:
+            ev[5].record(stream)
+        fq.nvfp4_quantize_2d(xin, o["amax"], o["q2"], o["sb2"], o["g2"])
+        if ev:
+            ev[6].record(stream)
+
+    for i in range(args.warmup):
+        flush.zero_()
+        step(i, x)
+    torch.cuda.synchronize(dev)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        step(i, x, evs[i])
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if ws > 1:
+        dist.barrier()
+    clocks = sampler.stop(t0, t1)
+
+    per_kernel_ms = {k: 0.0 for k in KERNELS}
+    step_ms = 0.0
+    for ev in evs:
+        for j, k in enumerate(KERNELS):
+            per_kernel_ms[k] += ev[j].elapsed_time(ev[j + 1])
+        step_ms += ev[0].elapsed_time(ev[6])
+    step_ms_max = max_over_ranks(step_ms, dev)
+    ms_per_step = step_ms_max / args.steps
+    value = ws * step_bytes * args.steps / (step_ms_max * 1e-3) / 1e9
+
+    peak, peak_kind = hbm_peak()
+    kernels = {}
+    for k in KERNELS:
+        ms = per_kernel_ms[k] / args.steps
+        gbs = nbytes[k] / (ms * 1e-3) / 1e9
+        kernels[k] = {"us": round(ms * 1e3, 2), "bytes": nbytes[k], "GB/s": round(gbs, 1),
+                      "frac": round(gbs / peak, 4)}
+    dom = max(KERNELS, key=lambda k: per_kernel_ms[k])
+    traffic = ncu_traffic(dom)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["GB/s"],
+                "peak": peak, "unit": "GB/s", "frac": kernels[dom]["frac"],
+                "traffic": traffic, "peak_source": f"hbm_gbs of {peak_kind}",
+                "algorithmic_bytes": nbytes[dom]}
+
+    # ---- end to end through host buffers: H2D input, all casts, D2H outputs
+    e2e_steps = max(3, min(args.steps, 30))
+    xh = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    offs_h = torch.from_numpy(offs_np).pin_memory()
+    xd = torch.empty_like(x)
+    outs_h = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items()}
+    h2d = xh.numel() * 2 + offs_h.numel() * 8
+    d2h = sum(v.numel() * v.element_size() for k, v in out.items())
+
+    def e2e_step(i):
+        xd.copy_(xh, non_blocking=True)
+        offs.copy_(offs_h, non_blocking=True)
+        step(i, xd)
+        for k, v in out.items():
+            outs_h[k].copy_(v, non_blocking=True)
+
+    e2e_step(0)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    e0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev) / e2e_steps
+    e2e_value = ws * step_bytes / (e2e_ms * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "K": K, "experts": G,
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                       "l2": "flushed between steps (256 MB write, outside the timed events)",
+                       "step_bytes": step_bytes},
+            "frac_of_hbm_peak": round(value / ws / peak, 4),
+            "kernels": kernels,
+            "roofline": roofline,
+            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+            "gpu_launches": len(KERNELS) * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "wall_s_timed_region": round(t1 - t0, 4),
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["fq", "reference"], default="fq")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,1 +1,227 @@
-"""placeholder"""
+"""Block-scaled FP4 / FP8 casts for GB300 -- Python binding of libfq.so.
+
+Every function here only marshals arguments: it checks tensor placement and
+dtype, allocates outputs with ``torch.empty`` when none are given, and calls
+the C entry point of the same name (declared in ``include/fq.h``) on the
+current CUDA stream.  All arithmetic runs in the sm_103a kernels of libfq.so;
+there is no CPU or PyTorch fallback -- if the library is missing, every call
+raises.
+
+Sources (page title, section):
+* "Practical FP4 Training for Large-Scale MoE Models on Hopper GPUs",
+  technical overview section 2: MXFP4 (BF16ToFP4Row), direct FP4->FP8
+  conversion with hierarchical scale alignment (FP4RowToFP8Row,
+  FP4RowToFP8Col), ragged expert groups.
+* "Train models faster with JAX and MaxText using NVFP4 on NVIDIA Blackwell",
+  section "Receta de pre-entrenamiento NVFP4": NVFP4 1x16 and 16x16 scaling,
+  stochastic rounding.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfq.so")
+
+FQ_COLS_MAX_GROUPS = 1024
+
+_vp, _i64, _i32, _u64, _int = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64,
+                               ctypes.c_int)
+
+# C signatures, by entry point (restype, argtypes); must match include/fq.h.
+SIGNATURES = {
+    "fq_status_string": (ctypes.c_char_p, [_int]),
+    "fq_last_cuda_error": (_int, []),
+    "fq_version": (_int, []),
+    "mxfp4_quantize_rows": (_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
+    "fp4_to_fp8_rows": (_int, [_vp, _vp, _i64, _i64, _int, _vp, _vp, _vp]),
+    "fp4_to_fp8_cols_scale_capacity": (_i64, [_i64, _i32]),
+    "fp4_to_fp8_cols": (_int, [_vp, _vp, _i64, _i64, _vp, _i32, _int, _vp, _vp, _i64, _vp, _vp]),
+    "nvfp4_amax": (_int, [_vp, _i64, _vp, _vp]),
+    "nvfp4_quantize": (_int, [_vp, _i64, _i64, _vp, _int, _u64, _u64, _vp, _vp, _vp, _vp]),
+    "nvfp4_quantize_2d": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FQError(RuntimeError):
+    """A libfq.so entry point returned a status other than FQ_OK."""
+
+    def __init__(self, name: str, status: int):
+        self.status = status
+        msg = abi().fq_status_string(status).decode()
+        if status == 5:
+            msg += f" (cudaError {abi().fq_last_cuda_error()})"
+        super().__init__(f"{name}: {msg}")
+
+
+def abi() -> ctypes.CDLL:
+    """The loaded libfq.so with typed entry points (raises if not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"libfq.so not found at {LIB_PATH}: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` (nvcc, sm_103a)")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+        return _lib
+
+
+def _call(name: str, *args) -> None:
+    status = getattr(abi(), name)(*args)
+    if status != 0:
+        raise FQError(name, status)
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _p(t: torch.Tensor | None):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _need(t: torch.Tensor, dtype, name: str, ndim: int | None = None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+
+
+def _bf16_2d(x: torch.Tensor, name: str):
+    if x.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise ValueError(f"{name} must be bfloat16 (or its 16-bit pattern)")
+    _need(x, x.dtype, name, 2)
+
+
+def _empty(shape, dtype, like: torch.Tensor):
+    return torch.empty(shape, dtype=dtype, device=like.device)
+
+
+# ---------------------------------------------------------------- MXFP4
+
+def mxfp4_quantize_rows(x: torch.Tensor, q: torch.Tensor | None = None,
+                        s: torch.Tensor | None = None):
+    """BF16 [M, K] -> (q uint8 [M, K/2] packed E2M1, s uint8 [M, K/32] UE8M0)."""
+    _bf16_2d(x, "x")
+    M, K = x.shape
+    q = _empty((M, K // 2), torch.uint8, x) if q is None else q
+    s = _empty((M, K // 32), torch.uint8, x) if s is None else s
+    _need(q, torch.uint8, "q")
+    _need(s, torch.uint8, "s")
+    if K % 32 == 0 and (q.numel() != M * K // 2 or s.numel() != M * K // 32):
+        raise ValueError("output sizes do not match x")
+    _call("mxfp4_quantize_rows", _p(x), M, K, _p(q), _p(s), _stream())
+    return q, s
+
+
+def fp4_to_fp8_rows(q: torch.Tensor, s: torch.Tensor, exp_offset_k: int = 0,
+                    y: torch.Tensor | None = None, ys: torch.Tensor | None = None):
+    """MXFP4 -> (y uint8 [M, K] E4M3, ys float32 [M, K/128])."""
+    _need(q, torch.uint8, "q", 2)
+    _need(s, torch.uint8, "s", 2)
+    M, K = q.shape[0], q.shape[1] * 2
+    if s.shape != (M, K // 32):
+        raise ValueError("s must be [M, K/32]")
+    y = _empty((M, K), torch.uint8, q) if y is None else y
+    ys = _empty((M, max(K // 128, 0)), torch.float32, q) if ys is None else ys
+    _need(y, torch.uint8, "y")
+    _need(ys, torch.float32, "ys")
+    if K % 128 == 0 and (y.numel() != M * K or ys.numel() != M * K // 128):
+        raise ValueError("output sizes do not match q")
+    _call("fp4_to_fp8_rows", _p(q), _p(s), M, K, int(exp_offset_k), _p(y), _p(ys), _stream())
+    return y, ys
+
+
+def fp4_to_fp8_cols_scale_capacity(M: int, G: int) -> int:
+    return int(abi().fp4_to_fp8_cols_scale_capacity(int(M), int(G)))
+
+
+def fp4_to_fp8_cols(q: torch.Tensor, s: torch.Tensor, group_offsets: torch.Tensor,
+                    exp_offset_k: int = 0, yT: torch.Tensor | None = None,
+                    yT_scale: torch.Tensor | None = None, dev_status: torch.Tensor | None = None):
+    """MXFP4 [M tokens, K] with int64 group offsets [G+1] (device) ->
+    (yT uint8 [K, M] E4M3, yT_scale float32 [K, cap])."""
+    _need(q, torch.uint8, "q", 2)
+    _need(s, torch.uint8, "s", 2)
+    _need(group_offsets, torch.int64, "group_offsets", 1)
+    M, K = q.shape[0], q.shape[1] * 2
+    G = group_offsets.numel() - 1
+    cap = fp4_to_fp8_cols_scale_capacity(M, max(G, 1))
+    yT = _empty((K, M), torch.uint8, q) if yT is None else yT
+    yT_scale = _empty((K, cap), torch.float32, q) if yT_scale is None else yT_scale
+    _need(yT, torch.uint8, "yT")
+    _need(yT_scale, torch.float32, "yT_scale", 2)
+    if dev_status is not None:
+        _need(dev_status, torch.int32, "dev_status")
+    if yT.numel() != K * M or yT_scale.shape[0] != K:
+        raise ValueError("output sizes do not match q")
+    _call("fp4_to_fp8_cols", _p(q), _p(s), M, K, _p(group_offsets), G, int(exp_offset_k), _p(yT),
+          _p(yT_scale), int(yT_scale.shape[1]), _p(dev_status), _stream())
+    return yT, yT_scale
+
+
+# ---------------------------------------------------------------- NVFP4
+
+def nvfp4_amax(x: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """max |x| of a BF16 tensor into a 1-element float32 device tensor."""
+    if x.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise ValueError("x must be bfloat16")
+    _need(x, x.dtype, "x")
+    out = _empty((1,), torch.float32, x) if out is None else out
+    _need(out, torch.float32, "out")
+    _call("nvfp4_amax", _p(x), x.numel(), _p(out), _stream())
+    return out
+
+
+def nvfp4_quantize(x: torch.Tensor, amax: torch.Tensor | None = None, use_sr: bool = False,
+                   seed: int = 0, offset: int = 0, q: torch.Tensor | None = None,
+                   sb: torch.Tensor | None = None, g: torch.Tensor | None = None):
+    """BF16 [M, K] -> (q uint8 [M, K/2], sb uint8 [M, K/16] E4M3, g float32 [1])."""
+    _bf16_2d(x, "x")
+    M, K = x.shape
+    amax = nvfp4_amax(x) if amax is None else amax
+    _need(amax, torch.float32, "amax")
+    q = _empty((M, K // 2), torch.uint8, x) if q is None else q
+    sb = _empty((M, K // 16), torch.uint8, x) if sb is None else sb
+    g = _empty((1,), torch.float32, x) if g is None else g
+    _need(q, torch.uint8, "q")
+    _need(sb, torch.uint8, "sb")
+    _need(g, torch.float32, "g")
+    _call("nvfp4_quantize", _p(x), M, K, _p(amax), int(bool(use_sr)), int(seed) & (2**64 - 1),
+          int(offset), _p(q), _p(sb), _p(g), _stream())
+    return q, sb, g
+
+
+def nvfp4_quantize_2d(w: torch.Tensor, amax: torch.Tensor | None = None,
+                      q: torch.Tensor | None = None, sb: torch.Tensor | None = None,
+                      g: torch.Tensor | None = None):
+    """BF16 [N, K] -> (q uint8 [N, K/2], sb uint8 [N/16, K/16] E4M3, g float32 [1])."""
+    _bf16_2d(w, "w")
+    N, K = w.shape
+    amax = nvfp4_amax(w) if amax is None else amax
+    _need(amax, torch.float32, "amax")
+    q = _empty((N, K // 2), torch.uint8, w) if q is None else q
+    sb = _empty((N // 16, K // 16), torch.uint8, w) if sb is None else sb
+    g = _empty((1,), torch.float32, w) if g is None else g
+    _need(q, torch.uint8, "q")
+    _need(sb, torch.uint8, "sb")
+    _need(g, torch.float32, "g")
+    _call("nvfp4_quantize_2d", _p(w), N, K, _p(amax), _p(q), _p(sb), _p(g), _stream())
+    return q, sb, g

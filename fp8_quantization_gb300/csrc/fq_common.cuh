@@ -1,0 +1,196 @@
+// Device helpers shared by the cast kernels of libfq.so (sm_103a only).
+//
+// Conversions use the PTX packed conversion instructions (cvt ... e2m1x2,
+// e4m3x2) whose rounding is round-to-nearest-even with saturation to the
+// largest finite value; the tests check their outputs against the CPU
+// oracle over every input the kernels can feed them.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fq.h"
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ < 1000)
+#error "libfq.so is written for sm_103a (Blackwell Ultra); build with -gencode arch=compute_103a,code=sm_103a"
+#endif
+
+namespace fq {
+
+constexpr int kThreads = 256;
+
+// ---------------------------------------------------------------- host side
+
+// Records the CUDA error of a failed launch for fq_last_cuda_error().
+void set_last_cuda_error(int err);
+// SM count of the current device (cached per device).
+int sm_count();
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline fq_status launch_status()
+{
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_last_cuda_error(static_cast<int>(e));
+        return FQ_ERR_CUDA;
+    }
+    return FQ_OK;
+}
+
+// Persistent grid: enough CTAs to fill every SM at the kernel's occupancy,
+// never more than there is work for.
+template <typename Kernel>
+inline int persistent_grid(Kernel kernel, int threads, size_t smem, int64_t work_ctas)
+{
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) !=
+            cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    int64_t g = static_cast<int64_t>(sm_count()) * per_sm;
+    if (work_ctas < g)
+        g = work_ctas;
+    return static_cast<int>(g < 1 ? 1 : g);
+}
+
+// ---------------------------------------------------------------- device side
+
+// BF16 halves of a 32-bit word as FP32 (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Element-wise max of two packed u16 pairs.  Applied to BF16 words with the
+// sign bits cleared, this is |x| max in which Inf (0x7F80) and NaN (above
+// 0x7F80) are the largest values.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint32_t w)
+{
+    return max_u16x2(acc, w & 0x7FFF7FFFu);
+}
+
+// Larger of the two u16 halves.
+__device__ __forceinline__ uint32_t hmax_u16x2(uint32_t w)
+{
+    uint32_t lo = w & 0xFFFFu, hi = w >> 16;
+    return lo > hi ? lo : hi;
+}
+
+// Eight FP32 values -> eight E2M1 codes in one word, value i in bits 4i..4i+3.
+// cvt ... e2m1x2 puts its first source in the high nibble.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float v0, float v1, float v2, float v3, float v4,
+                                               float v5, float v6, float v7)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
+    return r;
+}
+
+// Non-negative FP32 -> E4M3 byte (round to nearest even, saturating at 448).
+__device__ __forceinline__ uint32_t cvt_e4m3(float t)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(t));
+    return static_cast<uint32_t>(r) & 0xFFu;
+}
+
+// E4M3 magnitude of code b (0..126) as FP32, exact.
+__device__ __forceinline__ float e4m3_value(uint32_t b)
+{
+    uint32_t E = b >> 3, m = b & 7u;
+    if (E == 0)
+        return __uint2float_rn(m) * 0x1p-9f;
+    return __uint_as_float((b + 960u) << 20);  // exponent field E - 7 + 127
+}
+
+// Byte permute (prmt.b32): result byte i chosen by selector nibble i from the
+// eight bytes {b:a}; a selector with bit 3 set replicates that byte's msb.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// Eight E2M1 codes (one word, code i in bits 4i..4i+3) -> eight E4M3 bytes
+// through an 8-entry magnitude table {t1:t0}; the sign of each code becomes
+// bit 7 of its byte.
+__device__ __forceinline__ void fp4x8_to_fp8x8(uint32_t w, uint32_t t0, uint32_t t1,
+                                               uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t sel = w & 0x77777777u;
+    const uint32_t w4 = w << 4;
+    const uint32_t mlo = prmt(t0, t1, sel);
+    const uint32_t mhi = prmt(t0, t1, sel >> 16);
+    const uint32_t slo = prmt(w4, w, 0xD9C8u);  // msb of codes 0..3 replicated
+    const uint32_t shi = prmt(w4, w, 0xFBEAu);  // msb of codes 4..7 replicated
+    lo = mlo | (slo & 0x80808080u);
+    hi = mhi | (shi & 0x80808080u);
+}
+
+// FP32 bits of the FP8 block scale 2^(S - 127 - k); NaN for S = 0xFF.
+__device__ __forceinline__ uint32_t fp8_block_scale_bits(uint32_t S, int k)
+{
+    if (S == 0xFFu)
+        return 0x7FC00000u;
+    int ex = static_cast<int>(S) - k;  // biased exponent of the result, >= -6
+    if (ex >= 1)
+        return static_cast<uint32_t>(ex) << 23;
+    return 1u << (ex + 22);  // binary32 subnormal 2^(ex - 127)
+}
+
+// Table of E4M3 bytes for E2M1 magnitude code c (0..7) shifted by 2^(6-u),
+// u = 0..19 (u = 19 covers every larger shift: all values flush to zero).
+constexpr int kShiftRows = 20;
+__device__ __forceinline__ void build_fp8_table(uint8_t *tab /* [kShiftRows * 8] */)
+{
+    for (int i = threadIdx.x; i < kShiftRows * 8; i += blockDim.x) {
+        int u = i >> 3, c = i & 7;
+        // E2M1 magnitude of c times 2^(6 - u), built exactly from bits
+        float v;
+        if (c == 0)
+            v = 0.0f;
+        else if (c == 1)
+            v = 0.5f;
+        else
+            v = __uint_as_float(((126u + (c >> 1)) << 23) | ((c & 1u) << 22));
+        v *= __uint_as_float(static_cast<uint32_t>(127 + 6 - u) << 23);
+        tab[i] = static_cast<uint8_t>(cvt_e4m3(v));
+    }
+}
+
+// Philox4x32-10 (Salmon et al., SC'11).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1)
+{
+#pragma unroll
+    for (int i = 0; i < 10; i++) {
+        if (i) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    }
+    return c;
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void *p)
+{
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+}  // namespace fq

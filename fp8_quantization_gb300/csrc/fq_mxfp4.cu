@@ -1,0 +1,183 @@
+// MXFP4 row quantization (BF16ToFP4Row) and direct FP4 -> FP8 row conversion
+// (FP4RowToFP8Row).
+//
+// Source: "Practical FP4 Training for Large-Scale MoE Models on Hopper GPUs",
+// technical overview section 2 -- 32-element MX blocks with a UE8M0 scale and
+// E2M1 elements, two values per byte; the bitwise FP4->FP8 conversion that
+// aligns the four MX exponents of a 128-element block to their maximum.
+//
+// Both kernels stream HBM once: 128-bit loads, warp-shuffle block amax, packed
+// conversion instructions, coalesced stores; persistent grids sized to the
+// SM count.  Rows play no role: with K a multiple of the block, a row-major
+// tensor is a flat sequence of blocks.
+#include "fq_common.cuh"
+
+namespace fq {
+
+// ---------------------------------------------------------------- a1: BF16 -> MXFP4
+
+// One warp tile = 32 MX blocks = 1024 elements.  Lane l owns the 16-byte
+// chunks l, l+32, l+64, l+96 of the tile; chunk c is quarter (c & 3) of MX
+// block c >> 2, so the four lanes 4g..4g+3 hold block g + 8i of unroll i and
+// a two-step xor shuffle gives the block amax.  Every load and every code
+// store of the warp covers 512 / 128 contiguous bytes.
+__global__ void __launch_bounds__(kThreads) mxfp4_quantize_rows_kernel(
+    const uint16_t *__restrict__ x, int64_t nblk, uint8_t *__restrict__ q,
+    uint8_t *__restrict__ s)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t ntiles = (nblk + 31) >> 5;
+
+    for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
+        const int64_t blk0 = tile << 5;
+        uint4 v[4];
+        bool ok[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int64_t blk = blk0 + (lane >> 2) + 8 * i;
+            ok[i] = blk < nblk;
+            v[i] = ok[i] ? ld_nc_v4(x + blk * 32 + (lane & 3) * 8) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            uint32_t m = absmax_bf16x2(absmax_bf16x2(v[i].x & 0x7FFF7FFFu, v[i].y), v[i].z);
+            m = absmax_bf16x2(m, v[i].w);
+            m = max_u16x2(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = max_u16x2(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            const uint32_t amax = hmax_u16x2(m);  // |x| bits of the block max
+            // e = max(E - 2, 0) for the block max's exponent field E (BF16
+            // subnormals and zero have E = 0); 0xFF if the block has NaN/Inf.
+            const bool special = amax >= 0x7F80u;
+            const int E = static_cast<int>(amax >> 7);
+            const uint32_t e = static_cast<uint32_t>(E > 2 ? E - 2 : 0);  // <= 252
+            const float mul = __uint_as_float((254u - e) << 23);             // 2^(127 - e)
+            uint32_t codes = cvt_e2m1x8(
+                __fmul_rn(bf16_lo(v[i].x), mul), __fmul_rn(bf16_hi(v[i].x), mul),
+                __fmul_rn(bf16_lo(v[i].y), mul), __fmul_rn(bf16_hi(v[i].y), mul),
+                __fmul_rn(bf16_lo(v[i].z), mul), __fmul_rn(bf16_hi(v[i].z), mul),
+                __fmul_rn(bf16_lo(v[i].w), mul), __fmul_rn(bf16_hi(v[i].w), mul));
+            if (special)
+                codes = 0;
+            if (ok[i]) {
+                const int64_t blk = blk0 + (lane >> 2) + 8 * i;
+                *reinterpret_cast<uint32_t *>(q + blk * 16 + (lane & 3) * 4) = codes;
+                if ((lane & 3) == 0)
+                    s[blk] = static_cast<uint8_t>(special ? 0xFFu : e);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- a2: FP4 -> FP8 rows
+
+// One warp pass = 4 FP8 blocks (128 elements each): lane l converts 16 codes
+// (8 bytes of q) of FP8 block (l >> 3), i.e. half of MX block (l & 7) >> 1,
+// into 16 E4M3 bytes.  The four scale bytes of an FP8 block are one aligned
+// 32-bit word.  Per MX block an 8-entry magnitude table row is fetched from
+// shared memory by shift; codes are translated with byte permutes.
+constexpr int kRowsUnroll = 8;
+
+__global__ void __launch_bounds__(kThreads) fp4_to_fp8_rows_kernel(
+    const uint8_t *__restrict__ q, const uint8_t *__restrict__ s, int64_t nfb, int k,
+    uint8_t *__restrict__ y, float *__restrict__ ys)
+{
+    __shared__ __align__(16) uint8_t tab[kShiftRows * 8];
+    build_fp8_table(tab);
+    __syncthreads();
+
+    const int lane = threadIdx.x & 31;
+    const int part = lane & 7;  // 8-byte part of the 64-byte FP8 block
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t ntiles = (nfb + 4 * kRowsUnroll - 1) / (4 * kRowsUnroll);
+
+    for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
+        const int64_t fb0 = tile * (4 * kRowsUnroll);
+        uint2 c[kRowsUnroll];
+        uint32_t sw[kRowsUnroll];
+#pragma unroll
+        for (int i = 0; i < kRowsUnroll; i++) {
+            const int64_t fb = fb0 + 4 * i + (lane >> 3);
+            if (fb < nfb) {
+                c[i] = __ldg(reinterpret_cast<const uint2 *>(q + fb * 64 + part * 8));
+                sw[i] = __ldg(reinterpret_cast<const uint32_t *>(s) + fb);
+            } else {
+                c[i] = make_uint2(0, 0);
+                sw[i] = 0;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kRowsUnroll; i++) {
+            const int64_t fb = fb0 + 4 * i + (lane >> 3);
+            const uint32_t w = sw[i];
+            const uint32_t b0 = w & 0xFFu, b1 = (w >> 8) & 0xFFu, b2 = (w >> 16) & 0xFFu,
+                           b3 = w >> 24;
+            const uint32_t S = max(max(b0, b1), max(b2, b3));
+            const uint32_t e = (w >> (8 * (part >> 1))) & 0xFFu;
+            int u = static_cast<int>(S - e) - k + 6;
+            u = u < kShiftRows - 1 ? u : kShiftRows - 1;
+            const uint2 t = *reinterpret_cast<const uint2 *>(tab + 8 * u);
+            uint4 out;
+            fp4x8_to_fp8x8(c[i].x, t.x, t.y, out.x, out.y);
+            fp4x8_to_fp8x8(c[i].y, t.x, t.y, out.z, out.w);
+            if (S == 0xFFu)
+                out = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+            if (fb < nfb) {
+                *reinterpret_cast<uint4 *>(y + fb * 128 + part * 16) = out;
+                if (part == 0)
+                    reinterpret_cast<uint32_t *>(ys)[fb] = fp8_block_scale_bits(S, k);
+            }
+        }
+    }
+}
+
+}  // namespace fq
+
+using namespace fq;
+
+extern "C" fq_status mxfp4_quantize_rows(const void *x, int64_t M, int64_t K, uint8_t *q,
+                                         uint8_t *s, void *stream)
+{
+    if (M < 0 || K <= 0 || K % 32 != 0)
+        return FQ_ERR_SHAPE;
+    if (M > 0 && K > INT64_MAX / M)
+        return FQ_ERR_SHAPE;
+    if (M == 0)
+        return FQ_OK;
+    if (!x || !q || !s)
+        return FQ_ERR_NULL;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(s))
+        return FQ_ERR_ALIGN;
+    const int64_t nblk = M * (K / 32);
+    const int64_t work = (nblk + 32 * (kThreads / 32) - 1) / (32 * (kThreads / 32));
+    const int grid = persistent_grid(mxfp4_quantize_rows_kernel, kThreads, 0, work);
+    mxfp4_quantize_rows_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(x), nblk, q, s);
+    return launch_status();
+}
+
+extern "C" fq_status fp4_to_fp8_rows(const uint8_t *q, const uint8_t *s, int64_t M, int64_t K,
+                                     int exp_offset_k, uint8_t *y, float *ys, void *stream)
+{
+    if (M < 0 || K <= 0 || K % 128 != 0)
+        return FQ_ERR_SHAPE;
+    if (M > 0 && K > INT64_MAX / M)
+        return FQ_ERR_SHAPE;
+    if (exp_offset_k < 0 || exp_offset_k > 6)
+        return FQ_ERR_ARG;
+    if (M == 0)
+        return FQ_OK;
+    if (!q || !s || !y || !ys)
+        return FQ_ERR_NULL;
+    if (!aligned16(q) || !aligned16(s) || !aligned16(y) || !aligned16(ys))
+        return FQ_ERR_ALIGN;
+    const int64_t nfb = M * (K / 128);
+    const int64_t per_cta = 4 * kRowsUnroll * (kThreads / 32);
+    const int grid =
+        persistent_grid(fp4_to_fp8_rows_kernel, kThreads, 0, (nfb + per_cta - 1) / per_cta);
+    fp4_to_fp8_rows_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        q, s, nfb, exp_offset_k, y, ys);
+    return launch_status();
+}

@@ -1,0 +1,310 @@
+// NVFP4 quantization: per-tensor amax, 1x16 micro-blocks (round to nearest
+// even or stochastic rounding) and 16x16 2D weight blocks.
+//
+// Source: "Train models faster with JAX and MaxText using NVFP4 on NVIDIA
+// Blackwell", section "Receta de pre-entrenamiento NVFP4": 16-element
+// micro-block scaling, E4M3 block scale factors under an FP32 per-tensor
+// scale, 2D 16x16 weight scaling, stochastic rounding for gradients (round
+// to nearest even for weights and activations).
+//
+// The scale arithmetic is IEEE binary32 with one rounding per operation
+// (explicit __fdiv_rn / __frcp_rn / __fmul_rn), so every code is a function
+// of the inputs alone:
+//   g = A / 2688 (1 if A == 0); t = amax_blk / (6 g); b = E4M3(t);
+//   r = min(1 / (b g), FLT_MAX) (0 if b == 0); code = E2M1(|x| r), sign of x.
+#include <cfloat>
+
+#include "fq_common.cuh"
+
+namespace fq {
+
+// ---------------------------------------------------------------- amax
+
+__global__ void __launch_bounds__(kThreads) nvfp4_amax_kernel(const uint16_t *__restrict__ x,
+                                                              int64_t n,
+                                                              uint32_t *__restrict__ out_bits)
+{
+    __shared__ uint32_t red[kThreads / 32];
+    const int64_t nvec = n >> 3;  // 16-byte chunks
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    uint32_t m = 0;
+    int64_t i = gtid;
+    for (; i + 3 * nthr < nvec; i += 4 * nthr) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++)
+            v[u] = ld_nc_v4(x + (i + u * nthr) * 8);
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            m = absmax_bf16x2(m, v[u].x);
+            m = absmax_bf16x2(m, v[u].y);
+            m = absmax_bf16x2(m, v[u].z);
+            m = absmax_bf16x2(m, v[u].w);
+        }
+    }
+    for (; i < nvec; i += nthr) {
+        const uint4 v = ld_nc_v4(x + i * 8);
+        m = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m, v.x), v.y), v.z), v.w);
+    }
+    for (int64_t t = nvec * 8 + gtid; t < n; t += nthr)
+        m = max_u16x2(m, x[t] & 0x7FFFu);
+    uint32_t h = hmax_u16x2(m);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1)
+        h = max(h, __shfl_xor_sync(0xffffffffu, h, d));
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = h;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t b = 0;
+        for (int w = 0; w < kThreads / 32; w++)
+            b = max(b, red[w]);
+        // |x| as binary32 bits: non-negative floats order like their bits,
+        // and NaN patterns sit above infinity.
+        atomicMax(out_bits, b << 16);
+    }
+}
+
+// ---------------------------------------------------------------- block scale
+
+struct BlockScale {
+    uint32_t b;  // E4M3 byte
+    float r;     // element multiplier
+};
+
+__device__ __forceinline__ BlockScale nvfp4_block_scale(uint32_t amax_bits16, float g, float six_g)
+{
+    const float amax = __uint_as_float(amax_bits16 << 16);
+    const float t = __fdiv_rn(amax, six_g);
+    BlockScale bs;
+    bs.b = cvt_e4m3(t);
+    const float den = __fmul_rn(e4m3_value(bs.b), g);
+    bs.r = bs.b ? fminf(__frcp_rn(den), FLT_MAX) : 0.0f;
+    return bs;
+}
+
+__device__ __forceinline__ float tensor_scale(const float *amax)
+{
+    const float A = *amax;
+    return A > 0.0f ? __fdiv_rn(A, 2688.0f) : 1.0f;
+}
+
+// Stochastic rounding of y >= 0 to an E2M1 magnitude code with 16 random
+// bits R: round up iff R < floor(2^16 * (y - lo) / (hi - lo)).
+// Y = floor(y * 2^17) comes exactly from the mantissa of y + 64 rounded
+// toward zero; the grid step is 2^(16 + sh) in units of Y.
+__device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t R)
+{
+    const uint32_t Y = __float_as_uint(__fadd_rz(y, 64.0f)) & 0x7FFFFFu;
+    const uint32_t sh = Y >> 18;  // 0: y < 2, 1: y < 4, 2: y < 6
+    const uint32_t lo = (Y >> (16 + sh)) + 2 * sh;
+    const uint32_t F = (Y >> sh) & 0xFFFFu;
+    const uint32_t c = lo + (R < F ? 1u : 0u);
+    return y >= 6.0f ? 7u : c;
+}
+
+// Eight BF16 values (one uint4) times r -> eight E2M1 codes in a word.
+__device__ __forceinline__ uint32_t encode8_rne(uint4 v, float r)
+{
+    return cvt_e2m1x8(__fmul_rn(bf16_lo(v.x), r), __fmul_rn(bf16_hi(v.x), r),
+                      __fmul_rn(bf16_lo(v.y), r), __fmul_rn(bf16_hi(v.y), r),
+                      __fmul_rn(bf16_lo(v.z), r), __fmul_rn(bf16_hi(v.z), r),
+                      __fmul_rn(bf16_lo(v.w), r), __fmul_rn(bf16_hi(v.w), r));
+}
+
+__device__ __forceinline__ uint32_t encode8_sr(uint4 v, float r, uint4 rnd)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t R[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+    uint32_t out = 0;
+#pragma unroll
+    for (int h = 0; h < 4; h++) {
+        const float ylo = __fmul_rn(__uint_as_float((w[h] << 16) & 0x7FFF0000u), r);
+        const float yhi = __fmul_rn(__uint_as_float(w[h] & 0x7FFF0000u), r);
+        const uint32_t clo = e2m1_sr(ylo, R[h] & 0xFFFFu) | ((w[h] >> 12) & 8u);
+        const uint32_t chi = e2m1_sr(yhi, R[h] >> 16) | ((w[h] >> 28) & 8u);
+        out |= (clo | (chi << 4)) << (8 * h);
+    }
+    return out;
+}
+
+// ---------------------------------------------------------------- 1x16
+
+// Two lanes per 16-element block (8 elements = 16 bytes each); a warp pass
+// covers 16 blocks = 512 contiguous bytes of input, unrolled 4 times.
+template <bool kSR>
+__global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
+    const uint16_t *__restrict__ x, int64_t nblk, const float *__restrict__ amax, uint64_t seed,
+    uint64_t offset, uint8_t *__restrict__ q, uint8_t *__restrict__ sb, float *__restrict__ g_out)
+{
+    const float g = tensor_scale(amax);
+    const float six_g = __fmul_rn(6.0f, g);
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        *g_out = g;
+    const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+
+    const int lane = threadIdx.x & 31;
+    const int half = lane & 1;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t ntiles = (nblk + 63) >> 6;
+
+    for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
+        uint4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int64_t blk = (tile << 6) + 16 * i + (lane >> 1);
+            v[i] = blk < nblk ? ld_nc_v4(x + blk * 16 + half * 8) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int64_t blk = (tile << 6) + 16 * i + (lane >> 1);
+            uint32_t m = absmax_bf16x2(absmax_bf16x2(v[i].x & 0x7FFF7FFFu, v[i].y), v[i].z);
+            m = absmax_bf16x2(m, v[i].w);
+            m = max_u16x2(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            const BlockScale bs = nvfp4_block_scale(hmax_u16x2(m), g, six_g);
+            uint32_t codes;
+            if (kSR) {
+                const uint64_t c = (offset + static_cast<uint64_t>(blk) * 16 + half * 8) >> 3;
+                const uint4 rnd = philox4x32_10(
+                    make_uint4(static_cast<uint32_t>(c), static_cast<uint32_t>(c >> 32), 0u, 0u),
+                    k0, k1);
+                codes = encode8_sr(v[i], bs.r, rnd);
+            } else {
+                codes = encode8_rne(v[i], bs.r);
+            }
+            if (blk < nblk) {
+                *reinterpret_cast<uint32_t *>(q + blk * 8 + half * 4) = codes;
+                if (!half)
+                    sb[blk] = static_cast<uint8_t>(bs.b);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- 16x16
+
+// A warp owns a 16-row strip x 256 columns: lane l holds columns 8l..8l+7 of
+// all 16 rows (lanes 2t, 2t+1 form tile t), so every row load / store of the
+// warp is 512 / 128 contiguous bytes.
+__global__ void __launch_bounds__(kThreads, 2) nvfp4_quantize_2d_kernel(
+    const uint16_t *__restrict__ w, int64_t N, int64_t K, const float *__restrict__ amax,
+    uint8_t *__restrict__ q, uint8_t *__restrict__ sb, float *__restrict__ g_out)
+{
+    const float g = tensor_scale(amax);
+    const float six_g = __fmul_rn(6.0f, g);
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        *g_out = g;
+
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t ncg = (K + 255) >> 8;  // 256-column groups
+    const int64_t nunits = (N >> 4) * ncg;
+
+    for (int64_t unit = warp; unit < nunits; unit += nwarps) {
+        const int64_t strip = unit / ncg;
+        const int64_t col = ((unit - strip * ncg) << 8) + 8 * lane;
+        const bool ok = col < K;
+        const uint16_t *src = w + (strip << 4) * K + col;
+        uint4 v[16];
+#pragma unroll
+        for (int r = 0; r < 16; r++)
+            v[r] = ok ? ld_nc_v4(src + r * K) : make_uint4(0, 0, 0, 0);
+        uint32_t m = 0;
+#pragma unroll
+        for (int r = 0; r < 16; r++) {
+            m = absmax_bf16x2(m, v[r].x);
+            m = absmax_bf16x2(m, v[r].y);
+            m = absmax_bf16x2(m, v[r].z);
+            m = absmax_bf16x2(m, v[r].w);
+        }
+        m = max_u16x2(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        const BlockScale bs = nvfp4_block_scale(hmax_u16x2(m), g, six_g);
+        if (ok) {
+            uint8_t *dst = q + (strip << 4) * (K >> 1) + (col >> 1);
+#pragma unroll
+            for (int r = 0; r < 16; r++)
+                *reinterpret_cast<uint32_t *>(dst + r * (K >> 1)) = encode8_rne(v[r], bs.r);
+            if (!(lane & 1))
+                sb[strip * (K >> 4) + (col >> 4)] = static_cast<uint8_t>(bs.b);
+        }
+    }
+}
+
+}  // namespace fq
+
+using namespace fq;
+
+extern "C" fq_status nvfp4_amax(const void *x, int64_t n, float *amax, void *stream)
+{
+    if (n < 0)
+        return FQ_ERR_SHAPE;
+    if (!amax || (n > 0 && !x))
+        return FQ_ERR_NULL;
+    if ((n > 0 && !aligned16(x)) || !aligned16(amax))
+        return FQ_ERR_ALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(amax, 0, sizeof(float), st) != cudaSuccess)
+        return launch_status();
+    if (n == 0)
+        return FQ_OK;
+    const int64_t work = (n / 8 + 4 * kThreads - 1) / (4 * kThreads);
+    const int grid = persistent_grid(nvfp4_amax_kernel, kThreads, 0, work < 1 ? 1 : work);
+    nvfp4_amax_kernel<<<grid, kThreads, 0, st>>>(static_cast<const uint16_t *>(x), n,
+                                                  reinterpret_cast<uint32_t *>(amax));
+    return launch_status();
+}
+
+extern "C" fq_status nvfp4_quantize(const void *x, int64_t M, int64_t K, const float *amax,
+                                    int use_sr, uint64_t seed, uint64_t offset, uint8_t *q,
+                                    uint8_t *sb, float *g, void *stream)
+{
+    if (M < 0 || K <= 0 || K % 16 != 0)
+        return FQ_ERR_SHAPE;
+    if (M > 0 && K > INT64_MAX / M)
+        return FQ_ERR_SHAPE;
+    if (offset % 16 != 0 || (use_sr != 0 && use_sr != 1))
+        return FQ_ERR_ARG;
+    if (M == 0)
+        return FQ_OK;
+    if (!x || !amax || !q || !sb || !g)
+        return FQ_ERR_NULL;
+    if (!aligned16(x) || !aligned16(amax) || !aligned16(q) || !aligned16(sb) || !aligned16(g))
+        return FQ_ERR_ALIGN;
+    const int64_t nblk = M * (K / 16);
+    const int64_t work = (nblk + 64 * (kThreads / 32) - 1) / (64 * (kThreads / 32));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (use_sr) {
+        const int grid = persistent_grid(nvfp4_quantize_kernel<true>, kThreads, 0, work);
+        nvfp4_quantize_kernel<true><<<grid, kThreads, 0, st>>>(
+            static_cast<const uint16_t *>(x), nblk, amax, seed, offset, q, sb, g);
+    } else {
+        const int grid = persistent_grid(nvfp4_quantize_kernel<false>, kThreads, 0, work);
+        nvfp4_quantize_kernel<false><<<grid, kThreads, 0, st>>>(
+            static_cast<const uint16_t *>(x), nblk, amax, seed, offset, q, sb, g);
+    }
+    return launch_status();
+}
+
+extern "C" fq_status nvfp4_quantize_2d(const void *w, int64_t N, int64_t K, const float *amax,
+                                       uint8_t *q, uint8_t *sb, float *g, void *stream)
+{
+    if (N < 0 || K <= 0 || N % 16 != 0 || K % 16 != 0)
+        return FQ_ERR_SHAPE;
+    if (N > 0 && K > INT64_MAX / N)
+        return FQ_ERR_SHAPE;
+    if (N == 0)
+        return FQ_OK;
+    if (!w || !amax || !q || !sb || !g)
+        return FQ_ERR_NULL;
+    if (!aligned16(w) || !aligned16(amax) || !aligned16(q) || !aligned16(sb) || !aligned16(g))
+        return FQ_ERR_ALIGN;
+    const int64_t units = (N / 16) * ((K + 255) / 256);
+    const int grid =
+        persistent_grid(nvfp4_quantize_2d_kernel, kThreads, 0, (units + 7) / 8);
+    nvfp4_quantize_2d_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(w), N, K, amax, q, sb, g);
+    return launch_status();
+}

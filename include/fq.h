@@ -1,0 +1,196 @@
+/*
+ * fq.h -- C ABI of libfq.so: block-scaled FP4 / FP8 casts of training
+ * tensors on GB300 (sm_103a).
+ *
+ * Formats and operations follow two sources, cited by page title and section:
+ *   [MoE-FP4] "Practical FP4 Training for Large-Scale MoE Models on Hopper
+ *             GPUs", technical overview, section 2 (Methodology):
+ *             item 1 -- MXFP4 = 32-element blocks sharing a power-of-two UE8M0
+ *             scale, E2M1 elements; direct bitwise FP4->FP8 conversion without
+ *             a BF16 intermediate; hierarchical scale alignment that maps four
+ *             32-element MX blocks onto one 128-element E4M3 block by aligning
+ *             exponents to the largest of the four scales;
+ *             item 2 -- FP4 values packed two per uint8;
+ *             item 3 -- kernels BF16ToFP4Row, FP4RowToFP8Row, FP4RowToFP8Col
+ *             (transpose fused with the conversion, for Wgrad) and ragged
+ *             per-expert token groups handled without padding.
+ *   [NVFP4]   "Train models faster with JAX and MaxText using NVFP4 on NVIDIA
+ *             Blackwell", section "Receta de pre-entrenamiento NVFP4":
+ *             16-element micro-blocks, E4M3 block scales under one FP32
+ *             per-tensor scale, 16x16 2D block scaling of weights, stochastic
+ *             rounding for gradient quantizers.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor is dense, row-major, contiguous, and lives in device memory
+ *   of the current CUDA device; the caller allocates and owns every buffer.
+ *   The library allocates nothing and keeps no state between calls.
+ * - Every pointer must be 16-byte aligned.  Inputs and outputs must not
+ *   overlap.
+ * - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *   enqueued on it asynchronously; no entry point synchronizes the host.
+ * - Arguments are checked on the host before anything is enqueued; a failed
+ *   check returns a status other than FQ_OK and enqueues nothing.  A failed
+ *   launch returns FQ_ERR_CUDA (the CUDA error code is then available from
+ *   fq_last_cuda_error() in the calling thread).
+ * - A size of 0 rows is a successful no-op.
+ * - BF16 inputs are passed as 16-bit words.  Non-finite inputs are not an
+ *   error: MXFP4 marks the block (scale byte 0xFF); for NVFP4 a non-finite
+ *   per-tensor amax is a precondition violation that still writes only
+ *   inside the outputs.
+ *
+ * Encodings
+ * ---------
+ * - E2M1 code (4 bits): sign bit 3, magnitude code 0..7 = {0, 0.5, 1, 1.5,
+ *   2, 3, 4, 6}.  Element 2i is the low nibble of byte i, element 2i+1 the
+ *   high nibble.  Rounding is to nearest, ties to the even code, saturating
+ *   at 6; the sign of a value rounded to zero is kept.
+ * - UE8M0 byte e encodes 2^(e-127); 0xFF marks a block with NaN or Inf.
+ * - E4M3 ("fn": bias 7, 0x7F = NaN, largest finite 448), round to nearest
+ *   even, saturating at 448.
+ */
+#ifndef FQ_H
+#define FQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FQ_OK = 0,
+    FQ_ERR_NULL = 1,  /* a required pointer is NULL */
+    FQ_ERR_SHAPE = 2, /* a size is negative, too large, or not a multiple of the block */
+    FQ_ERR_ALIGN = 3, /* a pointer is not 16-byte aligned */
+    FQ_ERR_ARG = 4,   /* another argument is out of range */
+    FQ_ERR_CUDA = 5   /* the CUDA runtime reported an error */
+} fq_status;
+
+/* Static, human-readable name of a status. */
+const char *fq_status_string(int status);
+
+/* cudaError_t of the last FQ_ERR_CUDA returned in the calling thread (0 if none). */
+int fq_last_cuda_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int fq_version(void);
+
+/*
+ * MXFP4 row quantization of BF16 activations ([MoE-FP4] 2.1 and 2.3,
+ * BF16ToFP4Row).
+ *   x  : bf16 [M, K]            input
+ *   q  : uint8 [M, K/2]         packed E2M1 codes (output)
+ *   s  : uint8 [M, K/32]        UE8M0 scale per 32-element block (output)
+ * For each block of 32 consecutive elements of a row: amax = max |x|;
+ * e = clamp(floor(log2 amax) - 2 + 127, 0, 254) (e = 0 for an all-zero
+ * block); each element is rounded as x / 2^(e-127) to E2M1.  A block that
+ * holds NaN or Inf gets e = 0xFF and all-zero codes.
+ * Requires K > 0, K % 32 == 0, M >= 0.
+ */
+fq_status mxfp4_quantize_rows(const void *x, int64_t M, int64_t K, uint8_t *q, uint8_t *s,
+                              void *stream);
+
+/*
+ * Direct FP4 -> FP8 conversion, row layout ([MoE-FP4] 2.1, FP4RowToFP8Row).
+ *   q, s : MXFP4 [M, K/2], [M, K/32] as produced by mxfp4_quantize_rows
+ *   y    : uint8 [M, K]          E4M3 codes (output)
+ *   ys   : float [M, K/128]      FP32 dequantization scale per 128 elements (output)
+ * Each 128-element block covers four MX blocks with exponents e0..e3;
+ * S = max(e_i).  An element of MX block i with E2M1 value v becomes
+ * E4M3(v * 2^(k - (S - e_i))), sign kept; ys = 2^(S - 127 - k), so
+ * ys * y == 2^(e_i - 127) * v exactly wherever S - e_i <= k + 8.  If any
+ * e_i is 0xFF the block gets ys = NaN (0x7FC00000) and all codes 0x7F.
+ * `exp_offset_k` (k) in [0, 6]: 0 is the plain alignment to the largest
+ * scale; larger k keeps k more binades exact (6 * 2^6 <= 448).
+ * Requires K > 0, K % 128 == 0, M >= 0.
+ */
+fq_status fp4_to_fp8_rows(const uint8_t *q, const uint8_t *s, int64_t M, int64_t K,
+                          int exp_offset_k, uint8_t *y, float *ys, void *stream);
+
+/* Largest number of 128-token blocks fp4_to_fp8_cols can produce for M rows
+ * in G groups: ceil(M / 128) + G.  Returns -1 for M < 0 or G < 1. */
+int64_t fp4_to_fp8_cols_scale_capacity(int64_t M, int32_t G);
+
+/* Largest group count accepted by fp4_to_fp8_cols. */
+#define FQ_COLS_MAX_GROUPS 1024
+
+/*
+ * Direct FP4 -> FP8 conversion fused with the transpose, on ragged
+ * per-expert token groups without padding ([MoE-FP4] 2.3, FP4RowToFP8Col;
+ * the Wgrad operand layout).
+ *   q, s          : MXFP4 [M, K/2], [M, K/32] (M tokens, K features)
+ *   group_offsets : int64 [G+1] in DEVICE memory; group g owns tokens
+ *                   offsets[g] .. offsets[g+1]-1; offsets[0] = 0,
+ *                   non-decreasing, offsets[G] = M (empty groups allowed)
+ *   yT            : uint8 [K, M]   E4M3, element (feature k, token t) at k*M + t
+ *   yT_scale      : float [K, cap] FP32 scale of block b of group g at
+ *                   k*cap + base_g + b, base_g = sum_{h<g} ceil(count_h/128);
+ *                   slots past the last block are not written
+ *   cap           : >= fp4_to_fp8_cols_scale_capacity(M, G)
+ *   dev_status    : optional int32 in device memory; if the offsets are
+ *                   malformed the kernel clamps them (so nothing is written
+ *                   out of bounds) and ORs 1 into *dev_status
+ * Each group is cut into 128-token blocks starting at its first token (the
+ * last block of a group may be short).  For a block and a 32-feature MX
+ * column, S = max of the tokens' exponents; each element is converted as in
+ * fp4_to_fp8_rows with that S.  Requires K % 128 == 0, 1 <= G <=
+ * FQ_COLS_MAX_GROUPS, 0 <= M < 2^31, k in [0, 6].
+ */
+fq_status fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t M, int64_t K,
+                          const int64_t *group_offsets, int32_t G, int exp_offset_k,
+                          uint8_t *yT, float *yT_scale, int64_t cap, int32_t *dev_status,
+                          void *stream);
+
+/*
+ * Per-tensor amax for NVFP4's FP32 tensor scale ([NVFP4] "Receta"):
+ *   x      : bf16 [n]
+ *   amax   : float in device memory (output) = max |x| (NaN if x holds NaN;
+ *            0 for n == 0)
+ */
+fq_status nvfp4_amax(const void *x, int64_t n, float *amax, void *stream);
+
+/*
+ * NVFP4 1x16 quantization ([NVFP4] "Receta": 16-element micro-blocks with
+ * E4M3 block scales under one FP32 per-tensor scale; stochastic rounding).
+ *   x        : bf16 [M, K]
+ *   amax     : float in device memory, max |x| of the whole tensor (nvfp4_amax)
+ *   q        : uint8 [M, K/2]   packed E2M1 codes (output)
+ *   sb       : uint8 [M, K/16]  E4M3 block scales (output)
+ *   g        : float in device memory, per-tensor decode scale (output)
+ * With all arithmetic in IEEE binary32, one rounding per operation:
+ *   g = amax / 2688 (g = 1 if amax == 0);  per block: t = amax_blk / (6 g),
+ *   b = E4M3(t), r = min(1 / (b g), FLT_MAX) (r = 0 if b == 0),
+ *   element code = E2M1(|x| * r) with the sign of x.  Decode: x ~ v * b * g.
+ * use_sr = 0: round to nearest even.  use_sr = 1: stochastic rounding --
+ *   with lo <= y < hi on the grid, round up iff R < floor(2^16 (y-lo)/(hi-lo));
+ *   R is 16 bits of Philox4x32-10 with key (seed low, seed high word) and
+ *   counter (c low, c high, 0, 0), c = (offset + i) / 8, i the row-major
+ *   element index; output word ((offset + i) mod 8) / 2, low half for even
+ *   and high half for odd offset + i.  `offset` lets row shards of one tensor
+ *   reproduce the unsharded stream; it must be a multiple of 16.
+ * Requires K > 0, K % 16 == 0, M >= 0.
+ */
+fq_status nvfp4_quantize(const void *x, int64_t M, int64_t K, const float *amax, int use_sr,
+                         uint64_t seed, uint64_t offset, uint8_t *q, uint8_t *sb, float *g,
+                         void *stream);
+
+/*
+ * NVFP4 with 16x16 2D block scaling of weights ([NVFP4] "Escalado de pesos
+ * 2D": one scale per 16x16 tile so that FPROP and the transposed DGRAD use
+ * the same scales).
+ *   w   : bf16 [N, K];  amax: float in device memory, max |w|
+ *   q   : uint8 [N, K/2] packed E2M1 codes (output)
+ *   sb  : uint8 [N/16, K/16] E4M3 tile scales (output)
+ *   g   : float in device memory (output)
+ * As nvfp4_quantize with round-to-nearest-even, amax_blk taken over the tile.
+ * Requires N % 16 == 0, K % 16 == 0, K > 0, N >= 0.
+ */
+fq_status nvfp4_quantize_2d(const void *w, int64_t N, int64_t K, const float *amax, uint8_t *q,
+                            uint8_t *sb, float *g, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FQ_H */

@@ -1,0 +1,323 @@
+"""GPU parity: every cast of libfq.so against the CPU oracle, byte for byte.
+
+All outputs are integer codes or exact powers of two (MXFP4, FP4->FP8), or
+IEEE binary32 results of the same operations in the same order (NVFP4), so
+the bar is bit-exact everywhere.  Inputs are seeded synthetic tensors with the
+shapes and distributions of the workloads; edge cases cover tails of every
+tiling, empty and tiny groups, misaligned group starts, signed zeros,
+subnormals, non-finite blocks and all exponent shifts.  Output buffers carry
+canary tails that must stay untouched."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_quantization_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+CANARY = 0xA5
+
+
+@pytest.fixture(scope="module")
+def fq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import fp8_quantization_gb300 as m
+    m.abi()
+    return m
+
+
+def dev_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def canary_out(shape, dtype, extra=64):
+    """Tensor of `shape` that is a view into a larger canary-filled buffer."""
+    n = int(np.prod(shape))
+    itemsize = torch.empty((), dtype=dtype).element_size()
+    raw = torch.full(((n * itemsize + extra + 15) // 16 * 16,), CANARY, dtype=torch.uint8,
+                     device="cuda")
+    return raw, raw[: n * itemsize].view(dtype).view(shape)
+
+
+def check_canary(raw, n_bytes):
+    tail = raw[n_bytes:].cpu().numpy()
+    assert np.all(tail == CANARY), "write past the end of an output"
+
+
+def eq(gpu, ref, what=""):
+    got = gpu.cpu().numpy()
+    ref = np.asarray(ref)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    a, b = got.view(np.uint8), np.ascontiguousarray(ref).view(np.uint8)
+    if not np.array_equal(a, b):
+        idx = np.flatnonzero(a.ravel() != b.ravel())
+        raise AssertionError(f"{what}: {idx.size} bytes differ, first at {idx[:8].tolist()}: "
+                             f"gpu {a.ravel()[idx[:8]].tolist()} oracle {b.ravel()[idx[:8]].tolist()}")
+
+
+# ------------------------------------------------------------------ MXFP4
+
+def mx_inputs():
+    rng = np.random.default_rng(21)
+    out = {"pr1": workloads.pr1(), "tail": workloads.pr1(3, 96, seed=2),
+           "one_row": workloads.pr1(1, 32, seed=3), "moe_small": workloads.moe_dispatch(97, 7168, 4)}
+    x = rng.standard_normal((64, 256)).astype(np.float32)
+    x[0, :32] = 0.0
+    x[0, 32:64] = -0.0
+    x[1, :32] = np.float32(2.0 ** -133) * rng.integers(0, 128, 32)
+    x[2, 5] = np.nan
+    x[3, 40] = np.inf
+    x[4, 70] = -np.inf
+    x[5, :32] = np.float32(3.3e38)
+    x[6, :] *= np.float32(2.0 ** -126)
+    out["special"] = workloads.bf16_bits(x)
+    return out
+
+
+def all_bf16_below_8_blocks():
+    """Every BF16 value of magnitude < 8 (and its negative), 31 per block,
+    each block led by 4.0 so that its scale is 1: the E2M1 conversion sees
+    every value it can be given."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = workloads.bits_to_float(bits)
+    keep = np.isfinite(vals) & (np.abs(vals) < 8)
+    bits = bits[keep]
+    nblk = (bits.size + 30) // 31
+    pad = np.zeros(nblk * 31, dtype=np.uint16)
+    pad[: bits.size] = bits
+    blocks = np.empty((nblk, 32), dtype=np.uint16)
+    blocks[:, 0] = 0x4080  # 4.0
+    blocks[:, 1:] = pad.reshape(nblk, 31)
+    nrow = (nblk + 7) // 8
+    full = np.zeros((nrow * 8, 32), dtype=np.uint16)
+    full[:nblk] = blocks
+    full[nblk:, 0] = 0x4080
+    return full.reshape(nrow, 256)
+
+
+@pytest.mark.parametrize("name", ["pr1", "tail", "one_row", "moe_small", "special", "all_bf16"])
+def test_mxfp4_quantize_rows(fq, name):
+    bits = all_bf16_below_8_blocks() if name == "all_bf16" else mx_inputs()[name]
+    M, K = bits.shape
+    qraw, q = canary_out((M, K // 2), torch.uint8)
+    sraw, s = canary_out((M, K // 32), torch.uint8)
+    fq.mxfp4_quantize_rows(dev_bf16(bits), q, s)
+    rq, rs = oracle.mxfp4_quantize_rows(bits)
+    eq(q, rq, "q")
+    eq(s, rs, "s")
+    check_canary(qraw, M * K // 2)
+    check_canary(sraw, M * K // 32)
+
+
+def rand_mx(M, K, seed, spread=40, base=100, nan_frac=0.0):
+    rng = np.random.default_rng(seed)
+    q = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    s = (base + rng.integers(0, spread, (M, K // 32))).astype(np.uint8)
+    if nan_frac:
+        s[rng.random(s.shape) < nan_frac] = 0xFF
+    return q, s
+
+
+@pytest.mark.parametrize("k", [0, 3, 6])
+@pytest.mark.parametrize("shape,spread", [((256, 512), 3), ((37, 384), 40), ((5, 128), 255),
+                                          ((300, 7168), 20)])
+def test_fp4_to_fp8_rows(fq, k, shape, spread):
+    M, K = shape
+    q, s = rand_mx(M, K, seed=M + K + k, spread=spread, base=0 if spread == 255 else 100,
+                   nan_frac=0.01)
+    yraw, y = canary_out((M, K), torch.uint8)
+    ysraw, ys = canary_out((M, K // 128), torch.float32)
+    fq.fp4_to_fp8_rows(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), k, y, ys)
+    ry, rys = oracle.fp4_to_fp8_rows(q, s, k)
+    eq(y, ry, "y")
+    eq(ys, rys, "ys")
+    check_canary(yraw, M * K)
+    check_canary(ysraw, M * K // 128 * 4)
+
+
+def test_fp4_to_fp8_rows_every_shift(fq):
+    # every code against every shift d = 0..254 (scale pairs (S, e)), k = 0..6
+    codes = np.arange(256, dtype=np.uint8)
+    rows = []
+    scales = []
+    for d in range(255):
+        rows.append(np.tile(codes, 1))              # 256 bytes = 512 codes = 4 FP8 blocks
+        s = np.full((16,), 254 - d, dtype=np.uint8)
+        s[0::4] = 254                               # first MX block of each FP8 block is the max
+        scales.append(s)
+    q = np.stack(rows)
+    s = np.stack(scales)
+    for k in range(7):
+        y, ys = fq.fp4_to_fp8_rows(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), k)
+        ry, rys = oracle.fp4_to_fp8_rows(q, s, k)
+        eq(y, ry, f"y k={k}")
+        eq(ys, rys, f"ys k={k}")
+
+
+# ------------------------------------------------------------------ FP4 -> FP8 cols
+
+def run_cols(fq, q, s, offs, k, check=True):
+    M, K = q.shape[0], q.shape[1] * 2
+    G = offs.size - 1
+    cap = oracle.fp4_to_fp8_cols_scale_capacity(M, G)
+    yraw, yT = canary_out((K, M), torch.uint8)
+    sraw = torch.full((K * cap * 4 + 64,), CANARY, dtype=torch.uint8, device="cuda")
+    yTs = sraw[: K * cap * 4].view(torch.float32).view(K, cap)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fq.fp4_to_fp8_cols(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(),
+                       torch.from_numpy(offs).cuda(), k, yT, yTs, st)
+    check_canary(yraw, K * M)
+    check_canary(sraw, K * cap * 4)
+    if check:
+        ryT, ryTs = oracle.fp4_to_fp8_cols(q, s, offs, k)
+        nb = int(((np.diff(offs) + 127) // 128).sum())
+        eq(yT, ryT, "yT")
+        eq(yTs[:, :nb].contiguous(), np.ascontiguousarray(ryTs[:, :nb]), "yT scales")
+        # slots past the last block are never written
+        tail = yTs[:, nb:].contiguous().view(torch.uint8).cpu().numpy()
+        assert np.all(tail == CANARY)
+        assert int(st.item()) == 0
+    return yT, yTs, int(st.item())
+
+
+COLS_CASES = {
+    "g1_aligned": (512, 256, lambda M: np.array([0, M])),
+    "g1_ragged_tail": (333, 128, lambda M: np.array([0, M])),
+    "tiny_groups": (300, 256, lambda M: np.array([0, 0, 1, 1, 128, 129, 256, 257, 299, 300])),
+    "sizes_127_128_129": (512, 128, lambda M: np.array([0, 127, 255, 384, 512])),
+    "random_empty": (1000, 384, lambda M: workloads.random_group_offsets(M, 23, seed=4)),
+    "zipf32": (4096, 256, lambda M: workloads.zipf_group_offsets(M, 32, 1.1, 3)),
+    "m_not_mult_4": (1001, 128, lambda M: workloads.random_group_offsets(M, 9, seed=5)),
+    "small_m": (3, 128, lambda M: np.array([0, 1, 3])),
+    "many_groups": (2000, 128, lambda M: workloads.random_group_offsets(M, 1024, seed=6)),
+    "one_token_groups": (200, 128, lambda M: np.arange(M + 1)),
+}
+
+
+@pytest.mark.parametrize("case", sorted(COLS_CASES))
+@pytest.mark.parametrize("k", [0, 6])
+def test_fp4_to_fp8_cols(fq, case, k):
+    M, K, mk = COLS_CASES[case]
+    offs = np.asarray(mk(M), dtype=np.int64)
+    q, s = rand_mx(M, K, seed=M * 7 + K + k, spread=16, nan_frac=0.002)
+    run_cols(fq, q, s, offs, k)
+
+
+def test_fp4_to_fp8_cols_malformed_offsets(fq):
+    # malformed offsets: clamped in-kernel, status raised, nothing written
+    # outside the outputs (canaries checked inside run_cols)
+    M, K = 700, 256
+    q, s = rand_mx(M, K, seed=1)
+    for offs in ([0, 800], [5, 300, 200, 700], [0, -40, 700], [0, 100, 699], [10, 20, 700]):
+        _, _, st = run_cols(fq, q, s, np.array(offs, dtype=np.int64), 0, check=False)
+        assert st == 1, offs
+
+
+# ------------------------------------------------------------------ NVFP4
+
+def test_nvfp4_amax(fq):
+    for shape, seed in (((64, 512), 1), ((3, 7), 2), ((1, 1), 3), ((1000, 1000), 4)):
+        bits = workloads.nvfp4_act(*shape, seed=seed)
+        a = fq.nvfp4_amax(dev_bf16(bits))
+        assert a.item() == float(oracle.nvfp4_amax(bits))
+    x = workloads.bits_to_float(workloads.nvfp4_act(33, 17, seed=5)).copy()
+    x[7, 3] = np.nan
+    assert np.isnan(fq.nvfp4_amax(dev_bf16(workloads.bf16_bits(x))).item())
+    x[7, 3] = -np.inf
+    assert fq.nvfp4_amax(dev_bf16(workloads.bf16_bits(x))).item() == np.inf
+    empty = torch.empty((0,), dtype=torch.bfloat16, device="cuda")
+    assert fq.nvfp4_amax(empty).item() == 0.0
+
+
+NV_CASES = {"act": (128, 512, workloads.nvfp4_act), "tail": (3, 48, workloads.nvfp4_act),
+            "k16": (40, 16, workloads.nvfp4_act), "wide": (9, 14336, workloads.nvfp4_act),
+            "weight": (64, 4096, workloads.nvfp4_weight)}
+
+
+@pytest.mark.parametrize("case", sorted(NV_CASES))
+@pytest.mark.parametrize("sr", [False, True])
+def test_nvfp4_quantize(fq, case, sr):
+    M, K, gen = NV_CASES[case]
+    bits = gen(M, K, seed=M + K)
+    x = dev_bf16(bits)
+    amax = fq.nvfp4_amax(x)
+    ramax = oracle.nvfp4_amax(bits)
+    qraw, q = canary_out((M, K // 2), torch.uint8)
+    sraw, sb = canary_out((M, K // 16), torch.uint8)
+    g = torch.empty(1, dtype=torch.float32, device="cuda")
+    for seed, offset in ((1234, 0), (2**63 + 77, 16 * 1001)):
+        fq.nvfp4_quantize(x, amax, use_sr=sr, seed=seed, offset=offset, q=q, sb=sb, g=g)
+        rq, rsb, rg = oracle.nvfp4_quantize(bits, ramax, use_sr=sr, seed=seed, offset=offset)
+        eq(q, rq, "q")
+        eq(sb, rsb, "sb")
+        assert g.item() == float(rg)
+        check_canary(qraw, M * K // 2)
+        check_canary(sraw, M * K // 16)
+
+
+def test_nvfp4_special_values(fq):
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((32, 64)).astype(np.float32)
+    x[0, :16] = 0.0
+    x[1, :16] = -0.0
+    x[2, :16] = np.float32(2.0 ** -130)
+    x[3, :] *= np.float32(1e-30)
+    bits = workloads.bf16_bits(x)
+    for A in (float(oracle.nvfp4_amax(bits)), 0.0, 1e-38, 3.0e38):
+        amax = torch.tensor([A], dtype=torch.float32, device="cuda")
+        for sr in (False, True):
+            q, sb, g = fq.nvfp4_quantize(dev_bf16(bits), amax, use_sr=sr, seed=9)
+            rq, rsb, rg = oracle.nvfp4_quantize(bits, np.float32(A), use_sr=sr, seed=9)
+            eq(q, rq, f"q A={A}")
+            eq(sb, rsb, f"sb A={A}")
+
+
+def test_nvfp4_block_scale_every_bf16_amax(fq):
+    # every positive finite BF16 value as a block maximum, under three
+    # per-tensor scales: drives the E4M3 block-scale conversion over its range
+    bits = np.arange(1, 0x7F80, dtype=np.uint32).astype(np.uint16)
+    bits = np.concatenate([bits, np.full((-bits.size) % 16, 0x3F80, dtype=np.uint16)])
+    nblk = bits.size
+    x = np.zeros((nblk, 16), dtype=np.uint16)
+    x[:, 0] = bits
+    x[:, 1:] = (bits[:, None] >> 1).astype(np.uint16)
+    x = x.reshape(-1, 256)
+    for A in (1.0, 3.0e38, 1.0e-20):
+        amax = torch.tensor([A], dtype=torch.float32, device="cuda")
+        q, sb, g = fq.nvfp4_quantize(dev_bf16(x), amax)
+        rq, rsb, rg = oracle.nvfp4_quantize(x, np.float32(A))
+        eq(sb, rsb, f"sb A={A}")
+        eq(q, rq, f"q A={A}")
+
+
+@pytest.mark.parametrize("shape", [(16, 16), (48, 272), (64, 4096), (32, 528)])
+def test_nvfp4_quantize_2d(fq, shape):
+    N, K = shape
+    bits = workloads.nvfp4_weight(N, K, seed=N + K)
+    w = dev_bf16(bits)
+    amax = fq.nvfp4_amax(w)
+    qraw, q = canary_out((N, K // 2), torch.uint8)
+    sraw, sb = canary_out((N // 16, K // 16), torch.uint8)
+    g = torch.empty(1, dtype=torch.float32, device="cuda")
+    fq.nvfp4_quantize_2d(w, amax, q, sb, g)
+    rq, rsb, rg = oracle.nvfp4_quantize_2d(bits, oracle.nvfp4_amax(bits))
+    eq(q, rq, "q")
+    eq(sb, rsb, "sb")
+    assert g.item() == float(rg)
+    check_canary(qraw, N * K // 2)
+    check_canary(sraw, N * K // 256)
+
+
+def test_errors_are_reported(fq):
+    x = torch.zeros((4, 33), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fq.FQError, match="FQ_ERR_SHAPE"):
+        fq.mxfp4_quantize_rows(x)
+    q = torch.zeros((4, 64), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((4, 4), dtype=torch.uint8, device="cuda")
+    with pytest.raises(fq.FQError, match="FQ_ERR_ARG"):
+        fq.fp4_to_fp8_rows(q, s, 7)
+    raw = torch.zeros(4 * 128 + 1, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fq.FQError, match="FQ_ERR_ALIGN"):
+        fq.fp4_to_fp8_rows(q, s, 0, y=raw[1:].view(4, 128))

@@ -115,8 +115,9 @@ def test_power_of_two_invariance(oracle_mod):
 
 
 def test_sr_probability_exact_over_all_random_values(oracle_mod):
-    # For fixed y, enumerate all 2^16 random values: the number that round up
-    # is floor(frac * 2^16) exactly, and the result is always lo or hi.
+    # For fixed y, enumerate all 2^16 random values R: the number that round
+    # up (F + R >= 2^16) is floor(frac * 2^16) exactly, and the result is
+    # always lo or hi.
     grid = [Fraction(0), Fraction(1, 2), Fraction(1), Fraction(3, 2), Fraction(2), Fraction(3),
             Fraction(4), Fraction(6)]
     rng = np.random.default_rng(12)
@@ -169,9 +170,15 @@ def test_sr_shards_match_whole(oracle_mod):
     np.testing.assert_array_equal(np.concatenate([p[1] for p in parts]), sb)
 
 
+def bitrev16(v):
+    return int(f"{int(v):016b}"[::-1], 2)
+
+
 def test_sr_stream_definition(oracle_mod):
-    # Element i draws 16 bits of Philox4x32-10(key=seed, counter=(i/8, 0, 0)):
-    # reproduce one block's decision from the Philox outputs directly.
+    # Element j = offset + i draws 16 bits from word (j/4) mod 4 of
+    # Philox4x32-10(key=seed, counter=(j/16, 0, 0)): with W that word,
+    # P = W[23:16]W[7:0], Q = W[31:24]W[15:8], and elements j mod 4 = 0..3
+    # use P, rev(P), Q, rev(Q).  Reproduce one block from the raw words.
     x = np.full((1, 16), 2.5, dtype=np.float32)
     x[0, 0] = 6.0
     bits = workloads.bf16_bits(x)
@@ -180,14 +187,34 @@ def test_sr_stream_definition(oracle_mod):
     q, sb, g = oracle_mod.nvfp4_quantize(bits, A, use_sr=True, seed=seed, offset=32)
     codes = oracle_mod.unpack_nibbles(q)[0]
     key = [seed & 0xFFFFFFFF, seed >> 32]
-    words = np.concatenate([oracle_mod.philox4x32_10([[c, 0, 0, 0]], [key])[0]
-                            for c in (4, 5)])           # elements 32..47 -> counters 4, 5
-    R = np.stack([words & 0xFFFF, words >> 16], axis=1).ravel()
+    words = oracle_mod.philox4x32_10([[2, 0, 0, 0]], [key])[0]   # elements 32..47 -> counter 2
+    R = []
+    for W in words:
+        W = int(W)
+        P = (((W >> 16) & 0xFF) << 8) | (W & 0xFF)
+        Q = (((W >> 24) & 0xFF) << 8) | ((W >> 8) & 0xFF)
+        R += [P, bitrev16(P), Q, bitrev16(Q)]
     r = np.float32(1.0) / (np.float32(448.0) * np.float32(g))   # b = 448 here
     y = np.float32(2.5) * r
     assert sb[0, 0] == 0x7E
-    want = oracle_mod.e2m1_sr(np.full(16, float(y)), R)
+    want = oracle_mod.e2m1_sr(np.full(16, float(y)), np.array(R, dtype=np.uint32))
     np.testing.assert_array_equal(codes[1:], want[1:])
+    # y = 2.5 * 6 / 6 sits between 2 and 3 with frac ~ 1/2: both outcomes occur
+    assert set(codes[1:].tolist()) <= {4, 5}
+
+
+def test_sr_random_numbers_are_uniform(oracle_mod):
+    # Each element's 16-bit number is uniform: over many blocks the up-rate of
+    # a value with frac = 1/2 is 1/2 for every position in the block.
+    x = np.full((4096, 16), 1.25, dtype=np.float32)   # frac 1/2 between 1 and 1.5
+    x[:, 0] = 6.0
+    bits = workloads.bf16_bits(x)
+    A = oracle_mod.nvfp4_amax(bits)
+    q, sb, g = oracle_mod.nvfp4_quantize(bits, A, use_sr=True, seed=99)
+    assert np.all(sb == 0x7E)
+    codes = oracle_mod.unpack_nibbles(q)[:, 1:]
+    up = (codes == 3).mean(axis=0)
+    assert np.all(np.abs(up - 0.5) < 4 * 0.5 / np.sqrt(4096)), up
 
 
 def test_2d_transpose_relation(oracle_mod):

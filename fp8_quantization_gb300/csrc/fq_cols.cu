@@ -8,41 +8,43 @@
 // layout to avoid bank conflicts, and ragged expert groups are handled
 // without padding.  Scale alignment as in the row conversion (item 1).
 //
-// Design (GB300): persistent CTAs walk output tiles of 128 features x 128
-// tokens.  Tiles are aligned to 128 tokens of the OUTPUT (so every output row
-// segment is a full, aligned 128-byte line), not to the groups: a tile may
-// cut through several 128-token blocks of several groups, whose scale maxima
-// are reduced from a staged window of scale words.  The next tile's codes and
-// scale words are prefetched into registers while the current tile is
-// written out.
-#include <cstddef>
-
+// Two launches on the caller's stream:
+//  1. fp4_to_fp8_cols_scales_kernel -- one CTA per 128-token block (blocks
+//     start at each group's first token): the byte-wise max of the block's
+//     UE8M0 exponents for every MX column, written out as the FP32 block
+//     scales (an output of the operation).
+//  2. fp4_to_fp8_cols_kernel -- persistent CTAs walk output tiles of
+//     128 features x 128 tokens aligned to the OUTPUT, so every output row
+//     segment is a full, aligned 128-byte line; each token reads its block's
+//     aligned exponent back from the scale written by launch 1.  Codes are
+//     converted through a shared-memory tile (double buffered, one barrier
+//     per tile) and transposed with byte permutes; the next tile's inputs
+//     are prefetched into registers while the current one is converted.
 #include "fq_common.cuh"
 
 namespace fq {
 
-constexpr int kTok = 128;                // tokens per tile (output columns)
-constexpr int kQuadWords = 132;          // 128 words + 4 pad per 4-token group
-constexpr int kStage = 384;              // scale words staged: tokens [W-128, W+256)
+constexpr int kTok = 128;  // tokens per block / per tile
+// FP8 tile: 32 token-quads x 32 feature-words; the 16-byte slot holding
+// (four tokens) x (one feature word) is slot_index(quad, m).  Skew: odd quad
+// stride 45, +quad/4, +2*(m/8) -- conflict-free both for the conversion
+// stores (2 quads x 4 column blocks x 4 tokens per warp) and for the 128-bit
+// transposed reads (8 quads 4 apart per quarter warp).
+constexpr int kQuadStride = 45;
+constexpr int kTileSlots = (kTok / 4) * kQuadStride;
+constexpr int kTileWords = kTileSlots * 4;
 
-struct __align__(16) ColsTileSmem {
-    __align__(16) uint32_t tile[(kTok / 4) * kQuadWords];  // FP8 bytes, [token/4][kword][token%4]
-    uint32_t sw[kStage];                     // scale words (4 MX columns) of staged tokens
-    uint32_t smax[kTok];                     // per block: byte j = max exponent of column j
-    int32_t rel[kTok];                       // window token -> block index within the tile
-    int32_t bstart[kTok], bend[kTok], bslot[kTok];
-    int32_t nblocks;
-    __align__(16) uint8_t tab[kShiftRows * 8];
-};
-static_assert(offsetof(ColsTileSmem, tile) % 16 == 0, "tile is read with 128-bit loads");
-static_assert(offsetof(ColsTileSmem, tab) % 16 == 0, "table rows are read with 64-bit loads");
+__device__ __forceinline__ int slot_index(int quad, int m)
+{
+    return quad * kQuadStride + (quad >> 2) + m + 2 * (m >> 3);
+}
 
-// Largest g in [lo, hi] with off[g] <= t (off non-decreasing, off[lo] <= t).
-__device__ __forceinline__ int find_group(const int32_t *off, int lo, int hi, int32_t t)
+// Largest g in [lo, hi] with a[g] <= t (a non-decreasing, a[lo] <= t).
+__device__ __forceinline__ int find_last_le(const int32_t *a, int lo, int hi, int32_t t)
 {
     while (lo < hi) {
         int mid = (lo + hi + 1) >> 1;
-        if (off[mid] <= t)
+        if (a[mid] <= t)
             lo = mid;
         else
             hi = mid - 1;
@@ -50,8 +52,27 @@ __device__ __forceinline__ int find_group(const int32_t *off, int lo, int hi, in
     return lo;
 }
 
+// Same search for a warp-uniform t: with n <= 64 one or two ballots over the
+// array replace the binary search.
+__device__ __forceinline__ int warp_find_last_le(const int32_t *a, int n, int32_t t)
+{
+    if (n > 64)
+        return find_last_le(a, 0, n - 1, t);
+    const int lane = threadIdx.x & 31;
+    int g = 0;
+    for (int b0 = 0; b0 < n; b0 += 32) {
+        const int i = b0 + lane;
+        const unsigned m = __ballot_sync(0xffffffffu, i < n && a[i] <= t);
+        if (m)
+            g = b0 + 31 - __clz(m);
+        if (m != 0xffffffffu)
+            break;
+    }
+    return g;
+}
+
 // In-place inclusive scan (max or sum) of a[0..n) in shared memory by the
-// whole CTA; n <= 4 * 1024 + 1 is enough here.
+// whole CTA.
 template <bool kMax>
 __device__ void cta_scan(int32_t *a, int n, int32_t *warp_tot /* [kThreads/32] */)
 {
@@ -83,6 +104,37 @@ __device__ void cta_scan(int32_t *a, int n, int32_t *warp_tot /* [kThreads/32] *
     __syncthreads();
 }
 
+// Group structure of the offsets, in shared memory (once per CTA): off[0..G]
+// clamped into [0, M], non-decreasing, off[0] = 0, off[G] = M; base[g] = the
+// first scale slot of group g (number of 128-token blocks of the groups
+// before it), base[G] = total blocks.  Returns nonzero if the offsets given
+// were malformed.
+__device__ int load_groups(const int64_t *__restrict__ offs, int32_t G, int32_t M, int32_t *off,
+                           int32_t *base, int32_t *warp_tot)
+{
+    const int tid = threadIdx.x;
+    int bad = 0;
+    for (int i = tid; i <= G; i += kThreads) {
+        const int64_t o = offs[i];
+        const int64_t c = o < 0 ? 0 : (o > M ? M : o);
+        off[i] = static_cast<int32_t>(c);
+        if (c != o || (i == 0 && o != 0) || (i == G && o != M) || (i > 0 && o < offs[i - 1]))
+            bad = 1;
+    }
+    bad = __syncthreads_or(bad);
+    cta_scan<true>(off, G + 1, warp_tot);
+    if (tid == 0) {
+        off[0] = 0;
+        off[G] = M;
+    }
+    __syncthreads();
+    for (int g = tid; g <= G; g += kThreads)
+        base[g] = g == 0 ? 0 : (off[g] - off[g - 1] + kTok - 1) / kTok;
+    __syncthreads();
+    cta_scan<false>(base, G + 1, warp_tot);
+    return bad;
+}
+
 // 4x4 byte transpose: in = four words (rows), out[r] = byte r of each word.
 __device__ __forceinline__ void transpose4x4(uint4 v, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                              uint32_t &r3)
@@ -95,195 +147,229 @@ __device__ __forceinline__ void transpose4x4(uint4 v, uint32_t &r0, uint32_t &r1
     r3 = prmt(ab_hi, cd_hi, 0x7632u);
 }
 
-template <bool kAligned4>
+__device__ __forceinline__ uint32_t bytemax4(uint32_t a, uint32_t b)
+{
+    const uint32_t e02 = max_u16x2(a & 0x00FF00FFu, b & 0x00FF00FFu);
+    const uint32_t e13 = max_u16x2((a >> 8) & 0x00FF00FFu, (b >> 8) & 0x00FF00FFu);
+    return e02 | (e13 << 8);
+}
+
+// ---------------------------------------------------------------- launch 1: block scales
+
+// CTA per 128-token block (slot).  Threads split (token subset, 4-column
+// word): the exponent words of a token row are read coalesced, reduced
+// byte-wise across the token subsets in shared memory, and every feature
+// row's scale of the block is written.
+__global__ void __launch_bounds__(kThreads) fp4_to_fp8_cols_scales_kernel(
+    const uint8_t *__restrict__ s, int32_t M, int64_t K, const int64_t *__restrict__ offs,
+    int32_t G, int k, float *__restrict__ yTs, int64_t cap, int32_t *__restrict__ dev_status)
+{
+    __shared__ int32_t warp_tot[kThreads / 32];
+    __shared__ uint32_t red[kThreads];
+    extern __shared__ int32_t dyn[];
+    int32_t *off = dyn, *base = dyn + G + 1;
+    const int tid = threadIdx.x;
+    const int bad = load_groups(offs, G, M, off, base, warp_tot);
+    if (bad && blockIdx.x == 0 && tid == 0 && dev_status)
+        atomicOr(dev_status, 1);
+
+    const int32_t nblocks = base[G];
+    const int32_t J4 = static_cast<int32_t>(K / 128);  // exponent words per token row
+    const uint32_t *s32 = reinterpret_cast<const uint32_t *>(s);
+    uint32_t *out = reinterpret_cast<uint32_t *>(yTs);
+    for (int32_t slot = blockIdx.x; slot < nblocks; slot += gridDim.x) {
+        const int g = find_last_le(base, 0, G - 1, slot);
+        const int32_t bs = off[g] + (slot - base[g]) * kTok;
+        const int32_t be = min(bs + kTok, off[g + 1]);
+        for (int32_t j0 = 0; j0 < J4; j0 += kThreads) {
+            const int jn = min(kThreads, J4 - j0);
+            const int parts = kThreads / jn;
+            const int jj = tid % jn, part = tid / jn;
+            uint32_t m = 0;
+            if (part < parts) {
+                // 16 independent loads in flight per round
+                const uint32_t *src = s32 + static_cast<int64_t>(bs) * J4 + j0 + jj;
+                for (int32_t t0 = part; t0 < be - bs; t0 += 16 * parts) {
+                    uint32_t v[16];
+#pragma unroll
+                    for (int i = 0; i < 16; i++) {
+                        const int32_t t = t0 + i * parts;
+                        v[i] = t < be - bs ? __ldg(src + static_cast<int64_t>(t) * J4) : 0u;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; i++)
+                        m = bytemax4(m, v[i]);
+                }
+            }
+            red[tid] = m;
+            __syncthreads();
+            if (tid < jn)
+                for (int p = 1; p < parts; p++)
+                    m = bytemax4(m, red[tid + p * jn]);
+            __syncthreads();
+            if (tid < jn)
+                red[tid] = m;
+            __syncthreads();
+            // 4 MX columns x 32 feature rows per exponent word
+            for (int idx = tid; idx < 128 * jn; idx += kThreads) {
+                const int w = idx >> 7;
+                const uint32_t S = (red[w] >> (8 * ((idx >> 5) & 3))) & 0xFFu;
+                const int64_t row = static_cast<int64_t>(j0 + w) * 128 + (idx & 127);
+                out[row * cap + slot] = fp8_block_scale_bits(S, k);
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// ---------------------------------------------------------------- launch 2: convert + transpose
+
+// Tile (W, f): tokens W..W+127 (W a multiple of 128) x features
+// 128f..128f+127.  Thread t converts units (token t/4, column block t%4) and
+// (token t/4 + 64, column block t%4): each warp load covers eight token rows
+// x 64 contiguous bytes.  For the write-out, warp w handles feature words
+// 4w..4w+3 (lane/8 picks the word) and lane%8 picks 16 tokens: each 16-byte
+// store of a quarter warp fills one 128-byte output line.
+template <bool kAligned16>
 __global__ void __launch_bounds__(kThreads, 4) fp4_to_fp8_cols_kernel(
     const uint8_t *__restrict__ q, const uint8_t *__restrict__ s, int32_t M, int64_t K,
     const int64_t *__restrict__ offs, int32_t G, int k, uint8_t *__restrict__ yT,
-    float *__restrict__ yTs, int64_t cap, int32_t *__restrict__ dev_status)
+    const float *__restrict__ yTs, int64_t cap)
 {
-    __shared__ ColsTileSmem sm;
+    __shared__ __align__(16) uint8_t tab[kTabRows * 8];
     __shared__ int32_t warp_tot[kThreads / 32];
-    extern __shared__ int32_t dyn[];
-    int32_t *off = dyn;           // [G+1] clamped, monotone group offsets
-    int32_t *base = dyn + G + 1;  // [G+1] first scale slot of each group
+    extern __shared__ __align__(16) uint32_t dyn_words[];
+    uint32_t *tiles = dyn_words;  // [2][kTileWords]
+    int32_t *off = reinterpret_cast<int32_t *>(dyn_words + 2 * kTileWords);
+    int32_t *base = off + G + 1;
 
-    const int tid = threadIdx.x;
-    build_fp8_table(sm.tab);
-
-    // ---- group structure (once per CTA): clamp, make monotone, count blocks
-    int bad = 0;
-    for (int i = tid; i <= G; i += kThreads) {
-        const int64_t o = offs[i];
-        const int64_t c = o < 0 ? 0 : (o > M ? M : o);
-        off[i] = static_cast<int32_t>(c);
-        if (c != o || (i == 0 && o != 0) || (i == G && o != M) || (i > 0 && o < offs[i - 1]))
-            bad = 1;
-    }
-    bad = __syncthreads_or(bad);
-    if (bad && blockIdx.x == 0 && tid == 0 && dev_status)
-        atomicOr(dev_status, 1);
-    cta_scan<true>(off, G + 1, warp_tot);
-    if (tid == 0) {
-        off[0] = 0;
-        off[G] = M;
-    }
-    __syncthreads();
-    for (int g = tid; g <= G; g += kThreads)
-        base[g] = g == 0 ? 0 : (off[g] - off[g - 1] + kTok - 1) / kTok;
-    __syncthreads();
-    cta_scan<false>(base, G + 1, warp_tot);  // base[g] = blocks of groups < g
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    build_fp8_table(tab);
+    load_groups(offs, G, M, off, base, warp_tot);
 
     const int32_t nwin = (M + kTok - 1) / kTok;
     const int32_t nfeat = static_cast<int32_t>(K / 128);
-    const int64_t ntiles = static_cast<int64_t>(nwin) * nfeat;
+    const int32_t ntiles = nwin * nfeat;  // < 2^31, checked on the host
     const int64_t qrow = K / 2, srow = K / 32;
+    const int j = tid & 3;     // column block of both units
+    const int tl0 = tid >> 2;  // token of unit 0 (unit 1: tl0 + 64)
+    const uint32_t *ys32 = reinterpret_cast<const uint32_t *>(yTs);
 
-    // prefetch: unit u = tid + 256*r (r = 0, 1): token tl = u & 127, column
-    // block j = u >> 7 -> 16 bytes of q; staged scale words tokens W-128+tid
-    // and W+128+tid.
-    uint4 qv[2];
-    uint32_t sv[2];
-    auto prefetch = [&](int64_t tau) {
-        const int32_t win = static_cast<int32_t>(tau % nwin);
-        const int32_t f = static_cast<int32_t>(tau / nwin);
+    // tiles are (window, feature chunk) with the window index fastest; a CTA
+    // advances by gridDim.x tiles (32-bit, incremental: no division per tile)
+    const int32_t step_w = static_cast<int32_t>(gridDim.x) % nwin;
+    const int32_t step_f = static_cast<int32_t>(gridDim.x) / nwin;
+
+    // per unit: 16 bytes of codes, the token's exponent word (4 columns) and
+    // the FP32 scale of its block (column j), which encodes the block's S
+    auto prefetch = [&](int32_t win, int32_t f, uint4(&qv)[2], uint32_t(&ev)[2],
+                        uint32_t(&sv)[2]) {
         const int32_t W = win * kTok;
+        const int g0 = warp_find_last_le(off, G, W);
+        const int32_t end0 = off[g0 + 1];
+        const uint8_t *qrow0 = q + static_cast<int64_t>(W + tl0) * qrow + f * 64 + 16 * j;
+        const uint8_t *srow0 = s + static_cast<int64_t>(W + tl0) * srow + 4 * f;
+        const uint32_t *yscol = ys32 + (static_cast<int64_t>(f) * 128 + 32 * j) * cap;
 #pragma unroll
         for (int r = 0; r < 2; r++) {
-            const int u = tid + kThreads * r;
-            const int32_t t = W + (u & 127);
-            qv[r] = t < M ? ld_nc_v4(q + t * qrow + f * 64 + 16 * (u >> 7)) : make_uint4(0, 0, 0, 0);
-            const int32_t ts = W - 128 + tid + 256 * r;
-            sv[r] = (r == 0 || tid < 128) && ts >= 0 && ts < M
-                        ? __ldg(reinterpret_cast<const uint32_t *>(s + ts * srow + 4 * f))
-                        : 0u;
+            const int32_t t = W + tl0 + 64 * r;
+            if (t < M) {
+                qv[r] = ld_nc_v4(qrow0 + r * 64 * qrow);
+                ev[r] = __ldg(reinterpret_cast<const uint32_t *>(srow0 + r * 64 * srow));
+                const int g = t < end0 ? g0 : find_last_le(off, g0, G - 1, t);
+                const int32_t slot = base[g] + static_cast<int32_t>(static_cast<uint32_t>(t - off[g]) >> 7);
+                sv[r] = yscol[slot];
+            } else {
+                qv[r] = make_uint4(0, 0, 0, 0);
+                ev[r] = 0;
+                sv[r] = 0;
+            }
         }
     };
 
-    int64_t tau = blockIdx.x;
+    uint4 qv[2], qn[2];
+    uint32_t ev[2], en[2], sv[2], sn[2];
+    int32_t tau = blockIdx.x;
+    int32_t win = tau % nwin, f = tau / nwin;
     if (tau < ntiles)
-        prefetch(tau);
+        prefetch(win, f, qv, ev, sv);
+    int buf = 0;
     for (; tau < ntiles; tau += gridDim.x) {
-        const int32_t win = static_cast<int32_t>(tau % nwin);
-        const int32_t f = static_cast<int32_t>(tau / nwin);
         const int32_t W = win * kTok;
         const int32_t We = min(W + kTok, M);
-
-        // ---- stage scale words; find the groups at both ends of the window
-        sm.sw[tid] = sv[0];
-        if (tid < 128)
-            sm.sw[256 + tid] = sv[1];
-        const int g_first = find_group(off, 0, G - 1, W);
-        const int g_last = find_group(off, g_first, G - 1, We - 1);
-        const int32_t slot_lo = base[g_first] + (W - off[g_first]) / kTok;
-        __syncthreads();
-
-        // ---- every window token: its block; blocks starting here (or at W)
-        if (tid < kTok) {
-            const int32_t t = W + tid;
-            if (t < We) {
-                const int g = g_first == g_last ? g_first : find_group(off, g_first, g_last, t);
-                const int32_t bl = (t - off[g]) / kTok;
-                const int32_t r = base[g] + bl - slot_lo;
-                sm.rel[tid] = r;
-                const int32_t start = off[g] + bl * kTok;
-                if (t == W || t == start) {
-                    sm.bstart[r] = start;
-                    sm.bend[r] = min(start + kTok, off[g + 1]);
-                    sm.bslot[r] = base[g] + bl;
-                }
-                if (t == We - 1)
-                    sm.nblocks = r + 1;
-            }
+        int32_t win_n = win + step_w, f_n = f + step_f;
+        if (win_n >= nwin) {
+            win_n -= nwin;
+            f_n++;
         }
-        __syncthreads();
+        const bool more = tau + static_cast<int32_t>(gridDim.x) < ntiles;
+        if (more)
+            prefetch(win_n, f_n, qn, en, sn);
 
-        // ---- per block: byte-wise max of the staged scale words (warp per block)
-        {
-            const int lane = tid & 31, wid = tid >> 5;
-            const int nb = sm.nblocks;
-            for (int r = wid; r < nb; r += kThreads / 32) {
-                const int32_t a = sm.bstart[r], b = sm.bend[r];
-                uint32_t even = 0, odd = 0;  // bytes 0,2 and 1,3 as u16 pairs
-                for (int32_t t = a + lane; t < b; t += 32) {
-                    const uint32_t w = sm.sw[t - (W - 128)];
-                    even = max_u16x2(even, w & 0x00FF00FFu);
-                    odd = max_u16x2(odd, (w >> 8) & 0x00FF00FFu);
-                }
+        // ---- convert this thread's two units into the shared FP8 tile
+        uint32_t *tile = tiles + buf * kTileWords;
 #pragma unroll
-                for (int d = 16; d > 0; d >>= 1) {
-                    even = max_u16x2(even, __shfl_xor_sync(0xffffffffu, even, d));
-                    odd = max_u16x2(odd, __shfl_xor_sync(0xffffffffu, odd, d));
-                }
-                if (lane == 0)
-                    sm.smax[r] = even | (odd << 8);
-            }
-        }
-        __syncthreads();
-
-        // ---- convert the prefetched codes into the shared FP8 tile
-#pragma unroll
-        for (int rr = 0; rr < 2; rr++) {
-            const int u = tid + kThreads * rr;
-            const int tl = u & 127, j = u >> 7;
+        for (int r = 0; r < 2; r++) {
+            const int tl = tl0 + 64 * r;
             if (W + tl < We) {
-                const uint32_t Sw = sm.smax[sm.rel[tl]];
-                const uint32_t S = (Sw >> (8 * j)) & 0xFFu;
-                const uint32_t e = (sm.sw[tl + 128] >> (8 * j)) & 0xFFu;
-                int uu = static_cast<int>(S - e) - k + 6;
-                uu = uu < kShiftRows - 1 ? uu : kShiftRows - 1;
-                const uint2 t = *reinterpret_cast<const uint2 *>(sm.tab + 8 * uu);
+                const uint32_t S = fp8_block_scale_exponent(sv[r], k);
+                const uint32_t e = (ev[r] >> (8 * j)) & 0xFFu;
+                int u = static_cast<int>(S - e) - k + 6;
+                u = u < kShiftRows - 1 ? u : kShiftRows - 1;
+                const bool nan = S == 0xFFu;
+                const uint2 t = *reinterpret_cast<const uint2 *>(tab + 8 * (nan ? kNanRow : u));
+                const uint32_t smask = nan ? 0u : 0x80808080u;
                 uint32_t o[8];
-                fp4x8_to_fp8x8(qv[rr].x, t.x, t.y, o[0], o[1]);
-                fp4x8_to_fp8x8(qv[rr].y, t.x, t.y, o[2], o[3]);
-                fp4x8_to_fp8x8(qv[rr].z, t.x, t.y, o[4], o[5]);
-                fp4x8_to_fp8x8(qv[rr].w, t.x, t.y, o[6], o[7]);
-                uint32_t *dst = sm.tile + (tl >> 2) * kQuadWords + 32 * j + (tl & 3);
+                fp4x8_to_fp8x8(qv[r].x, t.x, t.y, o[0], o[1], smask);
+                fp4x8_to_fp8x8(qv[r].y, t.x, t.y, o[2], o[3], smask);
+                fp4x8_to_fp8x8(qv[r].z, t.x, t.y, o[4], o[5], smask);
+                fp4x8_to_fp8x8(qv[r].w, t.x, t.y, o[6], o[7], smask);
+                const int quad = tl >> 2, sub = tl & 3;
 #pragma unroll
                 for (int w = 0; w < 8; w++)
-                    dst[4 * w] = S == 0xFFu ? 0x7F7F7F7Fu : o[w];
+                    tile[4 * slot_index(quad, 8 * j + w) + sub] = o[w];
             }
         }
         __syncthreads();
 
-        // ---- prefetch the next tile, then write this one out
-        if (tau + gridDim.x < ntiles)
-            prefetch(tau + gridDim.x);
+        // ---- transpose 4x4 byte blocks; 16 tokens of 4 feature rows per thread
         {
-            const int lane = tid & 31, wid = tid >> 5;
-            const int32_t t0 = W + 4 * lane;
+            const int m = 4 * wid + (lane >> 3);  // word of 4 features
+            const int c = lane & 7;               // tokens 16c .. 16c+15
+            uint32_t rows[4][4];
 #pragma unroll
-            for (int i = 0; i < 4; i++) {
-                const int m = wid + 8 * i;  // word of 4 features
-                const uint4 v = *reinterpret_cast<const uint4 *>(sm.tile + lane * kQuadWords + 4 * m);
-                uint32_t r[4];
-                transpose4x4(v, r[0], r[1], r[2], r[3]);
+            for (int qq = 0; qq < 4; qq++) {
+                const uint4 v =
+                    *reinterpret_cast<const uint4 *>(tile + 4 * slot_index(4 * c + qq, m));
+                transpose4x4(v, rows[0][qq], rows[1][qq], rows[2][qq], rows[3][qq]);
+            }
+            const int32_t t0 = W + 16 * c;
+            uint8_t *dst = yT + (static_cast<int64_t>(f) * 128 + 4 * m) * M + t0;
 #pragma unroll
-                for (int rr = 0; rr < 4; rr++) {
-                    uint8_t *dst = yT + (static_cast<int64_t>(f) * 128 + 4 * m + rr) * M + t0;
-                    if (kAligned4 && t0 + 3 < We) {
-                        *reinterpret_cast<uint32_t *>(dst) = r[rr];
-                    } else {
+            for (int rr = 0; rr < 4; rr++) {
+                uint8_t *p = dst + static_cast<int64_t>(rr) * M;
+                if (kAligned16 && t0 + 16 <= We) {
+                    *reinterpret_cast<uint4 *>(p) =
+                        make_uint4(rows[rr][0], rows[rr][1], rows[rr][2], rows[rr][3]);
+                } else {
 #pragma unroll
-                        for (int b = 0; b < 4; b++)
-                            if (t0 + b < We)
-                                dst[b] = static_cast<uint8_t>(r[rr] >> (8 * b));
-                    }
+                    for (int b = 0; b < 16; b++)
+                        if (t0 + b < We)
+                            p[b] = static_cast<uint8_t>(rows[rr][b >> 2] >> (8 * (b & 3)));
                 }
             }
         }
-        // ---- scales of the blocks that start inside this window
-        {
-            const int nb = sm.nblocks;
-            for (int idx = tid; idx < nb * 128; idx += kThreads) {
-                const int r = idx >> 7, kf = idx & 127;
-                if (sm.bstart[r] >= W) {
-                    const uint32_t S = (sm.smax[r] >> (8 * (kf >> 5))) & 0xFFu;
-                    reinterpret_cast<uint32_t *>(yTs)[(static_cast<int64_t>(f) * 128 + kf) * cap +
-                                                      sm.bslot[r]] = fp8_block_scale_bits(S, k);
-                }
-            }
+        if (more) {
+            qv[0] = qn[0];
+            qv[1] = qn[1];
+            ev[0] = en[0];
+            ev[1] = en[1];
+            sv[0] = sn[0];
+            sv[1] = sn[1];
         }
-        __syncthreads();
+        win = win_n;
+        f = f_n;
+        buf ^= 1;
     }
 }
 
@@ -307,6 +393,8 @@ extern "C" fq_status fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
         return FQ_ERR_SHAPE;
     if (M > 0 && K > INT64_MAX / M)
         return FQ_ERR_SHAPE;
+    if (((M + 127) / 128) * (K / 128) > INT32_MAX - 4096)  // tile index is 32-bit
+        return FQ_ERR_SHAPE;
     if (G < 1 || G > FQ_COLS_MAX_GROUPS || exp_offset_k < 0 || exp_offset_k > 6)
         return FQ_ERR_ARG;
     if (cap < fp4_to_fp8_cols_scale_capacity(M, G))
@@ -318,19 +406,36 @@ extern "C" fq_status fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
     if (!aligned16(q) || !aligned16(s) || !aligned16(group_offsets) || !aligned16(yT) ||
         !aligned16(yT_scale))
         return FQ_ERR_ALIGN;
-    const size_t dyn = static_cast<size_t>(G + 1) * 2 * sizeof(int32_t);
-    const int64_t ntiles = ((M + 127) / 128) * (K / 128);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (M % 4 == 0) {
+    const size_t groups_bytes = static_cast<size_t>(G + 1) * 2 * sizeof(int32_t);
+
+    // launch 1: block scales (one CTA per block, at most cap blocks)
+    const int grid1 = persistent_grid(fp4_to_fp8_cols_scales_kernel, kThreads, groups_bytes, cap);
+    fp4_to_fp8_cols_scales_kernel<<<grid1, kThreads, groups_bytes, st>>>(
+        s, static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT_scale, cap, dev_status);
+    fq_status rc = launch_status();
+    if (rc != FQ_OK)
+        return rc;
+
+    // launch 2: convert + transpose (two FP8 tiles + the group arrays)
+    const size_t dyn = 2 * kTileWords * sizeof(uint32_t) + groups_bytes;
+    const int64_t ntiles = ((M + 127) / 128) * (K / 128);
+    if (M % 16 == 0) {
+        if (cudaFuncSetAttribute(fp4_to_fp8_cols_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(dyn)) != cudaSuccess)
+            return launch_status();
         const int grid = persistent_grid(fp4_to_fp8_cols_kernel<true>, kThreads, dyn, ntiles);
         fp4_to_fp8_cols_kernel<true><<<grid, kThreads, dyn, st>>>(
-            q, s, static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT, yT_scale, cap,
-            dev_status);
+            q, s, static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT, yT_scale, cap);
     } else {
+        if (cudaFuncSetAttribute(fp4_to_fp8_cols_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(dyn)) != cudaSuccess)
+            return launch_status();
         const int grid = persistent_grid(fp4_to_fp8_cols_kernel<false>, kThreads, dyn, ntiles);
         fp4_to_fp8_cols_kernel<false><<<grid, kThreads, dyn, st>>>(
-            q, s, static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT, yT_scale, cap,
-            dev_status);
+            q, s, static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT, yT_scale, cap);
     }
     return launch_status();
 }

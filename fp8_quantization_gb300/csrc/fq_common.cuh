@@ -127,9 +127,11 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 
 // Eight E2M1 codes (one word, code i in bits 4i..4i+3) -> eight E4M3 bytes
 // through an 8-entry magnitude table {t1:t0}; the sign of each code becomes
-// bit 7 of its byte.
+// bit 7 of its byte where `sign_mask` is 0x80808080 (0 keeps the table bytes
+// as they are, e.g. the all-NaN row).
 __device__ __forceinline__ void fp4x8_to_fp8x8(uint32_t w, uint32_t t0, uint32_t t1,
-                                               uint32_t &lo, uint32_t &hi)
+                                               uint32_t &lo, uint32_t &hi,
+                                               uint32_t sign_mask = 0x80808080u)
 {
     const uint32_t sel = w & 0x77777777u;
     const uint32_t w4 = w << 4;
@@ -137,8 +139,8 @@ __device__ __forceinline__ void fp4x8_to_fp8x8(uint32_t w, uint32_t t0, uint32_t
     const uint32_t mhi = prmt(t0, t1, sel >> 16);
     const uint32_t slo = prmt(w4, w, 0xD9C8u);  // msb of codes 0..3 replicated
     const uint32_t shi = prmt(w4, w, 0xFBEAu);  // msb of codes 4..7 replicated
-    lo = mlo | (slo & 0x80808080u);
-    hi = mhi | (shi & 0x80808080u);
+    lo = mlo | (slo & sign_mask);
+    hi = mhi | (shi & sign_mask);
 }
 
 // FP32 bits of the FP8 block scale 2^(S - 127 - k); NaN for S = 0xFF.
@@ -153,12 +155,19 @@ __device__ __forceinline__ uint32_t fp8_block_scale_bits(uint32_t S, int k)
 }
 
 // Table of E4M3 bytes for E2M1 magnitude code c (0..7) shifted by 2^(6-u),
-// u = 0..19 (u = 19 covers every larger shift: all values flush to zero).
+// u = 0..19 (u = 19 covers every larger shift: all values flush to zero),
+// plus row kNanRow of 0x7F (the E4M3 NaN) for blocks whose scale is NaN.
 constexpr int kShiftRows = 20;
-__device__ __forceinline__ void build_fp8_table(uint8_t *tab /* [kShiftRows * 8] */)
+constexpr int kNanRow = kShiftRows;
+constexpr int kTabRows = kShiftRows + 1;
+__device__ __forceinline__ void build_fp8_table(uint8_t *tab /* [kTabRows * 8] */)
 {
-    for (int i = threadIdx.x; i < kShiftRows * 8; i += blockDim.x) {
+    for (int i = threadIdx.x; i < kTabRows * 8; i += blockDim.x) {
         int u = i >> 3, c = i & 7;
+        if (u == kNanRow) {
+            tab[i] = 0x7F;
+            continue;
+        }
         // E2M1 magnitude of c times 2^(6 - u), built exactly from bits
         float v;
         if (c == 0)
@@ -170,6 +179,16 @@ __device__ __forceinline__ void build_fp8_table(uint8_t *tab /* [kShiftRows * 8]
         v *= __uint_as_float(static_cast<uint32_t>(127 + 6 - u) << 23);
         tab[i] = static_cast<uint8_t>(cvt_e4m3(v));
     }
+}
+
+// Inverse of fp8_block_scale_bits: the aligned exponent S from the FP32 block
+// scale 2^(S - 127 - k) (0xFF for the NaN scale).
+__device__ __forceinline__ uint32_t fp8_block_scale_exponent(uint32_t bits, int k)
+{
+    if (bits == 0x7FC00000u)
+        return 0xFFu;
+    const int ex = (bits >> 23) ? static_cast<int>(bits >> 23) : (31 - __clz(bits)) - 22;
+    return static_cast<uint32_t>(ex + k);
 }
 
 // Philox4x32-10 (Salmon et al., SC'11).

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kThreads) fp4_to_fp8_rows_kernel(
     const uint8_t *__restrict__ q, const uint8_t *__restrict__ s, int64_t nfb, int k,
     uint8_t *__restrict__ y, float *__restrict__ ys)
 {
-    __shared__ __align__(16) uint8_t tab[kShiftRows * 8];
+    __shared__ __align__(16) uint8_t tab[kTabRows * 8];
     build_fp8_table(tab);
     __syncthreads();
 

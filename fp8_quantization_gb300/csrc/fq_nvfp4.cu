@@ -20,7 +20,7 @@ namespace fq {
 
 // ---------------------------------------------------------------- amax
 
-__global__ void __launch_bounds__(kThreads) nvfp4_amax_kernel(const uint16_t *__restrict__ x,
+__global__ void __launch_bounds__(kThreads, 6) nvfp4_amax_kernel(const uint16_t *__restrict__ x,
                                                               int64_t n,
                                                               uint32_t *__restrict__ out_bits)
 {
@@ -90,21 +90,8 @@ __device__ __forceinline__ float tensor_scale(const float *amax)
     return A > 0.0f ? __fdiv_rn(A, 2688.0f) : 1.0f;
 }
 
-// Stochastic rounding of y >= 0 to an E2M1 magnitude code with 16 random
-// bits R: round up iff R < floor(2^16 * (y - lo) / (hi - lo)).
-// Y = floor(y * 2^17) comes exactly from the mantissa of y + 64 rounded
-// toward zero; the grid step is 2^(16 + sh) in units of Y.
-__device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t R)
-{
-    const uint32_t Y = __float_as_uint(__fadd_rz(y, 64.0f)) & 0x7FFFFFu;
-    const uint32_t sh = Y >> 18;  // 0: y < 2, 1: y < 4, 2: y < 6
-    const uint32_t lo = (Y >> (16 + sh)) + 2 * sh;
-    const uint32_t F = (Y >> sh) & 0xFFFFu;
-    const uint32_t c = lo + (R < F ? 1u : 0u);
-    return y >= 6.0f ? 7u : c;
-}
-
-// Eight BF16 values (one uint4) times r -> eight E2M1 codes in a word.
+// Eight BF16 values (one uint4) times r -> eight E2M1 codes in a word,
+// round to nearest even (sign kept, including -0).
 __device__ __forceinline__ uint32_t encode8_rne(uint4 v, float r)
 {
     return cvt_e2m1x8(__fmul_rn(bf16_lo(v.x), r), __fmul_rn(bf16_hi(v.x), r),
@@ -113,26 +100,29 @@ __device__ __forceinline__ uint32_t encode8_rne(uint4 v, float r)
                       __fmul_rn(bf16_lo(v.w), r), __fmul_rn(bf16_hi(v.w), r));
 }
 
-__device__ __forceinline__ uint32_t encode8_sr(uint4 v, float r, uint4 rnd)
+// Eight BF16 values times r -> eight E2M1 codes, stochastic rounding: the
+// Blackwell FP4 conversion adds 16 random bits below the kept precision of
+// each value and truncates.  Values 0..3 draw on random word w0, 4..7 on w1;
+// within a group of four, value i sits in nibble i (first source = nibble 3).
+__device__ __forceinline__ uint32_t encode8_sr(uint4 v, float r, uint32_t w0, uint32_t w1)
 {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    const uint32_t R[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
-    uint32_t out = 0;
-#pragma unroll
-    for (int h = 0; h < 4; h++) {
-        const float ylo = __fmul_rn(__uint_as_float((w[h] << 16) & 0x7FFF0000u), r);
-        const float yhi = __fmul_rn(__uint_as_float(w[h] & 0x7FFF0000u), r);
-        const uint32_t clo = e2m1_sr(ylo, R[h] & 0xFFFFu) | ((w[h] >> 12) & 8u);
-        const uint32_t chi = e2m1_sr(yhi, R[h] >> 16) | ((w[h] >> 28) & 8u);
-        out |= (clo | (chi << 4)) << (8 * h);
-    }
-    return out;
+    uint16_t lo, hi;
+    asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;"
+        : "=h"(lo)
+        : "f"(__fmul_rn(bf16_hi(v.y), r)), "f"(__fmul_rn(bf16_lo(v.y), r)),
+          "f"(__fmul_rn(bf16_hi(v.x), r)), "f"(__fmul_rn(bf16_lo(v.x), r)), "r"(w0));
+    asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;"
+        : "=h"(hi)
+        : "f"(__fmul_rn(bf16_hi(v.w), r)), "f"(__fmul_rn(bf16_lo(v.w), r)),
+          "f"(__fmul_rn(bf16_hi(v.z), r)), "f"(__fmul_rn(bf16_lo(v.z), r)), "r"(w1));
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
 // ---------------------------------------------------------------- 1x16
 
-// Two lanes per 16-element block (8 elements = 16 bytes each); a warp pass
-// covers 16 blocks = 512 contiguous bytes of input, unrolled 4 times.
+// One lane per 16-element block (32 bytes of input, 8 bytes of codes), two
+// blocks in flight per lane.  With stochastic rounding the block's Philox
+// call (counter = offset/16 + block) yields one random word per four values.
 template <bool kSR>
 __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
     const uint16_t *__restrict__ x, int64_t nblk, const float *__restrict__ amax, uint64_t seed,
@@ -143,42 +133,47 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
     if (blockIdx.x == 0 && threadIdx.x == 0)
         *g_out = g;
     const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+    const uint64_t c0 = offset >> 4;
 
-    const int lane = threadIdx.x & 31;
-    const int half = lane & 1;
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const int64_t ntiles = (nblk + 63) >> 6;
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
 
-    for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
-        uint4 v[4];
+    for (int64_t b0 = gtid; b0 < nblk; b0 += 2 * nthr) {
+        uint4 v[2][2];
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const int64_t blk = (tile << 6) + 16 * i + (lane >> 1);
-            v[i] = blk < nblk ? ld_nc_v4(x + blk * 16 + half * 8) : make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < 2; u++) {
+            const int64_t blk = b0 + u * nthr;
+            if (blk < nblk) {
+                v[u][0] = ld_nc_v4(x + blk * 16);
+                v[u][1] = ld_nc_v4(x + blk * 16 + 8);
+            } else {
+                v[u][0] = v[u][1] = make_uint4(0, 0, 0, 0);
+            }
         }
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const int64_t blk = (tile << 6) + 16 * i + (lane >> 1);
-            uint32_t m = absmax_bf16x2(absmax_bf16x2(v[i].x & 0x7FFF7FFFu, v[i].y), v[i].z);
-            m = absmax_bf16x2(m, v[i].w);
-            m = max_u16x2(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        for (int u = 0; u < 2; u++) {
+            const int64_t blk = b0 + u * nthr;
+            if (blk >= nblk)
+                break;
+            uint32_t m = absmax_bf16x2(absmax_bf16x2(v[u][0].x & 0x7FFF7FFFu, v[u][0].y), v[u][0].z);
+            m = absmax_bf16x2(absmax_bf16x2(m, v[u][0].w), v[u][1].x);
+            m = absmax_bf16x2(absmax_bf16x2(m, v[u][1].y), v[u][1].z);
+            m = absmax_bf16x2(m, v[u][1].w);
             const BlockScale bs = nvfp4_block_scale(hmax_u16x2(m), g, six_g);
-            uint32_t codes;
+            uint2 codes;
             if (kSR) {
-                const uint64_t c = (offset + static_cast<uint64_t>(blk) * 16 + half * 8) >> 3;
-                const uint4 rnd = philox4x32_10(
+                const uint64_t c = c0 + static_cast<uint64_t>(blk);
+                const uint4 w = philox4x32_10(
                     make_uint4(static_cast<uint32_t>(c), static_cast<uint32_t>(c >> 32), 0u, 0u),
                     k0, k1);
-                codes = encode8_sr(v[i], bs.r, rnd);
+                codes.x = encode8_sr(v[u][0], bs.r, w.x, w.y);
+                codes.y = encode8_sr(v[u][1], bs.r, w.z, w.w);
             } else {
-                codes = encode8_rne(v[i], bs.r);
+                codes.x = encode8_rne(v[u][0], bs.r);
+                codes.y = encode8_rne(v[u][1], bs.r);
             }
-            if (blk < nblk) {
-                *reinterpret_cast<uint32_t *>(q + blk * 8 + half * 4) = codes;
-                if (!half)
-                    sb[blk] = static_cast<uint8_t>(bs.b);
-            }
+            *reinterpret_cast<uint2 *>(q + blk * 8) = codes;
+            sb[blk] = static_cast<uint8_t>(bs.b);
         }
     }
 }
@@ -274,7 +269,7 @@ extern "C" fq_status nvfp4_quantize(const void *x, int64_t M, int64_t K, const f
     if (!aligned16(x) || !aligned16(amax) || !aligned16(q) || !aligned16(sb) || !aligned16(g))
         return FQ_ERR_ALIGN;
     const int64_t nblk = M * (K / 16);
-    const int64_t work = (nblk + 64 * (kThreads / 32) - 1) / (64 * (kThreads / 32));
+    const int64_t work = (nblk + 2 * kThreads - 1) / (2 * kThreads);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (use_sr) {
         const int grid = persistent_grid(nvfp4_quantize_kernel<true>, kThreads, 0, work);

@@ -16,7 +16,7 @@ Zipf(1.1) counts for the transposed ragged conversion):
 The metric is effective bandwidth: algorithmic bytes read + written by the
 kernels over their device time (CUDA events on the launching stream), as GB/s
 and as a fraction of the measured HBM copy bandwidth.  L2 is flushed (256 MB
-write) between steps, outside the timed events.
+written, then read back) between steps, outside the timed events.
 
 --impl reference times the CPU oracle (the plain C implementation the tests
 compare against) on a bounded sample of the same workload.
@@ -300,7 +300,14 @@ def run_gpu(args):
         "q2": torch.empty((M, K // 2), **u8), "sb2": torch.empty((M // 16, K // 16), **u8),
         "g2": torch.empty((1,), **f32),
     }
-    flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+
+    def flush():
+        # evict L2 (2x its size): write a buffer, then read it back so that
+        # the flush's own dirty lines are written out here, not in the next step
+        flush_buf.fill_(1)
+        flush_buf.sum(dtype=torch.int64)
+
     stream = torch.cuda.current_stream(dev)
 
     def step(i, xin, ev=None):
@@ -328,7 +335,7 @@ def run_gpu(args):
             ev[6].record(stream)
 
     for i in range(args.warmup):
-        flush.zero_()
+        flush()
         step(i, x)
     torch.cuda.synchronize(dev)
 
@@ -341,7 +348,7 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     t0 = time.time()
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         step(i, x, evs[i])
     torch.cuda.synchronize(dev)
     t1 = time.time()
@@ -414,7 +421,7 @@ def run_gpu(args):
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "M": M, "K": K, "experts": G,
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                       "l2": "flushed between steps (256 MB write, outside the timed events)",
+                       "l2": "flushed between steps (256 MB write + read, outside the timed events)",
                        "step_bytes": step_bytes},
             "frac_of_hbm_peak": round(value / ws / peak, 4),
             "kernels": kernels,

@@ -156,69 +156,75 @@ __device__ __forceinline__ uint32_t bytemax4(uint32_t a, uint32_t b)
 
 // ---------------------------------------------------------------- launch 1: block scales
 
-// CTA per 128-token block (slot).  Threads split (token subset, 4-column
-// word): the exponent words of a token row are read coalesced, reduced
-// byte-wise across the token subsets in shared memory, and every feature
-// row's scale of the block is written.
+// CTA (exponent word w, 32 consecutive blocks): warp i reduces blocks
+// 4i..4i+3 of the chunk -- each lane loads the word w of four tokens per
+// block (16 loads in flight), then a byte-wise warp max -- and the CTA writes
+// the 128 feature rows of word w (4 MX columns x 32 rows) for its 32 blocks,
+// one 128-byte line per row.
+constexpr int kScaleSlots = 32;
+
 __global__ void __launch_bounds__(kThreads) fp4_to_fp8_cols_scales_kernel(
     const uint8_t *__restrict__ s, int32_t M, int64_t K, const int64_t *__restrict__ offs,
     int32_t G, int k, float *__restrict__ yTs, int64_t cap, int32_t *__restrict__ dev_status)
 {
     __shared__ int32_t warp_tot[kThreads / 32];
-    __shared__ uint32_t red[kThreads];
+    __shared__ uint32_t smax[kScaleSlots];
     extern __shared__ int32_t dyn[];
     int32_t *off = dyn, *base = dyn + G + 1;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int bad = load_groups(offs, G, M, off, base, warp_tot);
-    if (bad && blockIdx.x == 0 && tid == 0 && dev_status)
+    if (bad && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0 && dev_status)
         atomicOr(dev_status, 1);
 
     const int32_t nblocks = base[G];
     const int32_t J4 = static_cast<int32_t>(K / 128);  // exponent words per token row
+    const int32_t word = blockIdx.x;                     // < J4
     const uint32_t *s32 = reinterpret_cast<const uint32_t *>(s);
     uint32_t *out = reinterpret_cast<uint32_t *>(yTs);
-    for (int32_t slot = blockIdx.x; slot < nblocks; slot += gridDim.x) {
-        const int g = find_last_le(base, 0, G - 1, slot);
-        const int32_t bs = off[g] + (slot - base[g]) * kTok;
-        const int32_t be = min(bs + kTok, off[g + 1]);
-        for (int32_t j0 = 0; j0 < J4; j0 += kThreads) {
-            const int jn = min(kThreads, J4 - j0);
-            const int parts = kThreads / jn;
-            const int jj = tid % jn, part = tid / jn;
-            uint32_t m = 0;
-            if (part < parts) {
-                // 16 independent loads in flight per round
-                const uint32_t *src = s32 + static_cast<int64_t>(bs) * J4 + j0 + jj;
-                for (int32_t t0 = part; t0 < be - bs; t0 += 16 * parts) {
-                    uint32_t v[16];
+
+    for (int32_t slot0 = blockIdx.y * kScaleSlots; slot0 < nblocks;
+         slot0 += gridDim.y * kScaleSlots) {
+        // ---- block maxima: warp wid owns slots slot0 + 4*wid .. +3
+        uint32_t v[4][4];
+        int32_t bs[4], be[4];
 #pragma unroll
-                    for (int i = 0; i < 16; i++) {
-                        const int32_t t = t0 + i * parts;
-                        v[i] = t < be - bs ? __ldg(src + static_cast<int64_t>(t) * J4) : 0u;
-                    }
+        for (int i = 0; i < 4; i++) {
+            const int32_t slot = slot0 + 4 * wid + i;
+            bs[i] = be[i] = 0;
+            if (slot < nblocks) {
+                const int g = find_last_le(base, 0, G - 1, slot);
+                bs[i] = off[g] + (slot - base[g]) * kTok;
+                be[i] = min(bs[i] + kTok, off[g + 1]);
+            }
 #pragma unroll
-                    for (int i = 0; i < 16; i++)
-                        m = bytemax4(m, v[i]);
-                }
+            for (int u = 0; u < 4; u++) {
+                const int32_t t = bs[i] + lane + 32 * u;
+                v[i][u] = t < be[i] ? __ldg(s32 + static_cast<int64_t>(t) * J4 + word) : 0u;
             }
-            red[tid] = m;
-            __syncthreads();
-            if (tid < jn)
-                for (int p = 1; p < parts; p++)
-                    m = bytemax4(m, red[tid + p * jn]);
-            __syncthreads();
-            if (tid < jn)
-                red[tid] = m;
-            __syncthreads();
-            // 4 MX columns x 32 feature rows per exponent word
-            for (int idx = tid; idx < 128 * jn; idx += kThreads) {
-                const int w = idx >> 7;
-                const uint32_t S = (red[w] >> (8 * ((idx >> 5) & 3))) & 0xFFu;
-                const int64_t row = static_cast<int64_t>(j0 + w) * 128 + (idx & 127);
-                out[row * cap + slot] = fp8_block_scale_bits(S, k);
-            }
-            __syncthreads();
         }
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const uint32_t m = bytemax4(bytemax4(v[i][0], v[i][1]), bytemax4(v[i][2], v[i][3]));
+            const uint32_t b0 = __reduce_max_sync(0xffffffffu, m & 0xFFu);
+            const uint32_t b1 = __reduce_max_sync(0xffffffffu, (m >> 8) & 0xFFu);
+            const uint32_t b2 = __reduce_max_sync(0xffffffffu, (m >> 16) & 0xFFu);
+            const uint32_t b3 = __reduce_max_sync(0xffffffffu, m >> 24);
+            if (lane == 0)
+                smax[4 * wid + i] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        }
+        __syncthreads();
+        // ---- scales: row 128*word + rr, lane = block within the chunk
+        const int32_t slot = slot0 + lane;
+        if (slot < nblocks) {
+            const uint32_t Sw = smax[lane];
+            uint32_t *dst = out + (static_cast<int64_t>(word) * 128 + wid) * cap + slot;
+#pragma unroll 4
+            for (int rr = wid; rr < 128; rr += kThreads / 32) {
+                *dst = fp8_block_scale_bits((Sw >> (8 * (rr >> 5))) & 0xFFu, k);
+                dst += (kThreads / 32) * cap;
+            }
+        }
+        __syncthreads();
     }
 }
 
@@ -315,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 4) fp4_to_fp8_cols_kernel(
                 const uint32_t S = fp8_block_scale_exponent(sv[r], k);
                 const uint32_t e = (ev[r] >> (8 * j)) & 0xFFu;
                 int u = static_cast<int>(S - e) - k + 6;
-                u = u < kShiftRows - 1 ? u : kShiftRows - 1;
+                u = min(max(u, 0), kShiftRows - 1);  // u >= 0: S is the max over the block
                 const bool nan = S == 0xFFu;
                 const uint2 t = *reinterpret_cast<const uint2 *>(tab + 8 * (nan ? kNanRow : u));
                 const uint32_t smask = nan ? 0u : 0x80808080u;
@@ -409,8 +415,10 @@ extern "C" fq_status fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t groups_bytes = static_cast<size_t>(G + 1) * 2 * sizeof(int32_t);
 
-    // launch 1: block scales (one CTA per block, at most cap blocks)
-    const int grid1 = persistent_grid(fp4_to_fp8_cols_scales_kernel, kThreads, groups_bytes, cap);
+    // launch 1: block scales, CTA per (exponent word, 32 blocks)
+    const int64_t chunks = (cap + kScaleSlots - 1) / kScaleSlots;
+    const dim3 grid1(static_cast<unsigned>(K / 128),
+                     static_cast<unsigned>(chunks < 65535 ? chunks : 65535));
     fp4_to_fp8_cols_scales_kernel<<<grid1, kThreads, groups_bytes, st>>>(
         s, static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT_scale, cap, dev_status);
     fq_status rc = launch_status();
@@ -419,13 +427,13 @@ extern "C" fq_status fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
 
     // launch 2: convert + transpose (two FP8 tiles + the group arrays)
     const size_t dyn = 2 * kTileWords * sizeof(uint32_t) + groups_bytes;
-    const int64_t ntiles = ((M + 127) / 128) * (K / 128);
+    const int64_t work_ctas = ((M + 127) / 128) * (K / 128);
     if (M % 16 == 0) {
         if (cudaFuncSetAttribute(fp4_to_fp8_cols_kernel<true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(dyn)) != cudaSuccess)
             return launch_status();
-        const int grid = persistent_grid(fp4_to_fp8_cols_kernel<true>, kThreads, dyn, ntiles);
+        const int grid = persistent_grid(fp4_to_fp8_cols_kernel<true>, kThreads, dyn, work_ctas);
         fp4_to_fp8_cols_kernel<true><<<grid, kThreads, dyn, st>>>(
             q, s, static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT, yT_scale, cap);
     } else {
@@ -433,7 +441,7 @@ extern "C" fq_status fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(dyn)) != cudaSuccess)
             return launch_status();
-        const int grid = persistent_grid(fp4_to_fp8_cols_kernel<false>, kThreads, dyn, ntiles);
+        const int grid = persistent_grid(fp4_to_fp8_cols_kernel<false>, kThreads, dyn, work_ctas);
         fp4_to_fp8_cols_kernel<false><<<grid, kThreads, dyn, st>>>(
             q, s, static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT, yT_scale, cap);
     }

@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kThreads) fp4_to_fp8_rows_kernel(
             if (S == 0xFFu)
                 out = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
             if (fb < nfb) {
-                *reinterpret_cast<uint4 *>(y + fb * 128 + part * 16) = out;
+                __stcs(reinterpret_cast<uint4 *>(y + fb * 128 + part * 16), out);  // evict-first: y is not re-read
                 if (part == 0)
                     reinterpret_cast<uint32_t *>(ys)[fb] = fp8_block_scale_bits(S, k);
             }

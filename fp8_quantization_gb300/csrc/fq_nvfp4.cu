@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
                 codes.x = encode8_rne(v[u][0], bs.r);
                 codes.y = encode8_rne(v[u][1], bs.r);
             }
-            *reinterpret_cast<uint2 *>(q + blk * 8) = codes;
+            __stcs(reinterpret_cast<uint2 *>(q + blk * 8), codes);
             sb[blk] = static_cast<uint8_t>(bs.b);
         }
     }
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 2) nvfp4_quantize_2d_kernel(
             uint8_t *dst = q + (strip << 4) * (K >> 1) + (col >> 1);
 #pragma unroll
             for (int r = 0; r < 16; r++)
-                *reinterpret_cast<uint32_t *>(dst + r * (K >> 1)) = encode8_rne(v[r], bs.r);
+                __stcs(reinterpret_cast<unsigned int *>(dst + r * (K >> 1)), encode8_rne(v[r], bs.r));
             if (!(lane & 1))
                 sb[strip * (K >> 4) + (col >> 4)] = static_cast<uint8_t>(bs.b);
         }

@@ -235,7 +235,17 @@ __global__ void __launch_bounds__(kThreads) fp4_to_fp8_cols_scales_kernel(
 // (token t/4 + 64, column block t%4): each warp load covers eight token rows
 // x 64 contiguous bytes.  For the write-out, warp w handles feature words
 // 4w..4w+3 (lane/8 picks the word) and lane%8 picks 16 tokens: each 16-byte
-// store of a quarter warp fills one 128-byte output line.
+// store of a quarter warp fills one 128-byte output line.  A window that is
+// full and lies in one group (the common case) takes a path without
+// per-token checks; the next tile's inputs are loaded into the other of two
+// register sets while the current tile is converted and written.
+
+struct ColsPrefetch {
+    uint4 q0, q1;      // 16 bytes of codes of the two units
+    uint32_t e0, e1;   // exponent words (4 MX columns) of the two tokens
+    uint32_t s0, s1;   // FP32 block scales (column j) of the two tokens
+};
+
 template <bool kAligned16>
 __global__ void __launch_bounds__(kThreads, 4) fp4_to_fp8_cols_kernel(
     const uint8_t *__restrict__ q, const uint8_t *__restrict__ s, int32_t M, int64_t K,
@@ -260,122 +270,149 @@ __global__ void __launch_bounds__(kThreads, 4) fp4_to_fp8_cols_kernel(
     const int j = tid & 3;     // column block of both units
     const int tl0 = tid >> 2;  // token of unit 0 (unit 1: tl0 + 64)
     const uint32_t *ys32 = reinterpret_cast<const uint32_t *>(yTs);
-
-    // tiles are (window, feature chunk) with the window index fastest; a CTA
-    // advances by gridDim.x tiles (32-bit, incremental: no division per tile)
+    // loop-invariant parts of the addresses
+    const int64_t qoff0 = static_cast<int64_t>(tl0) * qrow + 16 * j;
+    const int64_t qoff1 = qoff0 + 64 * qrow;
+    const int64_t soff0 = static_cast<int64_t>(tl0) * srow;
+    const int64_t soff1 = soff0 + 64 * srow;
+    // write-out: feature word m (4 rows) and tokens 16c..16c+15
+    const int m_out = 4 * wid + (lane >> 3);
+    const int c_out = lane & 7;
     const int32_t step_w = static_cast<int32_t>(gridDim.x) % nwin;
     const int32_t step_f = static_cast<int32_t>(gridDim.x) / nwin;
 
-    // per unit: 16 bytes of codes, the token's exponent word (4 columns) and
-    // the FP32 scale of its block (column j), which encodes the block's S
-    auto prefetch = [&](int32_t win, int32_t f, uint4(&qv)[2], uint32_t(&ev)[2],
-                        uint32_t(&sv)[2]) {
+    auto prefetch = [&](int32_t win, int32_t f, ColsPrefetch &P) {
         const int32_t W = win * kTok;
         const int g0 = warp_find_last_le(off, G, W);
         const int32_t end0 = off[g0 + 1];
-        const uint8_t *qrow0 = q + static_cast<int64_t>(W + tl0) * qrow + f * 64 + 16 * j;
-        const uint8_t *srow0 = s + static_cast<int64_t>(W + tl0) * srow + 4 * f;
-        const uint32_t *yscol = ys32 + (static_cast<int64_t>(f) * 128 + 32 * j) * cap;
-#pragma unroll
-        for (int r = 0; r < 2; r++) {
-            const int32_t t = W + tl0 + 64 * r;
-            if (t < M) {
-                qv[r] = ld_nc_v4(qrow0 + r * 64 * qrow);
-                ev[r] = __ldg(reinterpret_cast<const uint32_t *>(srow0 + r * 64 * srow));
-                const int g = t < end0 ? g0 : find_last_le(off, g0, G - 1, t);
-                const int32_t slot = base[g] + static_cast<int32_t>(static_cast<uint32_t>(t - off[g]) >> 7);
-                sv[r] = yscol[slot];
-            } else {
-                qv[r] = make_uint4(0, 0, 0, 0);
-                ev[r] = 0;
-                sv[r] = 0;
-            }
+        const uint8_t *qb = q + static_cast<int64_t>(W) * qrow + 64 * f;
+        const uint8_t *sp = s + static_cast<int64_t>(W) * srow + 4 * f;
+        const uint32_t *yc = ys32 + (static_cast<int64_t>(f) * 128 + 32 * j) * cap;
+        if (W + kTok <= end0) {  // full window inside group g0 (warp-uniform)
+            const int32_t t0 = W + tl0 - off[g0];
+            P.q0 = ld_nc_v4(qb + qoff0);
+            P.q1 = ld_nc_v4(qb + qoff1);
+            P.e0 = __ldg(reinterpret_cast<const uint32_t *>(sp + soff0));
+            P.e1 = __ldg(reinterpret_cast<const uint32_t *>(sp + soff1));
+            P.s0 = yc[base[g0] + (t0 >> 7)];
+            P.s1 = yc[base[g0] + ((t0 + 64) >> 7)];
+        } else {  // window crossing groups or past M
+            const int32_t tA = W + tl0, tB = tA + 64;
+            P.q0 = tA < M ? ld_nc_v4(qb + qoff0) : make_uint4(0, 0, 0, 0);
+            P.q1 = tB < M ? ld_nc_v4(qb + qoff1) : make_uint4(0, 0, 0, 0);
+            P.e0 = tA < M ? __ldg(reinterpret_cast<const uint32_t *>(sp + soff0)) : 0u;
+            P.e1 = tB < M ? __ldg(reinterpret_cast<const uint32_t *>(sp + soff1)) : 0u;
+            const int gA = tA < end0 ? g0 : find_last_le(off, g0, G - 1, min(tA, M - 1));
+            const int gB = tB < end0 ? g0 : find_last_le(off, g0, G - 1, min(tB, M - 1));
+            P.s0 = tA < M ? yc[base[gA] + ((tA - off[gA]) >> 7)] : 0u;
+            P.s1 = tB < M ? yc[base[gB] + ((tB - off[gB]) >> 7)] : 0u;
         }
     };
 
-    uint4 qv[2], qn[2];
-    uint32_t ev[2], en[2], sv[2], sn[2];
-    int32_t tau = blockIdx.x;
-    int32_t win = tau % nwin, f = tau / nwin;
-    if (tau < ntiles)
-        prefetch(win, f, qv, ev, sv);
-    int buf = 0;
-    for (; tau < ntiles; tau += gridDim.x) {
-        const int32_t W = win * kTok;
-        const int32_t We = min(W + kTok, M);
-        int32_t win_n = win + step_w, f_n = f + step_f;
-        if (win_n >= nwin) {
-            win_n -= nwin;
-            f_n++;
-        }
-        const bool more = tau + static_cast<int32_t>(gridDim.x) < ntiles;
-        if (more)
-            prefetch(win_n, f_n, qn, en, sn);
+    // one unit: 32 codes -> 32 E4M3 bytes into the shared tile
+    auto convert = [&](uint32_t *tile, int tl, uint4 qv, uint32_t ev, uint32_t sv) {
+        const uint32_t S = fp8_block_scale_exponent(sv, k);
+        const uint32_t e = (ev >> (8 * j)) & 0xFFu;
+        int u = static_cast<int>(S - e) - k + 6;
+        u = min(max(u, 0), kShiftRows - 1);  // u >= 0: S is the max over the block
+        const bool nan = S == 0xFFu;
+        const uint2 t = *reinterpret_cast<const uint2 *>(tab + 8 * (nan ? kNanRow : u));
+        const uint32_t smask = nan ? 0u : 0x80808080u;
+        uint32_t o[8];
+        fp4x8_to_fp8x8(qv.x, t.x, t.y, o[0], o[1], smask);
+        fp4x8_to_fp8x8(qv.y, t.x, t.y, o[2], o[3], smask);
+        fp4x8_to_fp8x8(qv.z, t.x, t.y, o[4], o[5], smask);
+        fp4x8_to_fp8x8(qv.w, t.x, t.y, o[6], o[7], smask);
+        uint32_t *dst = tile + 4 * slot_index(tl >> 2, 8 * j) + (tl & 3);
+#pragma unroll
+        for (int w = 0; w < 8; w++)
+            dst[4 * w] = o[w];
+    };
 
-        // ---- convert this thread's two units into the shared FP8 tile
-        uint32_t *tile = tiles + buf * kTileWords;
-#pragma unroll
-        for (int r = 0; r < 2; r++) {
-            const int tl = tl0 + 64 * r;
-            if (W + tl < We) {
-                const uint32_t S = fp8_block_scale_exponent(sv[r], k);
-                const uint32_t e = (ev[r] >> (8 * j)) & 0xFFu;
-                int u = static_cast<int>(S - e) - k + 6;
-                u = min(max(u, 0), kShiftRows - 1);  // u >= 0: S is the max over the block
-                const bool nan = S == 0xFFu;
-                const uint2 t = *reinterpret_cast<const uint2 *>(tab + 8 * (nan ? kNanRow : u));
-                const uint32_t smask = nan ? 0u : 0x80808080u;
-                uint32_t o[8];
-                fp4x8_to_fp8x8(qv[r].x, t.x, t.y, o[0], o[1], smask);
-                fp4x8_to_fp8x8(qv[r].y, t.x, t.y, o[2], o[3], smask);
-                fp4x8_to_fp8x8(qv[r].z, t.x, t.y, o[4], o[5], smask);
-                fp4x8_to_fp8x8(qv[r].w, t.x, t.y, o[6], o[7], smask);
-                const int quad = tl >> 2, sub = tl & 3;
-#pragma unroll
-                for (int w = 0; w < 8; w++)
-                    tile[4 * slot_index(quad, 8 * j + w) + sub] = o[w];
-            }
+    auto process = [&](int32_t win, int32_t f, const ColsPrefetch &P, uint32_t *tile) {
+        const int32_t W = win * kTok;
+        const bool full = W + kTok <= M;
+        if (full) {
+            convert(tile, tl0, P.q0, P.e0, P.s0);
+            convert(tile, tl0 + 64, P.q1, P.e1, P.s1);
+        } else {
+            if (W + tl0 < M)
+                convert(tile, tl0, P.q0, P.e0, P.s0);
+            if (W + tl0 + 64 < M)
+                convert(tile, tl0 + 64, P.q1, P.e1, P.s1);
         }
         __syncthreads();
-
-        // ---- transpose 4x4 byte blocks; 16 tokens of 4 feature rows per thread
-        {
-            const int m = 4 * wid + (lane >> 3);  // word of 4 features
-            const int c = lane & 7;               // tokens 16c .. 16c+15
-            uint32_t rows[4][4];
+        uint32_t rows[4][4];
 #pragma unroll
-            for (int qq = 0; qq < 4; qq++) {
-                const uint4 v =
-                    *reinterpret_cast<const uint4 *>(tile + 4 * slot_index(4 * c + qq, m));
-                transpose4x4(v, rows[0][qq], rows[1][qq], rows[2][qq], rows[3][qq]);
-            }
-            const int32_t t0 = W + 16 * c;
-            uint8_t *dst = yT + (static_cast<int64_t>(f) * 128 + 4 * m) * M + t0;
+        for (int qq = 0; qq < 4; qq++) {
+            const uint4 v =
+                *reinterpret_cast<const uint4 *>(tile + 4 * slot_index(4 * c_out + qq, m_out));
+            transpose4x4(v, rows[0][qq], rows[1][qq], rows[2][qq], rows[3][qq]);
+        }
+        const int32_t t0 = W + 16 * c_out;
+        uint8_t *p = yT + (static_cast<int64_t>(f) * 128 + 4 * m_out) * M + t0;
+        if (kAligned16 && full) {
 #pragma unroll
             for (int rr = 0; rr < 4; rr++) {
-                uint8_t *p = dst + static_cast<int64_t>(rr) * M;
-                if (kAligned16 && t0 + 16 <= We) {
-                    *reinterpret_cast<uint4 *>(p) =
-                        make_uint4(rows[rr][0], rows[rr][1], rows[rr][2], rows[rr][3]);
-                } else {
+                __stcs(reinterpret_cast<uint4 *>(p),  // evict-first: yT is not re-read
+                       make_uint4(rows[rr][0], rows[rr][1], rows[rr][2], rows[rr][3]));
+                p += M;
+            }
+        } else {
+            const int32_t We = min(W + kTok, M);
 #pragma unroll
+            for (int rr = 0; rr < 4; rr++) {
+                if (kAligned16 && t0 + 16 <= We) {
+                    __stcs(reinterpret_cast<uint4 *>(p),
+                           make_uint4(rows[rr][0], rows[rr][1], rows[rr][2], rows[rr][3]));
+                } else {
                     for (int b = 0; b < 16; b++)
                         if (t0 + b < We)
                             p[b] = static_cast<uint8_t>(rows[rr][b >> 2] >> (8 * (b & 3)));
                 }
+                p += M;
             }
         }
-        if (more) {
-            qv[0] = qn[0];
-            qv[1] = qn[1];
-            ev[0] = en[0];
-            ev[1] = en[1];
-            sv[0] = sn[0];
-            sv[1] = sn[1];
+    };
+
+    int32_t tau = blockIdx.x;
+    if (tau >= ntiles)
+        return;
+    int32_t win = tau % nwin, f = tau / nwin;
+    ColsPrefetch PA, PB;
+    prefetch(win, f, PA);
+    for (;;) {
+        // ---- tile in PA (buffer 0), prefetch the next into PB
+        int32_t win2 = win + step_w, f2 = f + step_f;
+        if (win2 >= nwin) {
+            win2 -= nwin;
+            f2++;
         }
-        win = win_n;
-        f = f_n;
-        buf ^= 1;
+        const bool more = tau + static_cast<int32_t>(gridDim.x) < ntiles;
+        if (more)
+            prefetch(win2, f2, PB);
+        process(win, f, PA, tiles);
+        if (!more)
+            break;
+        tau += gridDim.x;
+        win = win2;
+        f = f2;
+        // ---- tile in PB (buffer 1), prefetch the next into PA
+        win2 = win + step_w;
+        f2 = f + step_f;
+        if (win2 >= nwin) {
+            win2 -= nwin;
+            f2++;
+        }
+        const bool more2 = tau + static_cast<int32_t>(gridDim.x) < ntiles;
+        if (more2)
+            prefetch(win2, f2, PA);
+        process(win, f, PB, tiles + kTileWords);
+        if (!more2)
+            break;
+        tau += gridDim.x;
+        win = win2;
+        f = f2;
     }
 }
 

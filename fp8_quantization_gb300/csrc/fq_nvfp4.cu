@@ -120,9 +120,12 @@ __device__ __forceinline__ uint32_t encode8_sr(uint4 v, float r, uint32_t w0, ui
 
 // ---------------------------------------------------------------- 1x16
 
-// One lane per 16-element block (32 bytes of input, 8 bytes of codes), two
-// blocks in flight per lane.  With stochastic rounding the block's Philox
-// call (counter = offset/16 + block) yields one random word per four values.
+// One lane per 16-element block (32 bytes of input, 8 bytes of codes), four
+// blocks in flight per lane (their Philox chains interleave).  With
+// stochastic rounding the block's Philox call (counter = offset/16 + block)
+// yields one random word per four values.
+constexpr int kNvUnroll = 4;
+
 template <bool kSR>
 __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
     const uint16_t *__restrict__ x, int64_t nblk, const float *__restrict__ amax, uint64_t seed,
@@ -138,10 +141,10 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
 
-    for (int64_t b0 = gtid; b0 < nblk; b0 += 2 * nthr) {
-        uint4 v[2][2];
+    for (int64_t b0 = gtid; b0 < nblk; b0 += kNvUnroll * nthr) {
+        uint4 v[kNvUnroll][2];
 #pragma unroll
-        for (int u = 0; u < 2; u++) {
+        for (int u = 0; u < kNvUnroll; u++) {
             const int64_t blk = b0 + u * nthr;
             if (blk < nblk) {
                 v[u][0] = ld_nc_v4(x + blk * 16);
@@ -151,7 +154,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
             }
         }
 #pragma unroll
-        for (int u = 0; u < 2; u++) {
+        for (int u = 0; u < kNvUnroll; u++) {
             const int64_t blk = b0 + u * nthr;
             if (blk >= nblk)
                 break;
@@ -269,7 +272,7 @@ extern "C" fq_status nvfp4_quantize(const void *x, int64_t M, int64_t K, const f
     if (!aligned16(x) || !aligned16(amax) || !aligned16(q) || !aligned16(sb) || !aligned16(g))
         return FQ_ERR_ALIGN;
     const int64_t nblk = M * (K / 16);
-    const int64_t work = (nblk + 2 * kThreads - 1) / (2 * kThreads);
+    const int64_t work = (nblk + kNvUnroll * kThreads - 1) / (kNvUnroll * kThreads);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (use_sr) {
         const int grid = persistent_grid(nvfp4_quantize_kernel<true>, kThreads, 0, work);

@@ -504,7 +504,8 @@ float oracle_nvfp4_amax(const uint16_t *x, int64_t n)
 
 /* READING (two-level NVFP4 scaling, all binary32, one rounding per op):
  *   g  = A / 2688   (2688 = 448 * 6: E4M3 max times E2M1 max); g = 1 if A == 0
- *   t  = amax_blk / (6 * g)          block scale before rounding
+ *   e  = 1 / (6 * g)                 per-tensor encode factor
+ *   t  = amax_blk * e                block scale before rounding
  *   b  = E4M3(t), round to nearest even, saturating
  *   r  = min(1 / (b * g), FLT_MAX)   (r = 0 if b == 0)
  *   y  = |x| * r  -> E2M1 (RNE, or stochastic rounding), sign of x kept. */
@@ -513,7 +514,8 @@ static float nvfp4_tensor_scale(float A) { return (A > 0.0f) ? A / 2688.0f : 1.0
 static void nvfp4_block_scales(float amax_blk, float g, int *b_out, float *r_out)
 {
     float six_g = 6.0f * g;
-    float t = amax_blk / six_g;
+    float enc = 1.0f / six_g;
+    float t = amax_blk * enc;
     int b = e4m3_rne_satfinite((double)t);
     float r = 0.0f;
     if (b != 0) {

@@ -63,8 +63,9 @@ def test_block_scale_and_error_bound(oracle_mod):
     # the block holding the tensor maximum gets the top E4M3 code (448)
     r, c = np.unravel_index(np.argmax(amax_blk), amax_blk.shape)
     assert sb[r, c] == 0x7E
-    # block scale byte = library E4M3 cast of t = amax_blk / (6 g) (binary32)
-    t = (amax_blk.astype(np.float32) / (np.float32(6.0) * np.float32(g))).astype(np.float32)
+    # block scale byte = library E4M3 cast of t = amax_blk * (1 / (6 g)) (binary32)
+    enc = np.float32(1.0) / (np.float32(6.0) * np.float32(g))
+    t = (amax_blk.astype(np.float32) * enc).astype(np.float32)
     lib = torch.from_numpy(t).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     np.testing.assert_array_equal(sb, lib)
     # error bound: one E2M1 half-gap (<= 1) or the saturation loss (< 0.4)

@@ -116,6 +116,18 @@ __device__ __forceinline__ float e4m3_value(uint32_t b)
     return __uint_as_float((b + 960u) << 20);  // exponent field E - 7 + 127
 }
 
+// Two IEEE binary32 products (round to nearest) in one packed instruction.
+__device__ __forceinline__ void fmul2(float a0, float a1, float b, float &r0, float &r1)
+{
+    asm("{\n\t.reg .b64 x, y, z;\n\t"
+        "mov.b64 x, {%2, %3};\n\t"
+        "mov.b64 y, {%4, %4};\n\t"
+        "mul.rn.f32x2 z, x, y;\n\t"
+        "mov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(a0), "f"(a1), "f"(b));
+}
+
 // Byte permute (prmt.b32): result byte i chosen by selector nibble i from the
 // eight bytes {b:a}; a selector with bit 3 set replicates that byte's msb.
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)

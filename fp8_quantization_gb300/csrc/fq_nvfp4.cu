@@ -10,8 +10,10 @@
 // The scale arithmetic is IEEE binary32 with one rounding per operation
 // (explicit __fdiv_rn / __frcp_rn / __fmul_rn), so every code is a function
 // of the inputs alone:
-//   g = A / 2688 (1 if A == 0); t = amax_blk / (6 g); b = E4M3(t);
-//   r = min(1 / (b g), FLT_MAX) (0 if b == 0); code = E2M1(|x| r), sign of x.
+//   g = A / 2688 (1 if A == 0); enc = 1 / (6 g); t = amax_blk * enc;
+//   b = E4M3(t); r = min(1 / (b g), FLT_MAX) (0 if b == 0);
+//   code = E2M1(|x| r), sign of x.
+// enc and the 128 possible r values are computed once per CTA.
 #include <cfloat>
 
 #include "fq_common.cuh"
@@ -68,36 +70,49 @@ __global__ void __launch_bounds__(kThreads, 6) nvfp4_amax_kernel(const uint16_t 
 
 // ---------------------------------------------------------------- block scale
 
+// Per-tensor set-up, once per CTA: decode scale g, encode factor
+// enc = 1 / (6 g), and the table r[b] = min(1 / (b g), FLT_MAX) (r[0] = 0)
+// of element multipliers for every E4M3 block-scale byte b.
+struct TensorScales {
+    float g, enc;
+};
+
+__device__ __forceinline__ TensorScales nvfp4_tensor_setup(const float *amax, float *rtab /* [128] */)
+{
+    const float A = *amax;
+    TensorScales ts;
+    ts.g = A > 0.0f ? __fdiv_rn(A, 2688.0f) : 1.0f;
+    ts.enc = __frcp_rn(__fmul_rn(6.0f, ts.g));
+    for (int b = threadIdx.x; b < 128; b += blockDim.x)
+        rtab[b] = b ? fminf(__frcp_rn(__fmul_rn(e4m3_value(b), ts.g)), FLT_MAX) : 0.0f;
+    __syncthreads();
+    return ts;
+}
+
 struct BlockScale {
     uint32_t b;  // E4M3 byte
     float r;     // element multiplier
 };
 
-__device__ __forceinline__ BlockScale nvfp4_block_scale(uint32_t amax_bits16, float g, float six_g)
+__device__ __forceinline__ BlockScale nvfp4_block_scale(uint32_t amax_bits16, float enc,
+                                                        const float *rtab)
 {
-    const float amax = __uint_as_float(amax_bits16 << 16);
-    const float t = __fdiv_rn(amax, six_g);
     BlockScale bs;
-    bs.b = cvt_e4m3(t);
-    const float den = __fmul_rn(e4m3_value(bs.b), g);
-    bs.r = bs.b ? fminf(__frcp_rn(den), FLT_MAX) : 0.0f;
+    bs.b = cvt_e4m3(__fmul_rn(__uint_as_float(amax_bits16 << 16), enc));
+    bs.r = rtab[bs.b];
     return bs;
-}
-
-__device__ __forceinline__ float tensor_scale(const float *amax)
-{
-    const float A = *amax;
-    return A > 0.0f ? __fdiv_rn(A, 2688.0f) : 1.0f;
 }
 
 // Eight BF16 values (one uint4) times r -> eight E2M1 codes in a word,
 // round to nearest even (sign kept, including -0).
 __device__ __forceinline__ uint32_t encode8_rne(uint4 v, float r)
 {
-    return cvt_e2m1x8(__fmul_rn(bf16_lo(v.x), r), __fmul_rn(bf16_hi(v.x), r),
-                      __fmul_rn(bf16_lo(v.y), r), __fmul_rn(bf16_hi(v.y), r),
-                      __fmul_rn(bf16_lo(v.z), r), __fmul_rn(bf16_hi(v.z), r),
-                      __fmul_rn(bf16_lo(v.w), r), __fmul_rn(bf16_hi(v.w), r));
+    float p0, p1, p2, p3, p4, p5, p6, p7;
+    fmul2(bf16_lo(v.x), bf16_hi(v.x), r, p0, p1);
+    fmul2(bf16_lo(v.y), bf16_hi(v.y), r, p2, p3);
+    fmul2(bf16_lo(v.z), bf16_hi(v.z), r, p4, p5);
+    fmul2(bf16_lo(v.w), bf16_hi(v.w), r, p6, p7);
+    return cvt_e2m1x8(p0, p1, p2, p3, p4, p5, p6, p7);
 }
 
 // Eight BF16 values times r -> eight E2M1 codes, stochastic rounding: the
@@ -106,15 +121,18 @@ __device__ __forceinline__ uint32_t encode8_rne(uint4 v, float r)
 // within a group of four, value i sits in nibble i (first source = nibble 3).
 __device__ __forceinline__ uint32_t encode8_sr(uint4 v, float r, uint32_t w0, uint32_t w1)
 {
+    float p0, p1, p2, p3, p4, p5, p6, p7;
+    fmul2(bf16_lo(v.x), bf16_hi(v.x), r, p0, p1);
+    fmul2(bf16_lo(v.y), bf16_hi(v.y), r, p2, p3);
+    fmul2(bf16_lo(v.z), bf16_hi(v.z), r, p4, p5);
+    fmul2(bf16_lo(v.w), bf16_hi(v.w), r, p6, p7);
     uint16_t lo, hi;
     asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;"
         : "=h"(lo)
-        : "f"(__fmul_rn(bf16_hi(v.y), r)), "f"(__fmul_rn(bf16_lo(v.y), r)),
-          "f"(__fmul_rn(bf16_hi(v.x), r)), "f"(__fmul_rn(bf16_lo(v.x), r)), "r"(w0));
+        : "f"(p3), "f"(p2), "f"(p1), "f"(p0), "r"(w0));
     asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;"
         : "=h"(hi)
-        : "f"(__fmul_rn(bf16_hi(v.w), r)), "f"(__fmul_rn(bf16_lo(v.w), r)),
-          "f"(__fmul_rn(bf16_hi(v.z), r)), "f"(__fmul_rn(bf16_lo(v.z), r)), "r"(w1));
+        : "f"(p7), "f"(p6), "f"(p5), "f"(p4), "r"(w1));
     return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
@@ -131,10 +149,10 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
     const uint16_t *__restrict__ x, int64_t nblk, const float *__restrict__ amax, uint64_t seed,
     uint64_t offset, uint8_t *__restrict__ q, uint8_t *__restrict__ sb, float *__restrict__ g_out)
 {
-    const float g = tensor_scale(amax);
-    const float six_g = __fmul_rn(6.0f, g);
+    __shared__ float rtab[128];
+    const TensorScales ts = nvfp4_tensor_setup(amax, rtab);
     if (blockIdx.x == 0 && threadIdx.x == 0)
-        *g_out = g;
+        *g_out = ts.g;
     const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
     const uint64_t c0 = offset >> 4;
 
@@ -162,7 +180,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
             m = absmax_bf16x2(absmax_bf16x2(m, v[u][0].w), v[u][1].x);
             m = absmax_bf16x2(absmax_bf16x2(m, v[u][1].y), v[u][1].z);
             m = absmax_bf16x2(m, v[u][1].w);
-            const BlockScale bs = nvfp4_block_scale(hmax_u16x2(m), g, six_g);
+            const BlockScale bs = nvfp4_block_scale(hmax_u16x2(m), ts.enc, rtab);
             uint2 codes;
             if (kSR) {
                 const uint64_t c = c0 + static_cast<uint64_t>(blk);
@@ -190,10 +208,10 @@ __global__ void __launch_bounds__(kThreads, 2) nvfp4_quantize_2d_kernel(
     const uint16_t *__restrict__ w, int64_t N, int64_t K, const float *__restrict__ amax,
     uint8_t *__restrict__ q, uint8_t *__restrict__ sb, float *__restrict__ g_out)
 {
-    const float g = tensor_scale(amax);
-    const float six_g = __fmul_rn(6.0f, g);
+    __shared__ float rtab[128];
+    const TensorScales ts = nvfp4_tensor_setup(amax, rtab);
     if (blockIdx.x == 0 && threadIdx.x == 0)
-        *g_out = g;
+        *g_out = ts.g;
 
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -219,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 2) nvfp4_quantize_2d_kernel(
             m = absmax_bf16x2(m, v[r].w);
         }
         m = max_u16x2(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        const BlockScale bs = nvfp4_block_scale(hmax_u16x2(m), g, six_g);
+        const BlockScale bs = nvfp4_block_scale(hmax_u16x2(m), ts.enc, rtab);
         if (ok) {
             uint8_t *dst = q + (strip << 4) * (K >> 1) + (col >> 1);
 #pragma unroll

@@ -159,9 +159,10 @@ fq_status nvfp4_amax(const void *x, int64_t n, float *amax, void *stream);
  *   sb       : uint8 [M, K/16]  E4M3 block scales (output)
  *   g        : float in device memory, per-tensor decode scale (output)
  * With all arithmetic in IEEE binary32, one rounding per operation:
- *   g = amax / 2688 (g = 1 if amax == 0);  per block: t = amax_blk / (6 g),
- *   b = E4M3(t), r = min(1 / (b g), FLT_MAX) (r = 0 if b == 0),
- *   element code = E2M1(|x| * r) with the sign of x.  Decode: x ~ v * b * g.
+ *   g = amax / 2688 (g = 1 if amax == 0), enc = 1 / (6 g);  per block:
+ *   t = amax_blk * enc, b = E4M3(t), r = min(1 / (b g), FLT_MAX) (r = 0 if
+ *   b == 0), element code = E2M1(|x| * r) with the sign of x.
+ *   Decode: x ~ v * b * g.
  * use_sr = 0: round to nearest even.  use_sr = 1: stochastic rounding --
  *   with lo <= y < hi on the grid, round up iff R < floor(2^16 (y-lo)/(hi-lo));
  *   R is 16 bits of Philox4x32-10 with key (seed low, seed high word) and

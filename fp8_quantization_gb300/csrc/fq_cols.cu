@@ -113,6 +113,41 @@ __device__ int load_groups(const int64_t *__restrict__ offs, int32_t G, int32_t 
                            int32_t *base, int32_t *warp_tot)
 {
     const int tid = threadIdx.x;
+    if (G < 32) {
+        // one warp: clamp, max-scan and sum-scan with shuffles (G + 1 <= 32)
+        int bad = 0;
+        if (tid < 32) {
+            const int lane = tid;
+            int64_t o = lane <= G ? offs[lane] : M;
+            const int64_t prev = lane >= 1 && lane <= G ? offs[lane - 1] : 0;
+            const int64_t c = o < 0 ? 0 : (o > M ? M : o);
+            bad = lane <= G && (c != o || (lane == 0 && o != 0) || (lane == G && o != M) ||
+                                (lane > 0 && o < prev));
+            int32_t v = static_cast<int32_t>(c);
+            for (int d = 1; d < 32; d <<= 1) {
+                const int32_t u = __shfl_up_sync(0xffffffffu, v, d);
+                if (lane >= d)
+                    v = max(v, u);
+            }
+            if (lane == 0)
+                v = 0;
+            if (lane == G)
+                v = M;
+            const int32_t below = __shfl_up_sync(0xffffffffu, v, 1);
+            int32_t nb = lane >= 1 && lane <= G ? (v - below + kTok - 1) / kTok : 0;
+            for (int d = 1; d < 32; d <<= 1) {
+                const int32_t u = __shfl_up_sync(0xffffffffu, nb, d);
+                if (lane >= d)
+                    nb += u;
+            }
+            if (lane <= G) {
+                off[lane] = v;
+                base[lane] = nb;
+            }
+            bad = __any_sync(0xffffffffu, bad);
+        }
+        return __syncthreads_or(bad);
+    }
     int bad = 0;
     for (int i = tid; i <= G; i += kThreads) {
         const int64_t o = offs[i];
@@ -172,6 +207,7 @@ __global__ void __launch_bounds__(kThreads) fp4_to_fp8_cols_scales_kernel(
     extern __shared__ int32_t dyn[];
     int32_t *off = dyn, *base = dyn + G + 1;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    griddep_launch_dependents();  // the convert pass may start its set-up now
     const int bad = load_groups(offs, G, M, off, base, warp_tot);
     if (bad && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0 && dev_status)
         atomicOr(dev_status, 1);
@@ -262,6 +298,9 @@ __global__ void __launch_bounds__(kThreads, 4) fp4_to_fp8_cols_kernel(
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     build_fp8_table(tab);
     load_groups(offs, G, M, off, base, warp_tot);
+    // everything above reads only kernel arguments; the codes, exponents and
+    // block scales below come from earlier kernels on the stream
+    griddep_wait();
 
     const int32_t nwin = (M + kTok - 1) / kTok;
     const int32_t nfeat = static_cast<int32_t>(K / 128);
@@ -471,16 +510,20 @@ extern "C" fq_status fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
                                  static_cast<int>(dyn)) != cudaSuccess)
             return launch_status();
         const int grid = persistent_grid(fp4_to_fp8_cols_kernel<true>, kThreads, dyn, work_ctas);
-        fp4_to_fp8_cols_kernel<true><<<grid, kThreads, dyn, st>>>(
-            q, s, static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT, yT_scale, cap);
+        if (launch_pdl(fp4_to_fp8_cols_kernel<true>, dim3(grid), dim3(kThreads), dyn, st, q, s,
+                       static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT,
+                       static_cast<const float *>(yT_scale), cap) != cudaSuccess)
+            return launch_status();
     } else {
         if (cudaFuncSetAttribute(fp4_to_fp8_cols_kernel<false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(dyn)) != cudaSuccess)
             return launch_status();
         const int grid = persistent_grid(fp4_to_fp8_cols_kernel<false>, kThreads, dyn, work_ctas);
-        fp4_to_fp8_cols_kernel<false><<<grid, kThreads, dyn, st>>>(
-            q, s, static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT, yT_scale, cap);
+        if (launch_pdl(fp4_to_fp8_cols_kernel<false>, dim3(grid), dim3(kThreads), dyn, st, q, s,
+                       static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT,
+                       static_cast<const float *>(yT_scale), cap) != cudaSuccess)
+            return launch_status();
     }
     return launch_status();
 }

@@ -38,6 +38,25 @@ inline fq_status launch_status()
     return FQ_OK;
 }
 
+// Launch with programmatic stream serialization (the kernel may start while
+// the previous one on the stream finishes; it synchronises with griddep_wait).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Persistent grid: enough CTAs to fill every SM at the kernel's occupancy,
 // never more than there is work for.
 template <typename Kernel>
@@ -201,6 +220,18 @@ __device__ __forceinline__ uint32_t fp8_block_scale_exponent(uint32_t bits, int 
         return 0xFFu;
     const int ex = (bits >> 23) ? static_cast<int>(bits >> 23) : (31 - __clz(bits)) - 22;
     return static_cast<uint32_t>(ex + k);
+}
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel on the stream is still
+// running; it must read nothing that kernel writes, and write nothing,
+// before griddep_wait() returns (a hardware wait for that grid's
+// completion; a no-op for a normal launch).  griddep_launch_dependents()
+// lets the next such kernel start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Philox4x32-10 (Salmon et al., SC'11).

@@ -164,11 +164,14 @@ fq_status nvfp4_amax(const void *x, int64_t n, float *amax, void *stream);
  *   b == 0), element code = E2M1(|x| * r) with the sign of x.
  *   Decode: x ~ v * b * g.
  * use_sr = 0: round to nearest even.  use_sr = 1: stochastic rounding --
- *   with lo <= y < hi on the grid, round up iff R < floor(2^16 (y-lo)/(hi-lo));
- *   R is 16 bits of Philox4x32-10 with key (seed low, seed high word) and
- *   counter (c low, c high, 0, 0), c = (offset + i) / 8, i the row-major
- *   element index; output word ((offset + i) mod 8) / 2, low half for even
- *   and high half for odd offset + i.  `offset` lets row shards of one tensor
+ *   with lo <= y < hi the neighbouring grid points and
+ *   F = floor(2^16 (y - lo) / (hi - lo)), round up iff F + R >= 2^16, R a
+ *   16-bit random number.  Element j = offset + i (i its row-major index in
+ *   this call) takes R from W = output word (j / 4) mod 4 of Philox4x32-10
+ *   with key (seed low word, seed high word) and counter (c low word, c high
+ *   word, 0, 0), c = j / 16: with P = W[23:16] * 256 + W[7:0] and
+ *   Q = W[31:24] * 256 + W[15:8], elements j mod 4 = 0, 1, 2, 3 use P,
+ *   bitrev16(P), Q, bitrev16(Q).  `offset` lets row shards of one tensor
  *   reproduce the unsharded stream; it must be a multiple of 16.
  * Requires K > 0, K % 16 == 0, M >= 0.
  */

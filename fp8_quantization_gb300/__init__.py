@@ -40,6 +40,7 @@ SIGNATURES = {
     "mxfp4_quantize_rows": (_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
     "fp4_to_fp8_rows": (_int, [_vp, _vp, _i64, _i64, _int, _vp, _vp, _vp]),
     "fp4_to_fp8_cols_scale_capacity": (_i64, [_i64, _i32]),
+    "fp4_to_fp8_cols_launch_count": (_int, [_i64]),
     "fp4_to_fp8_cols": (_int, [_vp, _vp, _i64, _i64, _vp, _i32, _int, _vp, _vp, _i64, _vp, _vp]),
     "nvfp4_amax": (_int, [_vp, _i64, _vp, _vp]),
     "nvfp4_quantize": (_int, [_vp, _i64, _i64, _vp, _int, _u64, _u64, _vp, _vp, _vp, _vp]),
@@ -151,6 +152,10 @@ def fp4_to_fp8_rows(q: torch.Tensor, s: torch.Tensor, exp_offset_k: int = 0,
 
 def fp4_to_fp8_cols_scale_capacity(M: int, G: int) -> int:
     return int(abi().fp4_to_fp8_cols_scale_capacity(int(M), int(G)))
+
+
+def fp4_to_fp8_cols_launch_count(K: int) -> int:
+    return int(abi().fp4_to_fp8_cols_launch_count(int(K)))
 
 
 def fp4_to_fp8_cols(q: torch.Tensor, s: torch.Tensor, group_offsets: torch.Tensor,

@@ -2,6 +2,8 @@
 // version, and the per-device SM count used to size persistent grids.
 #include <atomic>
 
+#include <cudaTypedefs.h>
+
 #include "fq_common.cuh"
 
 namespace fq {
@@ -27,6 +29,41 @@ int sm_count()
         g_sm_count[dev].store(n, std::memory_order_relaxed);
     }
     return n;
+}
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static std::atomic<void *> fn{nullptr};
+    static std::atomic<int> looked_up{0};
+    if (!looked_up.load(std::memory_order_acquire)) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        fn.store(p, std::memory_order_relaxed);
+        looked_up.store(1, std::memory_order_release);
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn.load(std::memory_order_relaxed));
+}
+}  // namespace
+
+bool encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                             uint64_t row_pitch, uint32_t box_inner, uint32_t box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {row_pitch};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+               elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace fq

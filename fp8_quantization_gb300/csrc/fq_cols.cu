@@ -26,12 +26,15 @@ namespace fq {
 
 constexpr int kTok = 128;  // tokens per block / per tile
 // FP8 tile: 32 token-quads x 32 feature-words; the 16-byte slot holding
-// (four tokens) x (one feature word) is slot_index(quad, m).  Skew: odd quad
-// stride 45, +quad/4, +2*(m/8) -- conflict-free both for the conversion
-// stores (2 quads x 4 column blocks x 4 tokens per warp) and for the 128-bit
-// transposed reads (8 quads 4 apart per quarter warp).
-constexpr int kQuadStride = 45;
-constexpr int kTileSlots = (kTok / 4) * kQuadStride;
+// (four tokens) x (one feature word) is slot_index(quad, m).  Within a quad
+// the slots of an 8-word octet are consecutive (+2 between octets); the quad
+// stride 39 = -1 (mod 8) plus quad/4 makes the slot's bank group
+// (slot mod 8) = m + 2*(m/8) - quad + quad/4 (mod 8), which is
+// conflict-free both for the conversion stores (2 quads x 4 column blocks x
+// 4 tokens per warp) and for the 128-bit transposed reads (8 quads 4 apart
+// per quarter warp: -3c distinct for c = 0..7).
+constexpr int kQuadStride = 39;
+constexpr int kTileSlots = (kTok / 4 - 1) * kQuadStride + (kTok / 4 - 1) / 4 + 38;  // 1254
 constexpr int kTileWords = kTileSlots * 4;
 
 __device__ __forceinline__ int slot_index(int quad, int m)
@@ -264,6 +267,70 @@ __global__ void __launch_bounds__(kThreads) fp4_to_fp8_cols_scales_kernel(
     }
 }
 
+// ---------------------------------------------------------------- shared by both paths
+
+// One unit: the 32 codes of token tl in MX column j (16 bytes) -> 32 E4M3
+// bytes into the FP8 tile, for the block's aligned exponent S and the
+// token's own exponent e.
+__device__ __forceinline__ void convert_unit(uint32_t *tile, const uint8_t *tab, int tl, int j,
+                                             uint4 qv, uint32_t S, uint32_t e, int k)
+{
+    int u = static_cast<int>(S - e) - k + 6;
+    u = min(max(u, 0), kShiftRows - 1);  // u >= 0: S is the max over the block
+    const bool nan = S == 0xFFu;
+    const uint2 t = *reinterpret_cast<const uint2 *>(tab + 8 * (nan ? kNanRow : u));
+    const uint32_t smask = nan ? 0u : 0x80808080u;
+    uint32_t o[8];
+    fp4x8_to_fp8x8(qv.x, t.x, t.y, o[0], o[1], smask);
+    fp4x8_to_fp8x8(qv.y, t.x, t.y, o[2], o[3], smask);
+    fp4x8_to_fp8x8(qv.z, t.x, t.y, o[4], o[5], smask);
+    fp4x8_to_fp8x8(qv.w, t.x, t.y, o[6], o[7], smask);
+    uint32_t *dst = tile + 4 * slot_index(tl >> 2, 8 * j) + (tl & 3);
+#pragma unroll
+    for (int w = 0; w < 8; w++)
+        dst[4 * w] = o[w];
+}
+
+// Write-out of a converted tile (window W, feature block f): warp w handles
+// feature words 4w..4w+3 (m_out), lane%8 tokens 16c..16c+15 (c_out); each
+// 16-byte store of a quarter warp fills one 128-byte output line.
+template <bool kAligned16>
+__device__ __forceinline__ void write_tile(const uint32_t *tile, uint8_t *__restrict__ yT,
+                                           int32_t M, int32_t W, int32_t f, int m_out, int c_out)
+{
+    uint32_t rows[4][4];
+#pragma unroll
+    for (int qq = 0; qq < 4; qq++) {
+        const uint4 v =
+            *reinterpret_cast<const uint4 *>(tile + 4 * slot_index(4 * c_out + qq, m_out));
+        transpose4x4(v, rows[0][qq], rows[1][qq], rows[2][qq], rows[3][qq]);
+    }
+    const int32_t t0 = W + 16 * c_out;
+    uint8_t *p = yT + (static_cast<int64_t>(f) * 128 + 4 * m_out) * M + t0;
+    if (kAligned16 && W + kTok <= M) {
+#pragma unroll
+        for (int rr = 0; rr < 4; rr++) {
+            __stcs(reinterpret_cast<uint4 *>(p),  // evict-first: yT is not re-read
+                   make_uint4(rows[rr][0], rows[rr][1], rows[rr][2], rows[rr][3]));
+            p += M;
+        }
+    } else {
+        const int32_t We = min(W + kTok, M);
+#pragma unroll
+        for (int rr = 0; rr < 4; rr++) {
+            if (kAligned16 && t0 + 16 <= We) {
+                __stcs(reinterpret_cast<uint4 *>(p),
+                       make_uint4(rows[rr][0], rows[rr][1], rows[rr][2], rows[rr][3]));
+            } else {
+                for (int b = 0; b < 16; b++)
+                    if (t0 + b < We)
+                        p[b] = static_cast<uint8_t>(rows[rr][b >> 2] >> (8 * (b & 3)));
+            }
+            p += M;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- launch 2: convert + transpose
 
 // Tile (W, f): tokens W..W+127 (W a multiple of 128) x features
@@ -348,24 +415,9 @@ __global__ void __launch_bounds__(kThreads, 4) fp4_to_fp8_cols_kernel(
         }
     };
 
-    // one unit: 32 codes -> 32 E4M3 bytes into the shared tile
     auto convert = [&](uint32_t *tile, int tl, uint4 qv, uint32_t ev, uint32_t sv) {
-        const uint32_t S = fp8_block_scale_exponent(sv, k);
-        const uint32_t e = (ev >> (8 * j)) & 0xFFu;
-        int u = static_cast<int>(S - e) - k + 6;
-        u = min(max(u, 0), kShiftRows - 1);  // u >= 0: S is the max over the block
-        const bool nan = S == 0xFFu;
-        const uint2 t = *reinterpret_cast<const uint2 *>(tab + 8 * (nan ? kNanRow : u));
-        const uint32_t smask = nan ? 0u : 0x80808080u;
-        uint32_t o[8];
-        fp4x8_to_fp8x8(qv.x, t.x, t.y, o[0], o[1], smask);
-        fp4x8_to_fp8x8(qv.y, t.x, t.y, o[2], o[3], smask);
-        fp4x8_to_fp8x8(qv.z, t.x, t.y, o[4], o[5], smask);
-        fp4x8_to_fp8x8(qv.w, t.x, t.y, o[6], o[7], smask);
-        uint32_t *dst = tile + 4 * slot_index(tl >> 2, 8 * j) + (tl & 3);
-#pragma unroll
-        for (int w = 0; w < 8; w++)
-            dst[4 * w] = o[w];
+        convert_unit(tile, tab, tl, j, qv, fp8_block_scale_exponent(sv, k), (ev >> (8 * j)) & 0xFFu,
+                     k);
     };
 
     auto process = [&](int32_t win, int32_t f, const ColsPrefetch &P, uint32_t *tile) {
@@ -381,37 +433,7 @@ __global__ void __launch_bounds__(kThreads, 4) fp4_to_fp8_cols_kernel(
                 convert(tile, tl0 + 64, P.q1, P.e1, P.s1);
         }
         __syncthreads();
-        uint32_t rows[4][4];
-#pragma unroll
-        for (int qq = 0; qq < 4; qq++) {
-            const uint4 v =
-                *reinterpret_cast<const uint4 *>(tile + 4 * slot_index(4 * c_out + qq, m_out));
-            transpose4x4(v, rows[0][qq], rows[1][qq], rows[2][qq], rows[3][qq]);
-        }
-        const int32_t t0 = W + 16 * c_out;
-        uint8_t *p = yT + (static_cast<int64_t>(f) * 128 + 4 * m_out) * M + t0;
-        if (kAligned16 && full) {
-#pragma unroll
-            for (int rr = 0; rr < 4; rr++) {
-                __stcs(reinterpret_cast<uint4 *>(p),  // evict-first: yT is not re-read
-                       make_uint4(rows[rr][0], rows[rr][1], rows[rr][2], rows[rr][3]));
-                p += M;
-            }
-        } else {
-            const int32_t We = min(W + kTok, M);
-#pragma unroll
-            for (int rr = 0; rr < 4; rr++) {
-                if (kAligned16 && t0 + 16 <= We) {
-                    __stcs(reinterpret_cast<uint4 *>(p),
-                           make_uint4(rows[rr][0], rows[rr][1], rows[rr][2], rows[rr][3]));
-                } else {
-                    for (int b = 0; b < 16; b++)
-                        if (t0 + b < We)
-                            p[b] = static_cast<uint8_t>(rows[rr][b >> 2] >> (8 * (b & 3)));
-                }
-                p += M;
-            }
-        }
+        write_tile<kAligned16>(tile, yT, M, W, f, m_out, c_out);
     };
 
     int32_t tau = blockIdx.x;
@@ -455,6 +477,337 @@ __global__ void __launch_bounds__(kThreads, 4) fp4_to_fp8_cols_kernel(
     }
 }
 
+// ---------------------------------------------------------------- single pass (K % 512 == 0)
+
+// One launch, no block-scale pass, warp-specialised.  Work unit: the
+// super-tile (128-token window W) x (feature blocks 4F .. 4F+3), whose four
+// 128 x 128 tiles are converted one after the other; super-tiles are walked
+// window fastest by persistent CTAs.  One 16-byte exponent row per token
+// holds the UE8M0 exponents of all 16 MX columns of a super-tile, so its
+// block maxima are found once for four tiles.
+//  * The producer warp (warp 8) issues tensor-memory-access copies into
+//    shared memory: each tile's 128 x 64-byte codes into a ring of kStages
+//    code stages, and each super-tile's exponent rows of tokens
+//    W-128 .. W+255 (three 128-row copies; rows outside the tensor read as
+//    zero) into a ring of two exponent buffers.  Three tiles before a
+//    super-tile starts it computes its block maxima: the 128-token blocks
+//    meeting the window are numbered consecutively; the byte-wise max of a
+//    block's exponent rows (up to 127 tokens beyond the window on either
+//    side come from the neighbouring rows) gives S for the 16 MX columns,
+//    stored per token of the window, with the blocks whose first token lies
+//    in the window.  The first super-tile's maxima are computed by all nine
+//    warps at once.
+//  * The eight converting warps wait for a tile's codes (and, on a
+//    super-tile's first tile, for its maxima), write the FP32 scales of the
+//    blocks that start in the window (one feature row per thread), convert
+//    into the FP8 tile as in the two-launch path once every warp has
+//    written the previous tile out (named barrier), release the code stage
+//    (and, after the fourth tile, the exponent buffer), meet at a second
+//    named barrier and write the tile out transposed.
+// Every wait is bounded (mbar_wait); a wait that gives up ends the kernel
+// with bit 2 of *dev_status set.
+constexpr int kStages = 4;      // code stages
+constexpr int kExpBufs = 2;     // exponent buffers (super-tiles in flight)
+constexpr int kConvWarps = kThreads / 32;
+constexpr int kThreads1p = kThreads + 32;
+constexpr int kCodeBytes = kTok * 64;
+constexpr int kExpRowBytes = 16;
+constexpr int kExpBytes = 3 * kTok * kExpRowBytes;
+constexpr int kSmemAlign = 128;  // tensor-copy destinations
+static_assert(kCodeBytes % kSmemAlign == 0 && kExpBytes % kSmemAlign == 0, "aligned buffers");
+
+// per exponent buffer: S of every token (uint4) and the blocks that start in
+// the window (count, then (token, block) pairs)
+constexpr int kStartWords = 1 + 2 * kTok;
+
+inline size_t cols1_dyn_bytes(int32_t G)
+{
+    return kSmemAlign + static_cast<size_t>(kStages) * kCodeBytes +
+           static_cast<size_t>(kExpBufs) *
+               (kExpBytes + kTok * sizeof(uint4) + kStartWords * sizeof(int32_t)) +
+           kTileWords * sizeof(uint32_t) + static_cast<size_t>(G + 1) * 2 * sizeof(int32_t);
+}
+
+template <bool kAligned16>
+__global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
+    int32_t M, int32_t nfeat, const int64_t *__restrict__ offs, int32_t G, int k,
+    uint8_t *__restrict__ yT, float *__restrict__ yTs, int64_t cap,
+    int32_t *__restrict__ dev_status)
+{
+    __shared__ __align__(16) uint8_t tab[kTabRows * 8];
+    __shared__ int32_t warp_tot[kThreads1p / 32];
+    __shared__ __align__(8) uint64_t full_c[kStages];    // code copies landed
+    __shared__ __align__(8) uint64_t empty_c[kStages];   // code stage read by every converting warp
+    __shared__ __align__(8) uint64_t full_e[kExpBufs];   // exponent copies landed
+    __shared__ __align__(8) uint64_t sready[kExpBufs];   // block maxima written
+    __shared__ __align__(8) uint64_t empty_e[kExpBufs];  // exponents and maxima no longer read
+    extern __shared__ __align__(16) uint8_t dyn_raw[];
+    uint8_t *codes_ring = dyn_raw + ((kSmemAlign - (smem_u32(dyn_raw) & (kSmemAlign - 1))) &
+                                     (kSmemAlign - 1));
+    uint8_t *exp_ring = codes_ring + kStages * kCodeBytes;
+    uint4 *Sring = reinterpret_cast<uint4 *>(exp_ring + kExpBufs * kExpBytes);  // [kExpBufs][kTok]
+    uint32_t *tile = reinterpret_cast<uint32_t *>(Sring + kExpBufs * kTok);    // [kTileWords]
+    int32_t *starts = reinterpret_cast<int32_t *>(tile + kTileWords);         // [kExpBufs][kStartWords]
+    int32_t *off = starts + kExpBufs * kStartWords;                           // [G + 1]
+    int32_t *base = off + G + 1;                                              // [G + 1]
+
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int32_t nwin = (M + kTok - 1) / kTok;
+    const int32_t nquad = nfeat >> 2;
+    const int32_t nsuper = nwin * nquad;  // < 2^29, checked on the host
+    const int32_t grid = static_cast<int32_t>(gridDim.x);
+    // super-tiles of this CTA: blockIdx.x + m * grid, m < my_super
+    const int32_t my_super = (nsuper - static_cast<int32_t>(blockIdx.x) + grid - 1) / grid;
+    const int32_t my_tiles = 4 * my_super;
+    if (tid == 0) {
+        for (int i = 0; i < kStages; i++) {
+            mbar_init(&full_c[i], 1);
+            mbar_init(&empty_c[i], kConvWarps);
+        }
+        for (int i = 0; i < kExpBufs; i++) {
+            mbar_init(&full_e[i], 1);
+            mbar_init(&sready[i], 1);
+            mbar_init(&empty_e[i], kConvWarps);
+        }
+        mbar_init_fence();
+    }
+    build_fp8_table(tab);
+    griddep_wait();  // offsets, codes and exponents may come from the previous kernel
+    const int bad = load_groups(offs, G, M, off, base, warp_tot);  // ends with a CTA barrier
+    if (bad && blockIdx.x == 0 && tid == 0 && dev_status)
+        atomicOr(dev_status, 1);
+
+    auto super_xy = [&](int32_t m, int32_t &W, int32_t &F) {
+        const int32_t sg = static_cast<int32_t>(blockIdx.x) + m * grid;
+        W = (sg % nwin) * kTok;
+        F = sg / nwin;
+    };
+    // block maxima of super-tile m: warp w0 takes the blocks w0, w0 + wstep, ...
+    auto maxima = [&](int32_t m, int w0, int wstep) {
+        int32_t W, F;
+        super_xy(m, W, F);
+        const int bf = m % kExpBufs;
+        const uint4 *ex = reinterpret_cast<const uint4 *>(exp_ring + bf * kExpBytes);
+        uint4 *S_of = Sring + bf * kTok;
+        int32_t *st_list = starts + bf * kStartWords;
+        const int32_t We = min(W + kTok, M);
+        const int gW = warp_find_last_le(off, G, W);
+        const int32_t blkW = base[gW] + ((W - off[gW]) >> 7);
+        const int gL = warp_find_last_le(off, G, We - 1);
+        const int32_t nbw = base[gL] + ((We - 1 - off[gL]) >> 7) - blkW + 1;  // <= 128
+        if (w0 == 0 && lane == 0)
+            st_list[0] = nbw;
+        int g = gW;
+        for (int32_t jb = w0; jb < nbw; jb += wstep) {
+            const int32_t b = blkW + jb;
+            while (base[g + 1] <= b)  // group of block b (skips empty groups)
+                g++;
+            const int32_t bs = off[g] + ((b - base[g]) << 7);
+            const int32_t be = min(bs + kTok, off[g + 1]);  // W-127 <= bs, be <= W+255
+            uint4 m4 = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const int32_t t = bs + lane + 32 * u;
+                if (t < be) {
+                    const uint4 v = ex[t - W + kTok];
+                    m4.x = bytemax4(m4.x, v.x);
+                    m4.y = bytemax4(m4.y, v.y);
+                    m4.z = bytemax4(m4.z, v.z);
+                    m4.w = bytemax4(m4.w, v.w);
+                }
+            }
+            auto wmax = [](uint32_t w) {
+                return __reduce_max_sync(0xffffffffu, w & 0xFFu) |
+                       (__reduce_max_sync(0xffffffffu, (w >> 8) & 0xFFu) << 8) |
+                       (__reduce_max_sync(0xffffffffu, (w >> 16) & 0xFFu) << 16) |
+                       (__reduce_max_sync(0xffffffffu, w >> 24) << 24);
+            };
+            const uint4 S = make_uint4(wmax(m4.x), wmax(m4.y), wmax(m4.z), wmax(m4.w));
+            for (int32_t t = max(bs, W) + lane; t < min(be, We); t += 32)
+                S_of[t - W] = S;
+            if (lane == 0) {  // blocks that start here get their scales written
+                st_list[1 + 2 * jb] = bs >= W ? bs - W : -1;
+                st_list[2 + 2 * jb] = b;
+            }
+        }
+    };
+    auto issue_exps = [&](int32_t m) {  // one thread: super-tile m of this CTA
+        int32_t W, F;
+        super_xy(m, W, F);
+        const int bf = m % kExpBufs;
+        uint8_t *dst = exp_ring + bf * kExpBytes;
+        mbar_arrive_expect_tx(&full_e[bf], kExpBytes);
+#pragma unroll
+        for (int h = 0; h < 3; h++)
+            tma_load_2d(dst + h * kTok * kExpRowBytes, &tm_s, 16 * F, W + (h - 1) * kTok,
+                        &full_e[bf]);
+    };
+    auto issue_codes = [&](int32_t n) {  // one thread: tile n of this CTA
+        int32_t W, F;
+        super_xy(n >> 2, W, F);
+        const int st = n % kStages;
+        mbar_arrive_expect_tx(&full_c[st], kCodeBytes);
+        tma_load_2d(codes_ring + st * kCodeBytes, &tm_q, 64 * (4 * F + (n & 3)), W, &full_c[st]);
+    };
+
+    // ---- super-tile 0: copies, then its maxima with every warp
+    if (tid == kThreads) {
+        issue_exps(0);
+        for (int32_t n = 0; n < kStages - 1 && n < my_tiles; n++)
+            issue_codes(n);
+    }
+    const bool ok0 = !__syncthreads_or(!mbar_wait(&full_e[0], 0));
+    if (ok0)
+        maxima(0, wid, kThreads1p / 32);
+    __syncthreads();
+
+    if (wid == kConvWarps) {
+        // ================================================= producer warp
+        bool ok = ok0;
+        int32_t issued_c = min(kStages - 1, my_tiles), issued_e = 1;  // copies issued
+        int32_t waited_e = ok0 ? 1 : 0;  // exponent copies waited for
+        if (ok0 && lane == 0)
+            mbar_arrive(&sready[0]);
+        for (int32_t n = 0; ok && n < my_tiles; n++) {
+            // refill: codes of tile n + kStages - 1 into the stage of tile n - 1
+            const int32_t nn = n + kStages - 1;
+            if (nn < my_tiles) {
+                if (n >= 1) {
+                    const int32_t p = n - 1;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&empty_c[p % kStages],
+                                                           static_cast<uint32_t>(p / kStages) & 1u));
+                    if (!ok)
+                        break;
+                }
+                if (lane == 0)
+                    issue_codes(nn);
+                issued_c++;
+            }
+            // first tile of super-tile m - 1: the exponent copies of super-tile
+            // m (into the buffer super-tile m - 2 released); one tile later,
+            // three tiles before super-tile m starts, its maxima
+            if ((n & 3) == 0 && (n >> 2) + 1 < my_super) {
+                const int32_t m = (n >> 2) + 1;
+                const int32_t p = m - kExpBufs;  // last user of the buffer
+                if (p >= 0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&empty_e[p % kExpBufs],
+                                                           static_cast<uint32_t>(p / kExpBufs) & 1u));
+                    if (!ok)
+                        break;
+                }
+                if (lane == 0)
+                    issue_exps(m);
+                issued_e++;
+            }
+            if ((n & 3) == 1) {
+                const int32_t m = (n >> 2) + 1;
+                if (m < my_super) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&full_e[m % kExpBufs],
+                                                           static_cast<uint32_t>(m / kExpBufs) & 1u));
+                    if (!ok)
+                        break;
+                    waited_e = m + 1;
+                    maxima(m, 0, 1);
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&sready[m % kExpBufs]);
+                }
+            }
+        }
+        // every code copy issued is waited for by the converting warps and
+        // every exponent copy by this warp; if a wait gave up, report and
+        // wait (bounded) for the copies still in flight before the CTA's
+        // shared memory is released
+        if (!ok) {
+            if (lane == 0 && dev_status)
+                atomicOr(dev_status, 2);
+            for (int32_t m = waited_e; m < issued_e; m++)
+                mbar_wait(&full_e[m % kExpBufs], static_cast<uint32_t>(m / kExpBufs) & 1u);
+            for (int32_t n = 0; n < issued_c; n++)
+                mbar_wait(&full_c[n % kStages], static_cast<uint32_t>(n / kStages) & 1u);
+        }
+        return;
+    }
+
+    // ===================================================== converting warps
+    if (!ok0)
+        return;  // the producer reports it
+    const int j = tid & 3;     // MX column of both units
+    const int tl0 = tid >> 2;  // token of unit 0 (unit 1: tl0 + 64)
+    const int m_out = 4 * wid + (lane >> 3);
+    const int c_out = lane & 7;
+    const int32_t sg0 = blockIdx.x;  // first super-tile
+    int32_t win = sg0 % nwin, F = sg0 / nwin;
+    const int32_t step_w = grid % nwin, step_F = grid / nwin;
+    int st = 0, bf = 0;
+    uint32_t ph_c = 0, ph_e = 0;
+    for (int32_t n = 0; n < my_tiles; n++) {
+        const int i = n & 3;  // tile within the super-tile
+        const int32_t W = win * kTok, f = 4 * F + i;
+        const bool ok = mbar_wait(&full_c[st], ph_c) &&
+                        (i != 0 || (mbar_wait(&sready[bf], ph_e) && mbar_wait(&full_e[bf], ph_e)));
+        if (n > 0)
+            named_barrier_or(1, kThreads, false);  // the previous tile has been written out
+        if (ok && tid < kTok) {
+            // scales of the blocks that start in this window: feature row
+            // 128f + tid, MX column tid / 32
+            const int32_t *st_list = starts + bf * kStartWords;
+            const int32_t ns = st_list[0];
+            const uint32_t *S_w = reinterpret_cast<const uint32_t *>(Sring + bf * kTok);
+            uint32_t *dst = reinterpret_cast<uint32_t *>(yTs) +
+                            (static_cast<int64_t>(f) * 128 + tid) * cap;
+            for (int32_t q = 0; q < ns; q++) {
+                const int32_t tb = st_list[1 + 2 * q];
+                if (tb < 0)
+                    continue;
+                const uint32_t Sb = (S_w[tb * 4 + i] >> (8 * (tid >> 5))) & 0xFFu;
+                dst[st_list[2 + 2 * q]] = fp8_block_scale_bits(Sb, k);
+            }
+        }
+        if (ok) {
+            const uint4 *codes = reinterpret_cast<const uint4 *>(codes_ring + st * kCodeBytes);
+            const uint32_t *ex = reinterpret_cast<const uint32_t *>(exp_ring + bf * kExpBytes);
+            const uint32_t *S_of = reinterpret_cast<const uint32_t *>(Sring + bf * kTok);
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const int tl = tl0 + 64 * h;
+                if (W + tl < M) {
+                    const uint32_t S = (S_of[tl * 4 + i] >> (8 * j)) & 0xFFu;
+                    const uint32_t e = (ex[(kTok + tl) * 4 + i] >> (8 * j)) & 0xFFu;
+                    convert_unit(tile, tab, tl, j, codes[tl * 4 + j], S, e, k);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&empty_c[st]);  // this warp is done with the code stage
+            if (i == 3)
+                mbar_arrive(&empty_e[bf]);  // ... and with the super-tile's exponents
+        }
+        if (named_barrier_or(1, kThreads, !ok))
+            break;  // the producer reports it
+        write_tile<kAligned16>(tile, yT, M, W, f, m_out, c_out);
+
+        if (++st == kStages) {
+            st = 0;
+            ph_c ^= 1;
+        }
+        if (i == 3) {
+            win += step_w;
+            F += step_F;
+            if (win >= nwin) {
+                win -= nwin;
+                F++;
+            }
+            if (++bf == kExpBufs) {
+                bf = 0;
+                ph_e ^= 1;
+            }
+        }
+    }
+}
+
 }  // namespace fq
 
 using namespace fq;
@@ -464,6 +817,25 @@ extern "C" int64_t fp4_to_fp8_cols_scale_capacity(int64_t M, int32_t G)
     if (M < 0 || G < 1)
         return -1;
     return (M + 127) / 128 + G;
+}
+
+namespace {
+bool single_pass_ok(int64_t K)
+{
+    if (K % 512 != 0)
+        return false;
+    CUtensorMap probe;  // encoding touches no memory: a dummy 16-byte aligned base
+    return encode_tensor_map_2d_u8(&probe, reinterpret_cast<const void *>(uintptr_t{256}),
+                                   static_cast<uint64_t>(K / 32), 1, static_cast<uint64_t>(K / 32),
+                                   kExpRowBytes, kTok);
+}
+}  // namespace
+
+extern "C" int fp4_to_fp8_cols_launch_count(int64_t K)
+{
+    if (K <= 0 || K % 128 != 0)
+        return 0;
+    return single_pass_ok(K) ? 1 : 2;
 }
 
 extern "C" fq_status fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t M, int64_t K,
@@ -490,6 +862,30 @@ extern "C" fq_status fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
         return FQ_ERR_ALIGN;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t groups_bytes = static_cast<size_t>(G + 1) * 2 * sizeof(int32_t);
+    const int64_t work_ctas = ((M + 127) / 128) * (K / 128);
+
+    // single pass: exponent rows of K/32 bytes are a multiple of 16 bytes
+    CUtensorMap tm_q, tm_s;
+    if (K % 512 == 0 &&
+        encode_tensor_map_2d_u8(&tm_q, q, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(M),
+                                static_cast<uint64_t>(K / 2), 64, kTok) &&
+        encode_tensor_map_2d_u8(&tm_s, s, static_cast<uint64_t>(K / 32), static_cast<uint64_t>(M),
+                                static_cast<uint64_t>(K / 32), kExpRowBytes, kTok)) {
+        const size_t dyn = cols1_dyn_bytes(G);
+        auto kern = M % 16 == 0 ? fp4_to_fp8_cols_1pass_kernel<true>
+                                : fp4_to_fp8_cols_1pass_kernel<false>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(dyn)) != cudaSuccess ||
+            cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+            return launch_status();
+        const int grid = persistent_grid(kern, kThreads1p, dyn, work_ctas / 4);
+        if (launch_pdl(kern, dim3(grid), dim3(kThreads1p), dyn, st, tm_q, tm_s,
+                       static_cast<int32_t>(M), static_cast<int32_t>(K / 128), group_offsets, G,
+                       exp_offset_k, yT, yT_scale, cap, dev_status) != cudaSuccess)
+            return launch_status();
+        return launch_status();
+    }
 
     // launch 1: block scales, CTA per (exponent word, 32 blocks)
     const int64_t chunks = (cap + kScaleSlots - 1) / kScaleSlots;
@@ -503,7 +899,6 @@ extern "C" fq_status fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
 
     // launch 2: convert + transpose (two FP8 tiles + the group arrays)
     const size_t dyn = 2 * kTileWords * sizeof(uint32_t) + groups_bytes;
-    const int64_t work_ctas = ((M + 127) / 128) * (K / 128);
     if (M % 16 == 0) {
         if (cudaFuncSetAttribute(fp4_to_fp8_cols_kernel<true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -115,6 +115,12 @@ int64_t fp4_to_fp8_cols_scale_capacity(int64_t M, int32_t G);
 /* Largest group count accepted by fp4_to_fp8_cols. */
 #define FQ_COLS_MAX_GROUPS 1024
 
+/* Number of kernels fp4_to_fp8_cols enqueues for feature count K: 1 (a
+ * single pass that also computes the block scales) when K % 512 == 0 and the
+ * CUDA driver can encode tensor maps, else 2 (a block-scale pass, then the
+ * conversion); 0 for a K the conversion rejects.  Host only, no GPU work. */
+int fp4_to_fp8_cols_launch_count(int64_t K);
+
 /*
  * Direct FP4 -> FP8 conversion fused with the transpose, on ragged
  * per-expert token groups without padding ([MoE-FP4] 2.3, FP4RowToFP8Col;
@@ -130,7 +136,10 @@ int64_t fp4_to_fp8_cols_scale_capacity(int64_t M, int32_t G);
  *   cap           : >= fp4_to_fp8_cols_scale_capacity(M, G)
  *   dev_status    : optional int32 in device memory; if the offsets are
  *                   malformed the kernel clamps them (so nothing is written
- *                   out of bounds) and ORs 1 into *dev_status
+ *                   out of bounds) and ORs 1 into *dev_status; 2 is ORed in
+ *                   if a shared-memory copy of the single pass did not
+ *                   arrive within two seconds (the outputs are then
+ *                   incomplete; not expected to happen)
  * Each group is cut into 128-token blocks starting at its first token (the
  * last block of a group may be short).  For a block and a 32-feature MX
  * column, S = max of the tokens' exponents; each element is converted as in

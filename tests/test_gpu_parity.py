@@ -196,19 +196,35 @@ COLS_CASES = {
 }
 
 
+COLS_CASES["zipf32_k2048"] = (4096, 2048, lambda M: workloads.zipf_group_offsets(M, 32, 1.1, 8))
+COLS_CASES["g1_m_mult_16_k1536"] = (640, 1536, lambda M: np.array([0, M]))
+
+
+def cols_k(K, path):
+    """K of a case on one of the two paths: the single pass takes K % 512 == 0
+    (exponent rows a multiple of 16 bytes), the two-launch path the rest."""
+    if path == "single_pass":
+        return (K + 511) // 512 * 512
+    return K if K % 512 else K + 128
+
+
 @pytest.mark.parametrize("case", sorted(COLS_CASES))
 @pytest.mark.parametrize("k", [0, 6])
-def test_fp4_to_fp8_cols(fq, case, k):
+@pytest.mark.parametrize("path", ["single_pass", "two_launch"])
+def test_fp4_to_fp8_cols(fq, case, k, path):
     M, K, mk = COLS_CASES[case]
+    K = cols_k(K, path)
+    assert fq.fp4_to_fp8_cols_launch_count(K) == (1 if path == "single_pass" else 2)
     offs = np.asarray(mk(M), dtype=np.int64)
     q, s = rand_mx(M, K, seed=M * 7 + K + k, spread=16, nan_frac=0.002)
     run_cols(fq, q, s, offs, k)
 
 
-def test_fp4_to_fp8_cols_malformed_offsets(fq):
+@pytest.mark.parametrize("K", [256, 512])
+def test_fp4_to_fp8_cols_malformed_offsets(fq, K):
     # malformed offsets: clamped in-kernel, status raised, nothing written
     # outside the outputs (canaries checked inside run_cols)
-    M, K = 700, 256
+    M = 700
     q, s = rand_mx(M, K, seed=1)
     for offs in ([0, 800], [5, 300, 200, 700], [0, -40, 700], [0, 100, 699], [10, 20, 700]):
         _, _, st = run_cols(fq, q, s, np.array(offs, dtype=np.int64), 0, check=False)

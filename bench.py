@@ -80,9 +80,12 @@ def hbm_peak():
 
 
 def file_sha(name: str) -> str:
-    p = os.path.join(ROOT, "fp8_quantization_gb300", "csrc", name)
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256[:16] of a kernel's source file followed by the shared header."""
+    h = hashlib.sha256()
+    for part in (name, "fq_common.cuh"):
+        with open(os.path.join(ROOT, "fp8_quantization_gb300", "csrc", part), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel: str):

@@ -16,9 +16,14 @@ and shape of the workload it stands in for:
 * ``sweep``          Student-t(nu=3) rows x 7168 for the bandwidth sweep.
 
 All arrays are returned as BF16 bit patterns (``numpy.uint16``), row-major.
-BF16 rounding is round-to-nearest-even, done by ``torch`` on the host.
+BF16 rounding is round-to-nearest-even, done by ``torch`` on the host.  The
+Student-t generators draw blocks of rows from child seeds of one seed, in
+parallel threads, so that the largest sweep tensors take seconds.
 """
 from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import torch
@@ -67,9 +72,28 @@ def ragged_experts(M: int = 65536, K: int = 2048, G: int = 32, seed: int = 0):
     return bf16_bits(x), zipf_group_offsets(M, G, 1.1, seed)
 
 
+def _bf16_row_blocks(M: int, K: int, seed: int, draw) -> np.ndarray:
+    """BF16 bits [M, K]; rows c*R .. (c+1)*R - 1 (R rows of about 4M
+    elements) are draw(rng, shape) with rng seeded by the c-th child of
+    SeedSequence(seed).  A block's values do not depend on M."""
+    R = max(1, (1 << 22) // max(K, 1))
+    n = max(1, -(-M // R))
+    kids = np.random.SeedSequence(seed).spawn(n)
+    out = np.empty((M, K), dtype=np.uint16)
+
+    def work(c):
+        r0, r1 = c * R, min(M, (c + 1) * R)
+        if r1 > r0:
+            rng = np.random.default_rng(kids[c])
+            out[r0:r1] = bf16_bits(draw(rng, (r1 - r0, K)).astype(np.float32))
+
+    with ThreadPoolExecutor(max(1, min(n, os.cpu_count() or 1))) as ex:
+        list(ex.map(work, range(n)))
+    return out
+
+
 def nvfp4_act(M: int = 16384, K: int = 14336, seed: int = 0) -> np.ndarray:
-    rng = np.random.default_rng(seed)
-    return bf16_bits(rng.standard_t(4, (M, K)).astype(np.float32))
+    return _bf16_row_blocks(M, K, seed, lambda rng, shape: rng.standard_t(4, shape))
 
 
 def nvfp4_weight(N: int = 14336, K: int = 4096, seed: int = 0) -> np.ndarray:
@@ -78,8 +102,7 @@ def nvfp4_weight(N: int = 14336, K: int = 4096, seed: int = 0) -> np.ndarray:
 
 
 def sweep(M: int, K: int = 7168, seed: int = 0) -> np.ndarray:
-    rng = np.random.default_rng(seed)
-    return bf16_bits(rng.standard_t(3, (M, K)).astype(np.float32))
+    return _bf16_row_blocks(M, K, seed, lambda rng, shape: rng.standard_t(3, shape))
 
 
 def random_group_offsets(M: int, G: int, seed: int = 0, empty_frac: float = 0.2) -> np.ndarray:

@@ -1,0 +1,183 @@
+"""GPU parity at the workloads' full sizes, called the way the benchmark calls
+the library (one stream, caller-allocated outputs, the same entry points and
+arguments).
+
+Where the CPU oracle finishes in seconds every output byte is compared; for
+the largest bandwidth-sweep tensors the comparison runs on seeded samples the
+oracle computes on their own: whole rows for the row casts (rows are
+independent), whole 128-token windows for the transposed cast with one group
+(its blocks are then aligned to multiples of 128, so a window's output depends
+only on the window's tokens)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_quantization_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import fp8_quantization_gb300 as m
+    m.abi()
+    return m
+
+
+def dev_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def eq(gpu, ref, what):
+    got = gpu.contiguous().cpu().numpy() if isinstance(gpu, torch.Tensor) else np.asarray(gpu)
+    ref = np.ascontiguousarray(ref)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    a, b = got.view(np.uint8), ref.view(np.uint8)
+    if not np.array_equal(a, b):
+        idx = np.flatnonzero(a.ravel() != b.ravel())
+        raise AssertionError(f"{what}: {idx.size} bytes differ, first at {idx[:8].tolist()}")
+
+
+def cols_full(fq, q_d, s_d, offs, k):
+    M, K = q_d.shape[0], q_d.shape[1] * 2
+    G = offs.size - 1
+    cap = fq.fp4_to_fp8_cols_scale_capacity(M, G)
+    yT = torch.empty((K, M), dtype=torch.uint8, device="cuda")
+    yTs = torch.empty((K, cap), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fq.fp4_to_fp8_cols(q_d, s_d, torch.from_numpy(offs).cuda(), k, yT, yTs, st)
+    assert int(st.item()) == 0
+    return yT, yTs
+
+
+def test_moe_dispatch_16384x7168_all_casts(fq):
+    """The benchmark's workload and call sequence, every output compared."""
+    M, K, G = 16384, 7168, 32
+    bits = workloads.moe_dispatch(M, K, seed=0)
+    offs = workloads.zipf_group_offsets(M, G, 1.1, 0)
+    x = dev_bf16(bits)
+    q, s = fq.mxfp4_quantize_rows(x)
+    y, ys = fq.fp4_to_fp8_rows(q, s, 0)
+    yT, yTs = cols_full(fq, q, s, offs, 0)
+    amax = fq.nvfp4_amax(x)
+    q4, sb4, g4 = fq.nvfp4_quantize(x, amax, use_sr=True, seed=1000, offset=0)
+    q2, sb2, g2 = fq.nvfp4_quantize_2d(x, amax)
+
+    rq, rs = oracle.mxfp4_quantize_rows(bits)
+    eq(q, rq, "mxfp4 q")
+    eq(s, rs, "mxfp4 s")
+    ry, rys = oracle.fp4_to_fp8_rows(rq, rs, 0)
+    eq(y, ry, "fp8 rows y")
+    eq(ys, rys, "fp8 rows scales")
+    ryT, ryTs = oracle.fp4_to_fp8_cols(rq, rs, offs, 0)
+    nb = int(((np.diff(offs) + 127) // 128).sum())
+    eq(yT, ryT, "fp8 cols yT")
+    eq(yTs[:, :nb], ryTs[:, :nb], "fp8 cols scales")
+    ra = oracle.nvfp4_amax(bits)
+    assert amax.item() == float(ra)
+    rq4, rsb4, rg4 = oracle.nvfp4_quantize(bits, ra, use_sr=True, seed=1000, offset=0)
+    eq(q4, rq4, "nvfp4 SR q")
+    eq(sb4, rsb4, "nvfp4 SR scales")
+    assert g4.item() == float(rg4)
+    rq2, rsb2, rg2 = oracle.nvfp4_quantize_2d(bits, ra)
+    eq(q2, rq2, "nvfp4 2d q")
+    eq(sb2, rsb2, "nvfp4 2d scales")
+    assert g2.item() == float(rg2)
+
+
+@pytest.mark.parametrize("k", [0, 6])
+def test_ragged_experts_65536x2048(fq, k):
+    """Routed rows over 32 Zipf-sized experts: MXFP4 rows, then the
+    transposed conversion on the ragged groups, every output compared."""
+    bits, offs = workloads.ragged_experts(65536, 2048, 32, seed=0)
+    q, s = fq.mxfp4_quantize_rows(dev_bf16(bits))
+    yT, yTs = cols_full(fq, q, s, offs, k)
+    rq, rs = oracle.mxfp4_quantize_rows(bits)
+    eq(q, rq, "mxfp4 q")
+    eq(s, rs, "mxfp4 s")
+    ryT, ryTs = oracle.fp4_to_fp8_cols(rq, rs, offs, k)
+    nb = int(((np.diff(offs) + 127) // 128).sum())
+    eq(yT, ryT, "fp8 cols yT")
+    eq(yTs[:, :nb], ryTs[:, :nb], "fp8 cols scales")
+
+
+def test_nvfp4_activations_16384x14336(fq):
+    """Student-t(4) activations: amax, SR and RNE quantization, all compared."""
+    bits = workloads.nvfp4_act(16384, 14336, seed=0)
+    x = dev_bf16(bits)
+    amax = fq.nvfp4_amax(x)
+    ra = oracle.nvfp4_amax(bits)
+    assert amax.item() == float(ra)
+    for sr in (True, False):
+        q, sb, g = fq.nvfp4_quantize(x, amax, use_sr=sr, seed=20250, offset=0)
+        rq, rsb, rg = oracle.nvfp4_quantize(bits, ra, use_sr=sr, seed=20250, offset=0)
+        eq(q, rq, f"nvfp4 q sr={sr}")
+        eq(sb, rsb, f"nvfp4 scales sr={sr}")
+        assert g.item() == float(rg)
+
+
+def test_nvfp4_weights_2d_14336x4096(fq):
+    bits = workloads.nvfp4_weight(14336, 4096, seed=0)
+    w = dev_bf16(bits)
+    amax = fq.nvfp4_amax(w)
+    ra = oracle.nvfp4_amax(bits)
+    assert amax.item() == float(ra)
+    q, sb, g = fq.nvfp4_quantize_2d(w, amax)
+    rq, rsb, rg = oracle.nvfp4_quantize_2d(bits, ra)
+    eq(q, rq, "2d q")
+    eq(sb, rsb, "2d scales")
+    assert g.item() == float(rg)
+
+
+SWEEP_ROWS = [1024 << i for i in range(9)]  # 1K .. 262144 rows
+
+
+def test_bandwidth_sweep_chain(fq):
+    """BF16 -> MXFP4 -> FP8 rows and FP8 cols (one group) at every sweep size.
+    Sizes up to 16384 rows: every output; larger: 48 seeded rows (and the
+    last) and 6 seeded 128-token windows (and the last, ragged for no size
+    here but still checked)."""
+    K = 7168
+    big = workloads.sweep(SWEEP_ROWS[-1], K, seed=0)
+    x_all = dev_bf16(big)
+    rng = np.random.default_rng(7)
+    for M in SWEEP_ROWS:
+        x = x_all[:M]
+        q, s = fq.mxfp4_quantize_rows(x)
+        y, ys = fq.fp4_to_fp8_rows(q, s, 0)
+        offs = np.array([0, M], dtype=np.int64)
+        yT, yTs = cols_full(fq, q, s, offs, 0)
+        bits = big[:M]
+        if M <= 16384:
+            rq, rs = oracle.mxfp4_quantize_rows(bits)
+            eq(q, rq, f"M={M} q")
+            eq(s, rs, f"M={M} s")
+            ry, rys = oracle.fp4_to_fp8_rows(rq, rs, 0)
+            eq(y, ry, f"M={M} y")
+            eq(ys, rys, f"M={M} ys")
+            ryT, ryTs = oracle.fp4_to_fp8_cols(rq, rs, offs, 0)
+            nb = (M + 127) // 128
+            eq(yT, ryT, f"M={M} yT")
+            eq(yTs[:, :nb], ryTs[:, :nb], f"M={M} yTs")
+            continue
+        rows = np.unique(np.concatenate([rng.choice(M, 48, replace=False), [M - 1]]))
+        rq, rs = oracle.mxfp4_quantize_rows(bits[rows])
+        idx = torch.from_numpy(rows).cuda()
+        eq(q.index_select(0, idx), rq, f"M={M} sampled q")
+        eq(s.index_select(0, idx), rs, f"M={M} sampled s")
+        ry, rys = oracle.fp4_to_fp8_rows(rq, rs, 0)
+        eq(y.index_select(0, idx), ry, f"M={M} sampled y")
+        eq(ys.index_select(0, idx), rys, f"M={M} sampled ys")
+        nwin = (M + 127) // 128
+        wins = np.unique(np.concatenate([rng.choice(nwin, 6, replace=False), [nwin - 1]]))
+        for wi in wins:
+            t0, t1 = 128 * int(wi), min(M, 128 * int(wi) + 128)
+            wq, ws = oracle.mxfp4_quantize_rows(bits[t0:t1])
+            ryT, ryTs = oracle.fp4_to_fp8_cols(wq, ws, np.array([0, t1 - t0], dtype=np.int64), 0)
+            eq(yT[:, t0:t1].contiguous(), ryT, f"M={M} window {wi} yT")
+            eq(yTs[:, wi:wi + 1].contiguous(), ryTs[:, :1], f"M={M} window {wi} yTs")
+        del q, s, y, ys, yT, yTs
+        torch.cuda.empty_cache()

@@ -42,6 +42,8 @@ SIGNATURES = {
     "fp4_to_fp8_cols_scale_capacity": (_i64, [_i64, _i32]),
     "fp4_to_fp8_cols_launch_count": (_int, [_i64]),
     "fp4_to_fp8_cols": (_int, [_vp, _vp, _i64, _i64, _vp, _i32, _int, _vp, _vp, _i64, _vp, _vp]),
+    "bf16_to_mxfp4_fp8": (_int, [_vp, _i64, _i64, _vp, _i32, _int, _vp, _vp, _vp, _vp, _vp, _vp,
+                                 _i64, _vp, _vp]),
     "nvfp4_amax": (_int, [_vp, _i64, _vp, _vp]),
     "nvfp4_quantize": (_int, [_vp, _i64, _i64, _vp, _int, _u64, _u64, _vp, _vp, _vp, _vp]),
     "nvfp4_quantize_2d": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
@@ -180,6 +182,39 @@ def fp4_to_fp8_cols(q: torch.Tensor, s: torch.Tensor, group_offsets: torch.Tenso
     _call("fp4_to_fp8_cols", _p(q), _p(s), M, K, _p(group_offsets), G, int(exp_offset_k), _p(yT),
           _p(yT_scale), int(yT_scale.shape[1]), _p(dev_status), _stream())
     return yT, yT_scale
+
+
+def bf16_to_mxfp4_fp8(x: torch.Tensor, group_offsets: torch.Tensor, exp_offset_k: int = 0,
+                      q=None, s=None, y=None, ys=None, yT=None, yT_scale=None,
+                      dev_status: torch.Tensor | None = None):
+    """BF16 [M, K] + int64 group offsets [G+1] (device) -> (q, s, y, ys, yT,
+    yT_scale): the MXFP4 codes and scales, the FP8 rows and the transposed
+    FP8 columns, equal to the three separate calls."""
+    if x.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise ValueError("x must be bfloat16")
+    _need(x, x.dtype, "x", 2)
+    _need(group_offsets, torch.int64, "group_offsets", 1)
+    M, K = x.shape
+    G = group_offsets.numel() - 1
+    cap = fp4_to_fp8_cols_scale_capacity(M, max(G, 1))
+    q = _empty((M, K // 2), torch.uint8, x) if q is None else q
+    s = _empty((M, K // 32), torch.uint8, x) if s is None else s
+    y = _empty((M, K), torch.uint8, x) if y is None else y
+    ys = _empty((M, K // 128), torch.float32, x) if ys is None else ys
+    yT = _empty((K, M), torch.uint8, x) if yT is None else yT
+    yT_scale = _empty((K, cap), torch.float32, x) if yT_scale is None else yT_scale
+    for t, name, dt in ((q, "q", torch.uint8), (s, "s", torch.uint8), (y, "y", torch.uint8),
+                        (ys, "ys", torch.float32), (yT, "yT", torch.uint8)):
+        _need(t, dt, name)
+    _need(yT_scale, torch.float32, "yT_scale", 2)
+    if dev_status is not None:
+        _need(dev_status, torch.int32, "dev_status")
+    if (q.numel() * 2 != M * K or s.numel() * 32 != M * K or y.numel() != M * K or
+            ys.numel() * 128 != M * K or yT.numel() != M * K or yT_scale.shape[0] != K):
+        raise ValueError("output sizes do not match x")
+    _call("bf16_to_mxfp4_fp8", _p(x), M, K, _p(group_offsets), G, int(exp_offset_k), _p(q), _p(s),
+          _p(y), _p(ys), _p(yT), _p(yT_scale), int(yT_scale.shape[1]), _p(dev_status), _stream())
+    return q, s, y, ys, yT, yT_scale
 
 
 # ---------------------------------------------------------------- NVFP4

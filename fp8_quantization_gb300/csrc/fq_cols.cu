@@ -838,29 +838,11 @@ extern "C" int fp4_to_fp8_cols_launch_count(int64_t K)
     return single_pass_ok(K) ? 1 : 2;
 }
 
-extern "C" fq_status fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t M, int64_t K,
+fq_status fq::launch_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t M, int64_t K,
                                      const int64_t *group_offsets, int32_t G, int exp_offset_k,
                                      uint8_t *yT, float *yT_scale, int64_t cap,
-                                     int32_t *dev_status, void *stream)
+                                     int32_t *dev_status, cudaStream_t st)
 {
-    if (M < 0 || M > INT32_MAX - 512 || K <= 0 || K % 128 != 0)
-        return FQ_ERR_SHAPE;
-    if (M > 0 && K > INT64_MAX / M)
-        return FQ_ERR_SHAPE;
-    if (((M + 127) / 128) * (K / 128) > INT32_MAX - 4096)  // tile index is 32-bit
-        return FQ_ERR_SHAPE;
-    if (G < 1 || G > FQ_COLS_MAX_GROUPS || exp_offset_k < 0 || exp_offset_k > 6)
-        return FQ_ERR_ARG;
-    if (cap < fp4_to_fp8_cols_scale_capacity(M, G))
-        return FQ_ERR_ARG;
-    if (M == 0)
-        return FQ_OK;
-    if (!q || !s || !group_offsets || !yT || !yT_scale)
-        return FQ_ERR_NULL;
-    if (!aligned16(q) || !aligned16(s) || !aligned16(group_offsets) || !aligned16(yT) ||
-        !aligned16(yT_scale))
-        return FQ_ERR_ALIGN;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t groups_bytes = static_cast<size_t>(G + 1) * 2 * sizeof(int32_t);
     const int64_t work_ctas = ((M + 127) / 128) * (K / 128);
 
@@ -921,4 +903,30 @@ extern "C" fq_status fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
             return launch_status();
     }
     return launch_status();
+}
+
+extern "C" fq_status fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t M, int64_t K,
+                                     const int64_t *group_offsets, int32_t G, int exp_offset_k,
+                                     uint8_t *yT, float *yT_scale, int64_t cap,
+                                     int32_t *dev_status, void *stream)
+{
+    if (M < 0 || M > INT32_MAX - 512 || K <= 0 || K % 128 != 0)
+        return FQ_ERR_SHAPE;
+    if (M > 0 && K > INT64_MAX / M)
+        return FQ_ERR_SHAPE;
+    if (((M + 127) / 128) * (K / 128) > INT32_MAX - 4096)  // tile index is 32-bit
+        return FQ_ERR_SHAPE;
+    if (G < 1 || G > FQ_COLS_MAX_GROUPS || exp_offset_k < 0 || exp_offset_k > 6)
+        return FQ_ERR_ARG;
+    if (cap < fp4_to_fp8_cols_scale_capacity(M, G))
+        return FQ_ERR_ARG;
+    if (M == 0)
+        return FQ_OK;
+    if (!q || !s || !group_offsets || !yT || !yT_scale)
+        return FQ_ERR_NULL;
+    if (!aligned16(q) || !aligned16(s) || !aligned16(group_offsets) || !aligned16(yT) ||
+        !aligned16(yT_scale))
+        return FQ_ERR_ALIGN;
+    return launch_fp4_to_fp8_cols(q, s, M, K, group_offsets, G, exp_offset_k, yT, yT_scale, cap,
+                                  dev_status, static_cast<cudaStream_t>(stream));
 }

@@ -329,6 +329,16 @@ __device__ __forceinline__ bool named_barrier_or(int id, int count, bool pred)
     return r != 0;
 }
 
+// Host: launchers shared by the entry points (arguments already checked).
+// MXFP4 rows; with y != nullptr also the FP8 rows of the fresh codes.
+fq_status launch_mxfp4_rows(const void *x, int64_t M, int64_t K, uint8_t *q, uint8_t *s, int k,
+                            uint8_t *y, float *ys, cudaStream_t st);
+// FP4 -> FP8 transposed conversion on ragged groups.
+fq_status launch_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t M, int64_t K,
+                                 const int64_t *group_offsets, int32_t G, int k, uint8_t *yT,
+                                 float *yT_scale, int64_t cap, int32_t *dev_status,
+                                 cudaStream_t st);
+
 // Host: encoder of tensor maps (driver entry point, looked up once).
 // Returns false if the driver does not provide it.
 bool encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
@@ -353,6 +363,41 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 __device__ __forceinline__ uint4 ld_nc_v4(const void *p)
 {
     return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+// ---------------------------------------------------------------- L2 eviction policies
+
+// Lines touched with evict_last stay in L2 ahead of other lines (data the next
+// kernel reads back); evict_first lines leave first (streamed data).
+__device__ __forceinline__ uint64_t l2_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint4 ld_nc_v4_hint(const void *p, uint64_t pol)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ void st_u32_hint(void *p, uint32_t v, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void st_u8_hint(void *p, uint32_t v, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.b8 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol)
+                 : "memory");
 }
 
 }  // namespace fq

@@ -21,10 +21,27 @@ namespace fq {
 // block c >> 2, so the four lanes 4g..4g+3 hold block g + 8i of unroll i and
 // a two-step xor shuffle gives the block amax.  Every load and every code
 // store of the warp covers 512 / 128 contiguous bytes.
+//
+// kRows8 fuses the FP8 row conversion of the fresh codes (FP4RowToFP8Row):
+// unroll step i of a warp holds two whole 128-element FP8 blocks (lanes 0-15
+// and 16-31; lanes 4 and 8 apart hold the other MX blocks of a lane's FP8
+// block), so S is a two-shuffle byte max and each lane converts its 8 codes
+// with the shift table exactly as the FP8 row kernel does.  x is then read
+// and y written with an L2 evict-first policy and q, s written evict-last:
+// the transposed conversion that follows reads them back from L2.
+template <bool kRows8>
 __global__ void __launch_bounds__(kThreads) mxfp4_quantize_rows_kernel(
     const uint16_t *__restrict__ x, int64_t nblk, uint8_t *__restrict__ q,
-    uint8_t *__restrict__ s)
+    uint8_t *__restrict__ s, int k, uint8_t *__restrict__ y, float *__restrict__ ys)
 {
+    __shared__ __align__(16) uint8_t tab[kRows8 ? kTabRows * 8 : 8];
+    uint64_t keep = 0, stream = 0;
+    if (kRows8) {
+        build_fp8_table(tab);
+        __syncthreads();
+        keep = l2_evict_last();
+        stream = l2_evict_first();
+    }
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -38,7 +55,9 @@ __global__ void __launch_bounds__(kThreads) mxfp4_quantize_rows_kernel(
         for (int i = 0; i < 4; i++) {
             const int64_t blk = blk0 + (lane >> 2) + 8 * i;
             ok[i] = blk < nblk;
-            v[i] = ok[i] ? ld_nc_v4(x + blk * 32 + (lane & 3) * 8) : make_uint4(0, 0, 0, 0);
+            const uint16_t *src = x + blk * 32 + (lane & 3) * 8;
+            v[i] = ok[i] ? (kRows8 ? ld_nc_v4_hint(src, stream) : ld_nc_v4(src))
+                         : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int i = 0; i < 4; i++) {
@@ -60,11 +79,30 @@ __global__ void __launch_bounds__(kThreads) mxfp4_quantize_rows_kernel(
                 __fmul_rn(bf16_lo(v[i].w), mul), __fmul_rn(bf16_hi(v[i].w), mul));
             if (special)
                 codes = 0;
-            if (ok[i]) {
-                const int64_t blk = blk0 + (lane >> 2) + 8 * i;
+            const uint32_t eb = special ? 0xFFu : e;  // the block's scale byte
+            const int64_t blk = blk0 + (lane >> 2) + 8 * i;
+            if (kRows8) {
+                uint32_t S = max(eb, __shfl_xor_sync(0xffffffffu, eb, 4));
+                S = max(S, __shfl_xor_sync(0xffffffffu, S, 8));
+                int u = static_cast<int>(S - eb) - k + 6;  // >= 0: S is the max
+                u = u < kShiftRows - 1 ? u : kShiftRows - 1;
+                const bool nan = S == 0xFFu;
+                const uint2 t = *reinterpret_cast<const uint2 *>(tab + 8 * (nan ? kNanRow : u));
+                uint32_t lo, hi;
+                fp4x8_to_fp8x8(codes, t.x, t.y, lo, hi, nan ? 0u : 0x80808080u);
+                if (ok[i]) {
+                    st_u32_hint(q + blk * 16 + (lane & 3) * 4, codes, keep);
+                    if ((lane & 3) == 0)
+                        st_u8_hint(s + blk, eb, keep);
+                    __stcs(reinterpret_cast<uint2 *>(y + blk * 32 + (lane & 3) * 8),
+                           make_uint2(lo, hi));
+                    if ((lane & 15) == 0)
+                        reinterpret_cast<uint32_t *>(ys)[blk >> 2] = fp8_block_scale_bits(S, k);
+                }
+            } else if (ok[i]) {
                 *reinterpret_cast<uint32_t *>(q + blk * 16 + (lane & 3) * 4) = codes;
                 if ((lane & 3) == 0)
-                    s[blk] = static_cast<uint8_t>(special ? 0xFFu : e);
+                    s[blk] = static_cast<uint8_t>(eb);
             }
         }
     }
@@ -137,6 +175,27 @@ __global__ void __launch_bounds__(kThreads) fp4_to_fp8_rows_kernel(
 
 using namespace fq;
 
+namespace fq {
+
+fq_status launch_mxfp4_rows(const void *x, int64_t M, int64_t K, uint8_t *q, uint8_t *s, int k,
+                            uint8_t *y, float *ys, cudaStream_t st)
+{
+    const int64_t nblk = M * (K / 32);
+    const int64_t work = (nblk + 32 * (kThreads / 32) - 1) / (32 * (kThreads / 32));
+    if (y) {
+        const int grid = persistent_grid(mxfp4_quantize_rows_kernel<true>, kThreads, 0, work);
+        mxfp4_quantize_rows_kernel<true><<<grid, kThreads, 0, st>>>(
+            static_cast<const uint16_t *>(x), nblk, q, s, k, y, ys);
+    } else {
+        const int grid = persistent_grid(mxfp4_quantize_rows_kernel<false>, kThreads, 0, work);
+        mxfp4_quantize_rows_kernel<false><<<grid, kThreads, 0, st>>>(
+            static_cast<const uint16_t *>(x), nblk, q, s, 0, nullptr, nullptr);
+    }
+    return launch_status();
+}
+
+}  // namespace fq
+
 extern "C" fq_status mxfp4_quantize_rows(const void *x, int64_t M, int64_t K, uint8_t *q,
                                          uint8_t *s, void *stream)
 {
@@ -150,12 +209,8 @@ extern "C" fq_status mxfp4_quantize_rows(const void *x, int64_t M, int64_t K, ui
         return FQ_ERR_NULL;
     if (!aligned16(x) || !aligned16(q) || !aligned16(s))
         return FQ_ERR_ALIGN;
-    const int64_t nblk = M * (K / 32);
-    const int64_t work = (nblk + 32 * (kThreads / 32) - 1) / (32 * (kThreads / 32));
-    const int grid = persistent_grid(mxfp4_quantize_rows_kernel, kThreads, 0, work);
-    mxfp4_quantize_rows_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t *>(x), nblk, q, s);
-    return launch_status();
+    return launch_mxfp4_rows(x, M, K, q, s, 0, nullptr, nullptr,
+                             static_cast<cudaStream_t>(stream));
 }
 
 extern "C" fq_status fp4_to_fp8_rows(const uint8_t *q, const uint8_t *s, int64_t M, int64_t K,

@@ -152,6 +152,24 @@ fq_status fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t M, int64_t
                           void *stream);
 
 /*
+ * The MXFP4 forward cast in one call ([MoE-FP4] 2.1-2.3: BF16ToFP4Row,
+ * FP4RowToFP8Row and FP4RowToFP8Col without any BF16 intermediate): every
+ * output is byte-for-byte what mxfp4_quantize_rows(x) -> (q, s) followed by
+ * fp4_to_fp8_rows(q, s, k) -> (y, ys) and fp4_to_fp8_cols(q, s, offsets, k)
+ * -> (yT, yT_scale) produce; dev_status as in fp4_to_fp8_cols.  The BF16
+ * tensor is read once: the FP8 rows are made from the codes in registers,
+ * and the transposed stage reads q and s back (kept in L2 where they fit).
+ *   x : bf16 [M, K];  q, s, y, ys, yT, yT_scale, group_offsets, G, cap :
+ *   as in the three calls.  Requires K % 128 == 0, 1 <= G <=
+ *   FQ_COLS_MAX_GROUPS, 0 <= M < 2^31, k in [0, 6].  Enqueues
+ *   1 + fp4_to_fp8_cols_launch_count(K) kernels.
+ */
+fq_status bf16_to_mxfp4_fp8(const void *x, int64_t M, int64_t K, const int64_t *group_offsets,
+                            int32_t G, int exp_offset_k, uint8_t *q, uint8_t *s, uint8_t *y,
+                            float *ys, uint8_t *yT, float *yT_scale, int64_t cap,
+                            int32_t *dev_status, void *stream);
+
+/*
  * Per-tensor amax for NVFP4's FP32 tensor scale ([NVFP4] "Receta"):
  *   x      : bf16 [n]
  *   amax   : float in device memory (output) = max |x| (NaN if x holds NaN;

@@ -32,7 +32,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("mxfp4_quantize_rows", "fp4_to_fp8_rows", "fp4_to_fp8_cols",
-              "fp4_to_fp8_cols_scale_capacity", "fp4_to_fp8_cols_launch_count", "nvfp4_amax", "nvfp4_quantize",
+              "fp4_to_fp8_cols_scale_capacity", "fp4_to_fp8_cols_launch_count",
+              "bf16_to_mxfp4_fp8", "nvfp4_amax", "nvfp4_quantize",
               "nvfp4_quantize_2d", "fq_status_string", "fq_last_cuda_error", "fq_version"):
         assert n in names
 
@@ -104,6 +105,20 @@ def test_host_validation_rows_and_cols(lib):
     assert c(P, P, 100, 128, None, 4, 0, P, P, 5, None, None) == NULL
     assert c(P, P, 100, 128, PM, 4, 0, P, P, 5, None, None) == ALIGN
     assert c(P, P, 0, 128, P, 4, 0, P, P, 4, None, None) == OK
+
+
+def test_host_validation_fused(lib):
+    f = lib.bf16_to_mxfp4_fp8
+    # x, M, K, offs, G, k, q, s, y, ys, yT, yTs, cap, status, stream
+    assert f(P, 100, 96, P, 4, 0, P, P, P, P, P, P, 5, None, None) == SHAPE    # K % 128
+    assert f(P, -1, 128, P, 4, 0, P, P, P, P, P, P, 5, None, None) == SHAPE
+    assert f(P, 100, 128, P, 0, 0, P, P, P, P, P, P, 5, None, None) == ARG     # G < 1
+    assert f(P, 100, 128, P, 4, 7, P, P, P, P, P, P, 5, None, None) == ARG     # k > 6
+    assert f(P, 100, 128, P, 4, 0, P, P, P, P, P, P, 4, None, None) == ARG     # cap too small
+    assert f(P, 0, 128, P, 4, 0, P, P, P, P, P, P, 4, None, None) == OK        # empty
+    assert f(P, 100, 128, P, 4, 0, P, P, None, P, P, P, 5, None, None) == NULL
+    assert f(P, 100, 128, None, 4, 0, P, P, P, P, P, P, 5, None, None) == NULL
+    assert f(PM, 100, 128, P, 4, 0, P, P, P, P, P, P, 5, None, None) == ALIGN
 
 
 def test_host_validation_nvfp4(lib):

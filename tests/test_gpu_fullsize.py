@@ -65,6 +65,7 @@ def test_moe_dispatch_16384x7168_all_casts(fq):
     amax = fq.nvfp4_amax(x)
     q4, sb4, g4 = fq.nvfp4_quantize(x, amax, use_sr=True, seed=1000, offset=0)
     q2, sb2, g2 = fq.nvfp4_quantize_2d(x, amax)
+    fused = fq.bf16_to_mxfp4_fp8(x, torch.from_numpy(offs).cuda(), 0)
 
     rq, rs = oracle.mxfp4_quantize_rows(bits)
     eq(q, rq, "mxfp4 q")
@@ -76,6 +77,9 @@ def test_moe_dispatch_16384x7168_all_casts(fq):
     nb = int(((np.diff(offs) + 127) // 128).sum())
     eq(yT, ryT, "fp8 cols yT")
     eq(yTs[:, :nb], ryTs[:, :nb], "fp8 cols scales")
+    for got, ref, what in zip(fused[:5], (rq, rs, ry, rys, ryT), ("q", "s", "y", "ys", "yT")):
+        eq(got, ref, "fused " + what)
+    eq(fused[5][:, :nb], ryTs[:, :nb], "fused yT scales")
     ra = oracle.nvfp4_amax(bits)
     assert amax.item() == float(ra)
     rq4, rsb4, rg4 = oracle.nvfp4_quantize(bits, ra, use_sr=True, seed=1000, offset=0)
@@ -91,10 +95,13 @@ def test_moe_dispatch_16384x7168_all_casts(fq):
 @pytest.mark.parametrize("k", [0, 6])
 def test_ragged_experts_65536x2048(fq, k):
     """Routed rows over 32 Zipf-sized experts: MXFP4 rows, then the
-    transposed conversion on the ragged groups, every output compared."""
+    transposed conversion on the ragged groups, and the one-call forward cast,
+    every output compared."""
     bits, offs = workloads.ragged_experts(65536, 2048, 32, seed=0)
-    q, s = fq.mxfp4_quantize_rows(dev_bf16(bits))
+    x = dev_bf16(bits)
+    q, s = fq.mxfp4_quantize_rows(x)
     yT, yTs = cols_full(fq, q, s, offs, k)
+    fused = fq.bf16_to_mxfp4_fp8(x, torch.from_numpy(offs).cuda(), k)
     rq, rs = oracle.mxfp4_quantize_rows(bits)
     eq(q, rq, "mxfp4 q")
     eq(s, rs, "mxfp4 s")
@@ -102,6 +109,10 @@ def test_ragged_experts_65536x2048(fq, k):
     nb = int(((np.diff(offs) + 127) // 128).sum())
     eq(yT, ryT, "fp8 cols yT")
     eq(yTs[:, :nb], ryTs[:, :nb], "fp8 cols scales")
+    ry, rys = oracle.fp4_to_fp8_rows(rq, rs, k)
+    for got, ref, what in zip(fused[:5], (rq, rs, ry, rys, ryT), ("q", "s", "y", "ys", "yT")):
+        eq(got, ref, "fused " + what)
+    eq(fused[5][:, :nb], ryTs[:, :nb], "fused yT scales")
 
 
 def test_nvfp4_activations_16384x14336(fq):

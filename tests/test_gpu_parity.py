@@ -231,6 +231,64 @@ def test_fp4_to_fp8_cols_malformed_offsets(fq, K):
         assert st == 1, offs
 
 
+# ------------------------------------------------------------------ fused MXFP4 forward cast
+
+def fused_input(M, K, seed):
+    """PR1-like BF16 values with special blocks: zero and negative-zero
+    blocks, BF16 subnormals, NaN / Inf blocks, near-overflow values."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    x *= np.exp2(rng.integers(-20, 20, (M, 1))).astype(np.float32)
+    x[rng.random((M, K)) < 1e-3] *= 100.0
+    if M >= 8:
+        x[0, :32] = 0.0
+        x[1, :32] = -0.0
+        x[2, 32:64] *= np.float32(2.0 ** -130)
+        x[3, 70] = np.nan
+        x[4, 5] = np.inf
+        x[5, 200 % K] = -np.inf
+        x[6, :32] = np.float32(3.0e38)
+    return workloads.bf16_bits(x)
+
+
+@pytest.mark.parametrize("case", sorted(COLS_CASES))
+@pytest.mark.parametrize("path", ["single_pass", "two_launch"])
+def test_bf16_to_mxfp4_fp8(fq, case, path):
+    """The one-call forward cast equals the oracle's MXFP4 -> FP8 rows and
+    MXFP4 -> FP8 cols, byte for byte, with canaries on every output."""
+    M, K, mk = COLS_CASES[case]
+    K = cols_k(K, path)
+    offs = np.asarray(mk(M), dtype=np.int64)
+    G = offs.size - 1
+    k = (M + K) % 7
+    bits = fused_input(M, K, seed=M + 3 * K)
+    cap = oracle.fp4_to_fp8_cols_scale_capacity(M, G)
+    qraw, q = canary_out((M, K // 2), torch.uint8)
+    sraw, s = canary_out((M, K // 32), torch.uint8)
+    yraw, y = canary_out((M, K), torch.uint8)
+    ysraw, ys = canary_out((M, K // 128), torch.float32)
+    yTraw, yT = canary_out((K, M), torch.uint8)
+    yTsraw = torch.full((K * cap * 4 + 64,), CANARY, dtype=torch.uint8, device="cuda")
+    yTs = yTsraw[: K * cap * 4].view(torch.float32).view(K, cap)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fq.bf16_to_mxfp4_fp8(dev_bf16(bits), torch.from_numpy(offs).cuda(), k, q, s, y, ys, yT, yTs, st)
+    for raw, n in ((qraw, M * K // 2), (sraw, M * K // 32), (yraw, M * K), (ysraw, M * K // 32),
+                   (yTraw, K * M), (yTsraw, K * cap * 4)):
+        check_canary(raw, n)
+    rq, rs = oracle.mxfp4_quantize_rows(bits)
+    ry, rys = oracle.fp4_to_fp8_rows(rq, rs, k)
+    ryT, ryTs = oracle.fp4_to_fp8_cols(rq, rs, offs, k)
+    nb = int(((np.diff(offs) + 127) // 128).sum())
+    eq(q, rq, "q")
+    eq(s, rs, "s")
+    eq(y, ry, "y")
+    eq(ys, rys, "ys")
+    eq(yT, ryT, "yT")
+    eq(yTs[:, :nb].contiguous(), np.ascontiguousarray(ryTs[:, :nb]), "yT scales")
+    assert np.all(yTs[:, nb:].contiguous().view(torch.uint8).cpu().numpy() == CANARY)
+    assert int(st.item()) == 0
+
+
 # ------------------------------------------------------------------ NVFP4
 
 def test_nvfp4_amax(fq):

@@ -89,6 +89,11 @@ def lib():
                                                          u64, u64, vp, vp, vp]),
                 "oracle_nvfp4_quantize_2d": (ctypes.c_int, [vp, i64, i64, ctypes.c_float, vp, vp,
                                                             vp]),
+                "oracle_rht16": (ctypes.c_int, [vp, i64, ctypes.c_uint32, vp]),
+                "oracle_nvfp4_amax_rht": (ctypes.c_float, [vp, i64, ctypes.c_uint32]),
+                "oracle_nvfp4_quantize_rht": (ctypes.c_int, [vp, i64, i64, ctypes.c_float,
+                                                             ctypes.c_uint32, ctypes.c_int, u64,
+                                                             u64, vp, vp, vp]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -242,6 +247,37 @@ def nvfp4_quantize_2d(w, amax):
 
 # ---------------------------------------------------------------- decoding helpers
 # Plain table-free decoders used by tests to read results back as numbers.
+
+def rht16(x, sign_mask: int) -> np.ndarray:
+    """The 16-point random Hadamard transform of every 16-element block of
+    x (BF16 bits, size a multiple of 16): float32 array of x's shape."""
+    x = _bits(x)
+    y = np.zeros(x.shape, dtype=np.float32)
+    rc = lib().oracle_rht16(_p(x), x.size, int(sign_mask) & 0xFFFF, _p(y))
+    if rc:
+        raise ValueError("oracle_rht16: size must be a multiple of 16")
+    return y
+
+
+def nvfp4_amax_rht(x, sign_mask: int) -> np.float32:
+    x = _bits(x)
+    return np.float32(lib().oracle_nvfp4_amax_rht(_p(x), x.size, int(sign_mask) & 0xFFFF))
+
+
+def nvfp4_quantize_rht(x, amax, sign_mask: int, use_sr: bool = False, seed: int = 0,
+                       offset: int = 0):
+    x = _bits(x)
+    M, K = x.shape
+    q = np.zeros((M, K // 2), dtype=np.uint8)
+    sb = np.zeros((M, K // 16), dtype=np.uint8)
+    g = np.zeros(1, dtype=np.float32)
+    rc = lib().oracle_nvfp4_quantize_rht(_p(x), M, K, float(np.float32(amax)),
+                                         int(sign_mask) & 0xFFFF, int(bool(use_sr)), int(seed),
+                                         int(offset), _p(q), _p(sb), _p(g))
+    if rc:
+        raise ValueError("oracle_nvfp4_quantize_rht: bad arguments")
+    return q, sb, g[0]
+
 
 def e2m1_decode(codes) -> np.ndarray:
     codes = np.asarray(codes, dtype=np.uint8)

@@ -528,6 +528,31 @@ static void nvfp4_block_scales(float amax_blk, float g, int *b_out, float *r_out
     *r_out = r;
 }
 
+/* One 16-element micro-block of NVFP4 ([NVFP4] "Receta": 16-element blocks,
+ * E4M3 block scale, FP32 per-tensor scale g, RNE or stochastic rounding):
+ * v[16] are the block's values, j0 the linear index of v[0] (for the
+ * stochastic-rounding stream); codes go to element positions idx0 + i of q. */
+static void nvfp4_encode_block(const float *v, float g, int use_sr, uint64_t seed, uint64_t j0,
+                               uint8_t *q, int64_t idx0, uint8_t *sb_out)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < 16; i++) {
+        float a = fabsf(v[i]);
+        if (a > amax)
+            amax = a;
+    }
+    int b;
+    float rs;
+    nvfp4_block_scales(amax, g, &b, &rs);
+    *sb_out = (uint8_t)b;
+    for (int i = 0; i < 16; i++) {
+        float yv = fabsf(v[i]) * rs;
+        int c = use_sr ? e2m1_sr_sat((double)yv, sr_random16(seed, j0 + (uint64_t)i))
+                       : e2m1_rne_sat((double)yv);
+        put_nibble(q, idx0 + i, c | (signbit(v[i]) ? 8 : 0));
+    }
+}
+
 int oracle_nvfp4_quantize(const uint16_t *x, int64_t M, int64_t K, float A, int use_sr,
                           uint64_t seed, uint64_t offset, uint8_t *q, uint8_t *sb, float *g_out)
 {
@@ -540,29 +565,96 @@ int oracle_nvfp4_quantize(const uint16_t *x, int64_t M, int64_t K, float A, int 
     for (int64_t r = 0; r < M; r++) {
         for (int64_t j = 0; j < nb; j++) {
             int64_t base = r * K + 16 * j;
-            float amax = 0.0f;
-            for (int i = 0; i < 16; i++) {
-                float v = fabsf(bf16_bits_to_float(x[base + i]));
-                if (v > amax)
-                    amax = v;
-            }
-            int b;
-            float rs;
-            nvfp4_block_scales(amax, g, &b, &rs);
-            sb[r * nb + j] = (uint8_t)b;
-            for (int i = 0; i < 16; i++) {
-                float yv = fabsf(bf16_bits_to_float(x[base + i])) * rs;
-                int c = use_sr ? e2m1_sr_sat((double)yv, sr_random16(seed, offset + base + i))
-                               : e2m1_rne_sat((double)yv);
-                put_nibble(q, base + i, c | (bf16_sign(x[base + i]) ? 8 : 0));
-            }
+            float v[16];
+            for (int i = 0; i < 16; i++)
+                v[i] = bf16_bits_to_float(x[base + i]);
+            nvfp4_encode_block(v, g, use_sr, seed, offset + (uint64_t)base, q, base, &sb[r * nb + j]);
         }
     }
     return ORACLE_OK;
 }
 
-/* 16x16 2D weight scaling ([NVFP4] "Escalado de pesos 2D"): one E4M3 scale
- * per 16x16 tile, sb[N/16, K/16]; elements round to nearest even. */
+/* Random Hadamard transform of a 16-element block ([NVFP4] "Receta": a
+ * random Hadamard transform is applied to the WGRAD GEMM inputs only, to make
+ * their outliers Gaussian before 4-bit quantization).
+ * READING (the page gives no size, order, sign source or precision): per 16
+ * consecutive elements along the contiguous dimension,
+ *     y = (1/4) H16 diag(d) x,   H16[i][j] = (-1)^popcount(i & j)
+ * (the Sylvester-ordered Hadamard matrix; 1/4 = 1/sqrt(16) makes it
+ * orthogonal), d_i = -1 where bit i of sign_mask is set, else +1.  Computed
+ * in IEEE binary32 as the iterative fast Walsh-Hadamard transform: the inputs
+ * with their signs (exact); for h = 1, 2, 4, 8 every pair (j, j + h) with bit
+ * h of j clear becomes (a + b, a - b); then every value times 0.25. */
+static void rht16(const uint16_t *xb, uint32_t sign_mask, float *y)
+{
+    for (int i = 0; i < 16; i++) {
+        float v = bf16_bits_to_float(xb[i]);
+        y[i] = ((sign_mask >> i) & 1u) ? -v : v;
+    }
+    for (int h = 1; h < 16; h <<= 1)
+        for (int j = 0; j < 16; j++)
+            if (!(j & h)) {
+                float a = y[j], b = y[j + h];
+                y[j] = a + b;
+                y[j + h] = a - b;
+            }
+    for (int i = 0; i < 16; i++)
+        y[i] = y[i] * 0.25f;
+}
+
+/* The transform of every 16-element block of x[n] (n % 16 == 0). */
+int oracle_rht16(const uint16_t *x, int64_t n, uint32_t sign_mask, float *y)
+{
+    if (n < 0 || n % 16 != 0)
+        return ORACLE_EARG;
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < n / 16; b++)
+        rht16(x + 16 * b, sign_mask, y + 16 * b);
+    return ORACLE_OK;
+}
+
+/* max |y| over the transformed tensor (NaN if a transformed value is NaN). */
+float oracle_nvfp4_amax_rht(const uint16_t *x, int64_t n, uint32_t sign_mask)
+{
+    float a = 0.0f;
+    int nan = 0;
+    for (int64_t b = 0; b < n / 16; b++) {
+        float y[16];
+        rht16(x + 16 * b, sign_mask, y);
+        for (int i = 0; i < 16; i++) {
+            if (isnan(y[i]))
+                nan = 1;
+            if (fabsf(y[i]) > a)
+                a = fabsf(y[i]);
+        }
+    }
+    return nan ? float_from_bits(0x7FC00000u) : a;
+}
+
+/* NVFP4 1x16 quantization of the transformed tensor: every block is
+ * transformed (rht16) and quantized as in oracle_nvfp4_quantize; A is the
+ * amax of the transformed tensor. */
+int oracle_nvfp4_quantize_rht(const uint16_t *x, int64_t M, int64_t K, float A,
+                              uint32_t sign_mask, int use_sr, uint64_t seed, uint64_t offset,
+                              uint8_t *q, uint8_t *sb, float *g_out)
+{
+    if (M < 0 || K <= 0 || K % 16 != 0 || offset % 16 != 0)
+        return ORACLE_EARG;
+    float g = nvfp4_tensor_scale(A);
+    *g_out = g;
+    int64_t nb = K / 16;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < M; r++) {
+        for (int64_t j = 0; j < nb; j++) {
+            int64_t base = r * K + 16 * j;
+            float y[16];
+            rht16(x + base, sign_mask, y);
+            nvfp4_encode_block(y, g, use_sr, seed, offset + (uint64_t)base, q, base, &sb[r * nb + j]);
+        }
+    }
+    return ORACLE_OK;
+}
+
 int oracle_nvfp4_quantize_2d(const uint16_t *w, int64_t N, int64_t K, float A, uint8_t *q,
                              uint8_t *sb, float *g_out)
 {

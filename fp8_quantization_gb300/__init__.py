@@ -47,6 +47,9 @@ SIGNATURES = {
     "nvfp4_amax": (_int, [_vp, _i64, _vp, _vp]),
     "nvfp4_quantize": (_int, [_vp, _i64, _i64, _vp, _int, _u64, _u64, _vp, _vp, _vp, _vp]),
     "nvfp4_quantize_2d": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
+    "nvfp4_amax_rht": (_int, [_vp, _i64, ctypes.c_uint32, _vp, _vp]),
+    "nvfp4_quantize_rht": (_int, [_vp, _i64, _i64, _vp, ctypes.c_uint32, _int, _u64, _u64, _vp,
+                                  _vp, _vp, _vp]),
 }
 
 _lock = threading.Lock()
@@ -264,4 +267,39 @@ def nvfp4_quantize_2d(w: torch.Tensor, amax: torch.Tensor | None = None,
     _need(sb, torch.uint8, "sb")
     _need(g, torch.float32, "g")
     _call("nvfp4_quantize_2d", _p(w), N, K, _p(amax), _p(q), _p(sb), _p(g), _stream())
+    return q, sb, g
+
+
+# ---------------------------------------------------------------- NVFP4 with the Hadamard transform
+
+def nvfp4_amax_rht(x: torch.Tensor, sign_mask: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """max |y| of the 16-point random Hadamard transform y of a BF16 tensor."""
+    if x.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise ValueError("x must be bfloat16")
+    _need(x, x.dtype, "x")
+    out = torch.empty((1,), dtype=torch.float32, device=x.device) if out is None else out
+    _need(out, torch.float32, "out")
+    _call("nvfp4_amax_rht", _p(x), x.numel(), int(sign_mask) & 0xFFFF, _p(out), _stream())
+    return out
+
+
+def nvfp4_quantize_rht(x: torch.Tensor, amax: torch.Tensor, sign_mask: int, use_sr: bool = False,
+                       seed: int = 0, offset: int = 0, q=None, sb=None, g=None):
+    """NVFP4 1x16 quantization of the transformed BF16 tensor [M, K] ->
+    (q uint8 [M, K/2], sb uint8 [M, K/16], g float32 [1])."""
+    if x.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise ValueError("x must be bfloat16")
+    _need(x, x.dtype, "x", 2)
+    _need(amax, torch.float32, "amax")
+    M, K = x.shape
+    q = _empty((M, K // 2), torch.uint8, x) if q is None else q
+    sb = _empty((M, K // 16), torch.uint8, x) if sb is None else sb
+    g = _empty((1,), torch.float32, x) if g is None else g
+    _need(q, torch.uint8, "q")
+    _need(sb, torch.uint8, "sb")
+    _need(g, torch.float32, "g")
+    if q.numel() * 2 != M * K or sb.numel() * 16 != M * K:
+        raise ValueError("output sizes do not match x")
+    _call("nvfp4_quantize_rht", _p(x), M, K, _p(amax), int(sign_mask) & 0xFFFF, int(bool(use_sr)),
+          int(seed) & (2**64 - 1), int(offset), _p(q), _p(sb), _p(g), _stream())
     return q, sb, g

@@ -68,6 +68,124 @@ __global__ void __launch_bounds__(kThreads, 6) nvfp4_amax_kernel(const uint16_t 
     }
 }
 
+// ---------------------------------------------------------------- random Hadamard transform
+
+// 16-point random Hadamard transform of one block ("Transformada de Hadamard
+// Aleatoria" of the recipe, applied to the WGRAD inputs): y = 1/4 H16 diag(d) x
+// with H16[i][j] = (-1)^popcount(i & j) and d_i = -1 where bit i of the sign
+// mask is set.  The sign flips act on the BF16 words (flip[i] holds the sign
+// bits of elements 2i and 2i+1); then the four butterfly stages in binary32
+// (pair (j, j + h) with bit h of j clear -> (a + b, a - b), h = 1, 2, 4, 8) and
+// the factor 0.25, in that order, so the result is a fixed function of x.
+struct RhtFlip {
+    uint32_t w[8];
+};
+
+__device__ __forceinline__ RhtFlip rht_flip_words(uint32_t sign_mask)
+{
+    RhtFlip f;
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        f.w[i] = (((sign_mask >> (2 * i)) & 1u) << 15) | (((sign_mask >> (2 * i + 1)) & 1u) << 31);
+    return f;
+}
+
+// Packed IEEE binary32 pairs: (a, b) -> (a + b, a - b) element-wise on
+// (a0, a1) and (b0, b1), and (a0, a1) * c; one rounding per element, as the
+// scalar operations.
+__device__ __forceinline__ void addsub2(float &a0, float &a1, float &b0, float &b1)
+{
+    asm("{\n\t.reg .b64 A, B, S, D;\n\t"
+        "mov.b64 A, {%0, %1};\n\t"
+        "mov.b64 B, {%2, %3};\n\t"
+        "add.rn.f32x2 S, A, B;\n\t"
+        "sub.rn.f32x2 D, A, B;\n\t"
+        "mov.b64 {%0, %1}, S;\n\t"
+        "mov.b64 {%2, %3}, D;\n\t}"
+        : "+f"(a0), "+f"(a1), "+f"(b0), "+f"(b1));
+}
+
+// The butterflies, without the final factor 0.25 (z = H16 diag(d) x).
+__device__ __forceinline__ void rht16_z(const uint4 &a, const uint4 &b, const RhtFlip &f, float z[16])
+{
+    const uint32_t w[8] = {a.x ^ f.w[0], a.y ^ f.w[1], a.z ^ f.w[2], a.w ^ f.w[3],
+                           b.x ^ f.w[4], b.y ^ f.w[5], b.z ^ f.w[6], b.w ^ f.w[7]};
+    // stage h = 1 pairs the two halves of a BF16 word
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const float u = bf16_lo(w[i]), v = bf16_hi(w[i]);
+        z[2 * i] = __fadd_rn(u, v);
+        z[2 * i + 1] = __fsub_rn(u, v);
+    }
+    // stages h = 2, 4, 8 on pairs (j, j + 1)
+#pragma unroll
+    for (int h = 2; h < 16; h <<= 1)
+#pragma unroll
+        for (int j = 0; j < 16; j += 2)
+            if (!(j & h))
+                addsub2(z[j], z[j + 1], z[j + h], z[j + h + 1]);
+}
+
+__device__ __forceinline__ void rht16(const uint4 &a, const uint4 &b, const RhtFlip &f, float y[16])
+{
+    rht16_z(a, b, f, y);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2)
+        fmul2(y[i], y[i + 1], 0.25f, y[i], y[i + 1]);
+}
+
+// max |y| over the transformed tensor: |y| bits ordered as unsigned integers
+// (NaN above infinity above every finite value), one atomicMax per CTA.
+__global__ void __launch_bounds__(kThreads) nvfp4_amax_rht_kernel(const uint16_t *__restrict__ x,
+                                                                  int64_t nblk, uint32_t sign_mask,
+                                                                  uint32_t *__restrict__ out_bits)
+{
+    __shared__ uint32_t red[kThreads / 32];
+    const RhtFlip f = rht_flip_words(sign_mask);
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    uint32_t m = 0;
+    for (int64_t b0 = gtid; b0 < nblk; b0 += 2 * nthr) {
+        uint4 v[2][2];
+#pragma unroll
+        for (int u = 0; u < 2; u++) {
+            const int64_t blk = b0 + u * nthr;
+            if (blk < nblk) {
+                v[u][0] = ld_nc_v4(x + blk * 16);
+                v[u][1] = ld_nc_v4(x + blk * 16 + 8);
+            } else {
+                v[u][0] = v[u][1] = make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; u++) {
+            float z[16];
+            rht16_z(v[u][0], v[u][1], f, z);
+#pragma unroll
+            for (int i = 0; i < 16; i++)
+                m = max(m, __float_as_uint(z[i]) & 0x7FFFFFFFu);
+        }
+    }
+    // max |y| = max |z| * 0.25: rounding is monotone (NaN bit patterns stay NaN)
+    {
+        const float mz = __uint_as_float(m);
+        if (m <= 0x7F800000u)
+            m = __float_as_uint(__fmul_rn(mz, 0.25f));
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1)
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, d));
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t b = 0;
+        for (int w = 0; w < kThreads / 32; w++)
+            b = max(b, red[w]);
+        atomicMax(out_bits, b);
+    }
+}
+
 // ---------------------------------------------------------------- block scale
 
 // Per-tensor set-up, once per CTA: decode scale g, encode factor
@@ -136,6 +254,41 @@ __device__ __forceinline__ uint32_t encode8_sr(uint4 v, float r, uint32_t w0, ui
     return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
+// The same scale and encoders for binary32 block values (the transformed
+// blocks): amax over |y| with fmaxf, codes from y * r with y's sign.
+__device__ __forceinline__ BlockScale nvfp4_block_scale_f(float amax, float enc, const float *rtab)
+{
+    BlockScale bs;
+    bs.b = cvt_e4m3(__fmul_rn(amax, enc));
+    bs.r = rtab[bs.b];
+    return bs;
+}
+
+__device__ __forceinline__ uint32_t encode8f_rne(const float *y, float r)
+{
+    float p[8];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2)
+        fmul2(y[i], y[i + 1], r, p[i], p[i + 1]);
+    return cvt_e2m1x8(p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7]);
+}
+
+__device__ __forceinline__ uint32_t encode8f_sr(const float *y, float r, uint32_t w0, uint32_t w1)
+{
+    float p[8];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2)
+        fmul2(y[i], y[i + 1], r, p[i], p[i + 1]);
+    uint16_t lo, hi;
+    asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;"
+        : "=h"(lo)
+        : "f"(p[3]), "f"(p[2]), "f"(p[1]), "f"(p[0]), "r"(w0));
+    asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;"
+        : "=h"(hi)
+        : "f"(p[7]), "f"(p[6]), "f"(p[5]), "f"(p[4]), "r"(w1));
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
 // ---------------------------------------------------------------- 1x16
 
 // One lane per 16-element block (32 bytes of input, 8 bytes of codes), four
@@ -192,6 +345,66 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
             } else {
                 codes.x = encode8_rne(v[u][0], bs.r);
                 codes.y = encode8_rne(v[u][1], bs.r);
+            }
+            __stcs(reinterpret_cast<uint2 *>(q + blk * 8), codes);
+            sb[blk] = static_cast<uint8_t>(bs.b);
+        }
+    }
+}
+
+// 1x16 quantization of the transformed tensor: one lane per block as above
+// (two blocks in flight: the transform holds 16 values per block).
+template <bool kSR>
+__global__ void __launch_bounds__(kThreads) nvfp4_quantize_rht_kernel(
+    const uint16_t *__restrict__ x, int64_t nblk, const float *__restrict__ amax,
+    uint32_t sign_mask, uint64_t seed, uint64_t offset, uint8_t *__restrict__ q,
+    uint8_t *__restrict__ sb, float *__restrict__ g_out)
+{
+    __shared__ float rtab[128];
+    const TensorScales ts = nvfp4_tensor_setup(amax, rtab);
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        *g_out = ts.g;
+    const RhtFlip f = rht_flip_words(sign_mask);
+    const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+    const uint64_t c0 = offset >> 4;
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+
+    for (int64_t b0 = gtid; b0 < nblk; b0 += 2 * nthr) {
+        uint4 v[2][2];
+#pragma unroll
+        for (int u = 0; u < 2; u++) {
+            const int64_t blk = b0 + u * nthr;
+            if (blk < nblk) {
+                v[u][0] = ld_nc_v4(x + blk * 16);
+                v[u][1] = ld_nc_v4(x + blk * 16 + 8);
+            } else {
+                v[u][0] = v[u][1] = make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; u++) {
+            const int64_t blk = b0 + u * nthr;
+            if (blk >= nblk)
+                break;
+            float y[16];
+            rht16(v[u][0], v[u][1], f, y);
+            float a = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; i++)
+                a = fmaxf(a, fabsf(y[i]));
+            const BlockScale bs = nvfp4_block_scale_f(a, ts.enc, rtab);
+            uint2 codes;
+            if (kSR) {
+                const uint64_t c = c0 + static_cast<uint64_t>(blk);
+                const uint4 w = philox4x32_10(
+                    make_uint4(static_cast<uint32_t>(c), static_cast<uint32_t>(c >> 32), 0u, 0u),
+                    k0, k1);
+                codes.x = encode8f_sr(y, bs.r, w.x, w.y);
+                codes.y = encode8f_sr(y + 8, bs.r, w.z, w.w);
+            } else {
+                codes.x = encode8f_rne(y, bs.r);
+                codes.y = encode8f_rne(y + 8, bs.r);
             }
             __stcs(reinterpret_cast<uint2 *>(q + blk * 8), codes);
             sb[blk] = static_cast<uint8_t>(bs.b);
@@ -322,5 +535,61 @@ extern "C" fq_status nvfp4_quantize_2d(const void *w, int64_t N, int64_t K, cons
         persistent_grid(nvfp4_quantize_2d_kernel, kThreads, 0, (units + 7) / 8);
     nvfp4_quantize_2d_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t *>(w), N, K, amax, q, sb, g);
+    return launch_status();
+}
+
+extern "C" fq_status nvfp4_amax_rht(const void *x, int64_t n, uint32_t sign_mask, float *amax,
+                                    void *stream)
+{
+    if (n < 0 || n % 16 != 0)
+        return FQ_ERR_SHAPE;
+    if (!amax || (n > 0 && !x))
+        return FQ_ERR_NULL;
+    if ((n > 0 && !aligned16(x)) || !aligned16(amax))
+        return FQ_ERR_ALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(amax, 0, sizeof(float), st) != cudaSuccess)
+        return launch_status();
+    if (n == 0)
+        return FQ_OK;
+    const int64_t nblk = n / 16;
+    const int64_t work = (nblk + 2 * kThreads - 1) / (2 * kThreads);
+    const int grid = persistent_grid(nvfp4_amax_rht_kernel, kThreads, 0, work);
+    nvfp4_amax_rht_kernel<<<grid, kThreads, 0, st>>>(static_cast<const uint16_t *>(x), nblk,
+                                                      sign_mask & 0xFFFFu,
+                                                      reinterpret_cast<uint32_t *>(amax));
+    return launch_status();
+}
+
+extern "C" fq_status nvfp4_quantize_rht(const void *x, int64_t M, int64_t K, const float *amax,
+                                        uint32_t sign_mask, int use_sr, uint64_t seed,
+                                        uint64_t offset, uint8_t *q, uint8_t *sb, float *g,
+                                        void *stream)
+{
+    if (M < 0 || K <= 0 || K % 16 != 0)
+        return FQ_ERR_SHAPE;
+    if (M > 0 && K > INT64_MAX / M)
+        return FQ_ERR_SHAPE;
+    if (offset % 16 != 0 || (use_sr != 0 && use_sr != 1))
+        return FQ_ERR_ARG;
+    if (M == 0)
+        return FQ_OK;
+    if (!x || !amax || !q || !sb || !g)
+        return FQ_ERR_NULL;
+    if (!aligned16(x) || !aligned16(amax) || !aligned16(q) || !aligned16(sb) || !aligned16(g))
+        return FQ_ERR_ALIGN;
+    const int64_t nblk = M * (K / 16);
+    const int64_t work = (nblk + 2 * kThreads - 1) / (2 * kThreads);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint32_t mask = sign_mask & 0xFFFFu;
+    if (use_sr) {
+        const int grid = persistent_grid(nvfp4_quantize_rht_kernel<true>, kThreads, 0, work);
+        nvfp4_quantize_rht_kernel<true><<<grid, kThreads, 0, st>>>(
+            static_cast<const uint16_t *>(x), nblk, amax, mask, seed, offset, q, sb, g);
+    } else {
+        const int grid = persistent_grid(nvfp4_quantize_rht_kernel<false>, kThreads, 0, work);
+        nvfp4_quantize_rht_kernel<false><<<grid, kThreads, 0, st>>>(
+            static_cast<const uint16_t *>(x), nblk, amax, mask, seed, offset, q, sb, g);
+    }
     return launch_status();
 }

@@ -207,6 +207,30 @@ fq_status nvfp4_quantize(const void *x, int64_t M, int64_t K, const float *amax,
                          void *stream);
 
 /*
+ * Random Hadamard transform for the NVFP4 WGRAD inputs ([NVFP4] "Receta":
+ * a random Hadamard transform is applied only to the WGRAD GEMM inputs, to
+ * make outliers Gaussian before 4-bit quantization).  The page fixes neither
+ * size, order, sign source nor precision; this library reads it as: per 16
+ * consecutive elements along the contiguous dimension,
+ *     y = 1/4 H16 diag(d) x,   H16[i][j] = (-1)^popcount(i & j),
+ * d_i = -1 where bit i of sign_mask (low 16 bits) is set, else +1, computed
+ * in IEEE binary32: the signed inputs, then the butterfly stages h = 1, 2, 4,
+ * 8 (pair (j, j+h) with bit h of j clear -> (a + b, a - b)), then times 0.25.
+ * Pass the operand with its GEMM reduction dimension contiguous.
+ *
+ * nvfp4_amax_rht: amax (device float) = max |y| over the transformed
+ *   tensor x[n], n % 16 == 0 (NaN if a transformed value is NaN; 0 for n == 0).
+ * nvfp4_quantize_rht: nvfp4_quantize applied to y instead of x (amax = max |y|,
+ *   block amax over |y|, element codes E2M1(|y| r) with the sign of y; the
+ *   stochastic-rounding stream and `offset` as in nvfp4_quantize).  The
+ *   transformed amax must be finite.
+ */
+fq_status nvfp4_amax_rht(const void *x, int64_t n, uint32_t sign_mask, float *amax, void *stream);
+fq_status nvfp4_quantize_rht(const void *x, int64_t M, int64_t K, const float *amax,
+                             uint32_t sign_mask, int use_sr, uint64_t seed, uint64_t offset,
+                             uint8_t *q, uint8_t *sb, float *g, void *stream);
+
+/*
  * NVFP4 with 16x16 2D block scaling of weights ([NVFP4] "Escalado de pesos
  * 2D": one scale per 16x16 tile so that FPROP and the transposed DGRAD use
  * the same scales).

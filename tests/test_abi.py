@@ -33,7 +33,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("mxfp4_quantize_rows", "fp4_to_fp8_rows", "fp4_to_fp8_cols",
               "fp4_to_fp8_cols_scale_capacity", "fp4_to_fp8_cols_launch_count",
-              "bf16_to_mxfp4_fp8", "nvfp4_amax", "nvfp4_quantize",
+              "bf16_to_mxfp4_fp8", "nvfp4_amax", "nvfp4_amax_rht", "nvfp4_quantize_rht", "nvfp4_quantize",
               "nvfp4_quantize_2d", "fq_status_string", "fq_last_cuda_error", "fq_version"):
         assert n in names
 
@@ -119,6 +119,22 @@ def test_host_validation_fused(lib):
     assert f(P, 100, 128, P, 4, 0, P, P, None, P, P, P, 5, None, None) == NULL
     assert f(P, 100, 128, None, 4, 0, P, P, P, P, P, P, 5, None, None) == NULL
     assert f(PM, 100, 128, P, 4, 0, P, P, P, P, P, P, 5, None, None) == ALIGN
+
+
+def test_host_validation_rht(lib):
+    a = lib.nvfp4_amax_rht
+    assert a(P, 40, 0x1234, P, None) == SHAPE      # n % 16
+    assert a(P, -16, 0, P, None) == SHAPE
+    assert a(P, 32, 0, None, None) == NULL
+    assert a(PM, 32, 0, P, None) == ALIGN
+    f = lib.nvfp4_quantize_rht
+    # x, M, K, amax, mask, sr, seed, offset, q, sb, g, stream
+    assert f(P, 4, 24, P, 0, 0, 0, 0, P, P, P, None) == SHAPE
+    assert f(P, 4, 32, P, 0, 2, 0, 0, P, P, P, None) == ARG
+    assert f(P, 4, 32, P, 0, 1, 0, 8, P, P, P, None) == ARG       # offset % 16
+    assert f(P, 0, 32, P, 0, 0, 0, 0, None, None, None, None) == OK
+    assert f(P, 4, 32, None, 0, 0, 0, 0, P, P, P, None) == NULL
+    assert f(P, 4, 32, P, 0, 0, 0, 0, PM, P, P, None) == ALIGN
 
 
 def test_host_validation_nvfp4(lib):

@@ -130,6 +130,23 @@ def test_nvfp4_activations_16384x14336(fq):
         assert g.item() == float(rg)
 
 
+def test_nvfp4_rht_wgrad_inputs_16384x14336(fq):
+    """The transformed WGRAD operands at the activation size: RNE (the
+    activation operand) and SR (the gradient operand), every output compared."""
+    bits = workloads.nvfp4_act(16384, 14336, seed=1)
+    x = dev_bf16(bits)
+    mask = 0x9E37
+    amax = fq.nvfp4_amax_rht(x, mask)
+    ra = oracle.nvfp4_amax_rht(bits, mask)
+    assert amax.item() == float(ra)
+    for sr in (False, True):
+        q, sb, g = fq.nvfp4_quantize_rht(x, amax, mask, use_sr=sr, seed=777, offset=0)
+        rq, rsb, rg = oracle.nvfp4_quantize_rht(bits, ra, mask, use_sr=sr, seed=777, offset=0)
+        eq(q, rq, f"rht q sr={sr}")
+        eq(sb, rsb, f"rht scales sr={sr}")
+        assert g.item() == float(rg)
+
+
 def test_nvfp4_weights_2d_14336x4096(fq):
     bits = workloads.nvfp4_weight(14336, 4096, seed=0)
     w = dev_bf16(bits)

@@ -395,3 +395,63 @@ def test_errors_are_reported(fq):
     raw = torch.zeros(4 * 128 + 1, dtype=torch.uint8, device="cuda")
     with pytest.raises(fq.FQError, match="FQ_ERR_ALIGN"):
         fq.fp4_to_fp8_rows(q, s, 0, y=raw[1:].view(4, 128))
+
+
+# ------------------------------------------------------------------ NVFP4 with the Hadamard transform
+
+RHT_CASES = {"act": (128, 512, workloads.nvfp4_act), "tail": (3, 48, workloads.nvfp4_act),
+             "k16": (40, 16, workloads.nvfp4_act), "wide": (9, 14336, workloads.nvfp4_act),
+             "weight": (64, 4096, workloads.nvfp4_weight)}
+
+
+@pytest.mark.parametrize("case", sorted(RHT_CASES))
+@pytest.mark.parametrize("sr", [False, True])
+@pytest.mark.parametrize("mask", [0x0000, 0xA5C3, 0xFFFF])
+def test_nvfp4_quantize_rht(fq, case, sr, mask):
+    M, K, gen = RHT_CASES[case]
+    bits = gen(M, K, seed=M + K + mask)
+    x = dev_bf16(bits)
+    amax = fq.nvfp4_amax_rht(x, mask)
+    ramax = oracle.nvfp4_amax_rht(bits, mask)
+    assert amax.item() == float(ramax)
+    qraw, q = canary_out((M, K // 2), torch.uint8)
+    sraw, sb = canary_out((M, K // 16), torch.uint8)
+    g = torch.empty(1, dtype=torch.float32, device="cuda")
+    for seed, offset in ((4321, 0), (2**64 - 5, 16 * 777)):
+        fq.nvfp4_quantize_rht(x, amax, mask, use_sr=sr, seed=seed, offset=offset, q=q, sb=sb, g=g)
+        rq, rsb, rg = oracle.nvfp4_quantize_rht(bits, ramax, mask, use_sr=sr, seed=seed,
+                                                offset=offset)
+        eq(q, rq, "q")
+        eq(sb, rsb, "sb")
+        assert g.item() == float(rg)
+        check_canary(qraw, M * K // 2)
+        check_canary(sraw, M * K // 16)
+
+
+def test_nvfp4_rht_special_values(fq):
+    """Signed zeros, BF16 subnormals (their transform reaches binary32
+    subnormals), huge finite values, all-zero blocks, and a NaN propagating
+    through the transformed amax."""
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((16, 64)).astype(np.float32)
+    x[0, :16] = 0.0
+    x[1, :16] = -0.0
+    x[2, :16] = np.float32(2.0 ** -130) * rng.integers(-64, 65, 16)
+    x[3, 16:32] = np.float32(2.0 ** 120) * rng.standard_normal(16)
+    x[4, :] = np.float32(2.0 ** -120)
+    bits = workloads.bf16_bits(x)
+    for mask in (0, 0x1111, 0xFFFF):
+        xd = dev_bf16(bits)
+        amax = fq.nvfp4_amax_rht(xd, mask)
+        ra = oracle.nvfp4_amax_rht(bits, mask)
+        assert amax.item() == float(ra)
+        for sr in (False, True):
+            q, sb, g = fq.nvfp4_quantize_rht(xd, amax, mask, use_sr=sr, seed=5)
+            rq, rsb, rg = oracle.nvfp4_quantize_rht(bits, ra, mask, use_sr=sr, seed=5)
+            eq(q, rq, f"q mask={mask:x} sr={sr}")
+            eq(sb, rsb, f"sb mask={mask:x} sr={sr}")
+    bad = bits.copy()
+    bad[5, 3] = 0x7FC0
+    assert np.isnan(fq.nvfp4_amax_rht(dev_bf16(bad), 0x2222).item())
+    empty = torch.empty((0,), dtype=torch.bfloat16, device="cuda")
+    assert fq.nvfp4_amax_rht(empty, 1).item() == 0.0

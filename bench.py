@@ -389,35 +389,49 @@ def run_gpu(args):
                 "traffic": traffic, "peak_source": f"hbm_gbs of {peak_kind}",
                 "algorithmic_bytes": nbytes[dom]}
 
-    # ---- the one-call MXFP4 forward cast (BF16 read once) on the same tensor,
-    # timed per call with L2 flushed before each call
-    fused_steps = max(3, min(args.steps, 200))
-    fo = {k: torch.empty_like(out[k]) for k in ("q", "s", "y", "ys", "yT", "yTs")}
+    # ---- calls beyond the six casts, on the same tensor, each timed alone
+    # (L2 flushed before every call)
+    extra_steps = max(3, min(args.steps, 200))
 
-    def fused_call():
-        fq.bf16_to_mxfp4_fp8(x, offs, 0, fo["q"], fo["s"], fo["y"], fo["ys"], fo["yT"],
-                             fo["yTs"])
+    def timed_us(fn):
+        for _ in range(args.warmup):
+            flush()
+            fn()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(extra_steps)]
+        for i in range(extra_steps):
+            flush()
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), dev) / extra_steps * 1e3
 
-    for _ in range(args.warmup):
-        flush()
-        fused_call()
-    fev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(fused_steps)]
-    for i in range(fused_steps):
-        flush()
-        fev[i][0].record(stream)
-        fused_call()
-        fev[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    fused_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in fev), dev) / fused_steps
+    def entry(call, us, nbytes, launches, **kw):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        return {"call": call, "us": round(us, 2), "bytes": nbytes, "GB/s": round(gbs, 1),
+                "frac": round(gbs / peak, 4), "launches_per_call": launches, **kw}
+
     E = M * K
-    fused_bytes = 2 * E + E // 2 + E // 32 + E + 4 * (E // 128) + E + 4 * K * nb_cols + 8 * (G + 1)
+    fo = {k: torch.empty_like(out[k]) for k in ("q", "s", "y", "ys", "yT", "yTs")}
+    fused_us = timed_us(lambda: fq.bf16_to_mxfp4_fp8(x, offs, 0, fo["q"], fo["s"], fo["y"],
+                                                      fo["ys"], fo["yT"], fo["yTs"]))
     sep_us = sum(kernels[k]["us"] for k in ("mxfp4_quantize_rows", "fp4_to_fp8_rows",
                                              "fp4_to_fp8_cols"))
-    fused = {"call": "bf16_to_mxfp4_fp8", "us": round(fused_ms * 1e3, 2), "bytes": fused_bytes,
-             "GB/s": round(fused_bytes / (fused_ms * 1e-3) / 1e9, 1),
-             "frac": round(fused_bytes / (fused_ms * 1e-3) / 1e9 / peak, 4),
-             "separate_calls_us": round(sep_us, 2), "steps": fused_steps,
-             "launches_per_call": 1 + fq.fp4_to_fp8_cols_launch_count(K)}
+    rht_mask = 0x9E37
+    ar = torch.empty((1,), dtype=torch.float32, device=dev)
+    amax_rht_us = timed_us(lambda: fq.nvfp4_amax_rht(x, rht_mask, ar))
+    rht_us = timed_us(lambda: fq.nvfp4_quantize_rht(x, ar, rht_mask, True, 4242, 0, out["q4"],
+                                                     out["sb4"], out["g4"]))
+    next_rows = {
+        "bf16_to_mxfp4_fp8": entry(
+            "bf16_to_mxfp4_fp8", fused_us,
+            2 * E + E // 2 + E // 32 + E + 4 * (E // 128) + E + 4 * K * nb_cols + 8 * (G + 1),
+            1 + fq.fp4_to_fp8_cols_launch_count(K), separate_calls_us=round(sep_us, 2)),
+        "nvfp4_amax_rht": entry("nvfp4_amax_rht", amax_rht_us, 2 * E + 4, 1),
+        "nvfp4_quantize_rht_sr": entry("nvfp4_quantize_rht", rht_us, 2 * E + E // 2 + E // 16 + 8,
+                                       1, sign_mask=rht_mask),
+        "steps": extra_steps,
+    }
 
     # ---- end to end through host buffers: H2D input, all casts, D2H outputs
     e2e_steps = max(3, min(args.steps, 30))
@@ -465,7 +479,7 @@ def run_gpu(args):
             "frac_of_hbm_peak": round(value / ws / peak, 4),
             "kernels": kernels,
             "roofline": roofline,
-            "fused_mxfp4_forward": fused,
+            "next_rows": next_rows,
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
             "gpu_launches": launches_per_step * args.steps,

@@ -352,8 +352,11 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
     }
 }
 
-// 1x16 quantization of the transformed tensor: one lane per block as above
-// (two blocks in flight: the transform holds 16 values per block).
+// 1x16 quantization of the transformed tensor: one lane per block as above,
+// rht_unroll(kSR) blocks in flight (their transforms and Philox chains
+// interleave; with stochastic rounding two, as four cost occupancy).
+__host__ __device__ constexpr int rht_unroll(bool sr) { return sr ? 2 : 4; }
+
 template <bool kSR>
 __global__ void __launch_bounds__(kThreads) nvfp4_quantize_rht_kernel(
     const uint16_t *__restrict__ x, int64_t nblk, const float *__restrict__ amax,
@@ -367,13 +370,14 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_rht_kernel(
     const RhtFlip f = rht_flip_words(sign_mask);
     const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
     const uint64_t c0 = offset >> 4;
+    constexpr int kU = rht_unroll(kSR);
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
 
-    for (int64_t b0 = gtid; b0 < nblk; b0 += 2 * nthr) {
-        uint4 v[2][2];
+    for (int64_t b0 = gtid; b0 < nblk; b0 += kU * nthr) {
+        uint4 v[kU][2];
 #pragma unroll
-        for (int u = 0; u < 2; u++) {
+        for (int u = 0; u < kU; u++) {
             const int64_t blk = b0 + u * nthr;
             if (blk < nblk) {
                 v[u][0] = ld_nc_v4(x + blk * 16);
@@ -383,7 +387,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_rht_kernel(
             }
         }
 #pragma unroll
-        for (int u = 0; u < 2; u++) {
+        for (int u = 0; u < kU; u++) {
             const int64_t blk = b0 + u * nthr;
             if (blk >= nblk)
                 break;
@@ -579,7 +583,8 @@ extern "C" fq_status nvfp4_quantize_rht(const void *x, int64_t M, int64_t K, con
     if (!aligned16(x) || !aligned16(amax) || !aligned16(q) || !aligned16(sb) || !aligned16(g))
         return FQ_ERR_ALIGN;
     const int64_t nblk = M * (K / 16);
-    const int64_t work = (nblk + 2 * kThreads - 1) / (2 * kThreads);
+    const int u = rht_unroll(use_sr != 0);
+    const int64_t work = (nblk + u * kThreads - 1) / (u * kThreads);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint32_t mask = sign_mask & 0xFFFFu;
     if (use_sr) {

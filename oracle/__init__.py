@@ -90,6 +90,9 @@ def lib():
                 "oracle_nvfp4_quantize_2d": (ctypes.c_int, [vp, i64, i64, ctypes.c_float, vp, vp,
                                                             vp]),
                 "oracle_rht16": (ctypes.c_int, [vp, i64, ctypes.c_uint32, vp]),
+                "oracle_fp8_quantize_blocks": (ctypes.c_int, [vp, i64, i64, ctypes.c_int, vp, vp]),
+                "oracle_mxfp4_dequantize_rows": (ctypes.c_int, [vp, vp, i64, i64, vp]),
+                "oracle_bf16_rne_array": (None, [vp, i64, vp]),
                 "oracle_nvfp4_amax_rht": (ctypes.c_float, [vp, i64, ctypes.c_uint32]),
                 "oracle_nvfp4_quantize_rht": (ctypes.c_int, [vp, i64, i64, ctypes.c_float,
                                                              ctypes.c_uint32, ctypes.c_int, u64,
@@ -277,6 +280,37 @@ def nvfp4_quantize_rht(x, amax, sign_mask: int, use_sr: bool = False, seed: int 
     if rc:
         raise ValueError("oracle_nvfp4_quantize_rht: bad arguments")
     return q, sb, g[0]
+
+
+def fp8_quantize_blocks(x, block_rows: int):
+    """BF16 bits [M, K] -> (E4M3 codes uint8 [M, K], float32 scales
+    [M / block_rows, K / 128]); block_rows is 1 or 128."""
+    x = _bits(x)
+    M, K = x.shape
+    y = np.zeros((M, K), dtype=np.uint8)
+    sc = np.zeros((M // block_rows, K // 128), dtype=np.float32)
+    rc = lib().oracle_fp8_quantize_blocks(_p(x), M, K, int(block_rows), _p(y), _p(sc))
+    if rc:
+        raise ValueError("oracle_fp8_quantize_blocks: bad arguments")
+    return y, sc
+
+
+def mxfp4_dequantize_rows(q, s):
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = np.ascontiguousarray(s, dtype=np.uint8)
+    M, K = q.shape[0], q.shape[1] * 2
+    out = np.zeros((M, K), dtype=np.uint16)
+    rc = lib().oracle_mxfp4_dequantize_rows(_p(q), _p(s), M, K, _p(out))
+    if rc:
+        raise ValueError("oracle_mxfp4_dequantize_rows: bad arguments")
+    return out
+
+
+def bf16_rne(v) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.zeros(v.shape, dtype=np.uint16)
+    lib().oracle_bf16_rne_array(_p(v), v.size, _p(out))
+    return out
 
 
 def e2m1_decode(codes) -> np.ndarray:

@@ -688,3 +688,138 @@ int oracle_nvfp4_quantize_2d(const uint16_t *w, int64_t N, int64_t K, float A, u
     }
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------ FP8 E4M3 block quantization
+ * The backward-pass FP8 flow ([MoE-FP4] 2.2: gradients stay in standard
+ * FP8; 2.1: the Hopper FP8 pipeline the conversion targets is E4M3 with
+ * 128-element blocks and FP32 block scales).
+ * READING (the pages give the format, not the scale rule): per block,
+ *   amax = max |x|; a block holding NaN or Inf gets s = NaN and all codes
+ *   0x7F (as the FP4 -> FP8 conversion marks a NaN scale);
+ *   r = min(448 / amax, FLT_MAX), s = amax / 448 (both binary32, round to
+ *   nearest; an all-zero block gets r = FLT_MAX, s = 0);
+ *   code = E4M3_RNE_satfinite(|x * r|) with the sign of x (binary32
+ *   product).  Decode: x ~ s * E4M3(code).
+ * Blocks are 1 x 128 (128 consecutive elements of a row; s is [M, K/128])
+ * or 128 x 128 (tiles; s is [M/128, K/128]). */
+static void fp8_block_scales(float amax, float *r_out, float *s_out)
+{
+    float r = 448.0f / amax;
+    if (r > FLT_MAX)
+        r = FLT_MAX;
+    *r_out = r;
+    *s_out = amax / 448.0f;
+}
+
+int oracle_fp8_quantize_blocks(const uint16_t *x, int64_t M, int64_t K, int block_rows,
+                               uint8_t *y, float *s)
+{
+    if (M < 0 || K <= 0 || K % 128 != 0 || (block_rows != 1 && block_rows != 128) ||
+        M % block_rows != 0)
+        return ORACLE_EARG;
+    int64_t nbr = M / block_rows, nbc = K / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t br = 0; br < nbr; br++) {
+        for (int64_t bc = 0; bc < nbc; bc++) {
+            float amax = 0.0f;
+            int special = 0;
+            for (int64_t i = 0; i < block_rows; i++)
+                for (int64_t j = 0; j < 128; j++) {
+                    uint16_t h = x[(br * block_rows + i) * K + bc * 128 + j];
+                    if ((h & 0x7F80) == 0x7F80)
+                        special = 1;
+                    float a = fabsf(bf16_bits_to_float(h));
+                    if (a > amax)
+                        amax = a;
+                }
+            float r, sc;
+            fp8_block_scales(amax, &r, &sc);
+            s[br * nbc + bc] = special ? float_from_bits(0x7FC00000u) : sc;
+            for (int64_t i = 0; i < block_rows; i++)
+                for (int64_t j = 0; j < 128; j++) {
+                    int64_t idx = (br * block_rows + i) * K + bc * 128 + j;
+                    if (special) {
+                        y[idx] = 0x7F;
+                        continue;
+                    }
+                    float p = bf16_bits_to_float(x[idx]) * r;
+                    int c = e4m3_rne_satfinite(fabs((double)p));
+                    y[idx] = (uint8_t)(c | (signbit(p) ? 0x80 : 0));
+                }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------ MXFP4 -> BF16
+ * Dequantization of MXFP4 rows ([MoE-FP4] 2.1: value = E2M1 element x
+ * 2^(e-127) of its block's UE8M0 scale).  READING: the result is rounded to
+ * BF16 (round to nearest even; the products are exact in BF16 or overflow to
+ * infinity); a block with scale byte 0xFF gives 0x7FC0 (NaN) everywhere;
+ * the code's sign bit is kept (code 8 gives -0). */
+static uint16_t double_to_bf16_rne(double v)
+{
+    if (v != v)
+        return 0x7FC0;
+    int neg = signbit(v) ? 1 : 0;
+    double a = fabs(v);
+    uint16_t sign = (uint16_t)(neg << 15);
+    if (a == 0.0)
+        return sign;
+    /* largest finite BF16 is (2 - 2^-7) 2^127; round-to-nearest overflows at
+       the midpoint to 2^128 */
+    if (a >= ldexp(2.0 - ldexp(1.0, -8), 127))
+        return (uint16_t)(sign | 0x7F80);
+    int e;
+    frexp(a, &e); /* a = f 2^e, f in [0.5, 1) */
+    int q = e - 1;  /* a in [2^q, 2^(q+1)) */
+    if (q < -126)
+        q = -126; /* subnormal spacing 2^-133 */
+    double ulp = ldexp(1.0, q - 7);
+    double n = a / ulp; /* exact: division by a power of two */
+    double fl = floor(n);
+    double rem = n - fl;
+    if (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) != 0.0))
+        fl += 1.0;
+    double r = fl * ulp;
+    /* bits of r as BF16 */
+    uint16_t bits;
+    if (r < ldexp(1.0, -126)) {
+        bits = (uint16_t)(r / ldexp(1.0, -133)); /* subnormal: mantissa field */
+    } else {
+        int er;
+        double fr = frexp(r, &er); /* r = fr 2^er, fr in [0.5,1) */
+        int E = er - 1 + 127;
+        int mant = (int)((fr * 2.0 - 1.0) * 128.0);
+        bits = (uint16_t)((E << 7) | mant);
+    }
+    return (uint16_t)(sign | bits);
+}
+
+int oracle_mxfp4_dequantize_rows(const uint8_t *q, const uint8_t *s, int64_t M, int64_t K,
+                                 uint16_t *out)
+{
+    if (M < 0 || K <= 0 || K % 32 != 0)
+        return ORACLE_EARG;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < M; r++)
+        for (int64_t j = 0; j < K; j++) {
+            int64_t idx = r * K + j;
+            uint8_t e = s[r * (K / 32) + j / 32];
+            if (e == 0xFF) {
+                out[idx] = 0x7FC0;
+                continue;
+            }
+            int code = (q[idx / 2] >> (4 * (idx & 1))) & 0xF;
+            double v = ldexp(oracle_e2m1_magnitude(code & 7), (int)e - 127);
+            out[idx] = double_to_bf16_rne((code & 8) ? -v : v);
+        }
+    return ORACLE_OK;
+}
+
+/* BF16 rounding of an array of doubles (exposed for the pins). */
+void oracle_bf16_rne_array(const double *v, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = double_to_bf16_rne(v[i]);
+}

@@ -422,6 +422,13 @@ def run_gpu(args):
     amax_rht_us = timed_us(lambda: fq.nvfp4_amax_rht(x, rht_mask, ar))
     rht_us = timed_us(lambda: fq.nvfp4_quantize_rht(x, ar, rht_mask, True, 4242, 0, out["q4"],
                                                      out["sb4"], out["g4"]))
+    fy = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    fs1 = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
+    fs2 = torch.empty((M // 128, K // 128), dtype=torch.float32, device=dev)
+    fp8_1x128_us = timed_us(lambda: fq.fp8_quantize_1x128(x, fy, fs1))
+    fp8_128_us = timed_us(lambda: fq.fp8_quantize_128x128(x, fy, fs2))
+    deq = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    deq_us = timed_us(lambda: fq.mxfp4_dequantize_rows(out["q"], out["s"], deq))
     next_rows = {
         "bf16_to_mxfp4_fp8": entry(
             "bf16_to_mxfp4_fp8", fused_us,
@@ -430,6 +437,11 @@ def run_gpu(args):
         "nvfp4_amax_rht": entry("nvfp4_amax_rht", amax_rht_us, 2 * E + 4, 1),
         "nvfp4_quantize_rht_sr": entry("nvfp4_quantize_rht", rht_us, 2 * E + E // 2 + E // 16 + 8,
                                        1, sign_mask=rht_mask),
+        "fp8_quantize_1x128": entry("fp8_quantize_1x128", fp8_1x128_us, 3 * E + 4 * (E // 128), 1),
+        "fp8_quantize_128x128": entry("fp8_quantize_128x128", fp8_128_us,
+                                      3 * E + 4 * (E // 16384), 1),
+        "mxfp4_dequantize_rows": entry("mxfp4_dequantize_rows", deq_us,
+                                       E // 2 + E // 32 + 2 * E, 1),
         "steps": extra_steps,
     }
 

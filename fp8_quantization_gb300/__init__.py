@@ -48,6 +48,9 @@ SIGNATURES = {
     "nvfp4_quantize": (_int, [_vp, _i64, _i64, _vp, _int, _u64, _u64, _vp, _vp, _vp, _vp]),
     "nvfp4_quantize_2d": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_amax_rht": (_int, [_vp, _i64, ctypes.c_uint32, _vp, _vp]),
+    "fp8_quantize_1x128": (_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
+    "fp8_quantize_128x128": (_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
+    "mxfp4_dequantize_rows": (_int, [_vp, _vp, _i64, _i64, _vp, _vp]),
     "nvfp4_quantize_rht": (_int, [_vp, _i64, _i64, _vp, ctypes.c_uint32, _int, _u64, _u64, _vp,
                                   _vp, _vp, _vp]),
 }
@@ -303,3 +306,43 @@ def nvfp4_quantize_rht(x: torch.Tensor, amax: torch.Tensor, sign_mask: int, use_
     _call("nvfp4_quantize_rht", _p(x), M, K, _p(amax), int(sign_mask) & 0xFFFF, int(bool(use_sr)),
           int(seed) & (2**64 - 1), int(offset), _p(q), _p(sb), _p(g), _stream())
     return q, sb, g
+
+
+# ---------------------------------------------------------------- FP8 backward flow and dequantization
+
+def _fp8_blocks(name, x, block_rows, y=None, s=None):
+    if x.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise ValueError("x must be bfloat16")
+    _need(x, x.dtype, "x", 2)
+    M, K = x.shape
+    y = _empty((M, K), torch.uint8, x) if y is None else y
+    s = _empty((M // block_rows, K // 128), torch.float32, x) if s is None else s
+    _need(y, torch.uint8, "y")
+    _need(s, torch.float32, "s")
+    if y.numel() != M * K or s.numel() * 128 * block_rows != M * K:
+        raise ValueError("output sizes do not match x")
+    _call(name, _p(x), M, K, _p(y), _p(s), _stream())
+    return y, s
+
+
+def fp8_quantize_1x128(x: torch.Tensor, y=None, s=None):
+    """BF16 [M, K] -> (E4M3 codes uint8 [M, K], float32 scales [M, K/128])."""
+    return _fp8_blocks("fp8_quantize_1x128", x, 1, y, s)
+
+
+def fp8_quantize_128x128(w: torch.Tensor, y=None, s=None):
+    """BF16 [N, K] -> (E4M3 codes uint8 [N, K], float32 scales [N/128, K/128])."""
+    return _fp8_blocks("fp8_quantize_128x128", w, 128, y, s)
+
+
+def mxfp4_dequantize_rows(q: torch.Tensor, s: torch.Tensor, out: torch.Tensor | None = None):
+    """MXFP4 (q uint8 [M, K/2], s uint8 [M, K/32]) -> BF16 [M, K]."""
+    _need(q, torch.uint8, "q", 2)
+    _need(s, torch.uint8, "s", 2)
+    M, K = q.shape[0], q.shape[1] * 2
+    out = torch.empty((M, K), dtype=torch.bfloat16, device=q.device) if out is None else out
+    _need(out, torch.bfloat16, "out")
+    if out.numel() != M * K or s.numel() * 32 != M * K:
+        raise ValueError("sizes do not match q")
+    _call("mxfp4_dequantize_rows", _p(q), _p(s), M, K, _p(out), _stream())
+    return out

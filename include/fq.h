@@ -170,6 +170,37 @@ fq_status bf16_to_mxfp4_fp8(const void *x, int64_t M, int64_t K, const int64_t *
                             int32_t *dev_status, void *stream);
 
 /*
+ * BF16 -> FP8 E4M3 block quantization for the FP8 backward flow ([MoE-FP4]
+ * 2.2: gradients stay in standard FP8; 2.1: the Hopper FP8 pipeline is E4M3
+ * with 128-element blocks and FP32 block scales).  The pages give the format
+ * only; this library's rule, per block, in IEEE binary32:
+ *   r = min(448 / amax, FLT_MAX), s = amax / 448 (the dequantization scale),
+ *   code = E4M3(x * r), round to nearest even, saturating at 448, sign kept;
+ *   a block holding NaN or Inf gets s = NaN (0x7FC00000) and codes 0x7F.
+ *   Decode: x ~ s * E4M3(code).
+ * fp8_quantize_1x128:   x bf16 [M, K] -> y uint8 [M, K], s float [M, K/128]
+ *                       (blocks of 128 consecutive elements of a row);
+ *                       K % 128 == 0.
+ * fp8_quantize_128x128: w bf16 [N, K] -> y uint8 [N, K], s float [N/128, K/128]
+ *                       (128 x 128 tiles); N % 128 == 0, K % 128 == 0.
+ */
+fq_status fp8_quantize_1x128(const void *x, int64_t M, int64_t K, uint8_t *y, float *s,
+                             void *stream);
+fq_status fp8_quantize_128x128(const void *w, int64_t N, int64_t K, uint8_t *y, float *s,
+                               void *stream);
+
+/*
+ * MXFP4 -> BF16 dequantization ([MoE-FP4] 2.1: an element's value is its
+ * E2M1 value times 2^(e-127) of its block's UE8M0 scale byte e).
+ *   q, s : MXFP4 [M, K/2], [M, K/32];  x : bf16 [M, K] (output)
+ * Element = BF16(v * 2^(e-127)): exact, or +-infinity where the product
+ * exceeds BF16's range; the code's sign is kept (code 8 gives -0); a block
+ * with e = 0xFF gives 0x7FC0 everywhere.  Requires K % 32 == 0.
+ */
+fq_status mxfp4_dequantize_rows(const uint8_t *q, const uint8_t *s, int64_t M, int64_t K, void *x,
+                                void *stream);
+
+/*
  * Per-tensor amax for NVFP4's FP32 tensor scale ([NVFP4] "Receta"):
  *   x      : bf16 [n]
  *   amax   : float in device memory (output) = max |x| (NaN if x holds NaN;

@@ -33,7 +33,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("mxfp4_quantize_rows", "fp4_to_fp8_rows", "fp4_to_fp8_cols",
               "fp4_to_fp8_cols_scale_capacity", "fp4_to_fp8_cols_launch_count",
-              "bf16_to_mxfp4_fp8", "nvfp4_amax", "nvfp4_amax_rht", "nvfp4_quantize_rht", "nvfp4_quantize",
+              "bf16_to_mxfp4_fp8", "nvfp4_amax", "nvfp4_amax_rht", "nvfp4_quantize_rht",
+              "fp8_quantize_1x128", "fp8_quantize_128x128", "mxfp4_dequantize_rows", "nvfp4_quantize",
               "nvfp4_quantize_2d", "fq_status_string", "fq_last_cuda_error", "fq_version"):
         assert n in names
 
@@ -135,6 +136,23 @@ def test_host_validation_rht(lib):
     assert f(P, 0, 32, P, 0, 0, 0, 0, None, None, None, None) == OK
     assert f(P, 4, 32, None, 0, 0, 0, 0, P, P, P, None) == NULL
     assert f(P, 4, 32, P, 0, 0, 0, 0, PM, P, P, None) == ALIGN
+
+
+def test_host_validation_fp8_and_dequant(lib):
+    a = lib.fp8_quantize_1x128
+    assert a(P, 4, 96, P, P, None) == SHAPE
+    assert a(P, 0, 128, None, None, None) == OK
+    assert a(P, 4, 128, None, P, None) == NULL
+    assert a(PM, 4, 128, P, P, None) == ALIGN
+    b = lib.fp8_quantize_128x128
+    assert b(P, 100, 128, P, P, None) == SHAPE     # N % 128
+    assert b(P, 128, 64, P, P, None) == SHAPE
+    assert b(P, 128, 128, P, None, None) == NULL
+    d = lib.mxfp4_dequantize_rows
+    assert d(P, P, 4, 48, P, None) == SHAPE
+    assert d(P, P, 0, 64, None, None) == OK
+    assert d(P, None, 4, 64, P, None) == NULL
+    assert d(P, P, 4, 64, PM, None) == ALIGN
 
 
 def test_host_validation_nvfp4(lib):

@@ -147,6 +147,27 @@ def test_nvfp4_rht_wgrad_inputs_16384x14336(fq):
         assert g.item() == float(rg)
 
 
+def test_fp8_backward_and_dequant_full_size(fq):
+    """The FP8 backward-flow quantizers on the bench tensor (1x128) and the
+    NVFP4 weight shape (128x128), and the MXFP4 -> BF16 dequantizer on the
+    bench tensor's codes, every output compared."""
+    bits = workloads.moe_dispatch(16384, 7168, seed=0)
+    x = dev_bf16(bits)
+    y, sc = fq.fp8_quantize_1x128(x)
+    ry, rs = oracle.fp8_quantize_blocks(bits, 1)
+    eq(y, ry, "1x128 codes")
+    eq(sc, rs, "1x128 scales")
+    q, s = fq.mxfp4_quantize_rows(x)
+    rq, rsx = oracle.mxfp4_quantize_rows(bits)
+    out = fq.mxfp4_dequantize_rows(q, s)
+    eq(out.view(torch.uint16), oracle.mxfp4_dequantize_rows(rq, rsx), "dequant")
+    wbits = workloads.nvfp4_weight(14336, 4096, seed=2)
+    y2, s2 = fq.fp8_quantize_128x128(dev_bf16(wbits))
+    ry2, rs2 = oracle.fp8_quantize_blocks(wbits, 128)
+    eq(y2, ry2, "128x128 codes")
+    eq(s2, rs2, "128x128 scales")
+
+
 def test_nvfp4_weights_2d_14336x4096(fq):
     bits = workloads.nvfp4_weight(14336, 4096, seed=0)
     w = dev_bf16(bits)

@@ -455,3 +455,66 @@ def test_nvfp4_rht_special_values(fq):
     assert np.isnan(fq.nvfp4_amax_rht(dev_bf16(bad), 0x2222).item())
     empty = torch.empty((0,), dtype=torch.bfloat16, device="cuda")
     assert fq.nvfp4_amax_rht(empty, 1).item() == 0.0
+
+
+# ------------------------------------------------------------------ FP8 blocks and MXFP4 dequantization
+
+def fp8_input(M, K, seed):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    x *= np.exp2(rng.integers(-40, 40, (M, 1))).astype(np.float32)
+    x[rng.random((M, K)) < 2e-3] *= 1000.0
+    if M >= 6 and K >= 256:
+        x[0, :128] = 0.0
+        x[1, :128] = -0.0
+        x[2, 128:256] = np.float32(2.0 ** -130) * rng.integers(-100, 101, 128)
+        x[3, 5] = np.nan
+        x[4, 200] = np.inf
+        x[5, 130] = np.float32(3.3e38)
+    return workloads.bf16_bits(x)
+
+
+@pytest.mark.parametrize("shape", [(256, 512), (3, 128), (1, 7168), (130, 384), (512, 1024)])
+def test_fp8_quantize_1x128(fq, shape):
+    M, K = shape
+    bits = fp8_input(M, K, seed=M + K)
+    yraw, y = canary_out((M, K), torch.uint8)
+    sraw, sc = canary_out((M, K // 128), torch.float32)
+    fq.fp8_quantize_1x128(dev_bf16(bits), y, sc)
+    ry, rs = oracle.fp8_quantize_blocks(bits, 1)
+    eq(y, ry, "codes")
+    eq(sc, rs, "scales")
+    check_canary(yraw, M * K)
+    check_canary(sraw, M * K // 128 * 4)
+
+
+@pytest.mark.parametrize("shape", [(128, 128), (256, 512), (384, 1024), (128, 7168)])
+def test_fp8_quantize_128x128(fq, shape):
+    N, K = shape
+    bits = fp8_input(N, K, seed=N * 3 + K)
+    yraw, y = canary_out((N, K), torch.uint8)
+    sraw, sc = canary_out((N // 128, K // 128), torch.float32)
+    fq.fp8_quantize_128x128(dev_bf16(bits), y, sc)
+    ry, rs = oracle.fp8_quantize_blocks(bits, 128)
+    eq(y, ry, "codes")
+    eq(sc, rs, "scales")
+    check_canary(yraw, N * K)
+    check_canary(sraw, N * K // 16384 * 4)
+
+
+def test_mxfp4_dequantize_every_code_and_scale(fq):
+    q = np.tile(np.arange(256, dtype=np.uint8), (256, 1))
+    s = np.repeat(np.arange(256, dtype=np.uint8)[:, None], 16, axis=1)
+    oraw, out = canary_out((256, 512), torch.bfloat16)
+    fq.mxfp4_dequantize_rows(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), out)
+    eq(out.view(torch.uint16), oracle.mxfp4_dequantize_rows(q, s), "bf16")
+    check_canary(oraw, 256 * 512 * 2)
+
+
+@pytest.mark.parametrize("shape", [(3, 32), (97, 7168), (64, 96)])
+def test_mxfp4_dequantize_roundtrip_shapes(fq, shape):
+    M, K = shape
+    bits = workloads.moe_dispatch(M, K, seed=M)
+    q, s = oracle.mxfp4_quantize_rows(bits)
+    out = fq.mxfp4_dequantize_rows(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda())
+    eq(out.view(torch.uint16), oracle.mxfp4_dequantize_rows(q, s), "bf16")

@@ -91,6 +91,10 @@ def lib():
                                                             vp]),
                 "oracle_rht16": (ctypes.c_int, [vp, i64, ctypes.c_uint32, vp]),
                 "oracle_fp8_quantize_blocks": (ctypes.c_int, [vp, i64, i64, ctypes.c_int, vp, vp]),
+                "oracle_window_estimate": (ctypes.c_float, [vp, i32, ctypes.c_uint32]),
+                "oracle_nvfp4_quantize_delayed": (ctypes.c_int, [vp, i64, i64, vp, i32,
+                                                                 ctypes.c_uint32, ctypes.c_int,
+                                                                 u64, u64, vp, vp, vp]),
                 "oracle_mxfp4_dequantize_rows": (ctypes.c_int, [vp, vp, i64, i64, vp]),
                 "oracle_bf16_rne_array": (None, [vp, i64, vp]),
                 "oracle_nvfp4_amax_rht": (ctypes.c_float, [vp, i64, ctypes.c_uint32]),
@@ -311,6 +315,30 @@ def bf16_rne(v) -> np.ndarray:
     out = np.zeros(v.shape, dtype=np.uint16)
     lib().oracle_bf16_rne_array(_p(v), v.size, _p(out))
     return out
+
+
+def window_estimate(history, window: int, step: int) -> np.float32:
+    h = np.ascontiguousarray(history, dtype=np.uint64)
+    assert h.size == window + 1
+    return np.float32(lib().oracle_window_estimate(_p(h), int(window), int(step) & 0xFFFFFFFF))
+
+
+def nvfp4_quantize_delayed(x, history, window: int, step: int, use_sr: bool = False,
+                           seed: int = 0, offset: int = 0):
+    """Returns (q, sb, g, history after the step); `history` is not modified."""
+    x = _bits(x)
+    M, K = x.shape
+    h = np.array(history, dtype=np.uint64, copy=True)
+    assert h.size == window + 1
+    q = np.zeros((M, K // 2), dtype=np.uint8)
+    sb = np.zeros((M, K // 16), dtype=np.uint8)
+    g = np.zeros(1, dtype=np.float32)
+    rc = lib().oracle_nvfp4_quantize_delayed(_p(x), M, K, _p(h), int(window),
+                                             int(step) & 0xFFFFFFFF, int(bool(use_sr)), int(seed),
+                                             int(offset), _p(q), _p(sb), _p(g))
+    if rc:
+        raise ValueError("oracle_nvfp4_quantize_delayed: bad arguments")
+    return q, sb, g[0], h
 
 
 def e2m1_decode(codes) -> np.ndarray:

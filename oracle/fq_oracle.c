@@ -823,3 +823,54 @@ void oracle_bf16_rne_array(const double *v, int64_t n, uint16_t *out)
     for (int64_t i = 0; i < n; i++)
         out[i] = double_to_bf16_rne(v[i]);
 }
+
+/* ------------------------------------------------------------------ delayed scaling, Max-Window
+ * "Max-Window scale estimation for HiF8 W8A8 QAT" (手法 / 実験変数: the A_max
+ * estimate of delayed tensor scaling is the maximum over a 64-step history
+ * window; 貢献 2: it guarantees no scale-induced saturation for any step
+ * inside the window).  READING for NVFP4's per-tensor scale: the history is
+ * a ring of W + 1 entries, entry = (step tag << 32) | binary32 bits of that
+ * step's amax; the estimate at step t is the largest amax among entries tagged
+ * t-W .. t-1 (unsigned 32-bit tag arithmetic; none -> 0, i.e. g = 1); the
+ * tensor is quantized exactly as oracle_nvfp4_quantize with that amax, and
+ * entry t mod (W+1) becomes (t << 32) | bits(amax of this tensor), or keeps
+ * its value if it already carries tag t with a larger amax (an entry with any
+ * other tag is a step that has left the window). */
+static float window_estimate(const uint64_t *hist, int32_t W, uint32_t t)
+{
+    float a = 0.0f;
+    for (int32_t i = 0; i <= W; i++) {
+        uint32_t tag = (uint32_t)(hist[i] >> 32);
+        if ((uint32_t)(t - tag - 1u) < (uint32_t)W) {
+            float v = float_from_bits((uint32_t)hist[i]);
+            if (v > a || v != v)
+                a = v;
+        }
+    }
+    return a;
+}
+
+float oracle_window_estimate(const uint64_t *hist, int32_t W, uint32_t t)
+{
+    return window_estimate(hist, W, t);
+}
+
+int oracle_nvfp4_quantize_delayed(const uint16_t *x, int64_t M, int64_t K, uint64_t *hist,
+                                  int32_t W, uint32_t t, int use_sr, uint64_t seed,
+                                  uint64_t offset, uint8_t *q, uint8_t *sb, float *g_out)
+{
+    if (W < 1 || M < 0 || K <= 0 || K % 16 != 0 || offset % 16 != 0)
+        return ORACLE_EARG;
+    float A = window_estimate(hist, W, t);
+    int rc = oracle_nvfp4_quantize(x, M, K, A, use_sr, seed, offset, q, sb, g_out);
+    if (rc)
+        return rc;
+    float cur = oracle_nvfp4_amax(x, M * K);
+    uint32_t bits;
+    memcpy(&bits, &cur, 4);
+    uint64_t v = ((uint64_t)t << 32) | bits;
+    uint64_t *e = &hist[t % (uint32_t)(W + 1)];
+    if ((uint32_t)(*e >> 32) != t || bits > (uint32_t)*e)
+        *e = v;
+    return ORACLE_OK;
+}

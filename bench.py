@@ -429,6 +429,14 @@ def run_gpu(args):
     fp8_128_us = timed_us(lambda: fq.fp8_quantize_128x128(x, fy, fs2))
     deq = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
     deq_us = timed_us(lambda: fq.mxfp4_dequantize_rows(out["q"], out["s"], deq))
+    hist = fq.amax_history(64, device=dev)
+    dstep = [0]
+
+    def delayed_call():
+        fq.nvfp4_quantize_delayed(x, hist, dstep[0], True, 99, 0, out["q4"], out["sb4"], out["g4"])
+        dstep[0] += 1
+
+    delayed_us = timed_us(delayed_call)
     next_rows = {
         "bf16_to_mxfp4_fp8": entry(
             "bf16_to_mxfp4_fp8", fused_us,
@@ -442,6 +450,10 @@ def run_gpu(args):
                                       3 * E + 4 * (E // 16384), 1),
         "mxfp4_dequantize_rows": entry("mxfp4_dequantize_rows", deq_us,
                                        E // 2 + E // 32 + 2 * E, 1),
+        "nvfp4_quantize_delayed_sr": entry(
+            "nvfp4_quantize_delayed", delayed_us, 2 * E + E // 2 + E // 16 + 16 * 65, 1, window=64,
+            amax_then_quantize_us=round(kernels["nvfp4_amax"]["us"] +
+                                        kernels["nvfp4_quantize"]["us"], 2)),
         "steps": extra_steps,
     }
 

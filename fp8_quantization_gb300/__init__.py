@@ -49,6 +49,8 @@ SIGNATURES = {
     "nvfp4_quantize_2d": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_amax_rht": (_int, [_vp, _i64, ctypes.c_uint32, _vp, _vp]),
     "fp8_quantize_1x128": (_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
+    "nvfp4_quantize_delayed": (_int, [_vp, _i64, _i64, _vp, _i32, ctypes.c_uint32, _int, _u64, _u64,
+                                      _vp, _vp, _vp, _vp]),
     "fp8_quantize_128x128": (_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
     "mxfp4_dequantize_rows": (_int, [_vp, _vp, _i64, _i64, _vp, _vp]),
     "nvfp4_quantize_rht": (_int, [_vp, _i64, _i64, _vp, ctypes.c_uint32, _int, _u64, _u64, _vp,
@@ -346,3 +348,36 @@ def mxfp4_dequantize_rows(q: torch.Tensor, s: torch.Tensor, out: torch.Tensor | 
         raise ValueError("sizes do not match q")
     _call("mxfp4_dequantize_rows", _p(q), _p(s), M, K, _p(out), _stream())
     return out
+
+
+# ---------------------------------------------------------------- delayed scaling (Max-Window)
+
+def amax_history(window: int = 64, device="cuda") -> torch.Tensor:
+    """A zeroed Max-Window history for nvfp4_quantize_delayed: window + 1
+    entries (step tag << 32 | amax bits), held as int64."""
+    return torch.zeros((window + 1,), dtype=torch.int64, device=device)
+
+
+def nvfp4_quantize_delayed(x: torch.Tensor, history: torch.Tensor, step: int,
+                           use_sr: bool = False, seed: int = 0, offset: int = 0,
+                           q=None, sb=None, g=None):
+    """NVFP4 1x16 quantization of BF16 [M, K] with the per-tensor amax taken
+    from the Max-Window history (window = history.numel() - 1); records this
+    tensor's amax under `step`.  Returns (q, sb, g)."""
+    if x.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise ValueError("x must be bfloat16")
+    _need(x, x.dtype, "x", 2)
+    _need(history, torch.int64, "history", 1)
+    M, K = x.shape
+    q = _empty((M, K // 2), torch.uint8, x) if q is None else q
+    sb = _empty((M, K // 16), torch.uint8, x) if sb is None else sb
+    g = _empty((1,), torch.float32, x) if g is None else g
+    _need(q, torch.uint8, "q")
+    _need(sb, torch.uint8, "sb")
+    _need(g, torch.float32, "g")
+    if q.numel() * 2 != M * K or sb.numel() * 16 != M * K:
+        raise ValueError("output sizes do not match x")
+    _call("nvfp4_quantize_delayed", _p(x), M, K, _p(history), history.numel() - 1,
+          int(step) & 0xFFFFFFFF, int(bool(use_sr)), int(seed) & (2**64 - 1), int(offset), _p(q),
+          _p(sb), _p(g), _stream())
+    return q, sb, g

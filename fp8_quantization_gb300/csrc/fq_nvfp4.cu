@@ -195,9 +195,8 @@ struct TensorScales {
     float g, enc;
 };
 
-__device__ __forceinline__ TensorScales nvfp4_tensor_setup(const float *amax, float *rtab /* [128] */)
+__device__ __forceinline__ TensorScales nvfp4_tensor_setup_from(float A, float *rtab /* [128] */)
 {
-    const float A = *amax;
     TensorScales ts;
     ts.g = A > 0.0f ? __fdiv_rn(A, 2688.0f) : 1.0f;
     ts.enc = __frcp_rn(__fmul_rn(6.0f, ts.g));
@@ -205,6 +204,62 @@ __device__ __forceinline__ TensorScales nvfp4_tensor_setup(const float *amax, fl
         rtab[b] = b ? fminf(__frcp_rn(__fmul_rn(e4m3_value(b), ts.g)), FLT_MAX) : 0.0f;
     __syncthreads();
     return ts;
+}
+
+__device__ __forceinline__ TensorScales nvfp4_tensor_setup(const float *amax, float *rtab /* [128] */)
+{
+    return nvfp4_tensor_setup_from(*amax, rtab);
+}
+
+// ---------------------------------------------------------------- Max-Window history
+
+// Delayed per-tensor scaling ("Max-Window scale estimation for HiF8 W8A8
+// QAT": the A_max estimate is the maximum over a 64-step history window).
+// The history is a ring of W + 1 entries (step tag << 32 | binary32 bits of
+// that step's amax).  The estimate at step t is the largest amax tagged
+// t-W .. t-1 (unsigned tag arithmetic); entry t mod (W+1) then holds a step
+// that has left the window, so the CTAs' updates during the step cannot
+// change any CTA's estimate.
+__device__ float window_estimate(const uint64_t *__restrict__ hist, int32_t W, uint32_t t,
+                                 uint32_t *red /* [kThreads / 32] */)
+{
+    uint32_t m = 0;  // |amax| bits: NaN above infinity above every finite value
+    for (int i = threadIdx.x; i <= W; i += blockDim.x) {
+        const uint64_t e = hist[i];
+        const uint32_t tag = static_cast<uint32_t>(e >> 32);
+        if (t - tag - 1u < static_cast<uint32_t>(W))
+            m = max(m, static_cast<uint32_t>(e) & 0x7FFFFFFFu);
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1)
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, d));
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    uint32_t a = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); w++)
+        a = max(a, red[w]);
+    __syncthreads();
+    return __uint_as_float(a);
+}
+
+// Entry t mod (W+1) := (t, this CTA's amax) unless it already carries tag t
+// with a larger amax.  Each failed compare-and-swap means another CTA's
+// update landed, so the loop ends after at most grid-size rounds; the bound
+// only guards against misuse (the same history shared by concurrent calls).
+__device__ void window_record(uint64_t *hist, int32_t W, uint32_t t, uint32_t amax_bits)
+{
+    unsigned long long *e = reinterpret_cast<unsigned long long *>(hist + t % static_cast<uint32_t>(W + 1));
+    const unsigned long long mine = (static_cast<unsigned long long>(t) << 32) | amax_bits;
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(e);
+    for (int it = 0; it < (1 << 16); it++) {
+        if (static_cast<uint32_t>(old >> 32) == t && static_cast<uint32_t>(old) >= amax_bits)
+            return;
+        const unsigned long long prev = atomicCAS(e, old, mine);
+        if (prev == old)
+            return;
+        old = prev;
+    }
 }
 
 struct BlockScale {
@@ -297,13 +352,19 @@ __device__ __forceinline__ uint32_t encode8f_sr(const float *y, float r, uint32_
 // yields one random word per four values.
 constexpr int kNvUnroll = 4;
 
-template <bool kSR>
+// kDelayed: the per-tensor amax is the Max-Window estimate from `hist` (W, t)
+// instead of *amax, and the tensor's own amax is recorded under tag t.
+template <bool kSR, bool kDelayed>
 __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
     const uint16_t *__restrict__ x, int64_t nblk, const float *__restrict__ amax, uint64_t seed,
-    uint64_t offset, uint8_t *__restrict__ q, uint8_t *__restrict__ sb, float *__restrict__ g_out)
+    uint64_t offset, uint8_t *__restrict__ q, uint8_t *__restrict__ sb, float *__restrict__ g_out,
+    uint64_t *__restrict__ hist, int32_t W, uint32_t t)
 {
     __shared__ float rtab[128];
-    const TensorScales ts = nvfp4_tensor_setup(amax, rtab);
+    __shared__ uint32_t red[kThreads / 32];
+    const TensorScales ts = kDelayed ? nvfp4_tensor_setup_from(window_estimate(hist, W, t, red), rtab)
+                                     : nvfp4_tensor_setup(amax, rtab);
+    uint32_t own = 0;  // max of this thread's block maxima (BF16 bits)
     if (blockIdx.x == 0 && threadIdx.x == 0)
         *g_out = ts.g;
     const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
@@ -333,7 +394,10 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
             m = absmax_bf16x2(absmax_bf16x2(m, v[u][0].w), v[u][1].x);
             m = absmax_bf16x2(absmax_bf16x2(m, v[u][1].y), v[u][1].z);
             m = absmax_bf16x2(m, v[u][1].w);
-            const BlockScale bs = nvfp4_block_scale(hmax_u16x2(m), ts.enc, rtab);
+            const uint32_t amax16 = hmax_u16x2(m);
+            if (kDelayed)
+                own = max(own, amax16);
+            const BlockScale bs = nvfp4_block_scale(amax16, ts.enc, rtab);
             uint2 codes;
             if (kSR) {
                 const uint64_t c = c0 + static_cast<uint64_t>(blk);
@@ -348,6 +412,20 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
             }
             __stcs(reinterpret_cast<uint2 *>(q + blk * 8), codes);
             sb[blk] = static_cast<uint8_t>(bs.b);
+        }
+    }
+    if (kDelayed) {
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1)
+            own = max(own, __shfl_xor_sync(0xffffffffu, own, d));
+        if ((threadIdx.x & 31) == 0)
+            red[threadIdx.x >> 5] = own;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            uint32_t a = 0;
+            for (int w = 0; w < kThreads / 32; w++)
+                a = max(a, red[w]);
+            window_record(hist, W, t, a << 16);
         }
     }
 }
@@ -509,15 +587,10 @@ extern "C" fq_status nvfp4_quantize(const void *x, int64_t M, int64_t K, const f
     const int64_t nblk = M * (K / 16);
     const int64_t work = (nblk + kNvUnroll * kThreads - 1) / (kNvUnroll * kThreads);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (use_sr) {
-        const int grid = persistent_grid(nvfp4_quantize_kernel<true>, kThreads, 0, work);
-        nvfp4_quantize_kernel<true><<<grid, kThreads, 0, st>>>(
-            static_cast<const uint16_t *>(x), nblk, amax, seed, offset, q, sb, g);
-    } else {
-        const int grid = persistent_grid(nvfp4_quantize_kernel<false>, kThreads, 0, work);
-        nvfp4_quantize_kernel<false><<<grid, kThreads, 0, st>>>(
-            static_cast<const uint16_t *>(x), nblk, amax, seed, offset, q, sb, g);
-    }
+    auto kern = use_sr ? nvfp4_quantize_kernel<true, false> : nvfp4_quantize_kernel<false, false>;
+    const int grid = persistent_grid(kern, kThreads, 0, work);
+    kern<<<grid, kThreads, 0, st>>>(static_cast<const uint16_t *>(x), nblk, amax, seed, offset, q,
+                                    sb, g, nullptr, 0, 0u);
     return launch_status();
 }
 
@@ -596,5 +669,34 @@ extern "C" fq_status nvfp4_quantize_rht(const void *x, int64_t M, int64_t K, con
         nvfp4_quantize_rht_kernel<false><<<grid, kThreads, 0, st>>>(
             static_cast<const uint16_t *>(x), nblk, amax, mask, seed, offset, q, sb, g);
     }
+    return launch_status();
+}
+
+extern "C" fq_status nvfp4_quantize_delayed(const void *x, int64_t M, int64_t K,
+                                            uint64_t *amax_history, int32_t window, uint32_t step,
+                                            int use_sr, uint64_t seed, uint64_t offset, uint8_t *q,
+                                            uint8_t *sb, float *g, void *stream)
+{
+    if (M < 0 || K <= 0 || K % 16 != 0)
+        return FQ_ERR_SHAPE;
+    if (M > 0 && K > INT64_MAX / M)
+        return FQ_ERR_SHAPE;
+    if (window < 1 || window > FQ_AMAX_WINDOW_MAX || offset % 16 != 0 ||
+        (use_sr != 0 && use_sr != 1))
+        return FQ_ERR_ARG;
+    if (M == 0)
+        return FQ_OK;
+    if (!x || !amax_history || !q || !sb || !g)
+        return FQ_ERR_NULL;
+    if (!aligned16(x) || !aligned16(amax_history) || !aligned16(q) || !aligned16(sb) ||
+        !aligned16(g))
+        return FQ_ERR_ALIGN;
+    const int64_t nblk = M * (K / 16);
+    const int64_t work = (nblk + kNvUnroll * kThreads - 1) / (kNvUnroll * kThreads);
+    auto kern = use_sr ? nvfp4_quantize_kernel<true, true> : nvfp4_quantize_kernel<false, true>;
+    const int grid = persistent_grid(kern, kThreads, 0, work);
+    kern<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(x), nblk, nullptr, seed, offset, q, sb, g, amax_history,
+        window, step);
     return launch_status();
 }

@@ -261,6 +261,31 @@ fq_status nvfp4_quantize_rht(const void *x, int64_t M, int64_t K, const float *a
                              uint32_t sign_mask, int use_sr, uint64_t seed, uint64_t offset,
                              uint8_t *q, uint8_t *sb, float *g, void *stream);
 
+/* Largest history window accepted by nvfp4_quantize_delayed. */
+#define FQ_AMAX_WINDOW_MAX 4096
+
+/*
+ * NVFP4 1x16 quantization with delayed per-tensor scaling from a Max-Window
+ * amax history ("Max-Window scale estimation for HiF8 W8A8 QAT", 手法 and
+ * 貢献 2: the A_max estimate is the maximum over a 64-step history window,
+ * which rules out scale-induced saturation for every step inside it).  One
+ * pass over x: no separate amax read.
+ *   amax_history : uint64 [window + 1] in device memory, caller-owned,
+ *                  zero-initialised once; entry = (step << 32) | binary32
+ *                  bits of that step's amax.
+ *   window       : W in [1, FQ_AMAX_WINDOW_MAX] (64 in the source);
+ *   step         : t, the caller's step counter (32-bit, may wrap).
+ * The per-tensor amax A is the largest amax of the entries tagged t-W .. t-1
+ * (0 if none, so g = 1 until the history fills); x is quantized exactly as
+ * nvfp4_quantize with that A (a tensor larger than its estimate saturates);
+ * then entry t mod (W+1) becomes (t << 32) | bits(max |x|), unless it
+ * already carries tag t with a larger amax.  Calls sharing one history must
+ * be ordered on one stream.  Other arguments as in nvfp4_quantize.
+ */
+fq_status nvfp4_quantize_delayed(const void *x, int64_t M, int64_t K, uint64_t *amax_history,
+                                 int32_t window, uint32_t step, int use_sr, uint64_t seed,
+                                 uint64_t offset, uint8_t *q, uint8_t *sb, float *g, void *stream);
+
 /*
  * NVFP4 with 16x16 2D block scaling of weights ([NVFP4] "Escalado de pesos
  * 2D": one scale per 16x16 tile so that FPROP and the transposed DGRAD use

@@ -34,7 +34,8 @@ def test_header_declares_the_entry_points():
     for n in ("mxfp4_quantize_rows", "fp4_to_fp8_rows", "fp4_to_fp8_cols",
               "fp4_to_fp8_cols_scale_capacity", "fp4_to_fp8_cols_launch_count",
               "bf16_to_mxfp4_fp8", "nvfp4_amax", "nvfp4_amax_rht", "nvfp4_quantize_rht",
-              "fp8_quantize_1x128", "fp8_quantize_128x128", "mxfp4_dequantize_rows", "nvfp4_quantize",
+              "fp8_quantize_1x128", "fp8_quantize_128x128", "mxfp4_dequantize_rows",
+              "nvfp4_quantize_delayed", "nvfp4_quantize",
               "nvfp4_quantize_2d", "fq_status_string", "fq_last_cuda_error", "fq_version"):
         assert n in names
 
@@ -153,6 +154,18 @@ def test_host_validation_fp8_and_dequant(lib):
     assert d(P, P, 0, 64, None, None) == OK
     assert d(P, None, 4, 64, P, None) == NULL
     assert d(P, P, 4, 64, PM, None) == ALIGN
+
+
+def test_host_validation_delayed(lib):
+    f = lib.nvfp4_quantize_delayed
+    # x, M, K, hist, W, step, sr, seed, offset, q, sb, g, stream
+    assert f(P, 4, 24, P, 64, 0, 0, 0, 0, P, P, P, None) == SHAPE
+    assert f(P, 4, 32, P, 0, 0, 0, 0, 0, P, P, P, None) == ARG          # window < 1
+    assert f(P, 4, 32, P, 4097, 0, 0, 0, 0, P, P, P, None) == ARG       # window too large
+    assert f(P, 4, 32, P, 64, 0, 0, 0, 8, P, P, P, None) == ARG         # offset % 16
+    assert f(P, 0, 32, None, 64, 0, 0, 0, 0, None, None, None, None) == OK
+    assert f(P, 4, 32, None, 64, 0, 0, 0, 0, P, P, P, None) == NULL
+    assert f(P, 4, 32, PM, 64, 0, 0, 0, 0, P, P, P, None) == ALIGN
 
 
 def test_host_validation_nvfp4(lib):

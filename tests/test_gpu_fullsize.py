@@ -168,6 +168,23 @@ def test_fp8_backward_and_dequant_full_size(fq):
     eq(s2, rs2, "128x128 scales")
 
 
+def test_nvfp4_delayed_activations_16384x14336(fq):
+    """Three delayed-scaling steps at the activation size (RNE, SR, RNE):
+    outputs and history compared at every step."""
+    W = 64
+    hist_d = fq.amax_history(W)
+    hist = np.zeros(W + 1, dtype=np.uint64)
+    for t in range(3):
+        bits = workloads.nvfp4_act(16384, 14336, seed=10 + t)
+        q, sb, g = fq.nvfp4_quantize_delayed(dev_bf16(bits), hist_d, t, use_sr=(t == 1), seed=3)
+        rq, rsb, rg, hist = oracle.nvfp4_quantize_delayed(bits, hist, W, t, use_sr=(t == 1),
+                                                          seed=3)
+        eq(q, rq, f"delayed q t={t}")
+        eq(sb, rsb, f"delayed sb t={t}")
+        assert g.item() == float(rg)
+        assert np.array_equal(hist_d.cpu().numpy().view(np.uint64), hist)
+
+
 def test_nvfp4_weights_2d_14336x4096(fq):
     bits = workloads.nvfp4_weight(14336, 4096, seed=0)
     w = dev_bf16(bits)

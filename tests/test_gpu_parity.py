@@ -518,3 +518,49 @@ def test_mxfp4_dequantize_roundtrip_shapes(fq, shape):
     q, s = oracle.mxfp4_quantize_rows(bits)
     out = fq.mxfp4_dequantize_rows(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda())
     eq(out.view(torch.uint16), oracle.mxfp4_dequantize_rows(q, s), "bf16")
+
+
+# ------------------------------------------------------------------ delayed scaling (Max-Window)
+
+def spiky_tensor(rng, M, K, t):
+    """Student-t rows scaled per step, with occasional spikes, so the window
+    estimate both trails and exceeds the current amax."""
+    x = rng.standard_t(4, (M, K)).astype(np.float32) * np.float32(np.exp2(rng.uniform(-6, 6)))
+    if t % 11 == 3:
+        x[0, 0] = np.float32(2.0 ** 40)
+    return workloads.bf16_bits(x)
+
+
+@pytest.mark.parametrize("W", [1, 8, 64])
+def test_nvfp4_quantize_delayed_sequence(fq, W):
+    rng = np.random.default_rng(W)
+    M, K = 48, 320
+    hist_d = fq.amax_history(W)
+    hist = np.zeros(W + 1, dtype=np.uint64)
+    for t in range(2 * W + 30):
+        bits = spiky_tensor(rng, M, K, t)
+        sr = t % 3 == 0
+        q, sb, g = fq.nvfp4_quantize_delayed(dev_bf16(bits), hist_d, t, use_sr=sr, seed=17 + t,
+                                             offset=16 * t)
+        rq, rsb, rg, hist = oracle.nvfp4_quantize_delayed(bits, hist, W, t, use_sr=sr,
+                                                          seed=17 + t, offset=16 * t)
+        eq(q, rq, f"q t={t}")
+        eq(sb, rsb, f"sb t={t}")
+        assert g.item() == float(rg), t
+        assert np.array_equal(hist_d.cpu().numpy().view(np.uint64), hist), f"history t={t}"
+
+
+def test_nvfp4_quantize_delayed_tag_wrap(fq):
+    rng = np.random.default_rng(5)
+    W = 4
+    hist_d = fq.amax_history(W)
+    hist = np.zeros(W + 1, dtype=np.uint64)
+    for i in range(12):
+        t = (2**32 - 6 + i) % 2**32
+        bits = spiky_tensor(rng, 16, 64, i)
+        q, sb, g = fq.nvfp4_quantize_delayed(dev_bf16(bits), hist_d, t)
+        rq, rsb, rg, hist = oracle.nvfp4_quantize_delayed(bits, hist, W, t)
+        eq(q, rq, f"q i={i}")
+        eq(sb, rsb, f"sb i={i}")
+        assert g.item() == float(rg)
+        assert np.array_equal(hist_d.cpu().numpy().view(np.uint64), hist)

@@ -52,6 +52,10 @@ KERNEL_SRC = {
     "mxfp4_quantize_rows": "fq_mxfp4.cu", "fp4_to_fp8_rows": "fq_mxfp4.cu",
     "fp4_to_fp8_cols": "fq_cols.cu", "nvfp4_amax": "fq_nvfp4.cu",
     "nvfp4_quantize": "fq_nvfp4.cu", "nvfp4_quantize_2d": "fq_nvfp4.cu",
+    "bf16_to_mxfp4_fp8": "fq_mxfp4.cu", "nvfp4_amax_rht": "fq_nvfp4.cu",
+    "nvfp4_quantize_rht": "fq_nvfp4.cu", "fp8_quantize_1x128": "fq_fp8.cu",
+    "fp8_quantize_128x128": "fq_fp8.cu", "mxfp4_dequantize_rows": "fq_fp8.cu",
+    "nvfp4_quantize_delayed": "fq_nvfp4.cu",
 }
 FALLBACK_HBM_GBS = 6800.0
 
@@ -410,7 +414,8 @@ def run_gpu(args):
     def entry(call, us, nbytes, launches, **kw):
         gbs = nbytes / (us * 1e-6) / 1e9
         return {"call": call, "us": round(us, 2), "bytes": nbytes, "GB/s": round(gbs, 1),
-                "frac": round(gbs / peak, 4), "launches_per_call": launches, **kw}
+                "frac": round(gbs / peak, 4), "launches_per_call": launches,
+                "traffic": ncu_traffic(call), **kw}
 
     E = M * K
     fo = {k: torch.empty_like(out[k]) for k in ("q", "s", "y", "ys", "yT", "yTs")}

@@ -32,21 +32,25 @@ int sm_count()
 }
 
 namespace {
+// The driver's tensor-map encoder.  The runtime (and with it the driver and
+// the current device's primary context) is initialised first: in a process
+// whose first CUDA call is this lookup, the lookup and the encoder fail
+// otherwise.  Only a successful lookup is kept.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
     static std::atomic<void *> fn{nullptr};
-    static std::atomic<int> looked_up{0};
-    if (!looked_up.load(std::memory_order_acquire)) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        fn.store(p, std::memory_order_relaxed);
-        looked_up.store(1, std::memory_order_release);
-    }
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn.load(std::memory_order_relaxed));
+    void *p = fn.load(std::memory_order_acquire);
+    if (p)
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    if (cudaFree(nullptr) != cudaSuccess)  // initialises the runtime; frees nothing
+        cudaGetLastError();                 // (no device): not left for the caller
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    fn.store(p, std::memory_order_release);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
 }
 }  // namespace
 

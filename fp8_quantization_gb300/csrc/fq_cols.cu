@@ -269,6 +269,36 @@ __global__ void __launch_bounds__(kThreads) fp4_to_fp8_cols_scales_kernel(
 
 // ---------------------------------------------------------------- shared by both paths
 
+// The shift-table rows of four MX columns at once: byte i of the result is
+// min(S_i - e_i - k + 6, kShiftRows - 1), or kNanRow where S_i = 0xFF (S is
+// the block max, so S_i >= e_i and the byte-wise subtraction never borrows).
+__device__ __forceinline__ uint32_t shift_rows4(uint32_t S, uint32_t e, int k)
+{
+    const uint32_t ones = 0x01010101u;
+    const uint32_t d = S - e;
+    uint32_t u = __vminu4(d, static_cast<uint32_t>(kShiftRows - 1 - 6 + k) * ones) +
+                 static_cast<uint32_t>(6 - k) * ones;
+    const uint32_t nan = __vcmpeq4(S, 0xFFFFFFFFu);  // 0xFF in bytes where S = 0xFF
+    return (u & ~nan) | (static_cast<uint32_t>(kNanRow) * ones & nan);
+}
+
+// One unit from its shift-table row u (as convert_unit with u precomputed).
+__device__ __forceinline__ void convert_unit_row(uint32_t *tile, const uint8_t *tab, int tl, int j,
+                                                 uint4 qv, uint32_t u)
+{
+    const uint2 t = *reinterpret_cast<const uint2 *>(tab + 8 * u);
+    const uint32_t smask = u == static_cast<uint32_t>(kNanRow) ? 0u : 0x80808080u;
+    uint32_t o[8];
+    fp4x8_to_fp8x8(qv.x, t.x, t.y, o[0], o[1], smask);
+    fp4x8_to_fp8x8(qv.y, t.x, t.y, o[2], o[3], smask);
+    fp4x8_to_fp8x8(qv.z, t.x, t.y, o[4], o[5], smask);
+    fp4x8_to_fp8x8(qv.w, t.x, t.y, o[6], o[7], smask);
+    uint32_t *dst = tile + 4 * slot_index(tl >> 2, 8 * j) + (tl & 3);
+#pragma unroll
+    for (int w = 0; w < 8; w++)
+        dst[4 * w] = o[w];
+}
+
 // One unit: the 32 codes of token tl in MX column j (16 bytes) -> 32 E4M3
 // bytes into the FP8 tile, for the block's aligned exponent S and the
 // token's own exponent e.
@@ -524,7 +554,7 @@ inline size_t cols1_dyn_bytes(int32_t G)
 {
     return kSmemAlign + static_cast<size_t>(kStages) * kCodeBytes +
            static_cast<size_t>(kExpBufs) *
-               (kExpBytes + kTok * sizeof(uint4) + kStartWords * sizeof(int32_t)) +
+               (kExpBytes + 2 * kTok * sizeof(uint4) + kStartWords * sizeof(int32_t)) +
            kTileWords * sizeof(uint32_t) + static_cast<size_t>(G + 1) * 2 * sizeof(int32_t);
 }
 
@@ -547,7 +577,8 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
                                      (kSmemAlign - 1));
     uint8_t *exp_ring = codes_ring + kStages * kCodeBytes;
     uint4 *Sring = reinterpret_cast<uint4 *>(exp_ring + kExpBufs * kExpBytes);  // [kExpBufs][kTok]
-    uint32_t *tile = reinterpret_cast<uint32_t *>(Sring + kExpBufs * kTok);    // [kTileWords]
+    uint4 *Uring = Sring + kExpBufs * kTok;                                     // [kExpBufs][kTok]
+    uint32_t *tile = reinterpret_cast<uint32_t *>(Uring + kExpBufs * kTok);    // [kTileWords]
     int32_t *starts = reinterpret_cast<int32_t *>(tile + kTileWords);         // [kExpBufs][kStartWords]
     int32_t *off = starts + kExpBufs * kStartWords;                           // [G + 1]
     int32_t *base = off + G + 1;                                              // [G + 1]
@@ -590,6 +621,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
         const int bf = m % kExpBufs;
         const uint4 *ex = reinterpret_cast<const uint4 *>(exp_ring + bf * kExpBytes);
         uint4 *S_of = Sring + bf * kTok;
+        uint4 *U_of = Uring + bf * kTok;
         int32_t *st_list = starts + bf * kStartWords;
         const int32_t We = min(W + kTok, M);
         const int gW = warp_find_last_le(off, G, W);
@@ -624,8 +656,12 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
                        (__reduce_max_sync(0xffffffffu, w >> 24) << 24);
             };
             const uint4 S = make_uint4(wmax(m4.x), wmax(m4.y), wmax(m4.z), wmax(m4.w));
-            for (int32_t t = max(bs, W) + lane; t < min(be, We); t += 32)
+            for (int32_t t = max(bs, W) + lane; t < min(be, We); t += 32) {
                 S_of[t - W] = S;
+                const uint4 e = ex[t - W + kTok];
+                U_of[t - W] = make_uint4(shift_rows4(S.x, e.x, k), shift_rows4(S.y, e.y, k),
+                                         shift_rows4(S.z, e.z, k), shift_rows4(S.w, e.w, k));
+            }
             if (lane == 0) {  // blocks that start here get their scales written
                 st_list[1 + 2 * jb] = bs >= W ? bs - W : -1;
                 st_list[2 + 2 * jb] = b;
@@ -652,15 +688,17 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     };
 
     // ---- super-tile 0: copies, then its maxima with every warp
-    if (tid == kThreads) {
+    if (tid == kThreads) {  // a light first burst: the first tile's data only
         issue_exps(0);
-        for (int32_t n = 0; n < kStages - 1 && n < my_tiles; n++)
-            issue_codes(n);
+        issue_codes(0);
     }
     const bool ok0 = !__syncthreads_or(!mbar_wait(&full_e[0], 0));
     if (ok0)
         maxima(0, wid, kThreads1p / 32);
     __syncthreads();
+    if (tid == kThreads)
+        for (int32_t n = 1; n < kStages - 1 && n < my_tiles; n++)
+            issue_codes(n);
 
     if (wid == kConvWarps) {
         // ================================================= producer warp
@@ -718,13 +756,16 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
         // every code copy issued is waited for by the converting warps and
         // every exponent copy by this warp; if a wait gave up, report and
         // wait (bounded) for the copies still in flight before the CTA's
-        // shared memory is released
+        // shared memory is released.  A code stage that took a later copy
+        // was released first, so only the last kStages copies can be in
+        // flight (waiting on an older one would name a phase the stage has
+        // since passed, and run into the time limit)
         if (!ok) {
             if (lane == 0 && dev_status)
                 atomicOr(dev_status, 2);
             for (int32_t m = waited_e; m < issued_e; m++)
                 mbar_wait(&full_e[m % kExpBufs], static_cast<uint32_t>(m / kExpBufs) & 1u);
-            for (int32_t n = 0; n < issued_c; n++)
+            for (int32_t n = max(0, issued_c - kStages); n < issued_c; n++)
                 mbar_wait(&full_c[n % kStages], static_cast<uint32_t>(n / kStages) & 1u);
         }
         return;
@@ -745,8 +786,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     for (int32_t n = 0; n < my_tiles; n++) {
         const int i = n & 3;  // tile within the super-tile
         const int32_t W = win * kTok, f = 4 * F + i;
-        const bool ok = mbar_wait(&full_c[st], ph_c) &&
-                        (i != 0 || (mbar_wait(&sready[bf], ph_e) && mbar_wait(&full_e[bf], ph_e)));
+        const bool ok = mbar_wait(&full_c[st], ph_c) && (i != 0 || mbar_wait(&sready[bf], ph_e));
         if (n > 0)
             named_barrier_or(1, kThreads, false);  // the previous tile has been written out
         if (ok && tid < kTok) {
@@ -767,16 +807,13 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
         }
         if (ok) {
             const uint4 *codes = reinterpret_cast<const uint4 *>(codes_ring + st * kCodeBytes);
-            const uint32_t *ex = reinterpret_cast<const uint32_t *>(exp_ring + bf * kExpBytes);
-            const uint32_t *S_of = reinterpret_cast<const uint32_t *>(Sring + bf * kTok);
+            const uint32_t *U_w = reinterpret_cast<const uint32_t *>(Uring + bf * kTok);
 #pragma unroll
             for (int h = 0; h < 2; h++) {
                 const int tl = tl0 + 64 * h;
-                if (W + tl < M) {
-                    const uint32_t S = (S_of[tl * 4 + i] >> (8 * j)) & 0xFFu;
-                    const uint32_t e = (ex[(kTok + tl) * 4 + i] >> (8 * j)) & 0xFFu;
-                    convert_unit(tile, tab, tl, j, codes[tl * 4 + j], S, e, k);
-                }
+                if (W + tl < M)
+                    convert_unit_row(tile, tab, tl, j, codes[tl * 4 + j],
+                                     (U_w[tl * 4 + i] >> (8 * j)) & 0xFFu);
             }
         }
         __syncwarp();

@@ -118,7 +118,9 @@ int64_t fp4_to_fp8_cols_scale_capacity(int64_t M, int32_t G);
 /* Number of kernels fp4_to_fp8_cols enqueues for feature count K: 1 (a
  * single pass that also computes the block scales) when K % 512 == 0 and the
  * CUDA driver can encode tensor maps, else 2 (a block-scale pass, then the
- * conversion); 0 for a K the conversion rejects.  Host only, no GPU work. */
+ * conversion); 0 for a K the conversion rejects.  Host only: no kernel is
+ * launched (for K % 512 == 0 it initialises the CUDA runtime on the current
+ * device, as the conversion itself would). */
 int fp4_to_fp8_cols_launch_count(int64_t K);
 
 /*

@@ -220,6 +220,22 @@ def test_fp4_to_fp8_cols(fq, case, k, path):
     run_cols(fq, q, s, offs, k)
 
 
+def test_fp4_to_fp8_cols_launch_count_in_a_fresh_process(fq):
+    """The single pass is chosen even when the launch-count query is the
+    process's first CUDA call (the tensor-map encoder lookup initialises the
+    runtime itself, and a failed lookup is not kept)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import fp8_quantization_gb300 as fq; "
+            "print(fq.fp4_to_fp8_cols_launch_count(512), fq.fp4_to_fp8_cols_launch_count(7168))")
+    out = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                         timeout=300)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split() == ["1", "1"]
+
+
 @pytest.mark.parametrize("K", [256, 512])
 def test_fp4_to_fp8_cols_malformed_offsets(fq, K):
     # malformed offsets: clamped in-kernel, status raised, nothing written

@@ -309,8 +309,17 @@ __device__ __forceinline__ uint32_t encode8_sr(uint4 v, float r, uint32_t w0, ui
     return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
+// max(|a|, |b|, |c|) in one instruction; a NaN input is ignored (as by
+// fmaxf) unless all three are NaN.
+__device__ __forceinline__ float absmax3f(float a, float b, float c)
+{
+    float r;
+    asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // The same scale and encoders for binary32 block values (the transformed
-// blocks): amax over |y| with fmaxf, codes from y * r with y's sign.
+// blocks): amax over |y| (NaN ignored), codes from y * r with y's sign.
 __device__ __forceinline__ BlockScale nvfp4_block_scale_f(float amax, float enc, const float *rtab)
 {
     BlockScale bs;
@@ -464,6 +473,18 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_rht_kernel(
                 v[u][0] = v[u][1] = make_uint4(0, 0, 0, 0);
             }
         }
+        if (kSR) {
+            // with stochastic rounding the arithmetic below keeps each warp
+            // busy long enough that its next loads start late: the next
+            // iteration's blocks are requested into L2 now (no registers
+            // held; round to nearest is bound by HBM and gains nothing)
+#pragma unroll
+            for (int u = 0; u < kU; u++) {
+                const int64_t nb = b0 + (kU + u) * nthr;
+                if (nb < nblk)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(x + nb * 16));
+            }
+        }
 #pragma unroll
         for (int u = 0; u < kU; u++) {
             const int64_t blk = b0 + u * nthr;
@@ -471,10 +492,10 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_rht_kernel(
                 break;
             float y[16];
             rht16(v[u][0], v[u][1], f, y);
-            float a = 0.0f;
+            float a = 0.0f;  // max |y|, NaN ignored
 #pragma unroll
-            for (int i = 0; i < 16; i++)
-                a = fmaxf(a, fabsf(y[i]));
+            for (int i = 0; i < 16; i += 2)
+                a = absmax3f(a, y[i], y[i + 1]);
             const BlockScale bs = nvfp4_block_scale_f(a, ts.enc, rtab);
             uint2 codes;
             if (kSR) {

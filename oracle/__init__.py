@@ -89,6 +89,8 @@ def lib():
                                                          u64, u64, vp, vp, vp]),
                 "oracle_nvfp4_quantize_2d": (ctypes.c_int, [vp, i64, i64, ctypes.c_float, vp, vp,
                                                             vp]),
+                "oracle_nvfp4_quantize_2d_t": (ctypes.c_int, [vp, i64, i64, ctypes.c_float, vp,
+                                                              vp, vp, vp, vp]),
                 "oracle_rht16": (ctypes.c_int, [vp, i64, ctypes.c_uint32, vp]),
                 "oracle_fp8_quantize_blocks": (ctypes.c_int, [vp, i64, i64, ctypes.c_int, vp, vp]),
                 "oracle_window_estimate": (ctypes.c_float, [vp, i32, ctypes.c_uint32]),
@@ -250,6 +252,23 @@ def nvfp4_quantize_2d(w, amax):
     if rc:
         raise ValueError("oracle_nvfp4_quantize_2d: bad arguments")
     return q, sb, g[0]
+
+
+def nvfp4_quantize_2d_t(w, amax):
+    """2D weight quantization with the transposed (DGRAD) operand: (q [N, K/2],
+    sb [N/16, K/16], qT [K, N/2], sbT [K/16, N/16], g)."""
+    w = _bits(w)
+    N, K = w.shape
+    q = np.zeros((N, K // 2), dtype=np.uint8)
+    sb = np.zeros((N // 16, K // 16), dtype=np.uint8)
+    qT = np.zeros((K, N // 2), dtype=np.uint8)
+    sbT = np.zeros((K // 16, N // 16), dtype=np.uint8)
+    g = np.zeros(1, dtype=np.float32)
+    rc = lib().oracle_nvfp4_quantize_2d_t(_p(w), N, K, float(np.float32(amax)), _p(q), _p(sb),
+                                          _p(qT), _p(sbT), _p(g))
+    if rc:
+        raise ValueError("oracle_nvfp4_quantize_2d_t: bad arguments")
+    return q, sb, qT, sbT, g[0]
 
 
 # ---------------------------------------------------------------- decoding helpers

@@ -689,6 +689,32 @@ int oracle_nvfp4_quantize_2d(const uint16_t *w, int64_t N, int64_t K, float A, u
     return ORACLE_OK;
 }
 
+/* ------------------------------------------------------------------ 2D weights, both GEMM operands
+ * [NVFP4], section "Receta de pre-entrenamiento NVFP4" (2D weight scaling):
+ * one FP8 scale per 16x16 weight block, so FPROP and its transposed DGRAD use
+ * the same scale.
+ * READING (R20): the DGRAD operand is W^T [K, N] in the same layout as any 2D
+ * quantized tensor (codes [K, N/2], element (k, n) in nibble n of row k,
+ * scales [K/16, N/16]); block (j, i) of W^T is block (i, j) of W, so its scale
+ * is sb[i][j] and every code is W's code of the same element.  Written out:
+ * the 2D quantization of W, then the transposition of its codes and scales.
+ */
+int oracle_nvfp4_quantize_2d_t(const uint16_t *w, int64_t N, int64_t K, float A, uint8_t *q,
+                               uint8_t *sb, uint8_t *qT, uint8_t *sbT, float *g_out)
+{
+    int rc = oracle_nvfp4_quantize_2d(w, N, K, A, q, sb, g_out);
+    if (rc != ORACLE_OK)
+        return rc;
+    int64_t tn = N / 16, tk = K / 16;
+    for (int64_t k = 0; k < K; k++)
+        for (int64_t n = 0; n < N; n++)
+            put_nibble(qT, k * N + n, get_nibble(q, n * K + k));
+    for (int64_t j = 0; j < tk; j++)
+        for (int64_t i = 0; i < tn; i++)
+            sbT[j * tn + i] = sb[i * tk + j];
+    return ORACLE_OK;
+}
+
 /* ------------------------------------------------------------------ FP8 E4M3 block quantization
  * The backward-pass FP8 flow ([MoE-FP4] 2.2: gradients stay in standard
  * FP8; 2.1: the Hopper FP8 pipeline the conversion targets is E4M3 with

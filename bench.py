@@ -55,7 +55,7 @@ KERNEL_SRC = {
     "bf16_to_mxfp4_fp8": "fq_mxfp4.cu", "nvfp4_amax_rht": "fq_nvfp4.cu",
     "nvfp4_quantize_rht": "fq_nvfp4.cu", "fp8_quantize_1x128": "fq_fp8.cu",
     "fp8_quantize_128x128": "fq_fp8.cu", "mxfp4_dequantize_rows": "fq_fp8.cu",
-    "nvfp4_quantize_delayed": "fq_nvfp4.cu",
+    "nvfp4_quantize_delayed": "fq_nvfp4.cu", "nvfp4_quantize_2d_t": "fq_nvfp4.cu",
 }
 FALLBACK_HBM_GBS = 6800.0
 
@@ -443,6 +443,10 @@ def run_gpu(args):
         dstep[0] += 1
 
     delayed_us = timed_us(delayed_call)
+    qT = torch.empty((K, M // 2), dtype=torch.uint8, device=dev)
+    sbT = torch.empty((K // 16, M // 16), dtype=torch.uint8, device=dev)
+    w2t_us = timed_us(lambda: fq.nvfp4_quantize_2d_t(x, out["amax"], out["q2"], out["sb2"], qT,
+                                                     sbT, out["g2"]))
     next_rows = {
         "bf16_to_mxfp4_fp8": entry(
             "bf16_to_mxfp4_fp8", fused_us,
@@ -460,6 +464,9 @@ def run_gpu(args):
             "nvfp4_quantize_delayed", delayed_us, 2 * E + E // 2 + E // 16 + 16 * 65, 1, window=64,
             amax_then_quantize_us=round(kernels["nvfp4_amax"]["us"] +
                                         kernels["nvfp4_quantize"]["us"], 2)),
+        "nvfp4_quantize_2d_t": entry(
+            "nvfp4_quantize_2d_t", w2t_us, 2 * E + E // 2 + E // 256 + E // 2 + E // 256 + 8, 1,
+            without_transpose_us=kernels["nvfp4_quantize_2d"]["us"]),
         "steps": extra_steps,
     }
 

@@ -47,6 +47,7 @@ SIGNATURES = {
     "nvfp4_amax": (_int, [_vp, _i64, _vp, _vp]),
     "nvfp4_quantize": (_int, [_vp, _i64, _i64, _vp, _int, _u64, _u64, _vp, _vp, _vp, _vp]),
     "nvfp4_quantize_2d": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
+    "nvfp4_quantize_2d_t": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "nvfp4_amax_rht": (_int, [_vp, _i64, ctypes.c_uint32, _vp, _vp]),
     "fp8_quantize_1x128": (_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
     "nvfp4_quantize_delayed": (_int, [_vp, _i64, _i64, _vp, _i32, ctypes.c_uint32, _int, _u64, _u64,
@@ -273,6 +274,31 @@ def nvfp4_quantize_2d(w: torch.Tensor, amax: torch.Tensor | None = None,
     _need(g, torch.float32, "g")
     _call("nvfp4_quantize_2d", _p(w), N, K, _p(amax), _p(q), _p(sb), _p(g), _stream())
     return q, sb, g
+
+
+def nvfp4_quantize_2d_t(w: torch.Tensor, amax: torch.Tensor | None = None, q=None, sb=None,
+                        qT=None, sbT=None, g=None):
+    """BF16 [N, K] -> (q uint8 [N, K/2], sb uint8 [N/16, K/16], qT uint8
+    [K, N/2], sbT uint8 [K/16, N/16], g float32 [1]): the 2D-scaled weight for
+    FPROP and its transpose for DGRAD, sharing the 16x16 scales, in one read."""
+    _bf16_2d(w, "w")
+    N, K = w.shape
+    amax = nvfp4_amax(w) if amax is None else amax
+    _need(amax, torch.float32, "amax")
+    q = _empty((N, K // 2), torch.uint8, w) if q is None else q
+    sb = _empty((N // 16, K // 16), torch.uint8, w) if sb is None else sb
+    qT = _empty((K, N // 2), torch.uint8, w) if qT is None else qT
+    sbT = _empty((K // 16, N // 16), torch.uint8, w) if sbT is None else sbT
+    g = _empty((1,), torch.float32, w) if g is None else g
+    for t, name in ((q, "q"), (sb, "sb"), (qT, "qT"), (sbT, "sbT")):
+        _need(t, torch.uint8, name)
+    _need(g, torch.float32, "g")
+    if (q.numel() * 2 != N * K or qT.numel() * 2 != N * K or sb.numel() * 256 != N * K or
+            sbT.numel() * 256 != N * K):
+        raise ValueError("output sizes do not match w")
+    _call("nvfp4_quantize_2d_t", _p(w), N, K, _p(amax), _p(q), _p(sb), _p(qT), _p(sbT), _p(g),
+          _stream())
+    return q, sb, qT, sbT, g
 
 
 # ---------------------------------------------------------------- NVFP4 with the Hadamard transform

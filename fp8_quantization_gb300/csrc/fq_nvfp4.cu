@@ -309,17 +309,18 @@ __device__ __forceinline__ uint32_t encode8_sr(uint4 v, float r, uint32_t w0, ui
     return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
-// max(|a|, |b|, |c|) in one instruction; a NaN input is ignored (as by
-// fmaxf) unless all three are NaN.
-__device__ __forceinline__ float absmax3f(float a, float b, float c)
+// max(|a|, |b|, |c|) in one instruction, NaN if any input is NaN (a block
+// holding NaN gets the NaN scale byte, as the integer maximum of the BF16
+// paths gives).
+__device__ __forceinline__ float absmax3f_nan(float a, float b, float c)
 {
     float r;
-    asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    asm("max.NaN.abs.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
 }
 
 // The same scale and encoders for binary32 block values (the transformed
-// blocks): amax over |y| (NaN ignored), codes from y * r with y's sign.
+// blocks): amax over |y| (NaN propagates), codes from y * r with y's sign.
 __device__ __forceinline__ BlockScale nvfp4_block_scale_f(float amax, float enc, const float *rtab)
 {
     BlockScale bs;
@@ -492,10 +493,10 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_rht_kernel(
                 break;
             float y[16];
             rht16(v[u][0], v[u][1], f, y);
-            float a = 0.0f;  // max |y|, NaN ignored
+            float a = 0.0f;  // max |y|, NaN if the block holds NaN
 #pragma unroll
             for (int i = 0; i < 16; i += 2)
-                a = absmax3f(a, y[i], y[i + 1]);
+                a = absmax3f_nan(a, y[i], y[i + 1]);
             const BlockScale bs = nvfp4_block_scale_f(a, ts.enc, rtab);
             uint2 codes;
             if (kSR) {
@@ -517,9 +518,46 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_rht_kernel(
 
 // ---------------------------------------------------------------- 16x16
 
-// A warp owns a 16-row strip x 256 columns: lane l holds columns 8l..8l+7 of
-// all 16 rows (lanes 2t, 2t+1 form tile t), so every row load / store of the
-// warp is 512 / 128 contiguous bytes.
+// One warp's share of the 2D quantization: the 16-row strip `strip` x 256
+// columns from `col0`, lane l holding columns col0 + 8l .. + 7 of all 16 rows
+// (lanes 2t, 2t+1 form tile t), so every row load / store of the warp is
+// 512 / 128 contiguous bytes.  Writes the strip's codes and tile scales and
+// returns them (c[r] = the lane's eight codes of row r) for the caller.
+__device__ __forceinline__ uint32_t nvfp4_2d_strip(const uint16_t *__restrict__ w, int64_t K,
+                                                   int64_t strip, int64_t col, bool ok,
+                                                   const TensorScales &ts, const float *rtab,
+                                                   uint8_t *__restrict__ q,
+                                                   uint8_t *__restrict__ sb, uint32_t c[16])
+{
+    const int lane = threadIdx.x & 31;
+    const uint16_t *src = w + (strip << 4) * K + col;
+    uint4 v[16];
+#pragma unroll
+    for (int r = 0; r < 16; r++)
+        v[r] = ok ? ld_nc_v4(src + r * K) : make_uint4(0, 0, 0, 0);
+    uint32_t m = 0;
+#pragma unroll
+    for (int r = 0; r < 16; r++) {
+        m = absmax_bf16x2(m, v[r].x);
+        m = absmax_bf16x2(m, v[r].y);
+        m = absmax_bf16x2(m, v[r].z);
+        m = absmax_bf16x2(m, v[r].w);
+    }
+    m = max_u16x2(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    const BlockScale bs = nvfp4_block_scale(hmax_u16x2(m), ts.enc, rtab);
+    if (ok) {
+        uint8_t *dst = q + (strip << 4) * (K >> 1) + (col >> 1);
+#pragma unroll
+        for (int r = 0; r < 16; r++) {
+            c[r] = encode8_rne(v[r], bs.r);
+            __stcs(reinterpret_cast<unsigned int *>(dst + r * (K >> 1)), c[r]);
+        }
+        if (!(lane & 1))
+            sb[strip * (K >> 4) + (col >> 4)] = static_cast<uint8_t>(bs.b);
+    }
+    return bs.b;
+}
+
 __global__ void __launch_bounds__(kThreads, 2) nvfp4_quantize_2d_kernel(
     const uint16_t *__restrict__ w, int64_t N, int64_t K, const float *__restrict__ amax,
     uint8_t *__restrict__ q, uint8_t *__restrict__ sb, float *__restrict__ g_out)
@@ -538,30 +576,119 @@ __global__ void __launch_bounds__(kThreads, 2) nvfp4_quantize_2d_kernel(
     for (int64_t unit = warp; unit < nunits; unit += nwarps) {
         const int64_t strip = unit / ncg;
         const int64_t col = ((unit - strip * ncg) << 8) + 8 * lane;
-        const bool ok = col < K;
-        const uint16_t *src = w + (strip << 4) * K + col;
-        uint4 v[16];
+        uint32_t c[16];
+        nvfp4_2d_strip(w, K, strip, col, col < K, ts, rtab, q, sb, c);
+    }
+}
+
+// Transpose of an 8 x 8 matrix of nibbles held as eight words (A[i] nibble j
+// = M[i][j] -> A[j] nibble i = M[i][j]): the off-diagonal 4 x 4 and then 2 x 2
+// blocks swap with byte permutes, the 1 x 1 blocks with a masked exchange.
+__device__ __forceinline__ void transpose_nibbles8x8(uint32_t A[8])
+{
 #pragma unroll
-        for (int r = 0; r < 16; r++)
-            v[r] = ok ? ld_nc_v4(src + r * K) : make_uint4(0, 0, 0, 0);
-        uint32_t m = 0;
+    for (int i = 0; i < 4; i++) {
+        const uint32_t a = A[i], b = A[i + 4];
+        A[i] = prmt(a, b, 0x5410u);
+        A[i + 4] = prmt(a, b, 0x7632u);
+    }
 #pragma unroll
-        for (int r = 0; r < 16; r++) {
-            m = absmax_bf16x2(m, v[r].x);
-            m = absmax_bf16x2(m, v[r].y);
-            m = absmax_bf16x2(m, v[r].z);
-            m = absmax_bf16x2(m, v[r].w);
-        }
-        m = max_u16x2(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        const BlockScale bs = nvfp4_block_scale(hmax_u16x2(m), ts.enc, rtab);
+    for (int i = 0; i < 8; i += (i & 1) ? 3 : 1) {  // i = 0, 1, 4, 5
+        const uint32_t a = A[i], b = A[i + 2];
+        A[i] = prmt(a, b, 0x6240u);
+        A[i + 2] = prmt(a, b, 0x7351u);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+        const uint32_t t = ((A[i] >> 4) ^ A[i + 1]) & 0x0F0F0F0Fu;
+        A[i] ^= t << 4;
+        A[i + 1] ^= t;
+    }
+}
+
+// With the DGRAD operand W^T (the same codes and 16 x 16 scales, transposed).
+// A CTA unit is 8 consecutive strips (warp w: strip 8 sg + w) x one 256-column
+// group, i.e. a 128 x 256 block of W and a 256 x 128 block of W^T.  Each warp
+// quantizes its strip as above, transposes its lane's 16 x 8 codes in
+// registers (two 8 x 8 nibble transposes) and leaves the lane's eight W^T rows
+// (8 bytes each) in a shared tile of 256 rows x 64 bytes; the CTA then writes
+// every W^T row's 64 bytes with four 16-byte stores.  Tile slot (row, strip)
+// is stored at 2-word slot strip ^ ((row / 8) & 7), so the eight strips'
+// writes of one row phase spread over the banks.
+constexpr int kT2Strips = kThreads / 32;  // 8
+constexpr int kT2Rows = 256;              // W^T rows (columns of W) per unit
+
+__global__ void __launch_bounds__(kThreads, 2) nvfp4_quantize_2d_t_kernel(
+    const uint16_t *__restrict__ w, int64_t N, int64_t K, const float *__restrict__ amax,
+    uint8_t *__restrict__ q, uint8_t *__restrict__ sb, uint8_t *__restrict__ qT,
+    uint8_t *__restrict__ sbT, float *__restrict__ g_out)
+{
+    __shared__ float rtab[128];
+    __shared__ __align__(16) uint32_t tile[kT2Rows * 2 * kT2Strips];  // 16 KB
+    __shared__ uint8_t stile[16 * kT2Strips];  // [tile column][strip]
+    const TensorScales ts = nvfp4_tensor_setup(amax, rtab);
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        *g_out = ts.g;
+
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int64_t nstrips = N >> 4;
+    const int64_t nsg = (nstrips + kT2Strips - 1) / kT2Strips;
+    const int64_t ncg = (K + 255) >> 8;
+    const int64_t nunits = nsg * ncg;
+    const int64_t rowT = N >> 1;  // bytes per W^T row
+
+    for (int64_t unit = blockIdx.x; unit < nunits; unit += gridDim.x) {
+        const int64_t sg = unit / ncg, cg = unit - sg * ncg;
+        const int64_t strip = sg * kT2Strips + wid;
+        const int64_t col = (cg << 8) + 8 * lane;
+        const bool ok = strip < nstrips && col < K;
+        uint32_t c[16];
+        const uint32_t b = nvfp4_2d_strip(w, K, strip, col, ok, ts, rtab, q, sb, c);
         if (ok) {
-            uint8_t *dst = q + (strip << 4) * (K >> 1) + (col >> 1);
+            transpose_nibbles8x8(c);
+            transpose_nibbles8x8(c + 8);
+            // W^T row col + j: codes of strip rows 0..7 in the low word, 8..15 high
+            const int slot = 2 * (wid ^ (lane & 7));
 #pragma unroll
-            for (int r = 0; r < 16; r++)
-                __stcs(reinterpret_cast<unsigned int *>(dst + r * (K >> 1)), encode8_rne(v[r], bs.r));
+            for (int j = 0; j < 8; j++)
+                *reinterpret_cast<uint2 *>(&tile[(8 * lane + j) * 16 + slot]) =
+                    make_uint2(c[j], c[8 + j]);
             if (!(lane & 1))
-                sb[strip * (K >> 4) + (col >> 4)] = static_cast<uint8_t>(bs.b);
+                stile[(lane >> 1) * kT2Strips + wid] = static_cast<uint8_t>(b);
         }
+        __syncthreads();
+        const int rows = static_cast<int>(min(static_cast<int64_t>(kT2Rows), K - (cg << 8)));
+        const int strips = static_cast<int>(min(static_cast<int64_t>(kT2Strips), nstrips - sg * kT2Strips));
+        // four threads per W^T row, 16 bytes (strips 2p, 2p + 1) each
+        const int p = tid & 3;
+#pragma unroll
+        for (int i = 0; i < kT2Rows / (kThreads / 4); i++) {
+            const int r = (tid >> 2) + i * (kThreads / 4);
+            if (r < rows && 2 * p < strips) {
+                const int x = (r >> 3) & 7;
+                const uint2 lo = *reinterpret_cast<const uint2 *>(&tile[r * 16 + 2 * ((2 * p) ^ x)]);
+                uint8_t *dst = qT + ((cg << 8) + r) * rowT + sg * 64 + 16 * p;
+                if (2 * p + 1 < strips) {
+                    const uint2 hi =
+                        *reinterpret_cast<const uint2 *>(&tile[r * 16 + 2 * ((2 * p + 1) ^ x)]);
+                    if (!(rowT & 15)) {
+                        __stcs(reinterpret_cast<uint4 *>(dst), make_uint4(lo.x, lo.y, hi.x, hi.y));
+                    } else {
+                        __stcs(reinterpret_cast<uint2 *>(dst), lo);
+                        __stcs(reinterpret_cast<uint2 *>(dst + 8), hi);
+                    }
+                } else {
+                    __stcs(reinterpret_cast<uint2 *>(dst), lo);
+                }
+            }
+        }
+        // tile scales of W^T: row (16 cg + j) gets the unit's strips
+        if (tid < 16 * kT2Strips) {
+            const int j = tid / kT2Strips, s2 = tid % kT2Strips;
+            if (16 * j < rows && s2 < strips)
+                sbT[((cg << 4) + j) * (N >> 4) + sg * kT2Strips + s2] = stile[j * kT2Strips + s2];
+        }
+        __syncthreads();  // the tile is rewritten by the next unit
     }
 }
 
@@ -633,6 +760,28 @@ extern "C" fq_status nvfp4_quantize_2d(const void *w, int64_t N, int64_t K, cons
         persistent_grid(nvfp4_quantize_2d_kernel, kThreads, 0, (units + 7) / 8);
     nvfp4_quantize_2d_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t *>(w), N, K, amax, q, sb, g);
+    return launch_status();
+}
+
+extern "C" fq_status nvfp4_quantize_2d_t(const void *w, int64_t N, int64_t K, const float *amax,
+                                         uint8_t *q, uint8_t *sb, uint8_t *qT, uint8_t *sbT,
+                                         float *g, void *stream)
+{
+    if (N < 0 || K <= 0 || N % 16 != 0 || K % 16 != 0)
+        return FQ_ERR_SHAPE;
+    if (N > 0 && K > INT64_MAX / N)
+        return FQ_ERR_SHAPE;
+    if (N == 0)
+        return FQ_OK;
+    if (!w || !amax || !q || !sb || !qT || !sbT || !g)
+        return FQ_ERR_NULL;
+    if (!aligned16(w) || !aligned16(amax) || !aligned16(q) || !aligned16(sb) || !aligned16(qT) ||
+        !aligned16(sbT) || !aligned16(g))
+        return FQ_ERR_ALIGN;
+    const int64_t units = ((N / 16 + kT2Strips - 1) / kT2Strips) * ((K + 255) / 256);
+    const int grid = persistent_grid(nvfp4_quantize_2d_t_kernel, kThreads, 0, units);
+    nvfp4_quantize_2d_t_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(w), N, K, amax, q, sb, qT, sbT, g);
     return launch_status();
 }
 

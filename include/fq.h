@@ -302,6 +302,23 @@ fq_status nvfp4_quantize_delayed(const void *x, int64_t M, int64_t K, uint64_t *
 fq_status nvfp4_quantize_2d(const void *w, int64_t N, int64_t K, const float *amax, uint8_t *q,
                             uint8_t *sb, float *g, void *stream);
 
+/*
+ * The 2D weight quantization together with the DGRAD operand ([NVFP4]
+ * "Escalado de pesos 2D": FPROP and its transposed DGRAD use the same 16x16
+ * scales).  Reading: the DGRAD operand is W^T [K, N] laid out as any 2D
+ * quantized tensor, with block (j, i) scaled by sb[i][j] and every code equal
+ * to W's code of the same element; it is what nvfp4_quantize_2d gives for the
+ * BF16 transpose of w.  One read of w.
+ *   w, amax, q, sb, g : as in nvfp4_quantize_2d
+ *   qT  : uint8 [K, N/2] packed E2M1 codes of W^T (element (k, n) in nibble
+ *         n of row k, element 2i in the low nibble) (output)
+ *   sbT : uint8 [K/16, N/16] E4M3 tile scales of W^T, sbT[j][i] = sb[i][j]
+ *         (output)
+ * Requires N % 16 == 0, K % 16 == 0, K > 0, N >= 0; pointers 16-byte aligned.
+ */
+fq_status nvfp4_quantize_2d_t(const void *w, int64_t N, int64_t K, const float *amax, uint8_t *q,
+                              uint8_t *sb, uint8_t *qT, uint8_t *sbT, float *g, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -528,6 +528,36 @@ static void nvfp4_block_scales(float amax_blk, float g, int *b_out, float *r_out
     *r_out = r;
 }
 
+/* READING (R21, non-finite values; the pages are silent):
+ *  - the amax of a block (or 16x16 tile) holding NaN is NaN: NaN ranks above
+ *    +Inf, which ranks above every finite value.  Its scale byte is then
+ *    E4M3(NaN) = 0x7F, the format's NaN, and r is still min(1/(m(b) g),
+ *    FLT_MAX) with m the E4M3 magnitude formula (480 for the byte 0x7F);
+ *  - an element whose product |x| r is NaN (x NaN, or +-Inf times r = 0)
+ *    encodes as code 7 (+6, sign bit clear): Blackwell's FP4 conversion
+ *    turns every NaN, of either sign, into +6 (measured for both rounding
+ *    modes);
+ *  - +-Inf elements saturate to +-6 like any value >= 6.
+ * The block's codes do not matter to a reader (a NaN scale decodes the block
+ * to NaN); they are fixed so that every output byte is defined. */
+static float nvfp4_abs_max(float m, float v)
+{
+    float a = fabsf(v);
+    if (m != m || a != a)
+        return NAN;
+    return a > m ? a : m;
+}
+
+/* E2M1 code of |x| r with the sign of x (RNE or SR), NaN products per R21. */
+static int nvfp4_element_code(float x, float rs, int use_sr, uint32_t R)
+{
+    float yv = fabsf(x) * rs;
+    if (yv != yv)
+        return 7;
+    int c = use_sr ? e2m1_sr_sat((double)yv, R) : e2m1_rne_sat((double)yv);
+    return c | (signbit(x) ? 8 : 0);
+}
+
 /* One 16-element micro-block of NVFP4 ([NVFP4] "Receta": 16-element blocks,
  * E4M3 block scale, FP32 per-tensor scale g, RNE or stochastic rounding):
  * v[16] are the block's values, j0 the linear index of v[0] (for the
@@ -536,20 +566,15 @@ static void nvfp4_encode_block(const float *v, float g, int use_sr, uint64_t see
                                uint8_t *q, int64_t idx0, uint8_t *sb_out)
 {
     float amax = 0.0f;
-    for (int i = 0; i < 16; i++) {
-        float a = fabsf(v[i]);
-        if (a > amax)
-            amax = a;
-    }
+    for (int i = 0; i < 16; i++)
+        amax = nvfp4_abs_max(amax, v[i]);
     int b;
     float rs;
     nvfp4_block_scales(amax, g, &b, &rs);
     *sb_out = (uint8_t)b;
     for (int i = 0; i < 16; i++) {
-        float yv = fabsf(v[i]) * rs;
-        int c = use_sr ? e2m1_sr_sat((double)yv, sr_random16(seed, j0 + (uint64_t)i))
-                       : e2m1_rne_sat((double)yv);
-        put_nibble(q, idx0 + i, c | (signbit(v[i]) ? 8 : 0));
+        uint32_t R = use_sr ? sr_random16(seed, j0 + (uint64_t)i) : 0u;
+        put_nibble(q, idx0 + i, nvfp4_element_code(v[i], rs, use_sr, R));
     }
 }
 
@@ -668,11 +693,8 @@ int oracle_nvfp4_quantize_2d(const uint16_t *w, int64_t N, int64_t K, float A, u
         for (int64_t tc = 0; tc < tk; tc++) {
             float amax = 0.0f;
             for (int i = 0; i < 16; i++)
-                for (int j = 0; j < 16; j++) {
-                    float v = fabsf(bf16_bits_to_float(w[(16 * tr + i) * K + 16 * tc + j]));
-                    if (v > amax)
-                        amax = v;
-                }
+                for (int j = 0; j < 16; j++)
+                    amax = nvfp4_abs_max(amax, bf16_bits_to_float(w[(16 * tr + i) * K + 16 * tc + j]));
             int b;
             float rs;
             nvfp4_block_scales(amax, g, &b, &rs);
@@ -680,9 +702,7 @@ int oracle_nvfp4_quantize_2d(const uint16_t *w, int64_t N, int64_t K, float A, u
             for (int i = 0; i < 16; i++)
                 for (int j = 0; j < 16; j++) {
                     int64_t idx = (16 * tr + i) * K + 16 * tc + j;
-                    float yv = fabsf(bf16_bits_to_float(w[idx])) * rs;
-                    int c = e2m1_rne_sat((double)yv) | (bf16_sign(w[idx]) ? 8 : 0);
-                    put_nibble(q, idx, c);
+                    put_nibble(q, idx, nvfp4_element_code(bf16_bits_to_float(w[idx]), rs, 0, 0u));
                 }
         }
     }

@@ -181,6 +181,15 @@ def test_host_validation_nvfp4(lib):
     assert q2(P, 16, 24, P, P, P, P, None) == SHAPE
     assert q2(P, 16, 32, P, P, None, P, None) == NULL
     assert q2(P, 0, 32, P, P, P, P, None) == OK
+    t2 = lib.nvfp4_quantize_2d_t
+    # w, N, K, amax, q, sb, qT, sbT, g, stream
+    assert t2(P, 8, 32, P, P, P, P, P, P, None) == SHAPE                    # N % 16
+    assert t2(P, 16, 24, P, P, P, P, P, P, None) == SHAPE                   # K % 16
+    assert t2(P, 16, 0, P, P, P, P, P, P, None) == SHAPE
+    assert t2(P, 16, 32, P, P, P, None, P, P, None) == NULL                  # qT
+    assert t2(P, 16, 32, P, P, P, P, None, P, None) == NULL                  # sbT
+    assert t2(P, 16, 32, P, P, P, PM, P, P, None) == ALIGN
+    assert t2(P, 0, 32, P, P, P, None, None, P, None) == OK
     a = lib.nvfp4_amax
     assert a(P, -1, P, None) == SHAPE
     assert a(P, 4, None, None) == NULL

@@ -192,10 +192,17 @@ def test_nvfp4_weights_2d_14336x4096(fq):
     ra = oracle.nvfp4_amax(bits)
     assert amax.item() == float(ra)
     q, sb, g = fq.nvfp4_quantize_2d(w, amax)
-    rq, rsb, rg = oracle.nvfp4_quantize_2d(bits, ra)
+    rq, rsb, rqT, rsbT, rg = oracle.nvfp4_quantize_2d_t(bits, ra)
     eq(q, rq, "2d q")
     eq(sb, rsb, "2d scales")
     assert g.item() == float(rg)
+    # with the transposed DGRAD operand, in one read
+    q2, sb2, qT, sbT, g2 = fq.nvfp4_quantize_2d_t(w, amax)
+    eq(q2, rq, "2d_t q")
+    eq(sb2, rsb, "2d_t scales")
+    eq(qT, rqT, "2d_t qT")
+    eq(sbT, rsbT, "2d_t transposed scales")
+    assert g2.item() == float(rg)
 
 
 SWEEP_ROWS = [1024 << i for i in range(9)]  # 1K .. 262144 rows

@@ -354,8 +354,14 @@ def test_nvfp4_special_values(fq):
     x[1, :16] = -0.0
     x[2, :16] = np.float32(2.0 ** -130)
     x[3, :] *= np.float32(1e-30)
+    x[4, 5] = np.nan                    # NaN blocks take the NaN scale (R21)
+    x[5, 20] = -np.inf
+    x[6, 33] = np.inf
     bits = workloads.bf16_bits(x)
-    for A in (float(oracle.nvfp4_amax(bits)), 0.0, 1e-38, 3.0e38):
+    bits[7, 50] = 0xFFC1                # a negative NaN with a payload
+    finite = bits.copy()
+    finite[4, 5] = finite[5, 20] = finite[6, 33] = finite[7, 50] = 0
+    for A in (float(oracle.nvfp4_amax(finite)), 0.0, 1e-38, 3.0e38, float("inf"), float("nan")):
         amax = torch.tensor([A], dtype=torch.float32, device="cuda")
         for sr in (False, True):
             q, sb, g = fq.nvfp4_quantize(dev_bf16(bits), amax, use_sr=sr, seed=9)
@@ -398,6 +404,61 @@ def test_nvfp4_quantize_2d(fq, shape):
     assert g.item() == float(rg)
     check_canary(qraw, N * K // 2)
     check_canary(sraw, N * K // 256)
+
+
+@pytest.mark.parametrize("shape", [(16, 16), (32, 48), (48, 256), (64, 272), (256, 512),
+                                   (1024, 1040), (4096, 768)])
+def test_nvfp4_quantize_2d_t(fq, shape):
+    """The FPROP operand and the transposed DGRAD operand in one call, against
+    the oracle, with canaries on all four outputs."""
+    N, K = shape
+    bits = workloads.nvfp4_weight(N, K, seed=N * 3 + K)
+    w = dev_bf16(bits)
+    amax = fq.nvfp4_amax(w)
+    qraw, q = canary_out((N, K // 2), torch.uint8)
+    sraw, sb = canary_out((N // 16, K // 16), torch.uint8)
+    qTraw, qT = canary_out((K, N // 2), torch.uint8)
+    sTraw, sbT = canary_out((K // 16, N // 16), torch.uint8)
+    g = torch.empty(1, dtype=torch.float32, device="cuda")
+    fq.nvfp4_quantize_2d_t(w, amax, q, sb, qT, sbT, g)
+    rq, rsb, rqT, rsbT, rg = oracle.nvfp4_quantize_2d_t(bits, oracle.nvfp4_amax(bits))
+    eq(q, rq, "q")
+    eq(sb, rsb, "sb")
+    eq(qT, rqT, "qT")
+    eq(sbT, rsbT, "sbT")
+    assert g.item() == float(rg)
+    for raw, n in ((qraw, N * K // 2), (sraw, N * K // 256), (qTraw, N * K // 2),
+                   (sTraw, N * K // 256)):
+        check_canary(raw, n)
+
+
+def test_nvfp4_quantize_2d_t_special_tiles(fq):
+    """Zero and negative-zero tiles, BF16 subnormals, infinities, values near
+    the BF16 maximum and a tile far below the tensor maximum, through both
+    operands."""
+    rng = np.random.default_rng(11)
+    N, K = 64, 96
+    x = rng.normal(0.0, 0.02, (N, K)).astype(np.float32)
+    x[:16, :16] = 0.0
+    x[16:32, :16] = -0.0
+    x[:16, 16:32] = np.float32(2.0 ** -130) * rng.integers(-60, 61, (16, 16))
+    x[32, 40] = np.inf
+    x[50, 70] = -np.inf
+    x[48:64, 80:96] = np.float32(3.0e38) * rng.uniform(-1, 1, (16, 16))
+    x[32:48, :16] *= np.float32(1e-20)
+    x[20, 60] = np.nan
+    bits = workloads.bf16_bits(x)
+    bits[40, 90] = 0xFF81               # a negative NaN with a payload
+    for A in (float(oracle.nvfp4_amax(bits)), 1.0, 3.0e38, float("inf"), float("nan")):
+        amax = torch.tensor([A], dtype=torch.float32, device="cuda")
+        q, sb, qT, sbT, g = fq.nvfp4_quantize_2d_t(dev_bf16(bits), amax)
+        rq, rsb, rqT, rsbT, rg = oracle.nvfp4_quantize_2d_t(bits, np.float32(A))
+        for got, ref, what in ((q, rq, "q"), (sb, rsb, "sb"), (qT, rqT, "qT"), (sbT, rsbT, "sbT")):
+            eq(got, ref, f"{what} A={A}")
+        assert g.item() == float(rg) or (np.isnan(g.item()) and np.isnan(rg))
+        q2, sb2, _ = fq.nvfp4_quantize_2d(dev_bf16(bits), amax)
+        eq(q2, rq, f"2d q A={A}")
+        eq(sb2, rsb, f"2d sb A={A}")
 
 
 def test_errors_are_reported(fq):
@@ -469,6 +530,15 @@ def test_nvfp4_rht_special_values(fq):
     bad = bits.copy()
     bad[5, 3] = 0x7FC0
     assert np.isnan(fq.nvfp4_amax_rht(dev_bf16(bad), 0x2222).item())
+    # a NaN block of the transform takes the NaN scale, its NaN values code
+    # 7 (R21), under a finite, an infinite and a NaN per-tensor amax
+    for A in (float(oracle.nvfp4_amax_rht(bits, 0x2222)), float("inf"), float("nan")):
+        amax = torch.tensor([A], dtype=torch.float32, device="cuda")
+        for sr in (False, True):
+            q, sb, g = fq.nvfp4_quantize_rht(dev_bf16(bad), amax, 0x2222, use_sr=sr, seed=6)
+            rq, rsb, rg = oracle.nvfp4_quantize_rht(bad, np.float32(A), 0x2222, use_sr=sr, seed=6)
+            eq(q, rq, f"nan block q A={A} sr={sr}")
+            eq(sb, rsb, f"nan block sb A={A} sr={sr}")
     empty = torch.empty((0,), dtype=torch.bfloat16, device="cuda")
     assert fq.nvfp4_amax_rht(empty, 1).item() == 0.0
 
@@ -564,6 +634,30 @@ def test_nvfp4_quantize_delayed_sequence(fq, W):
         eq(sb, rsb, f"sb t={t}")
         assert g.item() == float(rg), t
         assert np.array_equal(hist_d.cpu().numpy().view(np.uint64), hist), f"history t={t}"
+
+
+def test_nvfp4_quantize_delayed_nan_step(fq):
+    """A step whose tensor holds NaN records a NaN amax; while it stays in the
+    window the estimate is NaN, so g = 1 (A > 0 fails), and the NaN step's own
+    blocks take the NaN scale (R21)."""
+    rng = np.random.default_rng(8)
+    W = 3
+    hist_d = fq.amax_history(W)
+    hist = np.zeros(W + 1, dtype=np.uint64)
+    for t in range(9):
+        bits = spiky_tensor(rng, 32, 64, t)
+        if t == 2:
+            bits[5, 9] = 0x7FC0
+        q, sb, g = fq.nvfp4_quantize_delayed(dev_bf16(bits), hist_d, t, use_sr=t % 2 == 1,
+                                             seed=3 + t)
+        rq, rsb, rg, hist = oracle.nvfp4_quantize_delayed(bits, hist, W, t, use_sr=t % 2 == 1,
+                                                          seed=3 + t)
+        eq(q, rq, f"q t={t}")
+        eq(sb, rsb, f"sb t={t}")
+        assert g.item() == float(rg), t
+        assert np.array_equal(hist_d.cpu().numpy().view(np.uint64), hist), f"history t={t}"
+        if 3 <= t <= 2 + W:
+            assert g.item() == 1.0
 
 
 def test_nvfp4_quantize_delayed_tag_wrap(fq):

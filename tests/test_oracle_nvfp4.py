@@ -260,3 +260,81 @@ def test_2d_error_bound_and_top_tile(oracle_mod):
     bg = np.repeat(np.repeat(oracle_mod.e4m3_decode(sb) * float(g), 16, axis=0), 16, axis=1)
     normal = np.repeat(np.repeat(sb >= 8, 16, axis=0), 16, axis=1)
     assert np.all(np.abs(x - xhat)[normal] <= bg[normal] * (1 + 1e-6))
+
+
+# ---- non-finite values (reading R21: NaN ranks above +Inf in a block's amax,
+# so a block holding NaN takes the NaN scale byte 0x7F; a NaN product encodes
+# as code 7 (+6, sign clear), which is what Blackwell's FP4 conversion gives
+# for any NaN; +-Inf saturates to +-6)
+
+def _codes(oracle_mod, q):
+    return oracle_mod.unpack_nibbles(q)
+
+
+@pytest.mark.parametrize("sr", [False, True])
+def test_nan_block_takes_the_nan_scale_and_nan_codes_are_plus_six(oracle_mod, sr):
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((2, 64)).astype(np.float32)
+    x[0, 3] = np.nan
+    bits = workloads.bf16_bits(x)
+    bits[1, 17] = 0xFFC1                       # a negative NaN with a payload
+    clean = bits.copy()
+    clean[0, 3] = 0
+    clean[1, 17] = 0
+    A = float(np.abs(f32(clean)).max())
+    q, sb, g = oracle_mod.nvfp4_quantize(bits, A, use_sr=sr, seed=5)
+    rq, rsb, rg = oracle_mod.nvfp4_quantize(clean, A, use_sr=sr, seed=5)
+    assert sb[0, 0] == 0x7F and sb[1, 1] == 0x7F          # the NaN blocks
+    others = np.ones(sb.shape, dtype=bool)
+    others[0, 0] = others[1, 1] = False
+    assert np.array_equal(sb[others], rsb[others])          # no other block moves
+    c, rc = _codes(oracle_mod, q), _codes(oracle_mod, rq)
+    assert c[0, 3] == 7 and c[1, 17] == 7                   # NaN of either sign -> +6
+    keep = np.ones(c.shape, dtype=bool)
+    keep[0, :16] = keep[1, 16:32] = False
+    assert np.array_equal(c[keep], rc[keep])
+
+
+def test_infinities_saturate_and_give_the_largest_block_scale(oracle_mod):
+    x = np.full((1, 32), 0.5, dtype=np.float32)
+    x[0, 2] = np.inf
+    x[0, 20] = -np.inf
+    bits = workloads.bf16_bits(x)
+    q, sb, g = oracle_mod.nvfp4_quantize(bits, 1.0)
+    # amax = Inf: t = Inf * enc saturates to the largest E4M3 scale, 448
+    assert sb.tolist() == [[0x7E, 0x7E]]
+    c = _codes(oracle_mod, q)
+    assert c[0, 2] == 0x7 and c[0, 20] == 0xF               # +6 and -6
+    # 0.5 * r with r = 1 / (448 g), g = 1/2688: 0.5 * 6 = 3 -> code 5
+    assert np.all(np.delete(c[0], [2, 20]) == 5)
+
+
+def test_infinite_tensor_scale(oracle_mod):
+    """A = +Inf: g = Inf and enc = 0, so finite blocks get scale 0 (codes +-0)
+    and a block holding +-Inf gets t = Inf * 0 = NaN -> the NaN scale byte,
+    r = 0, and its infinities give NaN products -> code 7."""
+    x = np.full((1, 48), -0.25, dtype=np.float32)
+    x[0, 1] = 2.0
+    x[0, 20] = -np.inf
+    bits = workloads.bf16_bits(x)
+    q, sb, g = oracle_mod.nvfp4_quantize(bits, float("inf"))
+    assert np.isinf(g)
+    assert sb.tolist() == [[0, 0x7F, 0]]
+    c = _codes(oracle_mod, q)[0]
+    assert c[1] == 0 and c[0] == 8 and np.all(c[32:] == 8)  # +0 for 2.0, -0 elsewhere
+    assert c[20] == 7 and np.all(np.delete(c[16:32], 4) == 8)
+
+
+def test_nan_tile_in_2d_scaling(oracle_mod):
+    rng = np.random.default_rng(22)
+    w = rng.normal(0.0, 0.02, (32, 32)).astype(np.float32)
+    bits = workloads.bf16_bits(w)
+    A = float(np.abs(f32(bits)).max())
+    rq, rsb, _ = oracle_mod.nvfp4_quantize_2d(bits, A)
+    bits[20, 5] = 0x7FC0
+    q, sb, _ = oracle_mod.nvfp4_quantize_2d(bits, A)
+    assert sb[1, 0] == 0x7F
+    assert sb[0, 0] == rsb[0, 0] and sb[0, 1] == rsb[0, 1] and sb[1, 1] == rsb[1, 1]
+    assert _codes(oracle_mod, q)[20, 5] == 7
+    _, _, qT, sbT, _ = oracle_mod.nvfp4_quantize_2d_t(bits, A)
+    assert sbT[0, 1] == 0x7F and _codes(oracle_mod, qT)[5, 20] == 7

@@ -254,3 +254,111 @@ def test_bandwidth_sweep_chain(fq):
             eq(yTs[:, wi:wi + 1].contiguous(), ryTs[:, :1], f"M={M} window {wi} yTs")
         del q, s, y, ys, yT, yTs
         torch.cuda.empty_cache()
+
+
+def test_more_than_2_31_elements(fq):
+    """131200 x 16384 BF16 = 2,149,580,800 elements, past 2^31: every call on
+    the whole tensor, and its outputs for rows at both ends and across element
+    2^31 (row 131072) checked against the oracle, with the tensor's amax and
+    the stochastic-rounding stream offsets of the sampled rows."""
+    M, K = 131200, 16384
+    assert M * K > 2**31 and (2**31) % K == 0
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(2**31 + 1)
+    x = torch.randn((M, K), generator=gen, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    strips = [0, 131056 // 16, 131072 // 16, M // 16 - 1]     # 16-row strips; 2^31 at row 131072
+    rows = np.concatenate([np.arange(16 * s, 16 * s + 16) for s in strips])
+    idx = torch.from_numpy(rows).cuda()
+    bits = x.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
+
+    def rows_of(t):
+        return t.index_select(0, idx)
+
+    # MXFP4 rows -> FP8 rows, and the one-call forward cast
+    q, s = fq.mxfp4_quantize_rows(x)
+    rq, rs = oracle.mxfp4_quantize_rows(bits)
+    eq(rows_of(q), rq, "mxfp4 q")
+    eq(rows_of(s), rs, "mxfp4 s")
+    y, ys = fq.fp4_to_fp8_rows(q, s, 3)
+    ry, rys = oracle.fp4_to_fp8_rows(rq, rs, 3)
+    eq(rows_of(y), ry, "fp8 rows y")
+    eq(rows_of(ys), rys, "fp8 rows ys")
+    del y, ys
+    # transposed, one group: the 128-token windows ending at and after 2^31
+    offs = np.array([0, M], dtype=np.int64)
+    yT, yTs = cols_full(fq, q, s, offs, 3)
+    for wi in (131072 // 128 - 1, M // 128 - 1):
+        t0 = 128 * wi
+        wbits = x[t0:t0 + 128].view(torch.int16).cpu().numpy().view(np.uint16)
+        wq, ws = oracle.mxfp4_quantize_rows(wbits)
+        ryT, ryTs = oracle.fp4_to_fp8_cols(wq, ws, np.array([0, 128], dtype=np.int64), 3)
+        eq(yT[:, t0:t0 + 128].contiguous(), ryT, f"window {wi} yT")
+        eq(yTs[:, wi:wi + 1].contiguous(), ryTs[:, :1], f"window {wi} yTs")
+    fused = fq.bf16_to_mxfp4_fp8(x, torch.from_numpy(offs).cuda(), 3)
+    assert torch.equal(fused[0], q) and torch.equal(fused[1], s) and torch.equal(fused[4], yT)
+    del q, s, yT, yTs, fused
+    torch.cuda.empty_cache()
+
+    # NVFP4: the amax, 1x16 with RNE and SR, 2D with the transposed operand
+    amax = fq.nvfp4_amax(x)
+    assert amax.item() == x.abs().max().float().item()
+    A = np.float32(amax.item())
+    for sr in (False, True):
+        q4, sb4, g4 = fq.nvfp4_quantize(x, amax, use_sr=sr, seed=77)
+        for sidx, st in enumerate(strips):
+            r0 = 16 * st
+            bq, bsb, bg = oracle.nvfp4_quantize(bits[16 * sidx:16 * sidx + 16], A, use_sr=sr,
+                                                seed=77, offset=r0 * K)
+            eq(q4[r0:r0 + 16], bq, f"nvfp4 q sr={sr} rows {r0}")
+            eq(sb4[r0:r0 + 16], bsb, f"nvfp4 sb sr={sr} rows {r0}")
+        assert g4.item() == float(bg)
+        del q4, sb4
+    q2, sb2, qT, sbT, g2 = fq.nvfp4_quantize_2d_t(x, amax)
+    for sidx, st in enumerate(strips):
+        r0 = 16 * st
+        bq, bsb, bqT, bsbT, _ = oracle.nvfp4_quantize_2d_t(bits[16 * sidx:16 * sidx + 16], A)
+        eq(q2[r0:r0 + 16], bq, f"2d q strip {st}")
+        eq(sb2[st:st + 1], bsb, f"2d sb strip {st}")
+        eq(qT[:, 8 * st:8 * st + 8].contiguous(), bqT, f"2d qT strip {st}")
+        eq(sbT[:, st:st + 1].contiguous(), bsbT, f"2d sbT strip {st}")
+    del q2, sb2, qT, sbT
+    # the transform (the GPU amax of the transform is the common A)
+    ar = fq.nvfp4_amax_rht(x, 0x5A5A)
+    Ar = np.float32(ar.item())
+    qh, sbh, gh = fq.nvfp4_quantize_rht(x, ar, 0x5A5A, use_sr=True, seed=5)
+    for sidx, st in enumerate(strips):
+        r0 = 16 * st
+        bq, bsb, _ = oracle.nvfp4_quantize_rht(bits[16 * sidx:16 * sidx + 16], Ar, 0x5A5A,
+                                               use_sr=True, seed=5, offset=r0 * K)
+        eq(qh[r0:r0 + 16], bq, f"rht q rows {r0}")
+        eq(sbh[r0:r0 + 16], bsb, f"rht sb rows {r0}")
+    del qh, sbh
+    # delayed scaling, first step of an empty history (estimate 0, g = 1)
+    hist = fq.amax_history(1)
+    qd, sbd, gd = fq.nvfp4_quantize_delayed(x, hist, 0, use_sr=True, seed=9)
+    assert gd.item() == 1.0
+    bq, bsb, _ = oracle.nvfp4_quantize(bits[-16:], np.float32(0.0), use_sr=True, seed=9,
+                                       offset=(M - 16) * K)
+    eq(qd[M - 16:], bq, "delayed q last rows")
+    eq(sbd[M - 16:], bsb, "delayed sb last rows")
+    assert int(hist.cpu().numpy().view(np.uint64)[0]) & 0xFFFFFFFF == int(
+        np.float32(amax.item()).view(np.uint32))
+    del qd, sbd
+    torch.cuda.empty_cache()
+
+    # FP8 1x128 rows, 128x128 tiles of the last 128 rows, MXFP4 -> BF16
+    yf, sf = fq.fp8_quantize_1x128(x)
+    by, bsf = oracle.fp8_quantize_blocks(bits, 1)
+    eq(rows_of(yf), by, "fp8 1x128 y")
+    eq(rows_of(sf), bsf, "fp8 1x128 s")
+    del yf, sf
+    yt, st2 = fq.fp8_quantize_128x128(x)
+    tb = x[M - 128:].view(torch.int16).cpu().numpy().view(np.uint16)
+    by2, bs2 = oracle.fp8_quantize_blocks(tb, 128)
+    eq(yt[M - 128:], by2, "fp8 128x128 y last tiles")
+    eq(st2[-1:], bs2, "fp8 128x128 s last tiles")
+    del yt, st2
+    q, s = fq.mxfp4_quantize_rows(x)
+    d = fq.mxfp4_dequantize_rows(q, s)
+    eq(rows_of(d).view(torch.int16), oracle.mxfp4_dequantize_rows(rq, rs).view(np.int16),
+       "dequant rows")

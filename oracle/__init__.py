@@ -79,6 +79,7 @@ def lib():
                 "oracle_e4m3_rne_array": (None, [vp, i64, vp]),
                 "oracle_fp4_to_fp8_element_array": (None, [vp, vp, ctypes.c_int, i64, vp]),
                 "oracle_num_threads": (ctypes.c_int, []),
+                "oracle_set_num_threads": (None, [ctypes.c_int]),
                 "oracle_mxfp4_quantize_rows": (ctypes.c_int, [vp, i64, i64, vp, vp]),
                 "oracle_fp4_to_fp8_rows": (ctypes.c_int, [vp, vp, i64, i64, ctypes.c_int, vp, vp]),
                 "oracle_fp4_to_fp8_cols_scale_capacity": (i64, [i64, i32]),
@@ -114,6 +115,11 @@ def lib():
 
 def num_threads() -> int:
     return int(lib().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's later calls from this thread (for timing)."""
+    lib().oracle_set_num_threads(int(n))
 
 
 # ---------------------------------------------------------------- scalars

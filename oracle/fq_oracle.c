@@ -323,6 +323,17 @@ int oracle_num_threads(void)
 #endif
 }
 
+/* Threads of the calling thread's later parallel loops (n >= 1). */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------ */
 /* a1: MXFP4 row quantization (BF16ToFP4Row, [MoE-FP4] 2.1 and 2.3)     */
 /* ------------------------------------------------------------------ */

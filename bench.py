@@ -317,7 +317,7 @@ def run_gpu(args):
     out = {
         "q": torch.empty((M, K // 2), **u8), "s": torch.empty((M, K // 32), **u8),
         "y": torch.empty((M, K), **u8), "ys": torch.empty((M, K // 128), **f32),
-        "yT": torch.empty((K, M), **u8), "yTs": torch.empty((K, cap), **f32),
+        "yT": torch.empty((K, M), **u8), "yTs": torch.empty((cap, K), **f32),
         "amax": torch.empty((1,), **f32),
         "q4": torch.empty((M, K // 2), **u8), "sb4": torch.empty((M, K // 16), **u8),
         "g4": torch.empty((1,), **f32),
@@ -563,6 +563,92 @@ def run_gpu(args):
     return 0
 
 
+# Launch order of --profile-configs (our kernels only), for reading an ncu
+# capture of it: (configuration, call) per launch.
+PROFILE_SWEEP = [1024 << i for i in range(9)]
+PROFILE_ORDER = (
+    [("cfg1 pr1 256x512", c) for c in ("mxfp4_quantize_rows", "fp4_to_fp8_rows k=0",
+                                        "fp4_to_fp8_rows k=6")] +
+    [("cfg2 moe_dispatch 16384x7168", c) for c in (
+        "mxfp4_quantize_rows", "fp4_to_fp8_rows", "fp4_to_fp8_cols (32 Zipf groups)",
+        "nvfp4_amax", "nvfp4_quantize SR", "nvfp4_quantize_2d")] +
+    [("cfg3 ragged_experts 65536x2048", c) for c in (
+        "mxfp4_quantize_rows", "fp4_to_fp8_cols (32 Zipf groups)")] +
+    [("cfg4 nvfp4 activations 16384x14336", c) for c in (
+        "nvfp4_amax", "nvfp4_quantize SR", "nvfp4_quantize RNE")] +
+    [("cfg4 nvfp4 weights 14336x4096", c) for c in ("nvfp4_amax", "nvfp4_quantize_2d")] +
+    [(f"cfg5 sweep {m}x7168", c) for m in PROFILE_SWEEP
+     for c in ("mxfp4_quantize_rows", "fp4_to_fp8_rows", "fp4_to_fp8_cols (1 group)")])
+
+
+def run_profile_configs():
+    """Every configuration's chain, one launch per call in PROFILE_ORDER, L2
+    cleaned before each: the launches an ncu pass over the configurations
+    captures.  Nothing is timed here; outputs are not checked (the tests do)."""
+    import torch
+    import numpy as np
+    import fp8_quantization_gb300 as fq
+    from fp8_quantization_gb300 import workloads
+    dev = torch.device("cuda", 0)
+    flush_buf = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+        flush_buf.sum(dtype=torch.int64)
+
+    def run(fn):
+        flush()
+        return fn()
+
+    def dev_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def offs_dev(o):
+        return torch.from_numpy(np.asarray(o, dtype=np.int64)).to(dev)
+
+    x = dev_bf16(workloads.pr1(256, 512, seed=0))
+    q, s = run(lambda: fq.mxfp4_quantize_rows(x))
+    run(lambda: fq.fp4_to_fp8_rows(q, s, 0))
+    run(lambda: fq.fp4_to_fp8_rows(q, s, 6))
+
+    x = dev_bf16(workloads.moe_dispatch(16384, 7168, seed=0))
+    o = offs_dev(workloads.zipf_group_offsets(16384, 32, 1.1, 0))
+    q, s = run(lambda: fq.mxfp4_quantize_rows(x))
+    run(lambda: fq.fp4_to_fp8_rows(q, s, 0))
+    run(lambda: fq.fp4_to_fp8_cols(q, s, o, 0))
+    amax = run(lambda: fq.nvfp4_amax(x))
+    run(lambda: fq.nvfp4_quantize(x, amax, use_sr=True, seed=1234))
+    run(lambda: fq.nvfp4_quantize_2d(x, amax))
+
+    bits, offs = workloads.ragged_experts(65536, 2048, 32, seed=0)
+    x = dev_bf16(bits)
+    q, s = run(lambda: fq.mxfp4_quantize_rows(x))
+    run(lambda: fq.fp4_to_fp8_cols(q, s, offs_dev(offs), 0))
+
+    x = dev_bf16(workloads.nvfp4_act(16384, 14336, seed=0))
+    amax = run(lambda: fq.nvfp4_amax(x))
+    run(lambda: fq.nvfp4_quantize(x, amax, use_sr=True, seed=1234))
+    run(lambda: fq.nvfp4_quantize(x, amax))
+    w = dev_bf16(workloads.nvfp4_weight(14336, 4096, seed=0))
+    wamax = run(lambda: fq.nvfp4_amax(w))
+    run(lambda: fq.nvfp4_quantize_2d(w, wamax))
+
+    del x, q, s, w
+    big = workloads.sweep(PROFILE_SWEEP[-1], 7168, seed=0)
+    xb = dev_bf16(big)
+    del big
+    for m in PROFILE_SWEEP:
+        xm = xb[:m]
+        q, s = run(lambda: fq.mxfp4_quantize_rows(xm))
+        run(lambda: fq.fp4_to_fp8_rows(q, s, 0))
+        run(lambda: fq.fp4_to_fp8_cols(q, s, offs_dev([0, m]), 0))
+        del q, s
+        torch.cuda.empty_cache()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_configs": len(PROFILE_ORDER)}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -570,7 +656,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["fq", "reference"], default="fq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-configs", action="store_true",
+                    help="run every configuration's calls once (for an ncu capture) and exit")
     args = ap.parse_args()
+    if args.profile_configs:
+        return run_profile_configs()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

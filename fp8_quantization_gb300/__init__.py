@@ -173,7 +173,8 @@ def fp4_to_fp8_cols(q: torch.Tensor, s: torch.Tensor, group_offsets: torch.Tenso
                     exp_offset_k: int = 0, yT: torch.Tensor | None = None,
                     yT_scale: torch.Tensor | None = None, dev_status: torch.Tensor | None = None):
     """MXFP4 [M tokens, K] with int64 group offsets [G+1] (device) ->
-    (yT uint8 [K, M] E4M3, yT_scale float32 [K, cap])."""
+    (yT uint8 [K, M] E4M3, yT_scale float32 [cap, K]: one row of K scales per
+    128-token block)."""
     _need(q, torch.uint8, "q", 2)
     _need(s, torch.uint8, "s", 2)
     _need(group_offsets, torch.int64, "group_offsets", 1)
@@ -181,15 +182,15 @@ def fp4_to_fp8_cols(q: torch.Tensor, s: torch.Tensor, group_offsets: torch.Tenso
     G = group_offsets.numel() - 1
     cap = fp4_to_fp8_cols_scale_capacity(M, max(G, 1))
     yT = _empty((K, M), torch.uint8, q) if yT is None else yT
-    yT_scale = _empty((K, cap), torch.float32, q) if yT_scale is None else yT_scale
+    yT_scale = _empty((cap, K), torch.float32, q) if yT_scale is None else yT_scale
     _need(yT, torch.uint8, "yT")
     _need(yT_scale, torch.float32, "yT_scale", 2)
     if dev_status is not None:
         _need(dev_status, torch.int32, "dev_status")
-    if yT.numel() != K * M or yT_scale.shape[0] != K:
+    if yT.numel() != K * M or yT_scale.shape[1] != K:
         raise ValueError("output sizes do not match q")
     _call("fp4_to_fp8_cols", _p(q), _p(s), M, K, _p(group_offsets), G, int(exp_offset_k), _p(yT),
-          _p(yT_scale), int(yT_scale.shape[1]), _p(dev_status), _stream())
+          _p(yT_scale), int(yT_scale.shape[0]), _p(dev_status), _stream())
     return yT, yT_scale
 
 
@@ -211,7 +212,7 @@ def bf16_to_mxfp4_fp8(x: torch.Tensor, group_offsets: torch.Tensor, exp_offset_k
     y = _empty((M, K), torch.uint8, x) if y is None else y
     ys = _empty((M, K // 128), torch.float32, x) if ys is None else ys
     yT = _empty((K, M), torch.uint8, x) if yT is None else yT
-    yT_scale = _empty((K, cap), torch.float32, x) if yT_scale is None else yT_scale
+    yT_scale = _empty((cap, K), torch.float32, x) if yT_scale is None else yT_scale
     for t, name, dt in ((q, "q", torch.uint8), (s, "s", torch.uint8), (y, "y", torch.uint8),
                         (ys, "ys", torch.float32), (yT, "yT", torch.uint8)):
         _need(t, dt, name)
@@ -219,10 +220,10 @@ def bf16_to_mxfp4_fp8(x: torch.Tensor, group_offsets: torch.Tensor, exp_offset_k
     if dev_status is not None:
         _need(dev_status, torch.int32, "dev_status")
     if (q.numel() * 2 != M * K or s.numel() * 32 != M * K or y.numel() != M * K or
-            ys.numel() * 128 != M * K or yT.numel() != M * K or yT_scale.shape[0] != K):
+            ys.numel() * 128 != M * K or yT.numel() != M * K or yT_scale.shape[1] != K):
         raise ValueError("output sizes do not match x")
     _call("bf16_to_mxfp4_fp8", _p(x), M, K, _p(group_offsets), G, int(exp_offset_k), _p(q), _p(s),
-          _p(y), _p(ys), _p(yT), _p(yT_scale), int(yT_scale.shape[1]), _p(dev_status), _stream())
+          _p(y), _p(ys), _p(yT), _p(yT_scale), int(yT_scale.shape[0]), _p(dev_status), _stream())
     return q, s, y, ys, yT, yT_scale
 
 

@@ -197,13 +197,13 @@ __device__ __forceinline__ uint32_t bytemax4(uint32_t a, uint32_t b)
 // CTA (exponent word w, 32 consecutive blocks): warp i reduces blocks
 // 4i..4i+3 of the chunk -- each lane loads the word w of four tokens per
 // block (16 loads in flight), then a byte-wise warp max -- and the CTA writes
-// the 128 feature rows of word w (4 MX columns x 32 rows) for its 32 blocks,
-// one 128-byte line per row.
+// the scales of the 128 features of word w (4 MX columns x 32) for its 32
+// blocks: 128 consecutive floats per block, one 128-byte line per warp store.
 constexpr int kScaleSlots = 32;
 
 __global__ void __launch_bounds__(kThreads) fp4_to_fp8_cols_scales_kernel(
     const uint8_t *__restrict__ s, int32_t M, int64_t K, const int64_t *__restrict__ offs,
-    int32_t G, int k, float *__restrict__ yTs, int64_t cap, int32_t *__restrict__ dev_status)
+    int32_t G, int k, float *__restrict__ yTs, int32_t *__restrict__ dev_status)
 {
     __shared__ int32_t warp_tot[kThreads / 32];
     __shared__ uint32_t smax[kScaleSlots];
@@ -252,17 +252,12 @@ __global__ void __launch_bounds__(kThreads) fp4_to_fp8_cols_scales_kernel(
                 smax[4 * wid + i] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
         }
         __syncthreads();
-        // ---- scales: row 128*word + rr, lane = block within the chunk
-        const int32_t slot = slot0 + lane;
-        if (slot < nblocks) {
-            const uint32_t Sw = smax[lane];
-            uint32_t *dst = out + (static_cast<int64_t>(word) * 128 + wid) * cap + slot;
-#pragma unroll 4
-            for (int rr = wid; rr < 128; rr += kThreads / 32) {
-                *dst = fp8_block_scale_bits((Sw >> (8 * (rr >> 5))) & 0xFFu, k);
-                dst += (kThreads / 32) * cap;
-            }
-        }
+        // ---- scales: feature 128*word + rr (rr = tid % 128) of the chunk's
+        // blocks tid / 128, tid / 128 + 2, ...
+        const int rr = tid & 127;
+        for (int c = tid >> 7; c < kScaleSlots && slot0 + c < nblocks; c += kThreads / 128)
+            out[static_cast<int64_t>(slot0 + c) * K + static_cast<int64_t>(word) * 128 + rr] =
+                fp8_block_scale_bits((smax[c] >> (8 * (rr >> 5))) & 0xFFu, k);
         __syncthreads();
     }
 }
@@ -383,7 +378,7 @@ template <bool kAligned16>
 __global__ void __launch_bounds__(kThreads, 4) fp4_to_fp8_cols_kernel(
     const uint8_t *__restrict__ q, const uint8_t *__restrict__ s, int32_t M, int64_t K,
     const int64_t *__restrict__ offs, int32_t G, int k, uint8_t *__restrict__ yT,
-    const float *__restrict__ yTs, int64_t cap)
+    const float *__restrict__ yTs)
 {
     __shared__ __align__(16) uint8_t tab[kTabRows * 8];
     __shared__ int32_t warp_tot[kThreads / 32];
@@ -423,15 +418,15 @@ __global__ void __launch_bounds__(kThreads, 4) fp4_to_fp8_cols_kernel(
         const int32_t end0 = off[g0 + 1];
         const uint8_t *qb = q + static_cast<int64_t>(W) * qrow + 64 * f;
         const uint8_t *sp = s + static_cast<int64_t>(W) * srow + 4 * f;
-        const uint32_t *yc = ys32 + (static_cast<int64_t>(f) * 128 + 32 * j) * cap;
+        const uint32_t *yc = ys32 + static_cast<int64_t>(f) * 128 + 32 * j;  // + slot * K
         if (W + kTok <= end0) {  // full window inside group g0 (warp-uniform)
             const int32_t t0 = W + tl0 - off[g0];
             P.q0 = ld_nc_v4(qb + qoff0);
             P.q1 = ld_nc_v4(qb + qoff1);
             P.e0 = __ldg(reinterpret_cast<const uint32_t *>(sp + soff0));
             P.e1 = __ldg(reinterpret_cast<const uint32_t *>(sp + soff1));
-            P.s0 = yc[base[g0] + (t0 >> 7)];
-            P.s1 = yc[base[g0] + ((t0 + 64) >> 7)];
+            P.s0 = yc[static_cast<int64_t>(base[g0] + (t0 >> 7)) * K];
+            P.s1 = yc[static_cast<int64_t>(base[g0] + ((t0 + 64) >> 7)) * K];
         } else {  // window crossing groups or past M
             const int32_t tA = W + tl0, tB = tA + 64;
             P.q0 = tA < M ? ld_nc_v4(qb + qoff0) : make_uint4(0, 0, 0, 0);
@@ -440,8 +435,8 @@ __global__ void __launch_bounds__(kThreads, 4) fp4_to_fp8_cols_kernel(
             P.e1 = tB < M ? __ldg(reinterpret_cast<const uint32_t *>(sp + soff1)) : 0u;
             const int gA = tA < end0 ? g0 : find_last_le(off, g0, G - 1, min(tA, M - 1));
             const int gB = tB < end0 ? g0 : find_last_le(off, g0, G - 1, min(tB, M - 1));
-            P.s0 = tA < M ? yc[base[gA] + ((tA - off[gA]) >> 7)] : 0u;
-            P.s1 = tB < M ? yc[base[gB] + ((tB - off[gB]) >> 7)] : 0u;
+            P.s0 = tA < M ? yc[static_cast<int64_t>(base[gA] + ((tA - off[gA]) >> 7)) * K] : 0u;
+            P.s1 = tB < M ? yc[static_cast<int64_t>(base[gB] + ((tB - off[gB]) >> 7)) * K] : 0u;
         }
     };
 
@@ -562,8 +557,7 @@ template <bool kAligned16>
 __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
     int32_t M, int32_t nfeat, const int64_t *__restrict__ offs, int32_t G, int k,
-    uint8_t *__restrict__ yT, float *__restrict__ yTs, int64_t cap,
-    int32_t *__restrict__ dev_status)
+    uint8_t *__restrict__ yT, float *__restrict__ yTs, int32_t *__restrict__ dev_status)
 {
     __shared__ __align__(16) uint8_t tab[kTabRows * 8];
     __shared__ int32_t warp_tot[kThreads1p / 32];
@@ -795,14 +789,15 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
             const int32_t *st_list = starts + bf * kStartWords;
             const int32_t ns = st_list[0];
             const uint32_t *S_w = reinterpret_cast<const uint32_t *>(Sring + bf * kTok);
-            uint32_t *dst = reinterpret_cast<uint32_t *>(yTs) +
-                            (static_cast<int64_t>(f) * 128 + tid) * cap;
+            // row of block b: K scales; this tile's 128 features are contiguous
+            uint32_t *dst = reinterpret_cast<uint32_t *>(yTs) + static_cast<int64_t>(f) * 128 + tid;
+            const int64_t nK = static_cast<int64_t>(nfeat) * 128;
             for (int32_t q = 0; q < ns; q++) {
                 const int32_t tb = st_list[1 + 2 * q];
                 if (tb < 0)
                     continue;
                 const uint32_t Sb = (S_w[tb * 4 + i] >> (8 * (tid >> 5))) & 0xFFu;
-                dst[st_list[2 + 2 * q]] = fp8_block_scale_bits(Sb, k);
+                dst[static_cast<int64_t>(st_list[2 + 2 * q]) * nK] = fp8_block_scale_bits(Sb, k);
             }
         }
         if (ok) {
@@ -887,9 +882,13 @@ fq_status fq::launch_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
     CUtensorMap tm_q, tm_s;
     if (K % 512 == 0 &&
         encode_tensor_map_2d_u8(&tm_q, q, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(M),
-                                static_cast<uint64_t>(K / 2), 64, kTok) &&
+                                static_cast<uint64_t>(K / 2), 64, kTok, false) &&
+        // a super-tile reads 16 of each exponent row's K/32 bytes; the rest of
+        // the 128-byte line belongs to super-tiles a whole pass of windows
+        // later, so whole-line promotion would fetch it again from DRAM once
+        // the tensor outgrows L2
         encode_tensor_map_2d_u8(&tm_s, s, static_cast<uint64_t>(K / 32), static_cast<uint64_t>(M),
-                                static_cast<uint64_t>(K / 32), kExpRowBytes, kTok)) {
+                                static_cast<uint64_t>(K / 32), kExpRowBytes, kTok, false)) {
         const size_t dyn = cols1_dyn_bytes(G);
         auto kern = M % 16 == 0 ? fp4_to_fp8_cols_1pass_kernel<true>
                                 : fp4_to_fp8_cols_1pass_kernel<false>;
@@ -901,7 +900,7 @@ fq_status fq::launch_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
         const int grid = persistent_grid(kern, kThreads1p, dyn, work_ctas / 4);
         if (launch_pdl(kern, dim3(grid), dim3(kThreads1p), dyn, st, tm_q, tm_s,
                        static_cast<int32_t>(M), static_cast<int32_t>(K / 128), group_offsets, G,
-                       exp_offset_k, yT, yT_scale, cap, dev_status) != cudaSuccess)
+                       exp_offset_k, yT, yT_scale, dev_status) != cudaSuccess)
             return launch_status();
         return launch_status();
     }
@@ -911,7 +910,7 @@ fq_status fq::launch_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
     const dim3 grid1(static_cast<unsigned>(K / 128),
                      static_cast<unsigned>(chunks < 65535 ? chunks : 65535));
     fp4_to_fp8_cols_scales_kernel<<<grid1, kThreads, groups_bytes, st>>>(
-        s, static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT_scale, cap, dev_status);
+        s, static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT_scale, dev_status);
     fq_status rc = launch_status();
     if (rc != FQ_OK)
         return rc;
@@ -926,7 +925,7 @@ fq_status fq::launch_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
         const int grid = persistent_grid(fp4_to_fp8_cols_kernel<true>, kThreads, dyn, work_ctas);
         if (launch_pdl(fp4_to_fp8_cols_kernel<true>, dim3(grid), dim3(kThreads), dyn, st, q, s,
                        static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT,
-                       static_cast<const float *>(yT_scale), cap) != cudaSuccess)
+                       static_cast<const float *>(yT_scale)) != cudaSuccess)
             return launch_status();
     } else {
         if (cudaFuncSetAttribute(fp4_to_fp8_cols_kernel<false>,
@@ -936,7 +935,7 @@ fq_status fq::launch_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
         const int grid = persistent_grid(fp4_to_fp8_cols_kernel<false>, kThreads, dyn, work_ctas);
         if (launch_pdl(fp4_to_fp8_cols_kernel<false>, dim3(grid), dim3(kThreads), dyn, st, q, s,
                        static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT,
-                       static_cast<const float *>(yT_scale), cap) != cudaSuccess)
+                       static_cast<const float *>(yT_scale)) != cudaSuccess)
             return launch_status();
     }
     return launch_status();

@@ -340,9 +340,12 @@ fq_status launch_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t M, 
                                  cudaStream_t st);
 
 // Host: encoder of tensor maps (driver entry point, looked up once).
-// Returns false if the driver does not provide it.
+// Returns false if the driver does not provide it.  promote_l2: fill whole
+// 128-byte L2 lines on a miss (for boxes whose neighbouring bytes are read
+// soon); otherwise only the 32-byte sectors the box touches are fetched.
 bool encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
-                             uint64_t row_pitch, uint32_t box_inner, uint32_t box_rows);
+                             uint64_t row_pitch, uint32_t box_inner, uint32_t box_rows,
+                             bool promote_l2 = true);
 
 // Philox4x32-10 (Salmon et al., SC'11).
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1)

@@ -132,9 +132,12 @@ int fp4_to_fp8_cols_launch_count(int64_t K);
  *                   offsets[g] .. offsets[g+1]-1; offsets[0] = 0,
  *                   non-decreasing, offsets[G] = M (empty groups allowed)
  *   yT            : uint8 [K, M]   E4M3, element (feature k, token t) at k*M + t
- *   yT_scale      : float [K, cap] FP32 scale of block b of group g at
- *                   k*cap + base_g + b, base_g = sum_{h<g} ceil(count_h/128);
- *                   slots past the last block are not written
+ *   yT_scale      : float [cap, K]: row base_g + b holds the FP32 scales of
+ *                   block b of group g, feature k at (base_g + b)*K + k,
+ *                   base_g = sum_{h<g} ceil(count_h/128) (one row of K
+ *                   scales per block, as a GEMM reading the scales of one
+ *                   token block wants them); rows past the last block are
+ *                   not written
  *   cap           : >= fp4_to_fp8_cols_scale_capacity(M, G)
  *   dev_status    : optional int32 in device memory; if the offsets are
  *                   malformed the kernel clamps them (so nothing is written

@@ -222,7 +222,7 @@ def fp4_to_fp8_cols(q, s, offs, k: int = 0, cap: int | None = None, fill_scale=n
     if cap is None:
         cap = fp4_to_fp8_cols_scale_capacity(M, G)
     yT = np.zeros((K, M), dtype=np.uint8)
-    yTs = np.full((K, cap), fill_scale, dtype=np.float32)
+    yTs = np.full((cap, K), fill_scale, dtype=np.float32)
     rc = lib().oracle_fp4_to_fp8_cols(_p(q), _p(s), M, K, _p(offs), G, int(k), _p(yT), _p(yTs),
                                       int(cap))
     if rc:

@@ -438,8 +438,9 @@ int64_t oracle_fp4_to_fp8_cols_scale_capacity(int64_t M, int32_t G)
  * READING: a group is cut into 128-token blocks starting at its first token;
  * the last block of a group may be short; blocks never straddle groups.
  * READING: element (feature k, token t) goes to yT[k*M + t] (the transpose of
- * the whole token matrix); block b of group g stores its scale at
- * yTs[k*cap + base_g + b], base_g = sum over h < g of ceil(count_h / 128).
+ * the whole token matrix); block b of group g stores the scale of feature k
+ * at yTs[(base_g + b)*K + k], base_g = sum over h < g of ceil(count_h / 128):
+ * one row of K scales per block, the feature index contiguous.
  * For one block and one 32-feature MX column, S is the max of the tokens'
  * exponents and each element is converted as in the row case. */
 int oracle_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t M, int64_t K,
@@ -474,7 +475,7 @@ int oracle_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t M, int64_
                         S = e;
                 }
                 for (int64_t kk = 32 * j; kk < 32 * j + 32; kk++) {
-                    yTs[kk * cap + base + b] =
+                    yTs[(base + b) * K + kk] =
                         special ? float_from_bits(0x7FC00000u) : ldexpf(1.0f, S - 127 - k);
                     for (int64_t t = t0; t < t1; t++) {
                         if (special) {

@@ -46,7 +46,7 @@ def cols_full(fq, q_d, s_d, offs, k):
     G = offs.size - 1
     cap = fq.fp4_to_fp8_cols_scale_capacity(M, G)
     yT = torch.empty((K, M), dtype=torch.uint8, device="cuda")
-    yTs = torch.empty((K, cap), dtype=torch.float32, device="cuda")
+    yTs = torch.empty((cap, K), dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     fq.fp4_to_fp8_cols(q_d, s_d, torch.from_numpy(offs).cuda(), k, yT, yTs, st)
     assert int(st.item()) == 0
@@ -76,10 +76,10 @@ def test_moe_dispatch_16384x7168_all_casts(fq):
     ryT, ryTs = oracle.fp4_to_fp8_cols(rq, rs, offs, 0)
     nb = int(((np.diff(offs) + 127) // 128).sum())
     eq(yT, ryT, "fp8 cols yT")
-    eq(yTs[:, :nb], ryTs[:, :nb], "fp8 cols scales")
+    eq(yTs[:nb], ryTs[:nb], "fp8 cols scales")
     for got, ref, what in zip(fused[:5], (rq, rs, ry, rys, ryT), ("q", "s", "y", "ys", "yT")):
         eq(got, ref, "fused " + what)
-    eq(fused[5][:, :nb], ryTs[:, :nb], "fused yT scales")
+    eq(fused[5][:nb], ryTs[:nb], "fused yT scales")
     ra = oracle.nvfp4_amax(bits)
     assert amax.item() == float(ra)
     rq4, rsb4, rg4 = oracle.nvfp4_quantize(bits, ra, use_sr=True, seed=1000, offset=0)
@@ -108,11 +108,11 @@ def test_ragged_experts_65536x2048(fq, k):
     ryT, ryTs = oracle.fp4_to_fp8_cols(rq, rs, offs, k)
     nb = int(((np.diff(offs) + 127) // 128).sum())
     eq(yT, ryT, "fp8 cols yT")
-    eq(yTs[:, :nb], ryTs[:, :nb], "fp8 cols scales")
+    eq(yTs[:nb], ryTs[:nb], "fp8 cols scales")
     ry, rys = oracle.fp4_to_fp8_rows(rq, rs, k)
     for got, ref, what in zip(fused[:5], (rq, rs, ry, rys, ryT), ("q", "s", "y", "ys", "yT")):
         eq(got, ref, "fused " + what)
-    eq(fused[5][:, :nb], ryTs[:, :nb], "fused yT scales")
+    eq(fused[5][:nb], ryTs[:nb], "fused yT scales")
 
 
 def test_nvfp4_activations_16384x14336(fq):
@@ -234,7 +234,7 @@ def test_bandwidth_sweep_chain(fq):
             ryT, ryTs = oracle.fp4_to_fp8_cols(rq, rs, offs, 0)
             nb = (M + 127) // 128
             eq(yT, ryT, f"M={M} yT")
-            eq(yTs[:, :nb], ryTs[:, :nb], f"M={M} yTs")
+            eq(yTs[:nb], ryTs[:nb], f"M={M} yTs")
             continue
         rows = np.unique(np.concatenate([rng.choice(M, 48, replace=False), [M - 1]]))
         rq, rs = oracle.mxfp4_quantize_rows(bits[rows])
@@ -251,7 +251,7 @@ def test_bandwidth_sweep_chain(fq):
             wq, ws = oracle.mxfp4_quantize_rows(bits[t0:t1])
             ryT, ryTs = oracle.fp4_to_fp8_cols(wq, ws, np.array([0, t1 - t0], dtype=np.int64), 0)
             eq(yT[:, t0:t1].contiguous(), ryT, f"M={M} window {wi} yT")
-            eq(yTs[:, wi:wi + 1].contiguous(), ryTs[:, :1], f"M={M} window {wi} yTs")
+            eq(yTs[wi:wi + 1], ryTs[:1], f"M={M} window {wi} yTs")
         del q, s, y, ys, yT, yTs
         torch.cuda.empty_cache()
 
@@ -293,7 +293,7 @@ def test_more_than_2_31_elements(fq):
         wq, ws = oracle.mxfp4_quantize_rows(wbits)
         ryT, ryTs = oracle.fp4_to_fp8_cols(wq, ws, np.array([0, 128], dtype=np.int64), 3)
         eq(yT[:, t0:t0 + 128].contiguous(), ryT, f"window {wi} yT")
-        eq(yTs[:, wi:wi + 1].contiguous(), ryTs[:, :1], f"window {wi} yTs")
+        eq(yTs[wi:wi + 1], ryTs[:1], f"window {wi} yTs")
     fused = fq.bf16_to_mxfp4_fp8(x, torch.from_numpy(offs).cuda(), 3)
     assert torch.equal(fused[0], q) and torch.equal(fused[1], s) and torch.equal(fused[4], yT)
     del q, s, yT, yTs, fused

@@ -224,8 +224,8 @@ def test_cols_equal_scales_is_transpose_of_rows(oracle_mod):
         np.testing.assert_array_equal(yT, y.T)
         counts = np.diff(offs)
         nb = int(((counts + 127) // 128).sum())
-        assert np.all(yTs[:, :nb] == np.float32(2.0 ** (117 - 127 - k)))
-        assert np.all(np.isnan(yTs[:, nb:]))   # unused slots untouched
+        assert np.all(yTs[:nb] == np.float32(2.0 ** (117 - 127 - k)))
+        assert np.all(np.isnan(yTs[nb:]))   # unused rows untouched
 
 
 def test_cols_ragged_equals_per_group_calls(oracle_mod):
@@ -240,7 +240,7 @@ def test_cols_ragged_equals_per_group_calls(oracle_mod):
         if b > a:
             yg, ygs = oracle_mod.fp4_to_fp8_cols(q[a:b], s[a:b], np.array([0, b - a]), 2)
             np.testing.assert_array_equal(yT[:, a:b], yg)
-            np.testing.assert_array_equal(yTs[:, base:base + nb], ygs[:, :nb])
+            np.testing.assert_array_equal(yTs[base:base + nb], ygs[:nb])
         base += nb
 
 
@@ -263,7 +263,7 @@ def test_cols_block_agrees_with_rows_on_runs(oracle_mod):
             y, ys = oracle_mod.fp4_to_fp8_rows(oracle_mod.pack_nibbles(row_codes),
                                                sig[:, j][None, :], k)
             np.testing.assert_array_equal(yT[f], y[0])
-            assert yTs[f, 0] == ys[0, 0]
+            assert yTs[0, f] == ys[0, 0]
 
 
 def test_cols_rejects_bad_offsets(oracle_mod):

@@ -519,16 +519,17 @@ __global__ void __launch_bounds__(kThreads, 4) fp4_to_fp8_cols_kernel(
 //    meeting the window are numbered consecutively; the byte-wise max of a
 //    block's exponent rows (up to 127 tokens beyond the window on either
 //    side come from the neighbouring rows) gives S for the 16 MX columns,
-//    stored per token of the window, with the blocks whose first token lies
-//    in the window.  The first super-tile's maxima are computed by all nine
-//    warps at once.
+//    from which it stores the shift-table row of every (token of the window,
+//    MX column) and, for a block whose first token lies in the window,
+//    writes the block's FP32 scales of the super-tile's 512 features (2 KB,
+//    contiguous in the block-major scale rows).  The first super-tile's
+//    maxima are computed by all nine warps at once.
 //  * The eight converting warps wait for a tile's codes (and, on a
-//    super-tile's first tile, for its maxima), write the FP32 scales of the
-//    blocks that start in the window (one feature row per thread), convert
-//    into the FP8 tile as in the two-launch path once every warp has
-//    written the previous tile out (named barrier), release the code stage
-//    (and, after the fourth tile, the exponent buffer), meet at a second
-//    named barrier and write the tile out transposed.
+//    super-tile's first tile, for its maxima), convert into the FP8 tile as
+//    in the two-launch path once every warp has written the previous tile
+//    out (named barrier), release the code stage (and, after the fourth
+//    tile, the exponent buffer), meet at a second named barrier and write
+//    the tile out transposed.
 // Every wait is bounded (mbar_wait); a wait that gives up ends the kernel
 // with bit 2 of *dev_status set.
 constexpr int kStages = 4;      // code stages
@@ -541,15 +542,12 @@ constexpr int kExpBytes = 3 * kTok * kExpRowBytes;
 constexpr int kSmemAlign = 128;  // tensor-copy destinations
 static_assert(kCodeBytes % kSmemAlign == 0 && kExpBytes % kSmemAlign == 0, "aligned buffers");
 
-// per exponent buffer: S of every token (uint4) and the blocks that start in
-// the window (count, then (token, block) pairs)
-constexpr int kStartWords = 1 + 2 * kTok;
-
+// per exponent buffer: the shift-table rows of every token (uint4: one byte
+// per MX column of the super-tile)
 inline size_t cols1_dyn_bytes(int32_t G)
 {
     return kSmemAlign + static_cast<size_t>(kStages) * kCodeBytes +
-           static_cast<size_t>(kExpBufs) *
-               (kExpBytes + 2 * kTok * sizeof(uint4) + kStartWords * sizeof(int32_t)) +
+           static_cast<size_t>(kExpBufs) * (kExpBytes + kTok * sizeof(uint4)) +
            kTileWords * sizeof(uint32_t) + static_cast<size_t>(G + 1) * 2 * sizeof(int32_t);
 }
 
@@ -570,11 +568,9 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     uint8_t *codes_ring = dyn_raw + ((kSmemAlign - (smem_u32(dyn_raw) & (kSmemAlign - 1))) &
                                      (kSmemAlign - 1));
     uint8_t *exp_ring = codes_ring + kStages * kCodeBytes;
-    uint4 *Sring = reinterpret_cast<uint4 *>(exp_ring + kExpBufs * kExpBytes);  // [kExpBufs][kTok]
-    uint4 *Uring = Sring + kExpBufs * kTok;                                     // [kExpBufs][kTok]
+    uint4 *Uring = reinterpret_cast<uint4 *>(exp_ring + kExpBufs * kExpBytes);  // [kExpBufs][kTok]
     uint32_t *tile = reinterpret_cast<uint32_t *>(Uring + kExpBufs * kTok);    // [kTileWords]
-    int32_t *starts = reinterpret_cast<int32_t *>(tile + kTileWords);         // [kExpBufs][kStartWords]
-    int32_t *off = starts + kExpBufs * kStartWords;                           // [G + 1]
+    int32_t *off = reinterpret_cast<int32_t *>(tile + kTileWords);             // [G + 1]
     int32_t *base = off + G + 1;                                              // [G + 1]
 
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -609,21 +605,21 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
         F = sg / nwin;
     };
     // block maxima of super-tile m: warp w0 takes the blocks w0, w0 + wstep, ...
+    // of those meeting the window; each writes the shift-table rows of the
+    // block's tokens in the window and, if the block starts in the window, the
+    // block's FP32 scales of the super-tile's 512 features: contiguous in the
+    // block's row of yTs, four 16-byte stores per lane
     auto maxima = [&](int32_t m, int w0, int wstep) {
         int32_t W, F;
         super_xy(m, W, F);
         const int bf = m % kExpBufs;
         const uint4 *ex = reinterpret_cast<const uint4 *>(exp_ring + bf * kExpBytes);
-        uint4 *S_of = Sring + bf * kTok;
         uint4 *U_of = Uring + bf * kTok;
-        int32_t *st_list = starts + bf * kStartWords;
         const int32_t We = min(W + kTok, M);
         const int gW = warp_find_last_le(off, G, W);
         const int32_t blkW = base[gW] + ((W - off[gW]) >> 7);
         const int gL = warp_find_last_le(off, G, We - 1);
         const int32_t nbw = base[gL] + ((We - 1 - off[gL]) >> 7) - blkW + 1;  // <= 128
-        if (w0 == 0 && lane == 0)
-            st_list[0] = nbw;
         int g = gW;
         for (int32_t jb = w0; jb < nbw; jb += wstep) {
             const int32_t b = blkW + jb;
@@ -651,14 +647,22 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
             };
             const uint4 S = make_uint4(wmax(m4.x), wmax(m4.y), wmax(m4.z), wmax(m4.w));
             for (int32_t t = max(bs, W) + lane; t < min(be, We); t += 32) {
-                S_of[t - W] = S;
                 const uint4 e = ex[t - W + kTok];
                 U_of[t - W] = make_uint4(shift_rows4(S.x, e.x, k), shift_rows4(S.y, e.y, k),
                                          shift_rows4(S.z, e.z, k), shift_rows4(S.w, e.w, k));
             }
-            if (lane == 0) {  // blocks that start here get their scales written
-                st_list[1 + 2 * jb] = bs >= W ? bs - W : -1;
-                st_list[2 + 2 * jb] = b;
+            if (bs >= W) {
+                // feature 512F + x, x = 4 lane + 128 c4 .. + 3: MX column x / 32
+                const uint32_t Sw[4] = {S.x, S.y, S.z, S.w};
+                uint4 *dst = reinterpret_cast<uint4 *>(
+                    yTs + static_cast<int64_t>(b) * (128 * static_cast<int64_t>(nfeat)) +
+                    512 * static_cast<int64_t>(F) + 4 * lane);
+#pragma unroll
+                for (int c4 = 0; c4 < 4; c4++) {
+                    const int c = 4 * c4 + (lane >> 3);  // MX column of x
+                    const uint32_t v = fp8_block_scale_bits((Sw[c >> 2] >> (8 * (c & 3))) & 0xFFu, k);
+                    dst[32 * c4] = make_uint4(v, v, v, v);
+                }
             }
         }
     };
@@ -783,23 +787,6 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
         const bool ok = mbar_wait(&full_c[st], ph_c) && (i != 0 || mbar_wait(&sready[bf], ph_e));
         if (n > 0)
             named_barrier_or(1, kThreads, false);  // the previous tile has been written out
-        if (ok && tid < kTok) {
-            // scales of the blocks that start in this window: feature row
-            // 128f + tid, MX column tid / 32
-            const int32_t *st_list = starts + bf * kStartWords;
-            const int32_t ns = st_list[0];
-            const uint32_t *S_w = reinterpret_cast<const uint32_t *>(Sring + bf * kTok);
-            // row of block b: K scales; this tile's 128 features are contiguous
-            uint32_t *dst = reinterpret_cast<uint32_t *>(yTs) + static_cast<int64_t>(f) * 128 + tid;
-            const int64_t nK = static_cast<int64_t>(nfeat) * 128;
-            for (int32_t q = 0; q < ns; q++) {
-                const int32_t tb = st_list[1 + 2 * q];
-                if (tb < 0)
-                    continue;
-                const uint32_t Sb = (S_w[tb * 4 + i] >> (8 * (tid >> 5))) & 0xFFu;
-                dst[static_cast<int64_t>(st_list[2 + 2 * q]) * nK] = fp8_block_scale_bits(Sb, k);
-            }
-        }
         if (ok) {
             const uint4 *codes = reinterpret_cast<const uint4 *>(codes_ring + st * kCodeBytes);
             const uint32_t *U_w = reinterpret_cast<const uint32_t *>(Uring + bf * kTok);

@@ -506,10 +506,18 @@ __global__ void __launch_bounds__(kThreads, 4) fp4_to_fp8_cols_kernel(
 
 // One launch, no block-scale pass, warp-specialised.  Work unit: the
 // super-tile (128-token window W) x (feature blocks 4F .. 4F+3), whose four
-// 128 x 128 tiles are converted one after the other; super-tiles are walked
-// window fastest by persistent CTAs.  One 16-byte exponent row per token
-// holds the UE8M0 exponents of all 16 MX columns of a super-tile, so its
-// block maxima are found once for four tiles.
+// 128 x 128 tiles are converted one after the other.  Persistent CTAs walk
+// the super-tiles window fastest when there are at most kWinFastMax windows
+// (the FP8 rows of one feature quad are then written in long runs, and one
+// pass over the windows of a feature quad, about 100 KB each, stays well
+// inside L2, so the next quad finds the rest of each exponent row there);
+// beyond that feature quad fastest: the super-tiles in flight then cover a
+// few whole windows, and the other 16-byte slices of their tokens' exponent
+// rows, and the neighbouring windows' rows, are read by CTAs running at the
+// same time (walked window fastest, a tensor much larger than L2 read its
+// exponents from DRAM about three times over).  One 16-byte exponent row
+// slice per token holds the UE8M0 exponents of all 16 MX columns of a
+// super-tile, so its block maxima are found once for four tiles.
 //  * The producer warp (warp 8) issues tensor-memory-access copies into
 //    shared memory: each tile's 128 x 64-byte codes into a ring of kStages
 //    code stages, and each super-tile's exponent rows of tokens
@@ -532,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 4) fp4_to_fp8_cols_kernel(
 //    the tile out transposed.
 // Every wait is bounded (mbar_wait); a wait that gives up ends the kernel
 // with bit 2 of *dev_status set.
+constexpr int32_t kWinFastMax = 512;  // windows walked fastest up to this many
 constexpr int kStages = 4;      // code stages
 constexpr int kExpBufs = 2;     // exponent buffers (super-tiles in flight)
 constexpr int kConvWarps = kThreads / 32;
@@ -577,6 +586,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     const int32_t nwin = (M + kTok - 1) / kTok;
     const int32_t nquad = nfeat >> 2;
     const int32_t nsuper = nwin * nquad;  // < 2^29, checked on the host
+    const bool wfast = nwin <= kWinFastMax;
     const int32_t grid = static_cast<int32_t>(gridDim.x);
     // super-tiles of this CTA: blockIdx.x + m * grid, m < my_super
     const int32_t my_super = (nsuper - static_cast<int32_t>(blockIdx.x) + grid - 1) / grid;
@@ -601,8 +611,8 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
 
     auto super_xy = [&](int32_t m, int32_t &W, int32_t &F) {
         const int32_t sg = static_cast<int32_t>(blockIdx.x) + m * grid;
-        W = (sg % nwin) * kTok;
-        F = sg / nwin;
+        W = (wfast ? sg % nwin : sg / nquad) * kTok;
+        F = wfast ? sg / nwin : sg % nquad;
     };
     // block maxima of super-tile m: warp w0 takes the blocks w0, w0 + wstep, ...
     // of those meeting the window; each writes the shift-table rows of the
@@ -777,8 +787,9 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     const int m_out = 4 * wid + (lane >> 3);
     const int c_out = lane & 7;
     const int32_t sg0 = blockIdx.x;  // first super-tile
-    int32_t win = sg0 % nwin, F = sg0 / nwin;
-    const int32_t step_w = grid % nwin, step_F = grid / nwin;
+    int32_t win = wfast ? sg0 % nwin : sg0 / nquad, F = wfast ? sg0 / nwin : sg0 % nquad;
+    const int32_t step_w = wfast ? grid % nwin : grid / nquad;
+    const int32_t step_F = wfast ? grid / nwin : grid % nquad;
     int st = 0, bf = 0;
     uint32_t ph_c = 0, ph_e = 0;
     for (int32_t n = 0; n < my_tiles; n++) {
@@ -815,9 +826,12 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
         if (i == 3) {
             win += step_w;
             F += step_F;
-            if (win >= nwin) {
+            if (wfast && win >= nwin) {
                 win -= nwin;
                 F++;
+            } else if (!wfast && F >= nquad) {
+                F -= nquad;
+                win++;
             }
             if (++bf == kExpBufs) {
                 bf = 0;

@@ -236,6 +236,19 @@ def test_fp4_to_fp8_cols_launch_count_in_a_fresh_process(fq):
     assert out.stdout.split() == ["1", "1"]
 
 
+@pytest.mark.parametrize("M", [65536, 66000])
+def test_fp4_to_fp8_cols_walk_orders(fq, M):
+    """Every output of the single pass on either side of the walk-order switch:
+    up to 512 128-token windows the super-tiles (window x 512 features) are
+    walked window fastest, beyond that feature quad fastest.  Two feature
+    quads, 32 Zipf groups, NaN scales."""
+    K = 1024
+    assert fq.fp4_to_fp8_cols_launch_count(K) == 1
+    offs = np.asarray(workloads.zipf_group_offsets(M, 32, 1.1, 11), dtype=np.int64)
+    q, s = rand_mx(M, K, seed=M + 5, spread=16, nan_frac=0.0005)
+    run_cols(fq, q, s, offs, 3)
+
+
 @pytest.mark.parametrize("K", [256, 512])
 def test_fp4_to_fp8_cols_malformed_offsets(fq, K):
     # malformed offsets: clamped in-kernel, status raised, nothing written

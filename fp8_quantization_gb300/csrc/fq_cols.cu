@@ -8,7 +8,11 @@
 // layout to avoid bank conflicts, and ragged expert groups are handled
 // without padding.  Scale alignment as in the row conversion (item 1).
 //
-// Two launches on the caller's stream:
+// When K % 512 == 0 (a token's 16-byte exponent row slice then covers a
+// super-tile of four 128-feature blocks) one launch does everything:
+// fp4_to_fp8_cols_1pass_kernel, warp-specialised, with tensor-memory-access
+// copies into shared memory (described at the kernel).  Otherwise two
+// launches on the caller's stream:
 //  1. fp4_to_fp8_cols_scales_kernel -- one CTA per 128-token block (blocks
 //     start at each group's first token): the byte-wise max of the block's
 //     UE8M0 exponents for every MX column, written out as the FP32 block

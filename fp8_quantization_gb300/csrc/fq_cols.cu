@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 4) fp4_to_fp8_cols_kernel(
 //    shared memory: each tile's 128 x 64-byte codes into a ring of kStages
 //    code stages, and each super-tile's exponent rows of tokens
 //    W-128 .. W+255 (three 128-row copies; rows outside the tensor read as
-//    zero) into a ring of two exponent buffers.  Three tiles before a
+//    zero) into a ring of kExps exponent buffers.  Three tiles before a
 //    super-tile starts it computes its block maxima: the 128-token blocks
 //    meeting the window are numbered consecutively; the byte-wise max of a
 //    block's exponent rows (up to 127 tokens beyond the window on either
@@ -540,13 +540,12 @@ __global__ void __launch_bounds__(kThreads, 4) fp4_to_fp8_cols_kernel(
 //    super-tile's first tile, for its maxima), convert into the FP8 tile as
 //    in the two-launch path once every warp has written the previous tile
 //    out (named barrier), release the code stage (and, after the fourth
-//    tile, the exponent buffer), meet at a second named barrier and write
+//    tile, the shift-row buffer), meet at a second named barrier and write
 //    the tile out transposed.
 // Every wait is bounded (mbar_wait); a wait that gives up ends the kernel
 // with bit 2 of *dev_status set.
 constexpr int32_t kWinFastMax = 512;  // windows walked fastest up to this many
-constexpr int kStages = 4;      // code stages
-constexpr int kExpBufs = 2;     // exponent buffers (super-tiles in flight)
+constexpr int kExpBufs = 2;     // shift-row buffers (super-tiles in flight)
 constexpr int kConvWarps = kThreads / 32;
 constexpr int kThreads1p = kThreads + 32;
 constexpr int kCodeBytes = kTok * 64;
@@ -555,16 +554,19 @@ constexpr int kExpBytes = 3 * kTok * kExpRowBytes;
 constexpr int kSmemAlign = 128;  // tensor-copy destinations
 static_assert(kCodeBytes % kSmemAlign == 0 && kExpBytes % kSmemAlign == 0, "aligned buffers");
 
-// per exponent buffer: the shift-table rows of every token (uint4: one byte
-// per MX column of the super-tile)
-inline size_t cols1_dyn_bytes(int32_t G)
+// Two configurations of the single pass (code stages x exponent buffers):
+// kStages x kExps = 4 x 2 up to kWinFastMax windows, 2 x 1 beyond (measured:
+// at 131072 x 7168 the 2 x 1 kernel is 6 % faster, at 16384 x 7168 7 %
+// slower).  Per shift-row buffer: the shift-table rows of every token of a
+// super-tile (uint4: one byte per MX column).
+inline size_t cols1_dyn_bytes(int32_t G, int stages, int exps)
 {
-    return kSmemAlign + static_cast<size_t>(kStages) * kCodeBytes +
-           static_cast<size_t>(kExpBufs) * (kExpBytes + kTok * sizeof(uint4)) +
+    return kSmemAlign + static_cast<size_t>(stages) * kCodeBytes +
+           static_cast<size_t>(exps) * kExpBytes + static_cast<size_t>(kExpBufs) * kTok * sizeof(uint4) +
            kTileWords * sizeof(uint32_t) + static_cast<size_t>(G + 1) * 2 * sizeof(int32_t);
 }
 
-template <bool kAligned16>
+template <bool kAligned16, int kStages, int kExps>
 __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
     int32_t M, int32_t nfeat, const int64_t *__restrict__ offs, int32_t G, int k,
@@ -574,14 +576,14 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     __shared__ int32_t warp_tot[kThreads1p / 32];
     __shared__ __align__(8) uint64_t full_c[kStages];    // code copies landed
     __shared__ __align__(8) uint64_t empty_c[kStages];   // code stage read by every converting warp
-    __shared__ __align__(8) uint64_t full_e[kExpBufs];   // exponent copies landed
+    __shared__ __align__(8) uint64_t full_e[kExps];      // exponent copies landed
     __shared__ __align__(8) uint64_t sready[kExpBufs];   // block maxima written
-    __shared__ __align__(8) uint64_t empty_e[kExpBufs];  // exponents and maxima no longer read
+    __shared__ __align__(8) uint64_t empty_e[kExpBufs];  // shift-table rows no longer read
     extern __shared__ __align__(16) uint8_t dyn_raw[];
     uint8_t *codes_ring = dyn_raw + ((kSmemAlign - (smem_u32(dyn_raw) & (kSmemAlign - 1))) &
                                      (kSmemAlign - 1));
     uint8_t *exp_ring = codes_ring + kStages * kCodeBytes;
-    uint4 *Uring = reinterpret_cast<uint4 *>(exp_ring + kExpBufs * kExpBytes);  // [kExpBufs][kTok]
+    uint4 *Uring = reinterpret_cast<uint4 *>(exp_ring + kExps * kExpBytes);  // [kExpBufs][kTok]
     uint32_t *tile = reinterpret_cast<uint32_t *>(Uring + kExpBufs * kTok);    // [kTileWords]
     int32_t *off = reinterpret_cast<int32_t *>(tile + kTileWords);             // [G + 1]
     int32_t *base = off + G + 1;                                              // [G + 1]
@@ -600,8 +602,9 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
             mbar_init(&full_c[i], 1);
             mbar_init(&empty_c[i], kConvWarps);
         }
-        for (int i = 0; i < kExpBufs; i++) {
+        for (int i = 0; i < kExps; i++)
             mbar_init(&full_e[i], 1);
+        for (int i = 0; i < kExpBufs; i++) {
             mbar_init(&sready[i], 1);
             mbar_init(&empty_e[i], kConvWarps);
         }
@@ -626,9 +629,8 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     auto maxima = [&](int32_t m, int w0, int wstep) {
         int32_t W, F;
         super_xy(m, W, F);
-        const int bf = m % kExpBufs;
-        const uint4 *ex = reinterpret_cast<const uint4 *>(exp_ring + bf * kExpBytes);
-        uint4 *U_of = Uring + bf * kTok;
+        const uint4 *ex = reinterpret_cast<const uint4 *>(exp_ring + (m % kExps) * kExpBytes);
+        uint4 *U_of = Uring + (m % kExpBufs) * kTok;
         const int32_t We = min(W + kTok, M);
         const int gW = warp_find_last_le(off, G, W);
         const int32_t blkW = base[gW] + ((W - off[gW]) >> 7);
@@ -683,13 +685,13 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     auto issue_exps = [&](int32_t m) {  // one thread: super-tile m of this CTA
         int32_t W, F;
         super_xy(m, W, F);
-        const int bf = m % kExpBufs;
-        uint8_t *dst = exp_ring + bf * kExpBytes;
-        mbar_arrive_expect_tx(&full_e[bf], kExpBytes);
+        const int be = m % kExps;
+        uint8_t *dst = exp_ring + be * kExpBytes;
+        mbar_arrive_expect_tx(&full_e[be], kExpBytes);
 #pragma unroll
         for (int h = 0; h < 3; h++)
             tma_load_2d(dst + h * kTok * kExpRowBytes, &tm_s, 16 * F, W + (h - 1) * kTok,
-                        &full_e[bf]);
+                        &full_e[be]);
     };
     auto issue_codes = [&](int32_t n) {  // one thread: tile n of this CTA
         int32_t W, F;
@@ -707,15 +709,21 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     const bool ok0 = !__syncthreads_or(!mbar_wait(&full_e[0], 0));
     if (ok0)
         maxima(0, wid, kThreads1p / 32);
-    __syncthreads();
-    if (tid == kThreads)
+    __syncthreads();  // every warp is done with exponent buffer 0
+    // with one exponent buffer the copy of super-tile 1 follows the first
+    // maxima (with two it is issued in the loop below)
+    const int32_t pre_e = kExps == 1 && ok0 && my_super > 1 ? 2 : 1;
+    if (tid == kThreads) {
         for (int32_t n = 1; n < kStages - 1 && n < my_tiles; n++)
             issue_codes(n);
+        if (pre_e == 2)
+            issue_exps(1);
+    }
 
     if (wid == kConvWarps) {
         // ================================================= producer warp
         bool ok = ok0;
-        int32_t issued_c = min(kStages - 1, my_tiles), issued_e = 1;  // copies issued
+        int32_t issued_c = min(kStages - 1, my_tiles), issued_e = pre_e;  // copies issued
         int32_t waited_e = ok0 ? 1 : 0;  // exponent copies waited for
         if (ok0 && lane == 0)
             mbar_arrive(&sready[0]);
@@ -734,12 +742,17 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
                     issue_codes(nn);
                 issued_c++;
             }
-            // first tile of super-tile m - 1: the exponent copies of super-tile
-            // m (into the buffer super-tile m - 2 released); one tile later,
-            // three tiles before super-tile m starts, its maxima
-            if ((n & 3) == 0 && (n >> 2) + 1 < my_super) {
+            // Super-tile m's maxima are computed on the second tile of
+            // super-tile m - 1, three tiles before m starts, into the
+            // shift-row buffer super-tile m - 2 released.  Two exponent
+            // buffers: super-tile m's exponent copy is issued one tile
+            // earlier (into the buffer super-tile m - 2's maxima read).  One
+            // buffer: the copy of super-tile m + 1 follows super-tile m's
+            // maxima (only this warp reads the exponent buffers after the
+            // first super-tile).
+            if (kExps == 2 && (n & 3) == 0 && (n >> 2) + 1 < my_super) {
                 const int32_t m = (n >> 2) + 1;
-                const int32_t p = m - kExpBufs;  // last user of the buffer
+                const int32_t p = m - kExpBufs;  // last user of the shift-row buffer
                 if (p >= 0) {
                     ok = __all_sync(0xffffffffu, mbar_wait(&empty_e[p % kExpBufs],
                                                            static_cast<uint32_t>(p / kExpBufs) & 1u));
@@ -753,15 +766,27 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
             if ((n & 3) == 1) {
                 const int32_t m = (n >> 2) + 1;
                 if (m < my_super) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(&full_e[m % kExpBufs],
-                                                           static_cast<uint32_t>(m / kExpBufs) & 1u));
+                    const int32_t p = m - kExpBufs;
+                    if (kExps == 1 && p >= 0) {
+                        ok = __all_sync(0xffffffffu, mbar_wait(&empty_e[p % kExpBufs],
+                                                               static_cast<uint32_t>(p / kExpBufs) & 1u));
+                        if (!ok)
+                            break;
+                    }
+                    ok = __all_sync(0xffffffffu, mbar_wait(&full_e[m % kExps],
+                                                           static_cast<uint32_t>(m / kExps) & 1u));
                     if (!ok)
                         break;
                     waited_e = m + 1;
                     maxima(m, 0, 1);
                     __syncwarp();
-                    if (lane == 0)
+                    if (lane == 0) {
                         mbar_arrive(&sready[m % kExpBufs]);
+                        if (kExps == 1 && m + 1 < my_super)
+                            issue_exps(m + 1);
+                    }
+                    if (kExps == 1 && m + 1 < my_super)
+                        issued_e++;
                 }
             }
         }
@@ -776,7 +801,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
             if (lane == 0 && dev_status)
                 atomicOr(dev_status, 2);
             for (int32_t m = waited_e; m < issued_e; m++)
-                mbar_wait(&full_e[m % kExpBufs], static_cast<uint32_t>(m / kExpBufs) & 1u);
+                mbar_wait(&full_e[m % kExps], static_cast<uint32_t>(m / kExps) & 1u);
             for (int32_t n = max(0, issued_c - kStages); n < issued_c; n++)
                 mbar_wait(&full_c[n % kStages], static_cast<uint32_t>(n / kStages) & 1u);
         }
@@ -894,9 +919,12 @@ fq_status fq::launch_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
         // the tensor outgrows L2
         encode_tensor_map_2d_u8(&tm_s, s, static_cast<uint64_t>(K / 32), static_cast<uint64_t>(M),
                                 static_cast<uint64_t>(K / 32), kExpRowBytes, kTok, false)) {
-        const size_t dyn = cols1_dyn_bytes(G);
-        auto kern = M % 16 == 0 ? fp4_to_fp8_cols_1pass_kernel<true>
-                                : fp4_to_fp8_cols_1pass_kernel<false>;
+        const bool large = (M + kTok - 1) / kTok > kWinFastMax;
+        const size_t dyn = large ? cols1_dyn_bytes(G, 2, 1) : cols1_dyn_bytes(G, 4, 2);
+        auto kern = large ? (M % 16 == 0 ? fp4_to_fp8_cols_1pass_kernel<true, 2, 1>
+                                         : fp4_to_fp8_cols_1pass_kernel<false, 2, 1>)
+                          : (M % 16 == 0 ? fp4_to_fp8_cols_1pass_kernel<true, 4, 2>
+                                         : fp4_to_fp8_cols_1pass_kernel<false, 4, 2>);
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(dyn)) != cudaSuccess ||
             cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,

@@ -428,6 +428,25 @@ def run_gpu(args):
                 "frac": round(gbs / peak, 4), "launches_per_call": launches,
                 "traffic": ncu_traffic(call), **kw}
 
+    # the six casts again, each alone with L2 flushed before every call: the
+    # per-kernel figure without the previous kernel's dirty lines (written
+    # back during the next kernel in the step)
+    alone = {
+        "mxfp4_quantize_rows": lambda: fq.mxfp4_quantize_rows(x, out["q"], out["s"]),
+        "fp4_to_fp8_rows": lambda: fq.fp4_to_fp8_rows(out["q"], out["s"], 0, out["y"], out["ys"]),
+        "fp4_to_fp8_cols": lambda: fq.fp4_to_fp8_cols(out["q"], out["s"], offs, 0, out["yT"],
+                                                      out["yTs"]),
+        "nvfp4_amax": lambda: fq.nvfp4_amax(x, out["amax"]),
+        "nvfp4_quantize": lambda: fq.nvfp4_quantize(x, out["amax"], use_sr=True, seed=7, offset=0,
+                                                    q=out["q4"], sb=out["sb4"], g=out["g4"]),
+        "nvfp4_quantize_2d": lambda: fq.nvfp4_quantize_2d(x, out["amax"], out["q2"], out["sb2"],
+                                                          out["g2"]),
+    }
+    for k, fn in alone.items():
+        us = timed_us(fn)
+        gbs = nbytes[k] / (us * 1e-6) / 1e9
+        kernels[k]["alone"] = {"us": round(us, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+
     E = M * K
     fo = {k: torch.empty_like(out[k]) for k in ("q", "s", "y", "ys", "yT", "yTs")}
     fused_us = timed_us(lambda: fq.bf16_to_mxfp4_fp8(x, offs, 0, fo["q"], fo["s"], fo["y"],

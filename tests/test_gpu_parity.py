@@ -236,12 +236,13 @@ def test_fp4_to_fp8_cols_launch_count_in_a_fresh_process(fq):
     assert out.stdout.split() == ["1", "1"]
 
 
-@pytest.mark.parametrize("M", [65536, 66000])
+@pytest.mark.parametrize("M", [65536, 66000, 66001])
 def test_fp4_to_fp8_cols_walk_orders(fq, M):
-    """Every output of the single pass on either side of the walk-order switch:
-    up to 512 128-token windows the super-tiles (window x 512 features) are
-    walked window fastest, beyond that feature quad fastest.  Two feature
-    quads, 32 Zipf groups, NaN scales."""
+    """Every output of the single pass on either side of the switch between
+    its two configurations: up to 512 128-token windows the super-tiles
+    (window x 512 features) are walked window fastest with 4 code stages and 2
+    exponent buffers, beyond that feature quad fastest with 2 and 1 (M % 16
+    != 0 included).  Two feature quads, 32 Zipf groups, NaN scales."""
     K = 1024
     assert fq.fp4_to_fp8_cols_launch_count(K) == 1
     offs = np.asarray(workloads.zipf_group_offsets(M, 32, 1.1, 11), dtype=np.int64)
@@ -288,9 +289,19 @@ def test_bf16_to_mxfp4_fp8(fq, case, path):
     M, K, mk = COLS_CASES[case]
     K = cols_k(K, path)
     offs = np.asarray(mk(M), dtype=np.int64)
+    check_fused(fq, M, K, offs, (M + K) % 7, fused_input(M, K, seed=M + 3 * K))
+
+
+def test_bf16_to_mxfp4_fp8_above_512_windows(fq):
+    """The one-call forward cast on 66000 tokens (516 windows: the transposed
+    kernel's large-tensor configuration) x 1024 features, 32 Zipf groups."""
+    M, K = 66000, 1024
+    offs = np.asarray(workloads.zipf_group_offsets(M, 32, 1.1, 13), dtype=np.int64)
+    check_fused(fq, M, K, offs, 2, fused_input(M, K, seed=17))
+
+
+def check_fused(fq, M, K, offs, k, bits):
     G = offs.size - 1
-    k = (M + K) % 7
-    bits = fused_input(M, K, seed=M + 3 * K)
     cap = oracle.fp4_to_fp8_cols_scale_capacity(M, G)
     qraw, q = canary_out((M, K // 2), torch.uint8)
     sraw, s = canary_out((M, K // 32), torch.uint8)

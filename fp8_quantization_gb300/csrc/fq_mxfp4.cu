@@ -42,6 +42,8 @@ __global__ void __launch_bounds__(kThreads) mxfp4_quantize_rows_kernel(
         keep = l2_evict_last();
         stream = l2_evict_first();
     }
+    griddep_wait();  // the previous kernel's outputs (PDL launch)
+    griddep_launch_dependents();  // the next kernel may start its set-up
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -124,6 +126,8 @@ __global__ void __launch_bounds__(kThreads) fp4_to_fp8_rows_kernel(
     __shared__ __align__(16) uint8_t tab[kTabRows * 8];
     build_fp8_table(tab);
     __syncthreads();
+    griddep_wait();  // the previous kernel's outputs (PDL launch)
+    griddep_launch_dependents();  // the next kernel may start its set-up
 
     const int lane = threadIdx.x & 31;
     const int part = lane & 7;  // 8-byte part of the 64-byte FP8 block
@@ -184,12 +188,13 @@ fq_status launch_mxfp4_rows(const void *x, int64_t M, int64_t K, uint8_t *q, uin
     const int64_t work = (nblk + 32 * (kThreads / 32) - 1) / (32 * (kThreads / 32));
     if (y) {
         const int grid = persistent_grid(mxfp4_quantize_rows_kernel<true>, kThreads, 0, work);
-        mxfp4_quantize_rows_kernel<true><<<grid, kThreads, 0, st>>>(
-            static_cast<const uint16_t *>(x), nblk, q, s, k, y, ys);
+        launch_pdl(mxfp4_quantize_rows_kernel<true>, dim3(grid), dim3(kThreads), 0, st,
+                   static_cast<const uint16_t *>(x), nblk, q, s, k, y, ys);
     } else {
         const int grid = persistent_grid(mxfp4_quantize_rows_kernel<false>, kThreads, 0, work);
-        mxfp4_quantize_rows_kernel<false><<<grid, kThreads, 0, st>>>(
-            static_cast<const uint16_t *>(x), nblk, q, s, 0, nullptr, nullptr);
+        launch_pdl(mxfp4_quantize_rows_kernel<false>, dim3(grid), dim3(kThreads), 0, st,
+                   static_cast<const uint16_t *>(x), nblk, q, s, 0, static_cast<uint8_t *>(nullptr),
+                   static_cast<float *>(nullptr));
     }
     return launch_status();
 }
@@ -232,7 +237,7 @@ extern "C" fq_status fp4_to_fp8_rows(const uint8_t *q, const uint8_t *s, int64_t
     const int64_t per_cta = 4 * kRowsUnroll * (kThreads / 32);
     const int grid =
         persistent_grid(fp4_to_fp8_rows_kernel, kThreads, 0, (nfb + per_cta - 1) / per_cta);
-    fp4_to_fp8_rows_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        q, s, nfb, exp_offset_k, y, ys);
+    launch_pdl(fp4_to_fp8_rows_kernel, dim3(grid), dim3(kThreads), 0,
+               static_cast<cudaStream_t>(stream), q, s, nfb, exp_offset_k, y, ys);
     return launch_status();
 }

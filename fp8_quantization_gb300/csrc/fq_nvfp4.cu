@@ -27,6 +27,8 @@ __global__ void __launch_bounds__(kThreads, 6) nvfp4_amax_kernel(const uint16_t 
                                                               uint32_t *__restrict__ out_bits)
 {
     __shared__ uint32_t red[kThreads / 32];
+    griddep_wait();  // the previous kernel's outputs (PDL launch)
+    griddep_launch_dependents();  // the next kernel may start its set-up
     const int64_t nvec = n >> 3;  // 16-byte chunks
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -375,6 +377,8 @@ __global__ void __launch_bounds__(kThreads, kDelayed ? 4 : 0) nvfp4_quantize_ker
 {
     __shared__ float rtab[128];
     __shared__ uint32_t red[kThreads / 32];
+    griddep_wait();  // the previous kernel's outputs (PDL launch)
+    griddep_launch_dependents();  // the next kernel may start its set-up
     const TensorScales ts = kDelayed ? nvfp4_tensor_setup_from(window_estimate(hist, W, t, red), rtab)
                                      : nvfp4_tensor_setup(amax, rtab);
     uint32_t own = 0;  // max of this thread's block maxima (BF16 bits)
@@ -566,6 +570,8 @@ __global__ void __launch_bounds__(kThreads, 2) nvfp4_quantize_2d_kernel(
     uint8_t *__restrict__ q, uint8_t *__restrict__ sb, float *__restrict__ g_out)
 {
     __shared__ float rtab[128];
+    griddep_wait();  // the previous kernel's outputs (PDL launch)
+    griddep_launch_dependents();  // the next kernel may start its set-up
     const TensorScales ts = nvfp4_tensor_setup(amax, rtab);
     if (blockIdx.x == 0 && threadIdx.x == 0)
         *g_out = ts.g;
@@ -714,8 +720,8 @@ extern "C" fq_status nvfp4_amax(const void *x, int64_t n, float *amax, void *str
         return FQ_OK;
     const int64_t work = (n / 8 + 4 * kThreads - 1) / (4 * kThreads);
     const int grid = persistent_grid(nvfp4_amax_kernel, kThreads, 0, work < 1 ? 1 : work);
-    nvfp4_amax_kernel<<<grid, kThreads, 0, st>>>(static_cast<const uint16_t *>(x), n,
-                                                  reinterpret_cast<uint32_t *>(amax));
+    launch_pdl(nvfp4_amax_kernel, dim3(grid), dim3(kThreads), 0, st,
+               static_cast<const uint16_t *>(x), n, reinterpret_cast<uint32_t *>(amax));
     return launch_status();
 }
 
@@ -740,8 +746,8 @@ extern "C" fq_status nvfp4_quantize(const void *x, int64_t M, int64_t K, const f
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto kern = use_sr ? nvfp4_quantize_kernel<true, false> : nvfp4_quantize_kernel<false, false>;
     const int grid = persistent_grid(kern, kThreads, 0, work);
-    kern<<<grid, kThreads, 0, st>>>(static_cast<const uint16_t *>(x), nblk, amax, seed, offset, q,
-                                    sb, g, nullptr, 0, 0u);
+    launch_pdl(kern, dim3(grid), dim3(kThreads), 0, st, static_cast<const uint16_t *>(x), nblk,
+               amax, seed, offset, q, sb, g, static_cast<uint64_t *>(nullptr), 0, 0u);
     return launch_status();
 }
 
@@ -761,8 +767,9 @@ extern "C" fq_status nvfp4_quantize_2d(const void *w, int64_t N, int64_t K, cons
     const int64_t units = (N / 16) * ((K + 255) / 256);
     const int grid =
         persistent_grid(nvfp4_quantize_2d_kernel, kThreads, 0, (units + 7) / 8);
-    nvfp4_quantize_2d_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t *>(w), N, K, amax, q, sb, g);
+    launch_pdl(nvfp4_quantize_2d_kernel, dim3(grid), dim3(kThreads), 0,
+               static_cast<cudaStream_t>(stream), static_cast<const uint16_t *>(w), N, K, amax, q, sb,
+               g);
     return launch_status();
 }
 

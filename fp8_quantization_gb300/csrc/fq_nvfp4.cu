@@ -701,6 +701,16 @@ __global__ void __launch_bounds__(kThreads, 2) nvfp4_quantize_2d_t_kernel(
     }
 }
 
+// The amax word zeroed by one thread, in the chain of programmatically
+// dependent launches (the kernel before may still read or write it until
+// griddepcontrol.wait returns).
+__global__ void zero_word_kernel(uint32_t *__restrict__ w)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    *w = 0u;
+}
+
 }  // namespace fq
 
 using namespace fq;
@@ -714,10 +724,11 @@ extern "C" fq_status nvfp4_amax(const void *x, int64_t n, float *amax, void *str
     if ((n > 0 && !aligned16(x)) || !aligned16(amax))
         return FQ_ERR_ALIGN;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(amax, 0, sizeof(float), st) != cudaSuccess)
+    if (launch_pdl(zero_word_kernel, dim3(1), dim3(1), 0, st, reinterpret_cast<uint32_t *>(amax)) !=
+        cudaSuccess)
         return launch_status();
     if (n == 0)
-        return FQ_OK;
+        return launch_status();
     const int64_t work = (n / 8 + 4 * kThreads - 1) / (4 * kThreads);
     const int grid = persistent_grid(nvfp4_amax_kernel, kThreads, 0, work < 1 ? 1 : work);
     launch_pdl(nvfp4_amax_kernel, dim3(grid), dim3(kThreads), 0, st,
@@ -805,10 +816,11 @@ extern "C" fq_status nvfp4_amax_rht(const void *x, int64_t n, uint32_t sign_mask
     if ((n > 0 && !aligned16(x)) || !aligned16(amax))
         return FQ_ERR_ALIGN;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(amax, 0, sizeof(float), st) != cudaSuccess)
+    if (launch_pdl(zero_word_kernel, dim3(1), dim3(1), 0, st, reinterpret_cast<uint32_t *>(amax)) !=
+        cudaSuccess)
         return launch_status();
     if (n == 0)
-        return FQ_OK;
+        return launch_status();
     const int64_t nblk = n / 16;
     const int64_t work = (nblk + 2 * kThreads - 1) / (2 * kThreads);
     const int grid = persistent_grid(nvfp4_amax_rht_kernel, kThreads, 0, work);

@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(kThreads) fp4_to_fp8_cols_scales_kernel(
     extern __shared__ int32_t dyn[];
     int32_t *off = dyn, *base = dyn + G + 1;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    griddep_wait();  // the previous kernel's outputs (PDL launch)
     griddep_launch_dependents();  // the convert pass may start its set-up now
     const int bad = load_groups(offs, G, M, off, base, warp_tot);
     if (bad && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0 && dev_status)
@@ -942,8 +943,8 @@ fq_status fq::launch_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
     const int64_t chunks = (cap + kScaleSlots - 1) / kScaleSlots;
     const dim3 grid1(static_cast<unsigned>(K / 128),
                      static_cast<unsigned>(chunks < 65535 ? chunks : 65535));
-    fp4_to_fp8_cols_scales_kernel<<<grid1, kThreads, groups_bytes, st>>>(
-        s, static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT_scale, dev_status);
+    launch_pdl(fp4_to_fp8_cols_scales_kernel, grid1, dim3(kThreads), groups_bytes, st, s,
+               static_cast<int32_t>(M), K, group_offsets, G, exp_offset_k, yT_scale, dev_status);
     fq_status rc = launch_status();
     if (rc != FQ_OK)
         return rc;

@@ -58,6 +58,8 @@ __device__ __forceinline__ uint2 fp8_encode8(uint4 v, float r)
 __global__ void __launch_bounds__(kThreads) fp8_quantize_1x128_kernel(
     const uint16_t *__restrict__ x, int64_t nblk, uint8_t *__restrict__ y, float *__restrict__ s)
 {
+    griddep_wait();  // the previous kernel's outputs (PDL launch)
+    griddep_launch_dependents();  // the next kernel may start its set-up
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -108,6 +110,8 @@ __global__ void __launch_bounds__(kThreads) fp8_quantize_128x128_kernel(
     float *__restrict__ s)
 {
     __shared__ uint32_t red[kThreads / 32];
+    griddep_wait();  // the previous kernel's outputs (PDL launch)
+    griddep_launch_dependents();  // the next kernel may start its set-up
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int64_t tcols = K >> 7;
     const int64_t ntiles = (N >> 7) * tcols;
@@ -196,6 +200,8 @@ __global__ void __launch_bounds__(kThreads) mxfp4_dequantize_rows_kernel(
     __shared__ __align__(16) uint8_t tab[256 * 16];
     build_dequant_table(tab);
     __syncthreads();
+    griddep_wait();  // the previous kernel's outputs (PDL launch)
+    griddep_launch_dependents();  // the next kernel may start its set-up
     const uint32_t *q32 = reinterpret_cast<const uint32_t *>(q);
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -250,8 +256,8 @@ extern "C" fq_status fp8_quantize_1x128(const void *x, int64_t M, int64_t K, uin
     const int64_t nblk = M * (K / 128);
     const int64_t work = (nblk + 8 * (kThreads / 32) - 1) / (8 * (kThreads / 32));
     const int grid = persistent_grid(fp8_quantize_1x128_kernel, kThreads, 0, work);
-    fp8_quantize_1x128_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t *>(x), nblk, y, s);
+    launch_pdl(fp8_quantize_1x128_kernel, dim3(grid), dim3(kThreads), 0,
+               static_cast<cudaStream_t>(stream), static_cast<const uint16_t *>(x), nblk, y, s);
     return launch_status();
 }
 
@@ -270,8 +276,8 @@ extern "C" fq_status fp8_quantize_128x128(const void *w, int64_t N, int64_t K, u
         return FQ_ERR_ALIGN;
     const int64_t tiles = (N / 128) * (K / 128);
     const int grid = persistent_grid(fp8_quantize_128x128_kernel, kThreads, 0, tiles);
-    fp8_quantize_128x128_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t *>(w), N, K, y, s);
+    launch_pdl(fp8_quantize_128x128_kernel, dim3(grid), dim3(kThreads), 0,
+               static_cast<cudaStream_t>(stream), static_cast<const uint16_t *>(w), N, K, y, s);
     return launch_status();
 }
 
@@ -291,7 +297,7 @@ extern "C" fq_status mxfp4_dequantize_rows(const uint8_t *q, const uint8_t *s, i
     const int64_t nw = M * (K / 8);
     const int64_t work = (nw + kDeqUnroll * kThreads - 1) / (kDeqUnroll * kThreads);
     const int grid = persistent_grid(mxfp4_dequantize_rows_kernel, kThreads, 0, work);
-    mxfp4_dequantize_rows_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        q, s, nw, static_cast<uint16_t *>(x));
+    launch_pdl(mxfp4_dequantize_rows_kernel, dim3(grid), dim3(kThreads), 0,
+               static_cast<cudaStream_t>(stream), q, s, nw, static_cast<uint16_t *>(x));
     return launch_status();
 }

@@ -143,6 +143,8 @@ __global__ void __launch_bounds__(kThreads) nvfp4_amax_rht_kernel(const uint16_t
                                                                   uint32_t *__restrict__ out_bits)
 {
     __shared__ uint32_t red[kThreads / 32];
+    griddep_wait();  // the previous kernel's outputs (PDL launch)
+    griddep_launch_dependents();  // the next kernel may start its set-up
     const RhtFlip f = rht_flip_words(sign_mask);
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -459,6 +461,8 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_rht_kernel(
     uint8_t *__restrict__ sb, float *__restrict__ g_out)
 {
     __shared__ float rtab[128];
+    griddep_wait();  // the previous kernel's outputs (PDL launch)
+    griddep_launch_dependents();  // the next kernel may start its set-up
     const TensorScales ts = nvfp4_tensor_setup(amax, rtab);
     if (blockIdx.x == 0 && threadIdx.x == 0)
         *g_out = ts.g;
@@ -635,6 +639,8 @@ __global__ void __launch_bounds__(kThreads, 2) nvfp4_quantize_2d_t_kernel(
     __shared__ float rtab[128];
     __shared__ __align__(16) uint32_t tile[kT2Rows * 2 * kT2Strips];  // 16 KB
     __shared__ uint8_t stile[16 * kT2Strips];  // [tile column][strip]
+    griddep_wait();  // the previous kernel's outputs (PDL launch)
+    griddep_launch_dependents();  // the next kernel may start its set-up
     const TensorScales ts = nvfp4_tensor_setup(amax, rtab);
     if (blockIdx.x == 0 && threadIdx.x == 0)
         *g_out = ts.g;
@@ -801,8 +807,9 @@ extern "C" fq_status nvfp4_quantize_2d_t(const void *w, int64_t N, int64_t K, co
         return FQ_ERR_ALIGN;
     const int64_t units = ((N / 16 + kT2Strips - 1) / kT2Strips) * ((K + 255) / 256);
     const int grid = persistent_grid(nvfp4_quantize_2d_t_kernel, kThreads, 0, units);
-    nvfp4_quantize_2d_t_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t *>(w), N, K, amax, q, sb, qT, sbT, g);
+    launch_pdl(nvfp4_quantize_2d_t_kernel, dim3(grid), dim3(kThreads), 0,
+               static_cast<cudaStream_t>(stream), static_cast<const uint16_t *>(w), N, K, amax, q,
+               sb, qT, sbT, g);
     return launch_status();
 }
 
@@ -824,9 +831,9 @@ extern "C" fq_status nvfp4_amax_rht(const void *x, int64_t n, uint32_t sign_mask
     const int64_t nblk = n / 16;
     const int64_t work = (nblk + 2 * kThreads - 1) / (2 * kThreads);
     const int grid = persistent_grid(nvfp4_amax_rht_kernel, kThreads, 0, work);
-    nvfp4_amax_rht_kernel<<<grid, kThreads, 0, st>>>(static_cast<const uint16_t *>(x), nblk,
-                                                      sign_mask & 0xFFFFu,
-                                                      reinterpret_cast<uint32_t *>(amax));
+    launch_pdl(nvfp4_amax_rht_kernel, dim3(grid), dim3(kThreads), 0, st,
+               static_cast<const uint16_t *>(x), nblk, sign_mask & 0xFFFFu,
+               reinterpret_cast<uint32_t *>(amax));
     return launch_status();
 }
 
@@ -854,12 +861,12 @@ extern "C" fq_status nvfp4_quantize_rht(const void *x, int64_t M, int64_t K, con
     const uint32_t mask = sign_mask & 0xFFFFu;
     if (use_sr) {
         const int grid = persistent_grid(nvfp4_quantize_rht_kernel<true>, kThreads, 0, work);
-        nvfp4_quantize_rht_kernel<true><<<grid, kThreads, 0, st>>>(
-            static_cast<const uint16_t *>(x), nblk, amax, mask, seed, offset, q, sb, g);
+        launch_pdl(nvfp4_quantize_rht_kernel<true>, dim3(grid), dim3(kThreads), 0, st,
+                   static_cast<const uint16_t *>(x), nblk, amax, mask, seed, offset, q, sb, g);
     } else {
         const int grid = persistent_grid(nvfp4_quantize_rht_kernel<false>, kThreads, 0, work);
-        nvfp4_quantize_rht_kernel<false><<<grid, kThreads, 0, st>>>(
-            static_cast<const uint16_t *>(x), nblk, amax, mask, seed, offset, q, sb, g);
+        launch_pdl(nvfp4_quantize_rht_kernel<false>, dim3(grid), dim3(kThreads), 0, st,
+                   static_cast<const uint16_t *>(x), nblk, amax, mask, seed, offset, q, sb, g);
     }
     return launch_status();
 }
@@ -887,8 +894,8 @@ extern "C" fq_status nvfp4_quantize_delayed(const void *x, int64_t M, int64_t K,
     const int64_t work = (nblk + kNvUnroll * kThreads - 1) / (kNvUnroll * kThreads);
     auto kern = use_sr ? nvfp4_quantize_kernel<true, true> : nvfp4_quantize_kernel<false, true>;
     const int grid = persistent_grid(kern, kThreads, 0, work);
-    kern<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t *>(x), nblk, nullptr, seed, offset, q, sb, g, amax_history,
-        window, step);
+    launch_pdl(kern, dim3(grid), dim3(kThreads), 0, static_cast<cudaStream_t>(stream),
+               static_cast<const uint16_t *>(x), nblk, static_cast<const float *>(nullptr), seed,
+               offset, q, sb, g, amax_history, window, step);
     return launch_status();
 }

@@ -29,10 +29,10 @@
  *   overlap.
  * - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *   enqueued on it asynchronously; no entry point synchronizes the host.
- *   Most kernels are launched with programmatic dependent launch: they may
+ *   Every kernel is launched with programmatic dependent launch: it may
  *   be scheduled while the stream's previous kernel is still running, but
- *   touch no global memory before it has completed, so stream order holds
- *   for every buffer.
+ *   touches no global memory before that kernel has completed, so stream
+ *   order holds for every buffer.
  * - Arguments are checked on the host before anything is enqueued; a failed
  *   check returns a status other than FQ_OK and enqueues nothing.  A failed
  *   launch returns FQ_ERR_CUDA (the CUDA error code is then available from

@@ -92,6 +92,54 @@ def test_moe_dispatch_16384x7168_all_casts(fq):
     assert g2.item() == float(rg2)
 
 
+def test_chained_steps_alternating_inputs(fq):
+    """The bench step's six calls repeated 24 times on one stream with no host
+    synchronisation, the input alternating between two tensors (and the
+    ragged offsets between two splits), so that every kernel overlaps the
+    launch of the next.  The outputs must be exactly those of the last step's
+    input computed alone (a kernel that read a buffer before the previous
+    kernel finished writing it would mix the two inputs)."""
+    M, K, G = 16384, 7168, 32
+    xs = [dev_bf16(workloads.moe_dispatch(M, K, seed=sd)) for sd in (0, 5)]
+    offs = [torch.from_numpy(workloads.zipf_group_offsets(M, G, 1.1, sd)).cuda() for sd in (0, 5)]
+    cap = fq.fp4_to_fp8_cols_scale_capacity(M, G)
+    dev = torch.device("cuda")
+
+    def outputs():
+        u8 = dict(dtype=torch.uint8, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        return dict(q=torch.zeros((M, K // 2), **u8), s=torch.zeros((M, K // 32), **u8),
+                    y=torch.zeros((M, K), **u8), ys=torch.zeros((M, K // 128), **f32),
+                    yT=torch.zeros((K, M), **u8), yTs=torch.zeros((cap, K), **f32),
+                    amax=torch.zeros((1,), **f32), q4=torch.zeros((M, K // 2), **u8),
+                    sb4=torch.zeros((M, K // 16), **u8), g4=torch.zeros((1,), **f32),
+                    q2=torch.zeros((M, K // 2), **u8), sb2=torch.zeros((M // 16, K // 16), **u8),
+                    g2=torch.zeros((1,), **f32))
+
+    def step(o, x, off, seed):
+        fq.mxfp4_quantize_rows(x, o["q"], o["s"])
+        fq.fp4_to_fp8_rows(o["q"], o["s"], 0, o["y"], o["ys"])
+        fq.fp4_to_fp8_cols(o["q"], o["s"], off, 0, o["yT"], o["yTs"])
+        fq.nvfp4_amax(x, o["amax"])
+        fq.nvfp4_quantize(x, o["amax"], True, seed, 0, o["q4"], o["sb4"], o["g4"])
+        fq.nvfp4_quantize_2d(x, o["amax"], o["q2"], o["sb2"], o["g2"])
+
+    chained = outputs()
+    torch.cuda.synchronize()
+    for i in range(24):
+        step(chained, xs[i % 2], offs[i % 2], 77)
+    torch.cuda.synchronize()
+    alone = outputs()
+    step(alone, xs[1], offs[1], 77)
+    torch.cuda.synchronize()
+    nb = int(((np.diff(offs[1].cpu().numpy()) + 127) // 128).sum())
+    for k in alone:
+        a, c = alone[k], chained[k]
+        if k == "yTs":
+            a, c = a[:nb], c[:nb]
+        assert torch.equal(a.view(torch.uint8), c.view(torch.uint8)), k
+
+
 @pytest.mark.parametrize("k", [0, 6])
 def test_ragged_experts_65536x2048(fq, k):
     """Routed rows over 32 Zipf-sized experts: MXFP4 rows, then the

@@ -620,6 +620,35 @@ PROFILE_ORDER = (
      for c in ("mxfp4_quantize_rows", "fp4_to_fp8_rows", "fp4_to_fp8_cols (1 group)")])
 
 
+def run_sweep_rows(m):
+    """The bandwidth-sweep chain at m rows x 7168 alone (mxfp4_quantize_rows,
+    fp4_to_fp8_rows, fp4_to_fp8_cols with one group), one launch per call with
+    L2 cleaned before each: a small case for a full ncu capture of one size."""
+    import torch
+    import numpy as np
+    import fp8_quantization_gb300 as fq
+    from fp8_quantization_gb300 import workloads
+    dev = torch.device("cuda", 0)
+    flush_buf = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+
+    def run(fn):
+        flush_buf.fill_(1)
+        flush_buf.sum(dtype=torch.int64)
+        return fn()
+
+    bits = workloads.sweep(m, 7168, seed=0)
+    x = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+    del bits
+    q, s = run(lambda: fq.mxfp4_quantize_rows(x))
+    del x
+    run(lambda: fq.fp4_to_fp8_rows(q, s, 0))
+    offs = torch.tensor([0, m], dtype=torch.int64, device=dev)
+    run(lambda: fq.fp4_to_fp8_cols(q, s, offs, 0))
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"sweep_rows": m}), flush=True)
+    return 0
+
+
 def run_profile_configs():
     """Every configuration's chain, one launch per call in PROFILE_ORDER, L2
     cleaned before each: the launches an ncu pass over the configurations
@@ -697,9 +726,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-configs", action="store_true",
                     help="run every configuration's calls once (for an ncu capture) and exit")
+    ap.add_argument("--sweep-rows", type=int, default=0,
+                    help="run the bandwidth-sweep chain at this many rows once (for an ncu "
+                         "capture of one size) and exit")
     args = ap.parse_args()
     if args.profile_configs:
         return run_profile_configs()
+    if args.sweep_rows:
+        return run_sweep_rows(args.sweep_rows)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

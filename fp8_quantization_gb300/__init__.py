@@ -1,7 +1,8 @@
 """Block-scaled FP4 / FP8 casts for GB300 -- Python binding of libfq.so.
 
-Every function here only marshals arguments: it checks tensor placement and
-dtype, allocates outputs with ``torch.empty`` when none are given, and calls
+Every function here only marshals arguments: it checks the dtype, layout and
+size of every tensor and that it lives on the current CUDA device, allocates
+outputs with ``torch.empty`` when none are given, and calls
 the C entry point of the same name (declared in ``include/fq.h``) on the
 current CUDA stream.  All arithmetic runs in the sm_103a kernels of libfq.so;
 there is no CPU or PyTorch fallback -- if the library is missing, every call
@@ -105,21 +106,46 @@ def _p(t: torch.Tensor | None):
     return ctypes.c_void_p(0 if t is None else t.data_ptr())
 
 
-def _need(t: torch.Tensor, dtype, name: str, ndim: int | None = None):
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+def _need(t: torch.Tensor, dtype, name: str, ndim: int | None = None,
+          numel: int | None = None, shape: tuple | None = None):
+    """dtype, contiguity and size of a tensor argument (placement is checked
+    by _on_device just before the call)."""
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if ndim is not None and t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dimensions")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements, got {t.numel()}")
+
+
+def _on_device(**tensors):
+    """Every tensor given is a CUDA tensor on the current device (the library
+    launches there); None entries are skipped."""
+    cur = torch.cuda.current_device() if torch.cuda.is_available() else None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.device.index != cur:
+            raise ValueError(f"{name} is on {t.device}, the current device is cuda:{cur}")
+
+
+def _bf16(x: torch.Tensor, name: str, ndim: int | None = None):
+    if not isinstance(x, torch.Tensor) or x.dtype not in (torch.bfloat16, torch.int16,
+                                                           torch.uint16):
+        raise ValueError(f"{name} must be bfloat16 (or its 16-bit pattern)")
+    _need(x, x.dtype, name, ndim)
 
 
 def _bf16_2d(x: torch.Tensor, name: str):
-    if x.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
-        raise ValueError(f"{name} must be bfloat16 (or its 16-bit pattern)")
-    _need(x, x.dtype, name, 2)
+    _bf16(x, name, 2)
 
 
 def _empty(shape, dtype, like: torch.Tensor):
@@ -127,6 +153,9 @@ def _empty(shape, dtype, like: torch.Tensor):
 
 
 # ---------------------------------------------------------------- MXFP4
+# Sizes are checked wherever the block size divides the tensor; a size the
+# block does not divide is passed on, and the library rejects it with
+# FQ_ERR_SHAPE.
 
 def mxfp4_quantize_rows(x: torch.Tensor, q: torch.Tensor | None = None,
                         s: torch.Tensor | None = None):
@@ -135,10 +164,10 @@ def mxfp4_quantize_rows(x: torch.Tensor, q: torch.Tensor | None = None,
     M, K = x.shape
     q = _empty((M, K // 2), torch.uint8, x) if q is None else q
     s = _empty((M, K // 32), torch.uint8, x) if s is None else s
-    _need(q, torch.uint8, "q")
-    _need(s, torch.uint8, "s")
-    if K % 32 == 0 and (q.numel() != M * K // 2 or s.numel() != M * K // 32):
-        raise ValueError("output sizes do not match x")
+    ok = K % 32 == 0
+    _need(q, torch.uint8, "q", numel=M * K // 2 if ok else None)
+    _need(s, torch.uint8, "s", numel=M * K // 32 if ok else None)
+    _on_device(x=x, q=q, s=s)
     _call("mxfp4_quantize_rows", _p(x), M, K, _p(q), _p(s), _stream())
     return q, s
 
@@ -147,16 +176,14 @@ def fp4_to_fp8_rows(q: torch.Tensor, s: torch.Tensor, exp_offset_k: int = 0,
                     y: torch.Tensor | None = None, ys: torch.Tensor | None = None):
     """MXFP4 -> (y uint8 [M, K] E4M3, ys float32 [M, K/128])."""
     _need(q, torch.uint8, "q", 2)
-    _need(s, torch.uint8, "s", 2)
     M, K = q.shape[0], q.shape[1] * 2
-    if s.shape != (M, K // 32):
-        raise ValueError("s must be [M, K/32]")
+    _need(s, torch.uint8, "s", 2, shape=(M, K // 32))
     y = _empty((M, K), torch.uint8, q) if y is None else y
     ys = _empty((M, max(K // 128, 0)), torch.float32, q) if ys is None else ys
-    _need(y, torch.uint8, "y")
-    _need(ys, torch.float32, "ys")
-    if K % 128 == 0 and (y.numel() != M * K or ys.numel() != M * K // 128):
-        raise ValueError("output sizes do not match q")
+    ok = K % 128 == 0
+    _need(y, torch.uint8, "y", numel=M * K if ok else None)
+    _need(ys, torch.float32, "ys", numel=M * K // 128 if ok else None)
+    _on_device(q=q, s=s, y=y, ys=ys)
     _call("fp4_to_fp8_rows", _p(q), _p(s), M, K, int(exp_offset_k), _p(y), _p(ys), _stream())
     return y, ys
 
@@ -169,6 +196,14 @@ def fp4_to_fp8_cols_launch_count(K: int) -> int:
     return int(abi().fp4_to_fp8_cols_launch_count(int(K)))
 
 
+def _groups(group_offsets: torch.Tensor) -> int:
+    _need(group_offsets, torch.int64, "group_offsets", 1)
+    G = group_offsets.numel() - 1
+    if G < 1:
+        raise ValueError("group_offsets must hold at least two entries (G >= 1)")
+    return G
+
+
 def fp4_to_fp8_cols(q: torch.Tensor, s: torch.Tensor, group_offsets: torch.Tensor,
                     exp_offset_k: int = 0, yT: torch.Tensor | None = None,
                     yT_scale: torch.Tensor | None = None, dev_status: torch.Tensor | None = None):
@@ -176,19 +211,22 @@ def fp4_to_fp8_cols(q: torch.Tensor, s: torch.Tensor, group_offsets: torch.Tenso
     (yT uint8 [K, M] E4M3, yT_scale float32 [cap, K]: one row of K scales per
     128-token block)."""
     _need(q, torch.uint8, "q", 2)
-    _need(s, torch.uint8, "s", 2)
-    _need(group_offsets, torch.int64, "group_offsets", 1)
     M, K = q.shape[0], q.shape[1] * 2
-    G = group_offsets.numel() - 1
-    cap = fp4_to_fp8_cols_scale_capacity(M, max(G, 1))
+    _need(s, torch.uint8, "s", 2, shape=(M, K // 32))
+    G = _groups(group_offsets)
+    cap = fp4_to_fp8_cols_scale_capacity(M, G)
     yT = _empty((K, M), torch.uint8, q) if yT is None else yT
     yT_scale = _empty((cap, K), torch.float32, q) if yT_scale is None else yT_scale
-    _need(yT, torch.uint8, "yT")
+    _need(yT, torch.uint8, "yT", numel=K * M)
     _need(yT_scale, torch.float32, "yT_scale", 2)
+    if yT_scale.shape[1] != K or yT_scale.shape[0] < cap:
+        raise ValueError(f"yT_scale must be [>= {cap}, {K}], got {tuple(yT_scale.shape)}")
     if dev_status is not None:
         _need(dev_status, torch.int32, "dev_status")
-    if yT.numel() != K * M or yT_scale.shape[1] != K:
-        raise ValueError("output sizes do not match q")
+        if dev_status.numel() < 1:
+            raise ValueError("dev_status must hold one int32")
+    _on_device(q=q, s=s, group_offsets=group_offsets, yT=yT, yT_scale=yT_scale,
+               dev_status=dev_status)
     _call("fp4_to_fp8_cols", _p(q), _p(s), M, K, _p(group_offsets), G, int(exp_offset_k), _p(yT),
           _p(yT_scale), int(yT_scale.shape[0]), _p(dev_status), _stream())
     return yT, yT_scale
@@ -200,28 +238,30 @@ def bf16_to_mxfp4_fp8(x: torch.Tensor, group_offsets: torch.Tensor, exp_offset_k
     """BF16 [M, K] + int64 group offsets [G+1] (device) -> (q, s, y, ys, yT,
     yT_scale): the MXFP4 codes and scales, the FP8 rows and the transposed
     FP8 columns, equal to the three separate calls."""
-    if x.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
-        raise ValueError("x must be bfloat16")
-    _need(x, x.dtype, "x", 2)
-    _need(group_offsets, torch.int64, "group_offsets", 1)
+    _bf16_2d(x, "x")
     M, K = x.shape
-    G = group_offsets.numel() - 1
-    cap = fp4_to_fp8_cols_scale_capacity(M, max(G, 1))
+    G = _groups(group_offsets)
+    cap = fp4_to_fp8_cols_scale_capacity(M, G)
     q = _empty((M, K // 2), torch.uint8, x) if q is None else q
     s = _empty((M, K // 32), torch.uint8, x) if s is None else s
     y = _empty((M, K), torch.uint8, x) if y is None else y
     ys = _empty((M, K // 128), torch.float32, x) if ys is None else ys
     yT = _empty((K, M), torch.uint8, x) if yT is None else yT
     yT_scale = _empty((cap, K), torch.float32, x) if yT_scale is None else yT_scale
-    for t, name, dt in ((q, "q", torch.uint8), (s, "s", torch.uint8), (y, "y", torch.uint8),
-                        (ys, "ys", torch.float32), (yT, "yT", torch.uint8)):
-        _need(t, dt, name)
+    ok = K % 128 == 0
+    for t, name, dt, n in ((q, "q", torch.uint8, M * K // 2), (s, "s", torch.uint8, M * K // 32),
+                           (y, "y", torch.uint8, M * K), (ys, "ys", torch.float32, M * K // 128),
+                           (yT, "yT", torch.uint8, M * K)):
+        _need(t, dt, name, numel=n if ok else None)
     _need(yT_scale, torch.float32, "yT_scale", 2)
+    if yT_scale.shape[1] != K or yT_scale.shape[0] < cap:
+        raise ValueError(f"yT_scale must be [>= {cap}, {K}], got {tuple(yT_scale.shape)}")
     if dev_status is not None:
         _need(dev_status, torch.int32, "dev_status")
-    if (q.numel() * 2 != M * K or s.numel() * 32 != M * K or y.numel() != M * K or
-            ys.numel() * 128 != M * K or yT.numel() != M * K or yT_scale.shape[1] != K):
-        raise ValueError("output sizes do not match x")
+        if dev_status.numel() < 1:
+            raise ValueError("dev_status must hold one int32")
+    _on_device(x=x, group_offsets=group_offsets, q=q, s=s, y=y, ys=ys, yT=yT, yT_scale=yT_scale,
+               dev_status=dev_status)
     _call("bf16_to_mxfp4_fp8", _p(x), M, K, _p(group_offsets), G, int(exp_offset_k), _p(q), _p(s),
           _p(y), _p(ys), _p(yT), _p(yT_scale), int(yT_scale.shape[0]), _p(dev_status), _stream())
     return q, s, y, ys, yT, yT_scale
@@ -229,15 +269,31 @@ def bf16_to_mxfp4_fp8(x: torch.Tensor, group_offsets: torch.Tensor, exp_offset_k
 
 # ---------------------------------------------------------------- NVFP4
 
+def _one_float(t: torch.Tensor, name: str):
+    _need(t, torch.float32, name)
+    if t.numel() < 1:
+        raise ValueError(f"{name} must hold one float32")
+
+
 def nvfp4_amax(x: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
     """max |x| of a BF16 tensor into a 1-element float32 device tensor."""
-    if x.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
-        raise ValueError("x must be bfloat16")
-    _need(x, x.dtype, "x")
+    _bf16(x, "x")
     out = _empty((1,), torch.float32, x) if out is None else out
-    _need(out, torch.float32, "out")
+    _one_float(out, "out")
+    _on_device(x=x, out=out)
     _call("nvfp4_amax", _p(x), x.numel(), _p(out), _stream())
     return out
+
+
+def _nvfp4_outputs(x, q, sb, g, sb_shape, ok):
+    M, K = x.shape
+    q = _empty((M, K // 2), torch.uint8, x) if q is None else q
+    sb = _empty(sb_shape, torch.uint8, x) if sb is None else sb
+    g = _empty((1,), torch.float32, x) if g is None else g
+    _need(q, torch.uint8, "q", numel=M * K // 2 if ok else None)
+    _need(sb, torch.uint8, "sb", numel=sb_shape[0] * sb_shape[1] if ok else None)
+    _one_float(g, "g")
+    return q, sb, g
 
 
 def nvfp4_quantize(x: torch.Tensor, amax: torch.Tensor | None = None, use_sr: bool = False,
@@ -246,14 +302,10 @@ def nvfp4_quantize(x: torch.Tensor, amax: torch.Tensor | None = None, use_sr: bo
     """BF16 [M, K] -> (q uint8 [M, K/2], sb uint8 [M, K/16] E4M3, g float32 [1])."""
     _bf16_2d(x, "x")
     M, K = x.shape
+    q, sb, g = _nvfp4_outputs(x, q, sb, g, (M, K // 16), K % 16 == 0)
     amax = nvfp4_amax(x) if amax is None else amax
-    _need(amax, torch.float32, "amax")
-    q = _empty((M, K // 2), torch.uint8, x) if q is None else q
-    sb = _empty((M, K // 16), torch.uint8, x) if sb is None else sb
-    g = _empty((1,), torch.float32, x) if g is None else g
-    _need(q, torch.uint8, "q")
-    _need(sb, torch.uint8, "sb")
-    _need(g, torch.float32, "g")
+    _one_float(amax, "amax")
+    _on_device(x=x, amax=amax, q=q, sb=sb, g=g)
     _call("nvfp4_quantize", _p(x), M, K, _p(amax), int(bool(use_sr)), int(seed) & (2**64 - 1),
           int(offset), _p(q), _p(sb), _p(g), _stream())
     return q, sb, g
@@ -265,14 +317,10 @@ def nvfp4_quantize_2d(w: torch.Tensor, amax: torch.Tensor | None = None,
     """BF16 [N, K] -> (q uint8 [N, K/2], sb uint8 [N/16, K/16] E4M3, g float32 [1])."""
     _bf16_2d(w, "w")
     N, K = w.shape
+    q, sb, g = _nvfp4_outputs(w, q, sb, g, (N // 16, K // 16), N % 16 == 0 and K % 16 == 0)
     amax = nvfp4_amax(w) if amax is None else amax
-    _need(amax, torch.float32, "amax")
-    q = _empty((N, K // 2), torch.uint8, w) if q is None else q
-    sb = _empty((N // 16, K // 16), torch.uint8, w) if sb is None else sb
-    g = _empty((1,), torch.float32, w) if g is None else g
-    _need(q, torch.uint8, "q")
-    _need(sb, torch.uint8, "sb")
-    _need(g, torch.float32, "g")
+    _one_float(amax, "amax")
+    _on_device(w=w, amax=amax, q=q, sb=sb, g=g)
     _call("nvfp4_quantize_2d", _p(w), N, K, _p(amax), _p(q), _p(sb), _p(g), _stream())
     return q, sb, g
 
@@ -284,19 +332,15 @@ def nvfp4_quantize_2d_t(w: torch.Tensor, amax: torch.Tensor | None = None, q=Non
     FPROP and its transpose for DGRAD, sharing the 16x16 scales, in one read."""
     _bf16_2d(w, "w")
     N, K = w.shape
-    amax = nvfp4_amax(w) if amax is None else amax
-    _need(amax, torch.float32, "amax")
-    q = _empty((N, K // 2), torch.uint8, w) if q is None else q
-    sb = _empty((N // 16, K // 16), torch.uint8, w) if sb is None else sb
+    ok = N % 16 == 0 and K % 16 == 0
+    q, sb, g = _nvfp4_outputs(w, q, sb, g, (N // 16, K // 16), ok)
     qT = _empty((K, N // 2), torch.uint8, w) if qT is None else qT
     sbT = _empty((K // 16, N // 16), torch.uint8, w) if sbT is None else sbT
-    g = _empty((1,), torch.float32, w) if g is None else g
-    for t, name in ((q, "q"), (sb, "sb"), (qT, "qT"), (sbT, "sbT")):
-        _need(t, torch.uint8, name)
-    _need(g, torch.float32, "g")
-    if (q.numel() * 2 != N * K or qT.numel() * 2 != N * K or sb.numel() * 256 != N * K or
-            sbT.numel() * 256 != N * K):
-        raise ValueError("output sizes do not match w")
+    _need(qT, torch.uint8, "qT", numel=N * K // 2 if ok else None)
+    _need(sbT, torch.uint8, "sbT", numel=N * K // 256 if ok else None)
+    amax = nvfp4_amax(w) if amax is None else amax
+    _one_float(amax, "amax")
+    _on_device(w=w, amax=amax, q=q, sb=sb, qT=qT, sbT=sbT, g=g)
     _call("nvfp4_quantize_2d_t", _p(w), N, K, _p(amax), _p(q), _p(sb), _p(qT), _p(sbT), _p(g),
           _stream())
     return q, sb, qT, sbT, g
@@ -306,11 +350,10 @@ def nvfp4_quantize_2d_t(w: torch.Tensor, amax: torch.Tensor | None = None, q=Non
 
 def nvfp4_amax_rht(x: torch.Tensor, sign_mask: int, out: torch.Tensor | None = None) -> torch.Tensor:
     """max |y| of the 16-point random Hadamard transform y of a BF16 tensor."""
-    if x.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
-        raise ValueError("x must be bfloat16")
-    _need(x, x.dtype, "x")
-    out = torch.empty((1,), dtype=torch.float32, device=x.device) if out is None else out
-    _need(out, torch.float32, "out")
+    _bf16(x, "x")
+    out = _empty((1,), torch.float32, x) if out is None else out
+    _one_float(out, "out")
+    _on_device(x=x, out=out)
     _call("nvfp4_amax_rht", _p(x), x.numel(), int(sign_mask) & 0xFFFF, _p(out), _stream())
     return out
 
@@ -319,19 +362,11 @@ def nvfp4_quantize_rht(x: torch.Tensor, amax: torch.Tensor, sign_mask: int, use_
                        seed: int = 0, offset: int = 0, q=None, sb=None, g=None):
     """NVFP4 1x16 quantization of the transformed BF16 tensor [M, K] ->
     (q uint8 [M, K/2], sb uint8 [M, K/16], g float32 [1])."""
-    if x.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
-        raise ValueError("x must be bfloat16")
-    _need(x, x.dtype, "x", 2)
-    _need(amax, torch.float32, "amax")
+    _bf16_2d(x, "x")
     M, K = x.shape
-    q = _empty((M, K // 2), torch.uint8, x) if q is None else q
-    sb = _empty((M, K // 16), torch.uint8, x) if sb is None else sb
-    g = _empty((1,), torch.float32, x) if g is None else g
-    _need(q, torch.uint8, "q")
-    _need(sb, torch.uint8, "sb")
-    _need(g, torch.float32, "g")
-    if q.numel() * 2 != M * K or sb.numel() * 16 != M * K:
-        raise ValueError("output sizes do not match x")
+    q, sb, g = _nvfp4_outputs(x, q, sb, g, (M, K // 16), K % 16 == 0)
+    _one_float(amax, "amax")
+    _on_device(x=x, amax=amax, q=q, sb=sb, g=g)
     _call("nvfp4_quantize_rht", _p(x), M, K, _p(amax), int(sign_mask) & 0xFFFF, int(bool(use_sr)),
           int(seed) & (2**64 - 1), int(offset), _p(q), _p(sb), _p(g), _stream())
     return q, sb, g
@@ -340,16 +375,14 @@ def nvfp4_quantize_rht(x: torch.Tensor, amax: torch.Tensor, sign_mask: int, use_
 # ---------------------------------------------------------------- FP8 backward flow and dequantization
 
 def _fp8_blocks(name, x, block_rows, y=None, s=None):
-    if x.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
-        raise ValueError("x must be bfloat16")
-    _need(x, x.dtype, "x", 2)
+    _bf16_2d(x, "x")
     M, K = x.shape
     y = _empty((M, K), torch.uint8, x) if y is None else y
     s = _empty((M // block_rows, K // 128), torch.float32, x) if s is None else s
-    _need(y, torch.uint8, "y")
-    _need(s, torch.float32, "s")
-    if y.numel() != M * K or s.numel() * 128 * block_rows != M * K:
-        raise ValueError("output sizes do not match x")
+    ok = K % 128 == 0 and M % block_rows == 0
+    _need(y, torch.uint8, "y", numel=M * K)
+    _need(s, torch.float32, "s", numel=(M // block_rows) * (K // 128) if ok else None)
+    _on_device(x=x, y=y, s=s)
     _call(name, _p(x), M, K, _p(y), _p(s), _stream())
     return y, s
 
@@ -367,12 +400,11 @@ def fp8_quantize_128x128(w: torch.Tensor, y=None, s=None):
 def mxfp4_dequantize_rows(q: torch.Tensor, s: torch.Tensor, out: torch.Tensor | None = None):
     """MXFP4 (q uint8 [M, K/2], s uint8 [M, K/32]) -> BF16 [M, K]."""
     _need(q, torch.uint8, "q", 2)
-    _need(s, torch.uint8, "s", 2)
     M, K = q.shape[0], q.shape[1] * 2
+    _need(s, torch.uint8, "s", 2, shape=(M, K // 32))
     out = torch.empty((M, K), dtype=torch.bfloat16, device=q.device) if out is None else out
-    _need(out, torch.bfloat16, "out")
-    if out.numel() != M * K or s.numel() * 32 != M * K:
-        raise ValueError("sizes do not match q")
+    _need(out, torch.bfloat16, "out", numel=M * K)
+    _on_device(q=q, s=s, out=out)
     _call("mxfp4_dequantize_rows", _p(q), _p(s), M, K, _p(out), _stream())
     return out
 
@@ -391,19 +423,13 @@ def nvfp4_quantize_delayed(x: torch.Tensor, history: torch.Tensor, step: int,
     """NVFP4 1x16 quantization of BF16 [M, K] with the per-tensor amax taken
     from the Max-Window history (window = history.numel() - 1); records this
     tensor's amax under `step`.  Returns (q, sb, g)."""
-    if x.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
-        raise ValueError("x must be bfloat16")
-    _need(x, x.dtype, "x", 2)
+    _bf16_2d(x, "x")
     _need(history, torch.int64, "history", 1)
+    if history.numel() < 2:
+        raise ValueError("history must hold window + 1 >= 2 entries")
     M, K = x.shape
-    q = _empty((M, K // 2), torch.uint8, x) if q is None else q
-    sb = _empty((M, K // 16), torch.uint8, x) if sb is None else sb
-    g = _empty((1,), torch.float32, x) if g is None else g
-    _need(q, torch.uint8, "q")
-    _need(sb, torch.uint8, "sb")
-    _need(g, torch.float32, "g")
-    if q.numel() * 2 != M * K or sb.numel() * 16 != M * K:
-        raise ValueError("output sizes do not match x")
+    q, sb, g = _nvfp4_outputs(x, q, sb, g, (M, K // 16), K % 16 == 0)
+    _on_device(x=x, history=history, q=q, sb=sb, g=g)
     _call("nvfp4_quantize_delayed", _p(x), M, K, _p(history), history.numel() - 1,
           int(step) & 0xFFFFFFFF, int(bool(use_sr)), int(seed) & (2**64 - 1), int(offset), _p(q),
           _p(sb), _p(g), _stream())

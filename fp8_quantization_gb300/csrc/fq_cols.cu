@@ -811,7 +811,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
 
     // ===================================================== converting warps
     if (!ok0)
-        return;  // the producer reports it
+        return;  // the producer, which reached no refill, reports it
     const int j = tid & 3;     // MX column of both units
     const int tl0 = tid >> 2;  // token of unit 0 (unit 1: tl0 + 64)
     const int m_out = 4 * wid + (lane >> 3);
@@ -845,8 +845,13 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
             if (i == 3)
                 mbar_arrive(&empty_e[bf]);  // ... and with the super-tile's exponents
         }
-        if (named_barrier_or(1, kThreads, !ok))
-            break;  // the producer reports it
+        if (named_barrier_or(1, kThreads, !ok)) {
+            // a code or maxima wait gave up; the producer may already be past
+            // its last wait, so the converting warps report it themselves
+            if (tid == 0 && dev_status)
+                atomicOr(dev_status, 2);
+            break;
+        }
         write_tile<kAligned16>(tile, yT, M, W, f, m_out, c_out);
 
         if (++st == kStages) {

@@ -104,6 +104,11 @@ def lib():
                 "oracle_nvfp4_quantize_rht": (ctypes.c_int, [vp, i64, i64, ctypes.c_float,
                                                              ctypes.c_uint32, ctypes.c_int, u64,
                                                              u64, vp, vp, vp]),
+                "oracle_mxfp4_error_stats": (ctypes.c_int, [vp, i64, i64, vp, vp, vp]),
+                "oracle_nvfp4_error_stats": (ctypes.c_int, [vp, i64, i64, vp, vp, ctypes.c_float,
+                                                            ctypes.c_int, vp]),
+                "oracle_fp4_to_fp8_counts": (ctypes.c_int, [vp, vp, i64, i64, ctypes.c_int, vp,
+                                                            i32, vp]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -393,3 +398,57 @@ def unpack_nibbles(q) -> np.ndarray:
 def pack_nibbles(c) -> np.ndarray:
     c = np.asarray(c, dtype=np.uint8)
     return (c[..., 0::2] & 0xF) | ((c[..., 1::2] & 0xF) << 4)
+
+
+# ---------------------------------------------------------------- statistics of the method
+# Numbers about the formats on a given input (see fq_oracle.c): the
+# dequantization error of the quantizers and the exactness of the FP4 -> FP8
+# conversion.
+
+def mxfp4_error_stats(x, q, s) -> dict:
+    """Per 32-element block, max |x - xhat| / amax_blk over finite nonzero
+    blocks: largest and mean ratio, block count, blocks above the 1/4 bound."""
+    x = _bits(x)
+    M, K = x.shape
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = np.ascontiguousarray(s, dtype=np.uint8)
+    out = np.zeros(4, dtype=np.float64)
+    if lib().oracle_mxfp4_error_stats(_p(x), M, K, _p(q), _p(s), _p(out)):
+        raise ValueError("oracle_mxfp4_error_stats: bad arguments")
+    return {"max_ratio": float(out[0]), "mean_ratio": float(out[1]), "blocks": int(out[2]),
+            "over_bound": int(out[3]), "bound": 0.25}
+
+
+def nvfp4_error_stats(x, q, sb, g, tile_rows: int = 1) -> dict:
+    """Per 1x16 block (tile_rows = 1) or 16x16 tile, max |x - xhat| / amax_blk
+    over finite nonzero blocks with a normal scale byte (and, separately, the
+    count and largest ratio of blocks whose scale byte is subnormal or 0)."""
+    x = _bits(x)
+    M, K = x.shape
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    sb = np.ascontiguousarray(sb, dtype=np.uint8)
+    out = np.zeros(5, dtype=np.float64)
+    if lib().oracle_nvfp4_error_stats(_p(x), M, K, _p(q), _p(sb), float(np.float32(g)),
+                                      int(tile_rows), _p(out)):
+        raise ValueError("oracle_nvfp4_error_stats: bad arguments")
+    return {"max_ratio": float(out[0]), "mean_ratio": float(out[1]), "blocks": int(out[2]),
+            "small_scale_blocks": int(out[3]), "small_scale_max_ratio": float(out[4])}
+
+
+def fp4_to_fp8_counts(q, s, k: int = 0, offs=None) -> dict:
+    """Elements of the FP4 -> FP8 conversion (row blocks, or the ragged
+    transposed blocks of `offs`) that are exact, rounded, flushed to zero,
+    zero codes, or in blocks with a NaN scale."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = np.ascontiguousarray(s, dtype=np.uint8)
+    M, K = q.shape[0], q.shape[1] * 2
+    counts = np.zeros(5, dtype=np.int64)
+    if offs is None:
+        rc = lib().oracle_fp4_to_fp8_counts(_p(q), _p(s), M, K, int(k), None, 0, _p(counts))
+    else:
+        o = np.ascontiguousarray(offs, dtype=np.int64)
+        rc = lib().oracle_fp4_to_fp8_counts(_p(q), _p(s), M, K, int(k), _p(o), o.size - 1,
+                                            _p(counts))
+    if rc:
+        raise ValueError("oracle_fp4_to_fp8_counts: bad arguments")
+    return dict(zip(("exact", "rounded", "flushed", "zero", "nan_block"), map(int, counts)))

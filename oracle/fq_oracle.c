@@ -932,3 +932,202 @@ int oracle_nvfp4_quantize_delayed(const uint16_t *x, int64_t M, int64_t K, uint6
         *e = v;
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------ statistics of the method
+ * Measurement helpers: the dequantization error of the quantizers and the
+ * exactness of the FP4 -> FP8 conversion on a given input.  They report
+ * numbers about the formats; nothing in the casts above depends on them. */
+
+/* MXFP4 ([MoE-FP4] 2.1): for every block with a finite scale byte and a
+ * nonzero amax, ratio = max_i |x_i - xhat_i| / amax_blk, xhat_i =
+ * v_i * 2^(e - 127).  out[0] largest ratio, out[1] mean ratio, out[2] blocks
+ * counted, out[3] blocks above 1/4 (the closed-form bound: the top binade
+ * [4, 8) of y = |x| 2^(127-e) has grid step 2, the largest value saturates
+ * to 6, and amax_blk 2^(127-e) >= 4). */
+int oracle_mxfp4_error_stats(const uint16_t *x, int64_t M, int64_t K, const uint8_t *q,
+                             const uint8_t *s, double *out)
+{
+    if (M < 0 || K <= 0 || K % 32 != 0)
+        return ORACLE_EARG;
+    const int64_t nb = K / 32, nblk = M * nb;
+    double worst = 0.0, sum = 0.0, count = 0.0, over = 0.0;
+#pragma omp parallel for schedule(static) reduction(max : worst) reduction(+ : sum, count, over)
+    for (int64_t b = 0; b < nblk; b++) {
+        const int e = s[b];
+        if (e == 0xFF)
+            continue;
+        double amax = 0.0, err = 0.0;
+        for (int i = 0; i < 32; i++) {
+            const int64_t idx = 32 * b + i;
+            const double v = (double)bf16_bits_to_float(x[idx]);
+            const int c = get_nibble(q, idx);
+            double xh = ldexp(oracle_e2m1_magnitude(c & 7), e - 127);
+            if (c & 8)
+                xh = -xh;
+            amax = fmax(amax, fabs(v));
+            err = fmax(err, fabs(v - xh));
+        }
+        if (amax == 0.0)
+            continue;
+        const double ratio = err / amax;
+        worst = fmax(worst, ratio);
+        sum += ratio;
+        count += 1.0;
+        if (ratio > 0.25)
+            over += 1.0;
+    }
+    out[0] = worst;
+    out[1] = count > 0 ? sum / count : 0.0;
+    out[2] = count;
+    out[3] = over;
+    return ORACLE_OK;
+}
+
+/* NVFP4 ([NVFP4] "Receta"): xhat = v * E4M3(b) * g with blocks of 1 x 16
+ * (tile_rows = 1) or 16 x 16 tiles (tile_rows = 16).  Blocks with a nonzero,
+ * finite amax and a normal scale byte (E4M3 exponent field >= 1) give
+ * out[0] largest ratio max |x - xhat| / amax_blk, out[1] mean ratio, out[2]
+ * their count; out[3] counts the other nonzero finite blocks (scale byte
+ * subnormal or zero: their amax is below 2^-6 * 6 g), out[4] the largest
+ * ratio among those. */
+int oracle_nvfp4_error_stats(const uint16_t *x, int64_t M, int64_t K, const uint8_t *q,
+                             const uint8_t *sb, float g, int tile_rows, double *out)
+{
+    if (M < 0 || K <= 0 || K % 16 != 0 || (tile_rows != 1 && tile_rows != 16) ||
+        M % tile_rows != 0)
+        return ORACLE_EARG;
+    const int64_t ncol = K / 16, nrow = M / tile_rows, nblk = nrow * ncol;
+    double worst = 0.0, sum = 0.0, count = 0.0, other = 0.0, worst_other = 0.0;
+#pragma omp parallel for schedule(static) \
+    reduction(max : worst, worst_other) reduction(+ : sum, count, other)
+    for (int64_t b = 0; b < nblk; b++) {
+        const int64_t br = b / ncol, bc = b % ncol;
+        const int sbyte = sb[b];
+        if ((sbyte & 0x7F) == 0x7F)
+            continue; /* NaN scale */
+        const double scale = oracle_e4m3_magnitude(sbyte & 0x7F) * (double)g;
+        double amax = 0.0, err = 0.0;
+        int finite = 1;
+        for (int rr = 0; rr < tile_rows; rr++)
+            for (int i = 0; i < 16; i++) {
+                const int64_t idx = (br * tile_rows + rr) * K + 16 * bc + i;
+                if (bf16_is_nonfinite(x[idx]))
+                    finite = 0;
+                const double v = (double)bf16_bits_to_float(x[idx]);
+                const int c = get_nibble(q, idx);
+                double xh = oracle_e2m1_magnitude(c & 7) * scale;
+                if (c & 8)
+                    xh = -xh;
+                amax = fmax(amax, fabs(v));
+                err = fmax(err, fabs(v - xh));
+            }
+        if (!finite || amax == 0.0)
+            continue;
+        const double ratio = err / amax;
+        if ((sbyte & 0x78) != 0) {
+            worst = fmax(worst, ratio);
+            sum += ratio;
+            count += 1.0;
+        } else {
+            other += 1.0;
+            worst_other = fmax(worst_other, ratio);
+        }
+    }
+    out[0] = worst;
+    out[1] = count > 0 ? sum / count : 0.0;
+    out[2] = count;
+    out[3] = other;
+    out[4] = worst_other;
+    return ORACLE_OK;
+}
+
+/* FP4 -> FP8 ([MoE-FP4] 2.1, "numerical equivalence" of the aligned
+ * conversion): classify every element of MXFP4 [M, K] under the row blocks
+ * (offs == NULL) or under the ragged transposed blocks of groups offs[0..G]
+ * (the blocks of oracle_fp4_to_fp8_cols), for exponent offset k.  With v the
+ * E2M1 magnitude and d = S - e the element's shift, the FP8 value is
+ * E4M3(v 2^(k-d)):  counts[0] nonzero and exact, counts[1] nonzero and
+ * rounded to another nonzero value, counts[2] nonzero and flushed to zero,
+ * counts[3] zero codes, counts[4] elements of blocks with a NaN scale. */
+static void classify(int code, int d, int k, int64_t *c)
+{
+    const double v = oracle_e2m1_magnitude(code & 7);
+    if (v == 0.0) {
+        c[3]++;
+        return;
+    }
+    const double t = ldexp(v, k - d);
+    const double back = oracle_e4m3_magnitude(e4m3_rne_satfinite(t));
+    if (back == t)
+        c[0]++;
+    else if (back == 0.0)
+        c[2]++;
+    else
+        c[1]++;
+}
+
+int oracle_fp4_to_fp8_counts(const uint8_t *q, const uint8_t *s, int64_t M, int64_t K, int k,
+                             const int64_t *offs, int32_t G, int64_t *counts)
+{
+    if (M < 0 || K <= 0 || K % 128 != 0 || k < 0 || k > 6)
+        return ORACLE_EARG;
+    const int64_t nmx = K / 32;
+    int64_t c0 = 0, c1 = 0, c2 = 0, c3 = 0, c4 = 0;
+    if (!offs) {
+#pragma omp parallel for schedule(static) reduction(+ : c0, c1, c2, c3, c4)
+        for (int64_t r = 0; r < M; r++) {
+            int64_t c[5] = {0, 0, 0, 0, 0};
+            for (int64_t J = 0; J < K / 128; J++) {
+                const uint8_t *e = s + r * nmx + 4 * J;
+                int S = 0, nan = 0;
+                for (int i = 0; i < 4; i++) {
+                    nan |= e[i] == 0xFF;
+                    S = e[i] > S ? e[i] : S;
+                }
+                for (int i = 0; i < 128; i++) {
+                    if (nan)
+                        c[4]++;
+                    else
+                        classify(get_nibble(q, r * K + 128 * J + i), S - e[i / 32], k, c);
+                }
+            }
+            c0 += c[0], c1 += c[1], c2 += c[2], c3 += c[3], c4 += c[4];
+        }
+    } else {
+        if (G < 1 || offs[0] != 0 || offs[G] != M)
+            return ORACLE_EARG;
+        for (int32_t g = 0; g < G; g++) {
+            if (offs[g + 1] < offs[g])
+                return ORACLE_EARG;
+            const int64_t nblk = (offs[g + 1] - offs[g] + 127) / 128;
+            for (int64_t b = 0; b < nblk; b++) {
+                const int64_t t0 = offs[g] + 128 * b;
+                const int64_t t1 = t0 + 128 < offs[g + 1] ? t0 + 128 : offs[g + 1];
+#pragma omp parallel for schedule(static) reduction(+ : c0, c1, c2, c3, c4)
+                for (int64_t j = 0; j < nmx; j++) {
+                    int64_t c[5] = {0, 0, 0, 0, 0};
+                    int S = 0, nan = 0;
+                    for (int64_t t = t0; t < t1; t++) {
+                        const int e = s[t * nmx + j];
+                        nan |= e == 0xFF;
+                        S = e > S ? e : S;
+                    }
+                    for (int64_t t = t0; t < t1; t++)
+                        for (int64_t kk = 32 * j; kk < 32 * j + 32; kk++) {
+                            if (nan)
+                                c[4]++;
+                            else
+                                classify(get_nibble(q, t * K + kk), S - s[t * nmx + j], k, c);
+                        }
+                    c0 += c[0], c1 += c[1], c2 += c[2], c3 += c[3], c4 += c[4];
+                }
+            }
+        }
+    }
+    counts[0] = c0;
+    counts[1] = c1;
+    counts[2] = c2;
+    counts[3] = c3;
+    counts[4] = c4;
+    return ORACLE_OK;
+}

@@ -176,6 +176,11 @@ def bitrev16(v):
 
 
 def test_sr_stream_definition(oracle_mod):
+    """A definition check, not a pin: it restates the library's mapping of
+    Philox words onto elements (reading R12) and confirms the oracle follows
+    it, so it cannot catch a wrong mapping.  What pins the stream's
+    statistics is test_sr_up_rate_closed_form_every_position below (oracle)
+    and test_gpu_sr_closed_form.py (device)."""
     # Element j = offset + i draws 16 bits from word (j/4) mod 4 of
     # Philox4x32-10(key=seed, counter=(j/16, 0, 0)): with W that word,
     # P = W[23:16]W[7:0], Q = W[31:24]W[15:8], and elements j mod 4 = 0..3
@@ -216,6 +221,39 @@ def test_sr_random_numbers_are_uniform(oracle_mod):
     codes = oracle_mod.unpack_nibbles(q)[:, 1:]
     up = (codes == 3).mean(axis=0)
     assert np.all(np.abs(up - 0.5) < 4 * 0.5 / np.sqrt(4096)), up
+
+
+@pytest.mark.parametrize("setup", ["pow2", "near1"])
+@pytest.mark.parametrize("rht", [False, True])
+def test_sr_up_rate_closed_form_every_position(oracle_mod, setup, rht):
+    """The oracle's stochastic rounding against the closed form of unbiased
+    rounding (sr_closed_form): per value and per position in the block, the
+    up-rate over seeds is floor(2^16 frac) / 2^16 within 4 sigma, at
+    fractions derived from the E2M1 grid -- independent of how the Philox
+    words are mapped onto elements."""
+    import sr_closed_form as S
+    seeds, nblocks, mask = 48, 16384, 0xA5C3
+    d = S.build(setup, nblocks, mask if rht else None, K=1024)
+    types = d["types"]
+    nt = len(types)
+    tix = np.where(d["etype"] < 0, nt - 1, d["etype"])
+    lo = np.array([t[1] for t in types], dtype=np.uint8)[tix]
+    hi = np.array([t[2] for t in types], dtype=np.uint8)[tix]
+    ups = np.zeros(d["bits"].shape, dtype=np.int64)
+    for seed in range(seeds):
+        if rht:
+            q, sb, g = oracle_mod.nvfp4_quantize_rht(d["bits"], d["A"], mask, use_sr=True,
+                                                     seed=seed)
+        else:
+            q, sb, g = oracle_mod.nvfp4_quantize(d["bits"], d["A"], use_sr=True, seed=seed)
+        assert np.all(sb == d["b"]) and g == d["g"]
+        mag = oracle_mod.unpack_nibbles(q) & 7
+        assert np.all((mag == lo) | (mag == hi))
+        ups += (mag == hi) & (hi != lo)
+    idx = (tix * 16 + d["epos"]).ravel()
+    up_tp = np.bincount(idx, weights=ups.ravel(), minlength=nt * 16).reshape(nt, 16)
+    trials = np.bincount(idx, minlength=nt * 16).reshape(nt, 16) * seeds
+    S.check_counts(up_tp, trials, [t[3] for t in types], f"oracle rht={rht} {setup}")
 
 
 def test_2d_transpose_relation(oracle_mod):

@@ -1,31 +1,48 @@
 #!/usr/bin/env python3
 """Benchmark of the block-scaled cast path on one GB300 (or N replicas).
 
-One step = every cast of the path over one batch of the MoE-dispatch
-activations workload (BF16 16384 x 7168, N(0,1) rows times a per-row
-log-normal(0,1) magnitude, seed 0; the tokens are split over 32 experts with
-Zipf(1.1) counts for the transposed ragged conversion):
+Headline (value, ms_per_step, kernels, roofline): one step = every cast of
+the path over one batch of the MoE-dispatch activations workload (BF16
+16384 x 7168, N(0,1) rows times a per-row log-normal(0,1) magnitude, seed 0;
+the tokens are split over 32 experts with Zipf(1.1) counts for the
+transposed ragged conversion):
 
   1. mxfp4_quantize_rows   BF16 -> MXFP4 (packed E2M1 + UE8M0)
   2. fp4_to_fp8_rows       MXFP4 -> E4M3, 128-element blocks, k = 0
   3. fp4_to_fp8_cols       MXFP4 -> E4M3 transposed, 32 ragged expert groups
   4. nvfp4_amax            per-tensor amax
-  5. nvfp4_quantize        NVFP4 1x16, stochastic rounding (seed = step)
+  5. nvfp4_quantize        NVFP4 1x16, stochastic rounding (seed = pass)
   6. nvfp4_quantize_2d     NVFP4 16x16 on the same tensor
 
 The metric is effective bandwidth: algorithmic bytes read + written by the
 kernels over their device time (CUDA events on the launching stream), as GB/s
-and as a fraction of the measured HBM copy bandwidth.  L2 is flushed (256 MB
-written, then read back) between steps, outside the timed events.
+and as a fraction of the measured HBM copy bandwidth.  The timed region is
+--steps K steps, each step's pass repeated R times (R sized so that the
+region lasts about a second and a half, so that the clock sampler sees it);
+L2 is flushed (256 MB written, then read back) before every pass, outside
+the events, which sit at the two ends of every pass.
+
+`configs`: every configuration of the workload definition -- the 256 x 512
+outlier tensor, the MoE-dispatch tensor, the 65536 x 2048 ragged experts, the
+NVFP4 activations (16384 x 14336 Student-t(4)) and weights (14336 x 4096
+N(0, 0.02)), the 1K-262144 row bandwidth sweep at 7168, and a hidden size
+that is a multiple of 128 but not of 512 (the transposed conversion's
+two-launch path) -- each call timed inside its configuration's chain (an
+event between every two calls) and alone (L2 flushed before the call).
+
+`error_stats`: the oracle's numbers about the formats on each
+configuration's input (dequantization error per block; exact, rounded and
+flushed elements of the FP4 -> FP8 conversion at k = 0 and 6).
 
 --impl reference times the CPU oracle (the plain C implementation the tests
-compare against) on a bounded sample of the same workload.
+compare against) on a bounded sample of the headline workload.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -43,34 +60,74 @@ WORKLOAD = ("moe_dispatch bf16 16384x7168 (N(0,1) x row lognormal(0,1), seed 0),
             "fp4_to_fp8_cols(ragged) ; nvfp4_amax -> nvfp4_quantize(SR) ; nvfp4_quantize_2d")
 KERNELS = ["mxfp4_quantize_rows", "fp4_to_fp8_rows", "fp4_to_fp8_cols", "nvfp4_amax",
            "nvfp4_quantize", "nvfp4_quantize_2d"]
-# kernels of libfq.so each entry point launches (nvfp4_amax: the one-thread
-# zeroing of the amax word, then the reduction)
-LAUNCHES = {"mxfp4_quantize_rows": 1, "fp4_to_fp8_rows": 1, "fp4_to_fp8_cols": 2,  # or 1 (K)
-            "nvfp4_amax": 2, "nvfp4_quantize": 1, "nvfp4_quantize_2d": 1}
-# source file of each kernel (for the ncu traffic record's staleness check)
+# source file of each entry point's kernels (for the ncu traffic record's
+# staleness check)
 KERNEL_SRC = {
     "mxfp4_quantize_rows": "fq_mxfp4.cu", "fp4_to_fp8_rows": "fq_mxfp4.cu",
     "fp4_to_fp8_cols": "fq_cols.cu", "nvfp4_amax": "fq_nvfp4.cu",
     "nvfp4_quantize": "fq_nvfp4.cu", "nvfp4_quantize_2d": "fq_nvfp4.cu",
-    "bf16_to_mxfp4_fp8": "fq_mxfp4.cu", "nvfp4_amax_rht": "fq_nvfp4.cu",
+    "bf16_to_mxfp4_fp8": "fq_fused.cu", "nvfp4_amax_rht": "fq_nvfp4.cu",
     "nvfp4_quantize_rht": "fq_nvfp4.cu", "fp8_quantize_1x128": "fq_fp8.cu",
     "fp8_quantize_128x128": "fq_fp8.cu", "mxfp4_dequantize_rows": "fq_fp8.cu",
     "nvfp4_quantize_delayed": "fq_nvfp4.cu", "nvfp4_quantize_2d_t": "fq_nvfp4.cu",
 }
 FALLBACK_HBM_GBS = 6800.0
+TIMED_REGION_S = 1.5
+SWEEP_ROWS = [1024 << i for i in range(9)]
+TWO_LAUNCH_K = 7040   # a multiple of 128, not of 512
+
+
+# ------------------------------------------------------------------ algorithmic bytes
+
+def b_mxfp4(M, K):
+    E = M * K
+    return 2 * E + E // 2 + E // 32
+
+
+def b_rows(M, K):
+    E = M * K
+    return E // 2 + E // 32 + E + 4 * (E // 128)
+
+
+def b_cols(M, K, nb, G):
+    E = M * K
+    return E // 2 + E // 32 + E + 4 * K * nb + 8 * (G + 1)
+
+
+def b_amax(M, K):
+    return 2 * M * K + 4
+
+
+def b_nvfp4(M, K):
+    E = M * K
+    return 2 * E + E // 2 + E // 16 + 8
+
+
+def b_2d(M, K):
+    E = M * K
+    return 2 * E + E // 2 + E // 256 + 8
+
+
+def b_2d_t(M, K):
+    E = M * K
+    return 2 * E + E + 2 * (E // 256) + 8
+
+
+def b_fused(M, K, nb, G):
+    E = M * K
+    return 2 * E + E // 2 + E // 32 + E + 4 * (E // 128) + E + 4 * K * nb + 8 * (G + 1)
 
 
 def algorithmic_bytes(M: int, K: int, nblocks_cols: int, G: int) -> dict:
-    """Bytes each kernel must read + write (inputs once, outputs once)."""
-    E = M * K
-    return {
-        "mxfp4_quantize_rows": 2 * E + E // 2 + E // 32,
-        "fp4_to_fp8_rows": E // 2 + E // 32 + E + 4 * (E // 128),
-        "fp4_to_fp8_cols": E // 2 + E // 32 + E + 4 * K * nblocks_cols + 8 * (G + 1),
-        "nvfp4_amax": 2 * E + 4,
-        "nvfp4_quantize": 2 * E + E // 2 + E // 16 + 8,
-        "nvfp4_quantize_2d": 2 * E + E // 2 + E // 256 + 8,
-    }
+    """Bytes each kernel of the headline step must read + write."""
+    return {"mxfp4_quantize_rows": b_mxfp4(M, K), "fp4_to_fp8_rows": b_rows(M, K),
+            "fp4_to_fp8_cols": b_cols(M, K, nblocks_cols, G), "nvfp4_amax": b_amax(M, K),
+            "nvfp4_quantize": b_nvfp4(M, K), "nvfp4_quantize_2d": b_2d(M, K)}
+
+
+def col_blocks(offs) -> int:
+    import numpy as np
+    return int(((np.diff(np.asarray(offs)) + 127) // 128).sum())
 
 
 def hbm_peak():
@@ -152,7 +209,7 @@ class ClockSampler:
         if not rows:
             rows = [l for _, l in self.lines]
             window = "around timed region (none inside)"
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             f = [x.strip() for x in r.split(",")]
@@ -161,6 +218,7 @@ class ClockSampler:
             try:
                 sm.append(float(f[1]))
                 smax.append(float(f[2]))
+                power.append(float(f[3]))
             except ValueError:
                 continue
             for n, v in zip(names, f[5:9]):
@@ -168,6 +226,8 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
+                "sm_mhz_min": min(sm) if sm else None,
+                "power_w_max": max(power) if power else None,
                 "reasons": sorted(reasons), "samples": len(sm), "window": window}
 
 
@@ -205,9 +265,7 @@ def oracle_sample_pass(bits, offs_rows, K):
     oracle.nvfp4_quantize(bits, A, use_sr=True, seed=1)
     oracle.nvfp4_quantize_2d(bits, A)
     dt = time.perf_counter() - t0
-    import numpy as np
-    nb = int(((np.diff(offs_rows) + 127) // 128).sum())
-    return dt, sum(algorithmic_bytes(M, K, nb, G).values())
+    return dt, sum(algorithmic_bytes(M, K, col_blocks(offs_rows), G).values())
 
 
 def oracle_sample_inputs(rows: int):
@@ -241,6 +299,58 @@ def cpu_baseline(target_s: float = 12.0) -> dict:
                       f"once, {dt:.1f} s",
             "one_core": {"value": round(nbytes1 / dt1 / 1e9, 4), "unit": "GB/s",
                          "sample": f"first {rows1} rows, {dt1:.1f} s"}}
+
+
+def _r(d: dict, nd: int = 6) -> dict:
+    return {k: (round(v, nd) if isinstance(v, float) else v) for k, v in d.items()}
+
+
+def oracle_error_stats(host: dict) -> dict:
+    """The oracle's dequantization error per block and FP4 -> FP8 exactness
+    counts on every configuration's input (host BF16 bits)."""
+    import oracle
+    out = {}
+    t0 = time.perf_counter()
+
+    def mx_chain(bits, offs=None, rows=True):
+        q, s = oracle.mxfp4_quantize_rows(bits)
+        st = {"mxfp4 max|x-xhat|/amax_blk": _r(oracle.mxfp4_error_stats(bits, q, s))}
+        for k in (0, 6):
+            if rows:
+                st[f"fp4_to_fp8_rows k={k}"] = oracle.fp4_to_fp8_counts(q, s, k)
+            if offs is not None:
+                st[f"fp4_to_fp8_cols k={k}"] = oracle.fp4_to_fp8_counts(q, s, k, offs)
+        return st
+
+    out["pr1 256x512"] = mx_chain(host["pr1"])
+    x, offs = host["moe_dispatch"]
+    st = mx_chain(x, offs)
+    A = oracle.nvfp4_amax(x)
+    q, sb, g = oracle.nvfp4_quantize(x, A, use_sr=True, seed=1000)
+    st["nvfp4 1x16 SR (seed 1000) max|x-xhat|/amax_blk"] = _r(oracle.nvfp4_error_stats(x, q, sb, g))
+    q, sb, g = oracle.nvfp4_quantize_2d(x, A)
+    st["nvfp4 16x16 max|x-xhat|/amax_blk"] = _r(oracle.nvfp4_error_stats(x, q, sb, g, 16))
+    out["moe_dispatch 16384x7168"] = st
+    x, offs = host["ragged_experts"]
+    out["ragged_experts 65536x2048"] = mx_chain(x, offs, rows=False)
+    x = host["nvfp4_act"]
+    A = oracle.nvfp4_amax(x)
+    st = {}
+    for sr in (False, True):
+        q, sb, g = oracle.nvfp4_quantize(x, A, use_sr=sr, seed=1234)
+        st[f"nvfp4 1x16 {'SR (seed 1234)' if sr else 'RNE'} max|x-xhat|/amax_blk"] = \
+            _r(oracle.nvfp4_error_stats(x, q, sb, g))
+    out["nvfp4 activations 16384x14336"] = st
+    w = host["nvfp4_weight"]
+    q, sb, g = oracle.nvfp4_quantize_2d(w, oracle.nvfp4_amax(w))
+    out["nvfp4 weights 14336x4096"] = {
+        "nvfp4 16x16 max|x-xhat|/amax_blk": _r(oracle.nvfp4_error_stats(w, q, sb, g, 16))}
+    xs = host["sweep_sample"]
+    import numpy as np
+    out[f"sweep Student-t(3) x 7168, first {xs.shape[0]} rows (every size is a prefix)"] = \
+        mx_chain(xs, np.array([0, xs.shape[0]], dtype=np.int64))
+    out["seconds"] = round(time.perf_counter() - t0, 1)
+    return out
 
 
 def run_reference(args):
@@ -282,6 +392,113 @@ def run_reference(args):
     return 0
 
 
+# ------------------------------------------------------------------ GPU timing helpers
+
+class Timer:
+    """CUDA-event timing on one stream, with an L2 flush (a 256 MB buffer
+    written, then read back, so that its dirty lines are written out before
+    the timed work) ahead of every timed call or pass, outside the events."""
+
+    def __init__(self, dev, warmup):
+        import torch
+        self.torch = torch
+        self.dev = dev
+        self.warmup = warmup
+        self.stream = torch.cuda.current_stream(dev)
+        self.flush_buf = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+
+    def flush(self):
+        self.flush_buf.fill_(1)
+        self.flush_buf.sum(dtype=self.torch.int64)
+
+    def event(self):
+        return self.torch.cuda.Event(enable_timing=True)
+
+    def alone_us(self, fn, reps):
+        """Mean device time of fn() with L2 flushed before every call."""
+        for _ in range(self.warmup):
+            self.flush()
+            fn()
+        ev = [(self.event(), self.event()) for _ in range(reps)]
+        for a, b in ev:
+            self.flush()
+            a.record(self.stream)
+            fn()
+            b.record(self.stream)
+        self.torch.cuda.synchronize(self.dev)
+        return sum(a.elapsed_time(b) for a, b in ev) / reps * 1e3
+
+    def chain_us(self, fns, reps):
+        """Per-call device times inside the chain (an event between every two
+        calls) and the chain's time with events at its two ends only."""
+        n = len(fns)
+        for _ in range(self.warmup):
+            self.flush()
+            for fn in fns:
+                fn()
+        ev = [[self.event() for _ in range(n + 1)] for _ in range(reps)]
+        for e in ev:
+            self.flush()
+            for j, fn in enumerate(fns):
+                e[j].record(self.stream)
+                fn()
+            e[n].record(self.stream)
+        ends = [(self.event(), self.event()) for _ in range(reps)]
+        for a, b in ends:
+            self.flush()
+            a.record(self.stream)
+            for fn in fns:
+                fn()
+            b.record(self.stream)
+        self.torch.cuda.synchronize(self.dev)
+        per = [sum(e[j].elapsed_time(e[j + 1]) for e in ev) / reps * 1e3 for j in range(n)]
+        total = sum(a.elapsed_time(b) for a, b in ends) / reps * 1e3
+        return per, total
+
+
+def link_rates(dev, nbytes=256 << 20, reps=5):
+    """Pinned host <-> device copy rates (GB/s): each direction alone and both
+    directions at once on two streams."""
+    import torch
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.ones(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def one(stream, fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            fn()
+            a.record(stream)
+            for _ in range(reps):
+                fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        return nbytes * reps / (a.elapsed_time(b) * 1e-3) / 1e9
+
+    h2d = one(s1, lambda: d_in.copy_(h_in, non_blocking=True))
+    d2h = one(s2, lambda: h_out.copy_(d_out, non_blocking=True))
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s1)
+    s2.wait_event(a)
+    with torch.cuda.stream(s1):
+        for _ in range(reps):
+            d_in.copy_(h_in, non_blocking=True)
+    with torch.cuda.stream(s2):
+        for _ in range(reps):
+            h_out.copy_(d_out, non_blocking=True)
+    e2 = torch.cuda.Event()
+    e2.record(s2)
+    s1.wait_event(e2)
+    b.record(s1)
+    torch.cuda.synchronize(dev)
+    both = 2 * nbytes * reps / (a.elapsed_time(b) * 1e-3) / 1e9
+    return {"h2d": round(h2d, 1), "d2h": round(d2h, 1), "both_directions_total": round(both, 1),
+            "copy_bytes": nbytes}
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def run_gpu(args):
@@ -299,21 +516,33 @@ def run_gpu(args):
     dev = torch.device("cuda", local if ws > 1 else 0)
     torch.cuda.set_device(dev)
     fq.abi()  # fail loudly if the library is missing
+    peak, peak_kind = hbm_peak()
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20))
+    T = Timer(dev, args.warmup)
+    stream = T.stream
+    u8 = dict(dtype=torch.uint8, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    wall0 = time.time()
 
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(
+            torch.bfloat16)
+
+    def frac(nbytes, us):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        return round(gbs, 1), round(gbs / peak, 4)
+
+    # ---------------------------------------------------------------- headline
     M, K, G = M_ROWS, K_COLS, EXPERTS
     bits = workloads.moe_dispatch(M, K, seed=0)
     offs_np = workloads.zipf_group_offsets(M, G, 1.1, 0)
-    nb_cols = int(((np.diff(offs_np) + 127) // 128).sum())
+    nb_cols = col_blocks(offs_np)
     nbytes = algorithmic_bytes(M, K, nb_cols, G)
-    launches_per_step = sum(LAUNCHES.values()) - LAUNCHES["fp4_to_fp8_cols"] + \
-        fq.fp4_to_fp8_cols_launch_count(K)
+    launches_per_pass = (1 + 1 + fq.fp4_to_fp8_cols_launch_count(K) + 2 + 1 + 1)
     step_bytes = sum(nbytes.values())
-
-    x = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    x = to_dev(bits)
     offs = torch.from_numpy(offs_np).to(dev)
     cap = fq.fp4_to_fp8_cols_scale_capacity(M, G)
-    u8 = dict(dtype=torch.uint8, device=dev)
-    f32 = dict(dtype=torch.float32, device=dev)
     out = {
         "q": torch.empty((M, K // 2), **u8), "s": torch.empty((M, K // 32), **u8),
         "y": torch.empty((M, K), **u8), "ys": torch.empty((M, K // 128), **f32),
@@ -324,51 +553,45 @@ def run_gpu(args):
         "q2": torch.empty((M, K // 2), **u8), "sb2": torch.empty((M // 16, K // 16), **u8),
         "g2": torch.empty((1,), **f32),
     }
-    flush_buf = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
 
-    def flush():
-        # evict L2 (2x its size): write a buffer, then read it back so that
-        # the flush's own dirty lines are written out here, not in the next step
-        flush_buf.fill_(1)
-        flush_buf.sum(dtype=torch.int64)
-
-    stream = torch.cuda.current_stream(dev)
-
-    def step(i, xin, ev=None, o=None, offs_d=None):
+    def step_calls(i, xin, o=None, offs_d=None):
         o = out if o is None else o
         offs_d = offs if offs_d is None else offs_d
-        if ev:
-            ev[0].record(stream)
-        fq.mxfp4_quantize_rows(xin, o["q"], o["s"])
-        if ev:
-            ev[1].record(stream)
-        fq.fp4_to_fp8_rows(o["q"], o["s"], 0, o["y"], o["ys"])
-        if ev:
-            ev[2].record(stream)
-        fq.fp4_to_fp8_cols(o["q"], o["s"], offs_d, 0, o["yT"], o["yTs"])
-        if ev:
-            ev[3].record(stream)
-        fq.nvfp4_amax(xin, o["amax"])
-        if ev:
-            ev[4].record(stream)
-        fq.nvfp4_quantize(xin, o["amax"], use_sr=True, seed=1000 + i, offset=0, q=o["q4"],
-                          sb=o["sb4"], g=o["g4"])
-        if ev:
-            ev[5].record(stream)
-        fq.nvfp4_quantize_2d(xin, o["amax"], o["q2"], o["sb2"], o["g2"])
-        if ev:
-            ev[6].record(stream)
+        return [
+            lambda: fq.mxfp4_quantize_rows(xin, o["q"], o["s"]),
+            lambda: fq.fp4_to_fp8_rows(o["q"], o["s"], 0, o["y"], o["ys"]),
+            lambda: fq.fp4_to_fp8_cols(o["q"], o["s"], offs_d, 0, o["yT"], o["yTs"]),
+            lambda: fq.nvfp4_amax(xin, o["amax"]),
+            lambda: fq.nvfp4_quantize(xin, o["amax"], use_sr=True, seed=1000 + i, offset=0,
+                                      q=o["q4"], sb=o["sb4"], g=o["g4"]),
+            lambda: fq.nvfp4_quantize_2d(xin, o["amax"], o["q2"], o["sb2"], o["g2"]),
+        ]
 
-    for i in range(args.warmup):
-        flush()
+    def step(i, xin, o=None, offs_d=None):
+        for fn in step_calls(i, xin, o, offs_d):
+            fn()
+
+    # warm-up passes, which also size the repetition count R of the timed steps
+    wev = [(T.event(), T.event(), T.event()) for _ in range(args.warmup)]
+    for i, (a, b, c) in enumerate(wev):
+        a.record(stream)
+        T.flush()
+        b.record(stream)
         step(i, x)
+        c.record(stream)
     torch.cuda.synchronize(dev)
+    pass_ms = min(b.elapsed_time(c) for a, b, c in wev)
+    flush_ms = min(a.elapsed_time(b) for a, b, c in wev)
+    reps = max(1, math.ceil(TIMED_REGION_S * 1e3 / (args.steps * (pass_ms + flush_ms + 0.01))))
+    if ws > 1:
+        reps = int(max_over_ranks(float(reps), dev))
 
-    # The timed region: CUDA events at the two ends of every step only.  An
-    # event recorded between two kernels holds the next launch until it is
-    # processed (about 2 us per kernel boundary), so the split of the step
-    # over its kernels is measured in a second pass below.
-    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    # The timed region: K steps x R passes, CUDA events at the two ends of
+    # every pass only.  An event recorded between two kernels holds the next
+    # launch until it is processed (about 2 us per kernel boundary), so the
+    # split of the step over its kernels is measured in a second pass below.
+    npass = args.steps * reps
+    sevs = [(T.event(), T.event()) for _ in range(npass)]
     sampler = ClockSampler(dev.index)
     sampler.start()
     time.sleep(0.3)  # let the sampler start before the timed region
@@ -376,112 +599,71 @@ def run_gpu(args):
         dist.barrier()
     torch.cuda.synchronize(dev)
     t0 = time.time()
-    for i in range(args.steps):
-        flush()
-        sevs[i][0].record(stream)
+    for i, (a, b) in enumerate(sevs):
+        T.flush()
+        a.record(stream)
         step(i, x)
-        sevs[i][1].record(stream)
+        b.record(stream)
     torch.cuda.synchronize(dev)
     t1 = time.time()
     if ws > 1:
         dist.barrier()
     clocks = sampler.stop(t0, t1)
-    step_ms = sum(a.elapsed_time(b) for a, b in sevs)
-    step_ms_max = max_over_ranks(step_ms, dev)
-    ms_per_step = step_ms_max / args.steps
-    value = ws * step_bytes * args.steps / (step_ms_max * 1e-3) / 1e9
+    pass_total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in sevs), dev)
+    ms_per_step = pass_total_ms / npass
+    value = ws * step_bytes * npass / (pass_total_ms * 1e-3) / 1e9
 
-    # the split: the same steps with an event between every two kernels
-    split_steps = max(3, min(args.steps, 200))
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(split_steps)]
-    for i in range(split_steps):
-        flush()
-        step(i, x, evs[i])
-    torch.cuda.synchronize(dev)
-    per_kernel_ms = {k: 0.0 for k in KERNELS}
-    split_ms = 0.0
-    for ev in evs:
-        for j, k in enumerate(KERNELS):
-            per_kernel_ms[k] += ev[j].elapsed_time(ev[j + 1])
-        split_ms += ev[0].elapsed_time(ev[6])
-    for k in KERNELS:
-        per_kernel_ms[k] = max_over_ranks(per_kernel_ms[k], dev) / split_steps
-    split_ms_per_step = max_over_ranks(split_ms, dev) / split_steps
-
-    peak, peak_kind = hbm_peak()
+    # the split: the same passes with an event between every two kernels,
+    # and each cast alone with L2 flushed before it
+    split_reps = max(3, min(args.steps, 200))
+    per_us, _ = T.chain_us(step_calls(0, x), split_reps)
     kernels = {}
-    for k in KERNELS:
-        ms = per_kernel_ms[k]
-        gbs = nbytes[k] / (ms * 1e-3) / 1e9
-        kernels[k] = {"us": round(ms * 1e3, 2), "bytes": nbytes[k], "GB/s": round(gbs, 1),
-                      "frac": round(gbs / peak, 4)}
-    dom = max(KERNELS, key=lambda k: per_kernel_ms[k])
-    traffic = ncu_traffic(dom)
+    for k, us in zip(KERNELS, per_us):
+        us = max_over_ranks(us, dev)
+        gbs, fr = frac(nbytes[k], us)
+        kernels[k] = {"us": round(us, 2), "bytes": nbytes[k], "GB/s": gbs, "frac": fr}
+    for k, fn in zip(KERNELS, step_calls(7, x)):
+        us = max_over_ranks(T.alone_us(fn, split_reps), dev)
+        gbs, fr = frac(nbytes[k], us)
+        kernels[k]["alone"] = {"us": round(us, 2), "GB/s": gbs, "frac": fr}
+    dom = max(KERNELS, key=lambda k: kernels[k]["us"])
     roofline = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["GB/s"],
                 "peak": peak, "unit": "GB/s", "frac": kernels[dom]["frac"],
-                "traffic": traffic, "peak_source": f"hbm_gbs of {peak_kind}",
-                "algorithmic_bytes": nbytes[dom]}
+                "traffic": ncu_traffic(dom), "peak_source": f"hbm_gbs of {peak_kind}",
+                "algorithmic_bytes": nbytes[dom],
+                "timing": "CUDA events around the kernel inside the step (split pass)"}
 
-    # ---- calls beyond the six casts, on the same tensor, each timed alone
-    # (L2 flushed before every call)
-    extra_steps = max(3, min(args.steps, 200))
-
-    def timed_us(fn):
-        for _ in range(args.warmup):
-            flush()
-            fn()
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(extra_steps)]
-        for i in range(extra_steps):
-            flush()
-            ev[i][0].record(stream)
-            fn()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize(dev)
-        return max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), dev) / extra_steps * 1e3
-
-    def entry(call, us, nbytes, launches, **kw):
-        gbs = nbytes / (us * 1e-6) / 1e9
-        return {"call": call, "us": round(us, 2), "bytes": nbytes, "GB/s": round(gbs, 1),
-                "frac": round(gbs / peak, 4), "launches_per_call": launches,
-                "traffic": ncu_traffic(call), **kw}
-
-    # the six casts again, each alone with L2 flushed before every call: the
-    # per-kernel figure without the previous kernel's dirty lines (written
-    # back during the next kernel in the step)
-    alone = {
-        "mxfp4_quantize_rows": lambda: fq.mxfp4_quantize_rows(x, out["q"], out["s"]),
-        "fp4_to_fp8_rows": lambda: fq.fp4_to_fp8_rows(out["q"], out["s"], 0, out["y"], out["ys"]),
-        "fp4_to_fp8_cols": lambda: fq.fp4_to_fp8_cols(out["q"], out["s"], offs, 0, out["yT"],
-                                                      out["yTs"]),
-        "nvfp4_amax": lambda: fq.nvfp4_amax(x, out["amax"]),
-        "nvfp4_quantize": lambda: fq.nvfp4_quantize(x, out["amax"], use_sr=True, seed=7, offset=0,
-                                                    q=out["q4"], sb=out["sb4"], g=out["g4"]),
-        "nvfp4_quantize_2d": lambda: fq.nvfp4_quantize_2d(x, out["amax"], out["q2"], out["sb2"],
-                                                          out["g2"]),
-    }
-    for k, fn in alone.items():
-        us = timed_us(fn)
-        gbs = nbytes[k] / (us * 1e-6) / 1e9
-        kernels[k]["alone"] = {"us": round(us, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
-
+    # ---------------------------------------------------------------- calls
+    # beyond the six casts, on the same tensor, each timed alone
+    extra_reps = max(3, min(args.steps, 200))
     E = M * K
+
+    def entry(call, us, nb, launches, **kw):
+        gbs, fr = frac(nb, us)
+        return {"call": call, "us": round(us, 2), "bytes": nb, "GB/s": gbs, "frac": fr,
+                "launches_per_call": launches, "traffic": ncu_traffic(call), **kw}
+
+    def alone(fn):
+        return max_over_ranks(T.alone_us(fn, extra_reps), dev)
+
     fo = {k: torch.empty_like(out[k]) for k in ("q", "s", "y", "ys", "yT", "yTs")}
-    fused_us = timed_us(lambda: fq.bf16_to_mxfp4_fp8(x, offs, 0, fo["q"], fo["s"], fo["y"],
-                                                      fo["ys"], fo["yT"], fo["yTs"]))
-    sep_us = sum(kernels[k]["us"] for k in ("mxfp4_quantize_rows", "fp4_to_fp8_rows",
-                                             "fp4_to_fp8_cols"))
+    fused_us = alone(lambda: fq.bf16_to_mxfp4_fp8(x, offs, 0, fo["q"], fo["s"], fo["y"], fo["ys"],
+                                                  fo["yT"], fo["yTs"]))
+    sep_us = sum(kernels[k]["alone"]["us"] for k in KERNELS[:3])
     rht_mask = 0x9E37
-    ar = torch.empty((1,), dtype=torch.float32, device=dev)
-    amax_rht_us = timed_us(lambda: fq.nvfp4_amax_rht(x, rht_mask, ar))
-    rht_us = timed_us(lambda: fq.nvfp4_quantize_rht(x, ar, rht_mask, True, 4242, 0, out["q4"],
+    ar = torch.empty((1,), **f32)
+    amax_rht_us = alone(lambda: fq.nvfp4_amax_rht(x, rht_mask, ar))
+    rht_us = alone(lambda: fq.nvfp4_quantize_rht(x, ar, rht_mask, True, 4242, 0, out["q4"],
+                                                 out["sb4"], out["g4"]))
+    rht_rne_us = alone(lambda: fq.nvfp4_quantize_rht(x, ar, rht_mask, False, 0, 0, out["q4"],
                                                      out["sb4"], out["g4"]))
-    fy = torch.empty((M, K), dtype=torch.uint8, device=dev)
-    fs1 = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
-    fs2 = torch.empty((M // 128, K // 128), dtype=torch.float32, device=dev)
-    fp8_1x128_us = timed_us(lambda: fq.fp8_quantize_1x128(x, fy, fs1))
-    fp8_128_us = timed_us(lambda: fq.fp8_quantize_128x128(x, fy, fs2))
+    fy = torch.empty((M, K), **u8)
+    fs1 = torch.empty((M, K // 128), **f32)
+    fs2 = torch.empty((M // 128, K // 128), **f32)
+    fp8_1x128_us = alone(lambda: fq.fp8_quantize_1x128(x, fy, fs1))
+    fp8_128_us = alone(lambda: fq.fp8_quantize_128x128(x, fy, fs2))
     deq = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
-    deq_us = timed_us(lambda: fq.mxfp4_dequantize_rows(out["q"], out["s"], deq))
+    deq_us = alone(lambda: fq.mxfp4_dequantize_rows(out["q"], out["s"], deq))
     hist = fq.amax_history(64, device=dev)
     dstep = [0]
 
@@ -489,38 +671,184 @@ def run_gpu(args):
         fq.nvfp4_quantize_delayed(x, hist, dstep[0], True, 99, 0, out["q4"], out["sb4"], out["g4"])
         dstep[0] += 1
 
-    delayed_us = timed_us(delayed_call)
-    qT = torch.empty((K, M // 2), dtype=torch.uint8, device=dev)
-    sbT = torch.empty((K // 16, M // 16), dtype=torch.uint8, device=dev)
-    w2t_us = timed_us(lambda: fq.nvfp4_quantize_2d_t(x, out["amax"], out["q2"], out["sb2"], qT,
-                                                     sbT, out["g2"]))
+    delayed_us = alone(delayed_call)
+    qT = torch.empty((K, M // 2), **u8)
+    sbT = torch.empty((K // 16, M // 16), **u8)
+    w2t_us = alone(lambda: fq.nvfp4_quantize_2d_t(x, out["amax"], out["q2"], out["sb2"], qT, sbT,
+                                                  out["g2"]))
     next_rows = {
-        "bf16_to_mxfp4_fp8": entry(
-            "bf16_to_mxfp4_fp8", fused_us,
-            2 * E + E // 2 + E // 32 + E + 4 * (E // 128) + E + 4 * K * nb_cols + 8 * (G + 1),
-            1 + fq.fp4_to_fp8_cols_launch_count(K), separate_calls_us=round(sep_us, 2)),
-        "nvfp4_amax_rht": entry("nvfp4_amax_rht", amax_rht_us, 2 * E + 4, 1),
-        "nvfp4_quantize_rht_sr": entry("nvfp4_quantize_rht", rht_us, 2 * E + E // 2 + E // 16 + 8,
-                                       1, sign_mask=rht_mask),
+        "bf16_to_mxfp4_fp8": entry("bf16_to_mxfp4_fp8", fused_us, b_fused(M, K, nb_cols, G),
+                                   1 + fq.fp4_to_fp8_cols_launch_count(K),
+                                   separate_calls_alone_us=round(sep_us, 2)),
+        "nvfp4_amax_rht": entry("nvfp4_amax_rht", amax_rht_us, 2 * E + 4, 2),
+        "nvfp4_quantize_rht_sr": entry("nvfp4_quantize_rht", rht_us, b_nvfp4(M, K), 1,
+                                       sign_mask=rht_mask),
+        "nvfp4_quantize_rht_rne": entry("nvfp4_quantize_rht", rht_rne_us, b_nvfp4(M, K), 1,
+                                        sign_mask=rht_mask),
         "fp8_quantize_1x128": entry("fp8_quantize_1x128", fp8_1x128_us, 3 * E + 4 * (E // 128), 1),
         "fp8_quantize_128x128": entry("fp8_quantize_128x128", fp8_128_us,
                                       3 * E + 4 * (E // 16384), 1),
         "mxfp4_dequantize_rows": entry("mxfp4_dequantize_rows", deq_us,
                                        E // 2 + E // 32 + 2 * E, 1),
         "nvfp4_quantize_delayed_sr": entry(
-            "nvfp4_quantize_delayed", delayed_us, 2 * E + E // 2 + E // 16 + 16 * 65, 1, window=64,
-            amax_then_quantize_us=round(kernels["nvfp4_amax"]["us"] +
-                                        kernels["nvfp4_quantize"]["us"], 2)),
-        "nvfp4_quantize_2d_t": entry(
-            "nvfp4_quantize_2d_t", w2t_us, 2 * E + E // 2 + E // 256 + E // 2 + E // 256 + 8, 1,
-            without_transpose_us=kernels["nvfp4_quantize_2d"]["us"]),
-        "steps": extra_steps,
+            "nvfp4_quantize_delayed", delayed_us, b_nvfp4(M, K) + 16 * 65, 1, window=64,
+            amax_then_quantize_alone_us=round(kernels["nvfp4_amax"]["alone"]["us"] +
+                                              kernels["nvfp4_quantize"]["alone"]["us"], 2)),
+        "nvfp4_quantize_2d_t": entry("nvfp4_quantize_2d_t", w2t_us, b_2d_t(M, K), 1,
+                                     without_transpose_alone_us=kernels["nvfp4_quantize_2d"][
+                                         "alone"]["us"]),
+        "reps": extra_reps, "timing": "alone, L2 flushed before every call",
     }
+    del fo, fy, fs1, fs2, deq, qT, sbT
 
-    # ---- end to end through host buffers: every step copies its input (and
-    # the group offsets) from pinned host memory, runs all casts and copies
-    # every output back to pinned host memory.  Three streams pipeline the
-    # steps (H2D of step i+1 and D2H of step i-1 overlap the casts of step i);
+    # ---------------------------------------------------------------- configs
+    cfg_reps = max(3, min(args.steps, 50))
+    host = {"pr1": workloads.pr1(256, 512, seed=0), "moe_dispatch": (bits, offs_np)}
+    configs = {}
+
+    def run_config(name, workload, calls):
+        """calls: (label, fn, bytes) in chain order."""
+        fns = [c[1] for c in calls]
+        per, total = T.chain_us(fns, cfg_reps)
+        res = {"workload": workload, "calls": {}}
+        tot_bytes = 0
+        for (label, fn, nbb), us_c in zip(calls, per):
+            us_c = max_over_ranks(us_c, dev)
+            us_a = max_over_ranks(T.alone_us(fn, cfg_reps), dev)
+            gc, fc = frac(nbb, us_c)
+            ga, fa = frac(nbb, us_a)
+            res["calls"][label] = {"bytes": nbb, "chained_us": round(us_c, 2), "chained_frac": fc,
+                                   "alone_us": round(us_a, 2), "alone_GB/s": ga, "alone_frac": fa,
+                                   "l2_resident": nbb <= l2_bytes}
+            tot_bytes += nbb
+        total = max_over_ranks(total, dev)
+        g, f = frac(tot_bytes, total)
+        res["chain"] = {"us": round(total, 2), "GB/s": g, "frac": f,
+                        "events": "at the chain's two ends"}
+        configs[name] = res
+
+    def mx_outputs(Mc, Kc, Gc):
+        capc = fq.fp4_to_fp8_cols_scale_capacity(Mc, Gc)
+        return {"q": torch.empty((Mc, Kc // 2), **u8), "s": torch.empty((Mc, Kc // 32), **u8),
+                "y": torch.empty((Mc, Kc), **u8), "ys": torch.empty((Mc, Kc // 128), **f32),
+                "yT": torch.empty((Kc, Mc), **u8), "yTs": torch.empty((capc, Kc), **f32)}
+
+    # PR1: 256 x 512 (L2-resident), MXFP4 then FP8 rows at k = 0 and 6
+    xp = to_dev(host["pr1"])
+    op = mx_outputs(256, 512, 1)
+    run_config("pr1 256x512", "N(0,1), 0.1% x100 (seed 0)", [
+        ("mxfp4_quantize_rows", lambda: fq.mxfp4_quantize_rows(xp, op["q"], op["s"]),
+         b_mxfp4(256, 512)),
+        ("fp4_to_fp8_rows k=0", lambda: fq.fp4_to_fp8_rows(op["q"], op["s"], 0, op["y"], op["ys"]),
+         b_rows(256, 512)),
+        ("fp4_to_fp8_rows k=6", lambda: fq.fp4_to_fp8_rows(op["q"], op["s"], 6, op["y"], op["ys"]),
+         b_rows(256, 512))])
+    del xp, op
+
+    # MoE dispatch: the headline chain (its figures are in `kernels` as well)
+    run_config("moe_dispatch 16384x7168", "N(0,1) x row lognormal(0,1), 32 Zipf(1.1) experts",
+               list(zip(KERNELS, step_calls(3, x), [nbytes[k] for k in KERNELS])))
+
+    # ragged experts: 65536 x 2048, 32 Zipf(1.1) groups: MXFP4, then the
+    # transposed conversion
+    Mr, Kr = 65536, 2048
+    bits_r, offs_r = workloads.ragged_experts(Mr, Kr, 32, seed=0)
+    host["ragged_experts"] = (bits_r, offs_r)
+    xr = to_dev(bits_r)
+    offr = torch.from_numpy(offs_r).to(dev)
+    orr = mx_outputs(Mr, Kr, 32)
+    run_config("ragged_experts 65536x2048", "N(0,1), 32 experts Zipf(1.1), no padding", [
+        ("mxfp4_quantize_rows", lambda: fq.mxfp4_quantize_rows(xr, orr["q"], orr["s"]),
+         b_mxfp4(Mr, Kr)),
+        ("fp4_to_fp8_cols", lambda: fq.fp4_to_fp8_cols(orr["q"], orr["s"], offr, 0, orr["yT"],
+                                                       orr["yTs"]),
+         b_cols(Mr, Kr, col_blocks(offs_r), 32))])
+    del xr, offr, orr
+
+    # NVFP4: activations 16384 x 14336 Student-t(4) (amax, SR, RNE) and
+    # weights 14336 x 4096 N(0, 0.02) (amax, 2D, 2D with the DGRAD operand)
+    Ma, Ka = 16384, 14336
+    host["nvfp4_act"] = workloads.nvfp4_act(Ma, Ka, seed=0)
+    xa = to_dev(host["nvfp4_act"])
+    aa = torch.empty((1,), **f32)
+    qa, sba, ga = (torch.empty((Ma, Ka // 2), **u8), torch.empty((Ma, Ka // 16), **u8),
+                   torch.empty((1,), **f32))
+    run_config("nvfp4 activations 16384x14336", "Student-t(4), seed 0", [
+        ("nvfp4_amax", lambda: fq.nvfp4_amax(xa, aa), b_amax(Ma, Ka)),
+        ("nvfp4_quantize SR", lambda: fq.nvfp4_quantize(xa, aa, True, 1234, 0, qa, sba, ga),
+         b_nvfp4(Ma, Ka)),
+        ("nvfp4_quantize RNE", lambda: fq.nvfp4_quantize(xa, aa, False, 0, 0, qa, sba, ga),
+         b_nvfp4(Ma, Ka))])
+    del xa, qa, sba
+    Nw, Kw = 14336, 4096
+    host["nvfp4_weight"] = workloads.nvfp4_weight(Nw, Kw, seed=0)
+    xw = to_dev(host["nvfp4_weight"])
+    aw = torch.empty((1,), **f32)
+    qw, sbw, gw = (torch.empty((Nw, Kw // 2), **u8), torch.empty((Nw // 16, Kw // 16), **u8),
+                   torch.empty((1,), **f32))
+    qwT, sbwT = torch.empty((Kw, Nw // 2), **u8), torch.empty((Kw // 16, Nw // 16), **u8)
+    run_config("nvfp4 weights 14336x4096", "N(0, 0.02), seed 0", [
+        ("nvfp4_amax", lambda: fq.nvfp4_amax(xw, aw), b_amax(Nw, Kw)),
+        ("nvfp4_quantize_2d", lambda: fq.nvfp4_quantize_2d(xw, aw, qw, sbw, gw), b_2d(Nw, Kw)),
+        ("nvfp4_quantize_2d_t", lambda: fq.nvfp4_quantize_2d_t(xw, aw, qw, sbw, qwT, sbwT, gw),
+         b_2d_t(Nw, Kw))])
+    del xw, qw, sbw, qwT, sbwT
+
+    # bandwidth sweep: M = 1K .. 256K rows x 7168 Student-t(3): MXFP4, FP8
+    # rows, FP8 columns (one group); every size is a prefix of the largest
+    Ks, Mmax = 7168, SWEEP_ROWS[-1]
+    bits_s = workloads.sweep(Mmax, Ks, seed=0)
+    host["sweep_sample"] = np.ascontiguousarray(bits_s[:16384])
+    xs = to_dev(bits_s)
+    del bits_s
+    qs, ss = torch.empty((Mmax, Ks // 2), **u8), torch.empty((Mmax, Ks // 32), **u8)
+    ys_, yss = torch.empty((Mmax, Ks), **u8), torch.empty((Mmax, Ks // 128), **f32)
+    yTflat = torch.empty((Mmax * Ks,), **u8)
+    yTsflat = torch.empty(((Mmax // 128 + 1) * Ks,), **f32)
+    for m in SWEEP_ROWS:
+        xm, qm, sm, ym, ysm = xs[:m], qs[:m], ss[:m], ys_[:m], yss[:m]
+        yTm = yTflat[: m * Ks].view(Ks, m)
+        capm = fq.fp4_to_fp8_cols_scale_capacity(m, 1)
+        yTsm = yTsflat[: capm * Ks].view(capm, Ks)
+        om = torch.tensor([0, m], dtype=torch.int64, device=dev)
+        run_config(f"sweep {m}x7168", "Student-t(3), seed 0 (prefix rows), one group", [
+            ("mxfp4_quantize_rows", lambda: fq.mxfp4_quantize_rows(xm, qm, sm), b_mxfp4(m, Ks)),
+            ("fp4_to_fp8_rows", lambda: fq.fp4_to_fp8_rows(qm, sm, 0, ym, ysm), b_rows(m, Ks)),
+            ("fp4_to_fp8_cols", lambda: fq.fp4_to_fp8_cols(qm, sm, om, 0, yTm, yTsm),
+             b_cols(m, Ks, (m + 127) // 128, 1))])
+    del xs, qs, ss, ys_, yss, yTflat, yTsflat
+
+    # a hidden size that is a multiple of 128 but not of 512: the transposed
+    # conversion's two-launch path, MoE-dispatch recipe, 32 Zipf experts
+    Mt, Kt = 16384, TWO_LAUNCH_K
+    xt = to_dev(workloads.moe_dispatch(Mt, Kt, seed=0))
+    offt = torch.from_numpy(offs_np).to(dev)
+    ot = mx_outputs(Mt, Kt, 32)
+    run_config(f"moe_dispatch {Mt}x{Kt} (K % 512 != 0)",
+               f"N(0,1) x row lognormal(0,1), 32 Zipf(1.1) experts; the transposed conversion "
+               f"launches {fq.fp4_to_fp8_cols_launch_count(Kt)} kernels", [
+                   ("mxfp4_quantize_rows", lambda: fq.mxfp4_quantize_rows(xt, ot["q"], ot["s"]),
+                    b_mxfp4(Mt, Kt)),
+                   ("fp4_to_fp8_cols", lambda: fq.fp4_to_fp8_cols(ot["q"], ot["s"], offt, 0,
+                                                                  ot["yT"], ot["yTs"]),
+                    b_cols(Mt, Kt, nb_cols, 32))])
+    del xt, offt, ot
+    torch.cuda.empty_cache()
+    # the bar: every call on a tensor of at least 4x L2 at >= 75 % alone
+    big = [(n, lab, c["alone_frac"]) for n, cf in configs.items() for lab, c in cf["calls"].items()
+           if c["bytes"] >= 4 * l2_bytes]
+    worst = min(big, key=lambda t: t[2]) if big else None
+    configs_summary = {"l2_bytes": l2_bytes, "reps": cfg_reps,
+                       "calls_at_least_4x_l2": len(big),
+                       "min_alone_frac_at_least_4x_l2": (
+                           {"config": worst[0], "call": worst[1], "frac": worst[2]}
+                           if worst else None)}
+
+    # ---------------------------------------------------------------- end to end
+    # through host buffers: every step copies its input (and the group
+    # offsets) from pinned host memory, runs all casts and copies every
+    # output back to pinned host memory.  Three streams pipeline the steps
+    # (H2D of step i+1 and D2H of step i-1 overlap the casts of step i);
     # device inputs and outputs are double buffered, ordered by events.
     e2e_steps = max(3, min(args.steps, 30))
     xh = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -566,10 +894,18 @@ def run_gpu(args):
         dist.barrier()
     e2e_ms = max_over_ranks(e2e_run(e2e_steps), dev) / e2e_steps
     e2e_value = ws * step_bytes / (e2e_ms * 1e-3) / 1e9
+    link = link_rates(dev)
+    # the link's bound on a step: its copies take at least the longer of each
+    # direction alone, and of both directions' bytes at the two-way rate
+    t_link = max(h2d / (link["h2d"] * 1e9), d2h / (link["d2h"] * 1e9),
+                 (h2d + d2h) / (link["both_directions_total"] * 1e9))
+    e2e_bound = ws * step_bytes / t_link / 1e9
+    del xds, outs, outs_h
 
-    cpu = None
+    cpu, errs = None, None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline()
+        errs = oracle_error_stats(host)
 
     if rank == 0:
         line = {
@@ -579,45 +915,34 @@ def run_gpu(args):
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "M": M, "K": K, "experts": G,
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                       "l2": "flushed between steps (256 MB write + read, outside the timed events)",
-                       "step_bytes": step_bytes},
+                       "l2": "flushed before every pass (256 MB write + read, outside the "
+                             "timed events)",
+                       "step_bytes": step_bytes,
+                       "reps_per_step": reps,
+                       "timing": f"each of the {args.steps} steps is one pass of the six casts "
+                                 f"repeated {reps} times; ms_per_step is per pass"},
             "frac_of_hbm_peak": round(value / ws / peak, 4),
             "kernels": kernels,
-            "kernels_pass": {"steps": split_steps, "ms_per_step": round(split_ms_per_step, 4),
-                             "events": "one between every two kernels (the timed steps have "
-                                       "events at their ends only)"},
             "roofline": roofline,
             "next_rows": next_rows,
+            "configs": configs,
+            "configs_summary": configs_summary,
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
-                    "pipelining": "H2D / casts / D2H on three streams, double-buffered"},
-            "gpu_launches": launches_per_step * args.steps,
+                    "pipelining": "H2D / casts / D2H on three streams, double-buffered",
+                    "link_gbs": link, "link_bound": round(e2e_bound, 1),
+                    "frac_of_link_bound": round(e2e_value / e2e_bound, 4)},
+            "gpu_launches": launches_per_pass * npass,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "error_stats": errs,
             "wall_s_timed_region": round(t1 - t0, 4),
+            "wall_s_total": round(time.time() - wall0, 1),
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
     return 0
-
-
-# Launch order of --profile-configs (our kernels only), for reading an ncu
-# capture of it: (configuration, call) per launch.
-PROFILE_SWEEP = [1024 << i for i in range(9)]
-PROFILE_ORDER = (
-    [("cfg1 pr1 256x512", c) for c in ("mxfp4_quantize_rows", "fp4_to_fp8_rows k=0",
-                                        "fp4_to_fp8_rows k=6")] +
-    [("cfg2 moe_dispatch 16384x7168", c) for c in (
-        "mxfp4_quantize_rows", "fp4_to_fp8_rows", "fp4_to_fp8_cols (32 Zipf groups)",
-        "nvfp4_amax", "nvfp4_quantize SR", "nvfp4_quantize_2d")] +
-    [("cfg3 ragged_experts 65536x2048", c) for c in (
-        "mxfp4_quantize_rows", "fp4_to_fp8_cols (32 Zipf groups)")] +
-    [("cfg4 nvfp4 activations 16384x14336", c) for c in (
-        "nvfp4_amax", "nvfp4_quantize SR", "nvfp4_quantize RNE")] +
-    [("cfg4 nvfp4 weights 14336x4096", c) for c in ("nvfp4_amax", "nvfp4_quantize_2d")] +
-    [(f"cfg5 sweep {m}x7168", c) for m in PROFILE_SWEEP
-     for c in ("mxfp4_quantize_rows", "fp4_to_fp8_rows", "fp4_to_fp8_cols (1 group)")])
 
 
 def run_sweep_rows(m):
@@ -629,11 +954,10 @@ def run_sweep_rows(m):
     import fp8_quantization_gb300 as fq
     from fp8_quantization_gb300 import workloads
     dev = torch.device("cuda", 0)
-    flush_buf = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+    T = Timer(dev, 0)
 
     def run(fn):
-        flush_buf.fill_(1)
-        flush_buf.sum(dtype=torch.int64)
+        T.flush()
         return fn()
 
     bits = workloads.sweep(m, 7168, seed=0)
@@ -649,89 +973,17 @@ def run_sweep_rows(m):
     return 0
 
 
-def run_profile_configs():
-    """Every configuration's chain, one launch per call in PROFILE_ORDER, L2
-    cleaned before each: the launches an ncu pass over the configurations
-    captures.  Nothing is timed here; outputs are not checked (the tests do)."""
-    import torch
-    import numpy as np
-    import fp8_quantization_gb300 as fq
-    from fp8_quantization_gb300 import workloads
-    dev = torch.device("cuda", 0)
-    flush_buf = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
-
-    def flush():
-        flush_buf.fill_(1)
-        flush_buf.sum(dtype=torch.int64)
-
-    def run(fn):
-        flush()
-        return fn()
-
-    def dev_bf16(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
-
-    def offs_dev(o):
-        return torch.from_numpy(np.asarray(o, dtype=np.int64)).to(dev)
-
-    x = dev_bf16(workloads.pr1(256, 512, seed=0))
-    q, s = run(lambda: fq.mxfp4_quantize_rows(x))
-    run(lambda: fq.fp4_to_fp8_rows(q, s, 0))
-    run(lambda: fq.fp4_to_fp8_rows(q, s, 6))
-
-    x = dev_bf16(workloads.moe_dispatch(16384, 7168, seed=0))
-    o = offs_dev(workloads.zipf_group_offsets(16384, 32, 1.1, 0))
-    q, s = run(lambda: fq.mxfp4_quantize_rows(x))
-    run(lambda: fq.fp4_to_fp8_rows(q, s, 0))
-    run(lambda: fq.fp4_to_fp8_cols(q, s, o, 0))
-    amax = run(lambda: fq.nvfp4_amax(x))
-    run(lambda: fq.nvfp4_quantize(x, amax, use_sr=True, seed=1234))
-    run(lambda: fq.nvfp4_quantize_2d(x, amax))
-
-    bits, offs = workloads.ragged_experts(65536, 2048, 32, seed=0)
-    x = dev_bf16(bits)
-    q, s = run(lambda: fq.mxfp4_quantize_rows(x))
-    run(lambda: fq.fp4_to_fp8_cols(q, s, offs_dev(offs), 0))
-
-    x = dev_bf16(workloads.nvfp4_act(16384, 14336, seed=0))
-    amax = run(lambda: fq.nvfp4_amax(x))
-    run(lambda: fq.nvfp4_quantize(x, amax, use_sr=True, seed=1234))
-    run(lambda: fq.nvfp4_quantize(x, amax))
-    w = dev_bf16(workloads.nvfp4_weight(14336, 4096, seed=0))
-    wamax = run(lambda: fq.nvfp4_amax(w))
-    run(lambda: fq.nvfp4_quantize_2d(w, wamax))
-
-    del x, q, s, w
-    big = workloads.sweep(PROFILE_SWEEP[-1], 7168, seed=0)
-    xb = dev_bf16(big)
-    del big
-    for m in PROFILE_SWEEP:
-        xm = xb[:m]
-        q, s = run(lambda: fq.mxfp4_quantize_rows(xm))
-        run(lambda: fq.fp4_to_fp8_rows(q, s, 0))
-        run(lambda: fq.fp4_to_fp8_cols(q, s, offs_dev([0, m]), 0))
-        del q, s
-        torch.cuda.empty_cache()
-    torch.cuda.synchronize()
-    print(json.dumps({"profile_configs": len(PROFILE_ORDER)}), flush=True)
-    return 0
-
-
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["fq", "reference"], default="fq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-configs", action="store_true",
-                    help="run every configuration's calls once (for an ncu capture) and exit")
     ap.add_argument("--sweep-rows", type=int, default=0,
                     help="run the bandwidth-sweep chain at this many rows once (for an ncu "
                          "capture of one size) and exit")
     args = ap.parse_args()
-    if args.profile_configs:
-        return run_profile_configs()
     if args.sweep_rows:
         return run_sweep_rows(args.sweep_rows)
     if args.warmup < 3:

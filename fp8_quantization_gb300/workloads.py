@@ -16,9 +16,11 @@ and shape of the workload it stands in for:
 * ``sweep``          Student-t(nu=3) rows x 7168 for the bandwidth sweep.
 
 All arrays are returned as BF16 bit patterns (``numpy.uint16``), row-major.
-BF16 rounding is round-to-nearest-even, done by ``torch`` on the host.  The
-Student-t generators draw blocks of rows from child seeds of one seed, in
-parallel threads, so that the largest sweep tensors take seconds.
+BF16 rounding is round-to-nearest-even, done by ``torch`` on the host.  Every
+generator but ``pr1`` draws blocks of rows (about 4M elements each) from
+child seeds of one seed, in parallel threads, so that the largest tensors
+take seconds; a block's values do not depend on the row count, so a smaller
+tensor is a prefix of a larger one drawn with the same seed.
 """
 from __future__ import annotations
 
@@ -49,10 +51,11 @@ def pr1(M: int = 256, K: int = 512, seed: int = 0) -> np.ndarray:
 
 
 def moe_dispatch(M: int = 16384, K: int = 7168, seed: int = 0) -> np.ndarray:
-    rng = np.random.default_rng(seed)
-    x = rng.standard_normal((M, K), dtype=np.float32)
-    x *= rng.lognormal(0.0, 1.0, (M, 1)).astype(np.float32)
-    return bf16_bits(x)
+    def draw(rng, shape):
+        x = rng.standard_normal(shape, dtype=np.float32)
+        x *= rng.lognormal(0.0, 1.0, (shape[0], 1)).astype(np.float32)
+        return x
+    return _bf16_row_blocks(M, K, seed, draw)
 
 
 def zipf_group_offsets(M: int, G: int = 32, s: float = 1.1, seed: int = 0) -> np.ndarray:
@@ -67,9 +70,8 @@ def zipf_group_offsets(M: int, G: int = 32, s: float = 1.1, seed: int = 0) -> np
 
 
 def ragged_experts(M: int = 65536, K: int = 2048, G: int = 32, seed: int = 0):
-    rng = np.random.default_rng(seed)
-    x = rng.standard_normal((M, K), dtype=np.float32)
-    return bf16_bits(x), zipf_group_offsets(M, G, 1.1, seed)
+    x = _bf16_row_blocks(M, K, seed, lambda rng, shape: rng.standard_normal(shape, dtype=np.float32))
+    return x, zipf_group_offsets(M, G, 1.1, seed)
 
 
 def _bf16_row_blocks(M: int, K: int, seed: int, draw) -> np.ndarray:
@@ -97,8 +99,7 @@ def nvfp4_act(M: int = 16384, K: int = 14336, seed: int = 0) -> np.ndarray:
 
 
 def nvfp4_weight(N: int = 14336, K: int = 4096, seed: int = 0) -> np.ndarray:
-    rng = np.random.default_rng(seed)
-    return bf16_bits(rng.normal(0.0, 0.02, (N, K)).astype(np.float32))
+    return _bf16_row_blocks(N, K, seed, lambda rng, shape: rng.normal(0.0, 0.02, shape))
 
 
 def sweep(M: int, K: int = 7168, seed: int = 0) -> np.ndarray:

@@ -54,9 +54,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 }
 }  // namespace
 
-bool encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
-                             uint64_t row_pitch, uint32_t box_inner, uint32_t box_rows,
-                             bool promote_l2)
+bool encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
+                          uint64_t inner, uint64_t rows, uint64_t row_pitch, uint32_t box_inner,
+                          uint32_t box_rows, CUtensorMapSwizzle swizzle, bool promote_l2)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc)
@@ -65,10 +65,18 @@ bool encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner,
     const cuuint64_t strides[1] = {row_pitch};
     const cuuint32_t box[2] = {box_inner, box_rows};
     const cuuint32_t elem_strides[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
-               elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+    return enc(map, dtype, 2, const_cast<void *>(base), dims, strides, box, elem_strides,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                promote_l2 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                             uint64_t row_pitch, uint32_t box_inner, uint32_t box_rows,
+                             bool promote_l2)
+{
+    return encode_tensor_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, inner, rows, row_pitch,
+                                box_inner, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE, promote_l2);
 }
 
 }  // namespace fq

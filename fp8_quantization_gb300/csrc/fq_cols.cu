@@ -24,177 +24,12 @@
 //     converted through a shared-memory tile (double buffered, one barrier
 //     per tile) and transposed with byte permutes; the next tile's inputs
 //     are prefetched into registers while the current one is converted.
-#include "fq_common.cuh"
+#include "fq_cols_common.cuh"
 
 namespace fq {
 
-constexpr int kTok = 128;  // tokens per block / per tile
-// FP8 tile: 32 token-quads x 32 feature-words; the 16-byte slot holding
-// (four tokens) x (one feature word) is slot_index(quad, m).  Within a quad
-// the slots of an 8-word octet are consecutive (+2 between octets); the quad
-// stride 39 = -1 (mod 8) plus quad/4 makes the slot's bank group
-// (slot mod 8) = m + 2*(m/8) - quad + quad/4 (mod 8), which is
-// conflict-free both for the conversion stores (2 quads x 4 column blocks x
-// 4 tokens per warp) and for the 128-bit transposed reads (8 quads 4 apart
-// per quarter warp: -3c distinct for c = 0..7).
-constexpr int kQuadStride = 39;
-constexpr int kTileSlots = (kTok / 4 - 1) * kQuadStride + (kTok / 4 - 1) / 4 + 38;  // 1254
+constexpr int kTileSlots = tile_slots(kTok / 4);  // 1254
 constexpr int kTileWords = kTileSlots * 4;
-
-__device__ __forceinline__ int slot_index(int quad, int m)
-{
-    return quad * kQuadStride + (quad >> 2) + m + 2 * (m >> 3);
-}
-
-// Largest g in [lo, hi] with a[g] <= t (a non-decreasing, a[lo] <= t).
-__device__ __forceinline__ int find_last_le(const int32_t *a, int lo, int hi, int32_t t)
-{
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (a[mid] <= t)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    return lo;
-}
-
-// Same search for a warp-uniform t: with n <= 64 one or two ballots over the
-// array replace the binary search.
-__device__ __forceinline__ int warp_find_last_le(const int32_t *a, int n, int32_t t)
-{
-    if (n > 64)
-        return find_last_le(a, 0, n - 1, t);
-    const int lane = threadIdx.x & 31;
-    int g = 0;
-    for (int b0 = 0; b0 < n; b0 += 32) {
-        const int i = b0 + lane;
-        const unsigned m = __ballot_sync(0xffffffffu, i < n && a[i] <= t);
-        if (m)
-            g = b0 + 31 - __clz(m);
-        if (m != 0xffffffffu)
-            break;
-    }
-    return g;
-}
-
-// In-place inclusive scan (max or sum) of a[0..n) in shared memory by the
-// whole CTA.
-template <bool kMax>
-__device__ void cta_scan(int32_t *a, int n, int32_t *warp_tot /* [kThreads/32] */)
-{
-    const int per = (n + kThreads - 1) / kThreads;
-    const int lo = threadIdx.x * per, hi = min(lo + per, n);
-    int32_t run = kMax ? INT32_MIN : 0;
-    for (int i = lo; i < hi; i++) {
-        run = kMax ? max(run, a[i]) : run + a[i];
-        a[i] = run;
-    }
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    int32_t incl = run;
-    for (int d = 1; d < 32; d <<= 1) {
-        int32_t o = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= d)
-            incl = kMax ? max(incl, o) : incl + o;
-    }
-    if (lane == 31)
-        warp_tot[wid] = incl;
-    __syncthreads();
-    int32_t before = kMax ? INT32_MIN : 0;
-    for (int w = 0; w < wid; w++)
-        before = kMax ? max(before, warp_tot[w]) : before + warp_tot[w];
-    int32_t excl = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane > 0)
-        before = kMax ? max(before, excl) : before + excl;
-    for (int i = lo; i < hi; i++)
-        a[i] = kMax ? max(before, a[i]) : before + a[i];
-    __syncthreads();
-}
-
-// Group structure of the offsets, in shared memory (once per CTA): off[0..G]
-// clamped into [0, M], non-decreasing, off[0] = 0, off[G] = M; base[g] = the
-// first scale slot of group g (number of 128-token blocks of the groups
-// before it), base[G] = total blocks.  Returns nonzero if the offsets given
-// were malformed.
-__device__ int load_groups(const int64_t *__restrict__ offs, int32_t G, int32_t M, int32_t *off,
-                           int32_t *base, int32_t *warp_tot)
-{
-    const int tid = threadIdx.x;
-    if (G < 32) {
-        // one warp: clamp, max-scan and sum-scan with shuffles (G + 1 <= 32)
-        int bad = 0;
-        if (tid < 32) {
-            const int lane = tid;
-            int64_t o = lane <= G ? offs[lane] : M;
-            const int64_t prev = lane >= 1 && lane <= G ? offs[lane - 1] : 0;
-            const int64_t c = o < 0 ? 0 : (o > M ? M : o);
-            bad = lane <= G && (c != o || (lane == 0 && o != 0) || (lane == G && o != M) ||
-                                (lane > 0 && o < prev));
-            int32_t v = static_cast<int32_t>(c);
-            for (int d = 1; d < 32; d <<= 1) {
-                const int32_t u = __shfl_up_sync(0xffffffffu, v, d);
-                if (lane >= d)
-                    v = max(v, u);
-            }
-            if (lane == 0)
-                v = 0;
-            if (lane == G)
-                v = M;
-            const int32_t below = __shfl_up_sync(0xffffffffu, v, 1);
-            int32_t nb = lane >= 1 && lane <= G ? (v - below + kTok - 1) / kTok : 0;
-            for (int d = 1; d < 32; d <<= 1) {
-                const int32_t u = __shfl_up_sync(0xffffffffu, nb, d);
-                if (lane >= d)
-                    nb += u;
-            }
-            if (lane <= G) {
-                off[lane] = v;
-                base[lane] = nb;
-            }
-            bad = __any_sync(0xffffffffu, bad);
-        }
-        return __syncthreads_or(bad);
-    }
-    int bad = 0;
-    for (int i = tid; i <= G; i += kThreads) {
-        const int64_t o = offs[i];
-        const int64_t c = o < 0 ? 0 : (o > M ? M : o);
-        off[i] = static_cast<int32_t>(c);
-        if (c != o || (i == 0 && o != 0) || (i == G && o != M) || (i > 0 && o < offs[i - 1]))
-            bad = 1;
-    }
-    bad = __syncthreads_or(bad);
-    cta_scan<true>(off, G + 1, warp_tot);
-    if (tid == 0) {
-        off[0] = 0;
-        off[G] = M;
-    }
-    __syncthreads();
-    for (int g = tid; g <= G; g += kThreads)
-        base[g] = g == 0 ? 0 : (off[g] - off[g - 1] + kTok - 1) / kTok;
-    __syncthreads();
-    cta_scan<false>(base, G + 1, warp_tot);
-    return bad;
-}
-
-// 4x4 byte transpose: in = four words (rows), out[r] = byte r of each word.
-__device__ __forceinline__ void transpose4x4(uint4 v, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                             uint32_t &r3)
-{
-    const uint32_t ab_lo = prmt(v.x, v.y, 0x5140u), ab_hi = prmt(v.x, v.y, 0x7362u);
-    const uint32_t cd_lo = prmt(v.z, v.w, 0x5140u), cd_hi = prmt(v.z, v.w, 0x7362u);
-    r0 = prmt(ab_lo, cd_lo, 0x5410u);
-    r1 = prmt(ab_lo, cd_lo, 0x7632u);
-    r2 = prmt(ab_hi, cd_hi, 0x5410u);
-    r3 = prmt(ab_hi, cd_hi, 0x7632u);
-}
-
-__device__ __forceinline__ uint32_t bytemax4(uint32_t a, uint32_t b)
-{
-    const uint32_t e02 = max_u16x2(a & 0x00FF00FFu, b & 0x00FF00FFu);
-    const uint32_t e13 = max_u16x2((a >> 8) & 0x00FF00FFu, (b >> 8) & 0x00FF00FFu);
-    return e02 | (e13 << 8);
-}
 
 // ---------------------------------------------------------------- launch 1: block scales
 
@@ -265,38 +100,6 @@ __global__ void __launch_bounds__(kThreads) fp4_to_fp8_cols_scales_kernel(
                 fp8_block_scale_bits((smax[c] >> (8 * (rr >> 5))) & 0xFFu, k);
         __syncthreads();
     }
-}
-
-// ---------------------------------------------------------------- shared by both paths
-
-// The shift-table rows of four MX columns at once: byte i of the result is
-// min(S_i - e_i - k + 6, kShiftRows - 1), or kNanRow where S_i = 0xFF (S is
-// the block max, so S_i >= e_i and the byte-wise subtraction never borrows).
-__device__ __forceinline__ uint32_t shift_rows4(uint32_t S, uint32_t e, int k)
-{
-    const uint32_t ones = 0x01010101u;
-    const uint32_t d = S - e;
-    uint32_t u = __vminu4(d, static_cast<uint32_t>(kShiftRows - 1 - 6 + k) * ones) +
-                 static_cast<uint32_t>(6 - k) * ones;
-    const uint32_t nan = __vcmpeq4(S, 0xFFFFFFFFu);  // 0xFF in bytes where S = 0xFF
-    return (u & ~nan) | (static_cast<uint32_t>(kNanRow) * ones & nan);
-}
-
-// One unit from its shift-table row u (as convert_unit with u precomputed).
-__device__ __forceinline__ void convert_unit_row(uint32_t *tile, const uint8_t *tab, int tl, int j,
-                                                 uint4 qv, uint32_t u)
-{
-    const uint2 t = *reinterpret_cast<const uint2 *>(tab + 8 * u);
-    const uint32_t smask = u == static_cast<uint32_t>(kNanRow) ? 0u : 0x80808080u;
-    uint32_t o[8];
-    fp4x8_to_fp8x8(qv.x, t.x, t.y, o[0], o[1], smask);
-    fp4x8_to_fp8x8(qv.y, t.x, t.y, o[2], o[3], smask);
-    fp4x8_to_fp8x8(qv.z, t.x, t.y, o[4], o[5], smask);
-    fp4x8_to_fp8x8(qv.w, t.x, t.y, o[6], o[7], smask);
-    uint32_t *dst = tile + 4 * slot_index(tl >> 2, 8 * j) + (tl & 3);
-#pragma unroll
-    for (int w = 0; w < 8; w++)
-        dst[4 * w] = o[w];
 }
 
 // One unit: the 32 codes of token tl in MX column j (16 bytes) -> 32 E4M3
@@ -611,17 +414,44 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
         }
         mbar_init_fence();
     }
-    build_fp8_table(tab);
-    griddep_wait();  // offsets, codes and exponents may come from the previous kernel
-    const int bad = load_groups(offs, G, M, off, base, warp_tot);  // ends with a CTA barrier
-    if (bad && blockIdx.x == 0 && tid == 0 && dev_status)
-        atomicOr(dev_status, 1);
-
     auto super_xy = [&](int32_t m, int32_t &W, int32_t &F) {
         const int32_t sg = static_cast<int32_t>(blockIdx.x) + m * grid;
         W = (wfast ? sg % nwin : sg / nquad) * kTok;
         F = wfast ? sg / nwin : sg % nquad;
     };
+    auto issue_exps = [&](int32_t m) {  // one thread: super-tile m of this CTA
+        int32_t W, F;
+        super_xy(m, W, F);
+        const int be = m % kExps;
+        uint8_t *dst = exp_ring + be * kExpBytes;
+        mbar_arrive_expect_tx(&full_e[be], kExpBytes);
+#pragma unroll
+        for (int h = 0; h < 3; h++)
+            tma_load_2d(dst + h * kTok * kExpRowBytes, &tm_s, 16 * F, W + (h - 1) * kTok,
+                        &full_e[be]);
+    };
+    auto issue_codes = [&](int32_t n) {  // one thread: tile n of this CTA
+        int32_t W, F;
+        super_xy(n >> 2, W, F);
+        const int st = n % kStages;
+        mbar_arrive_expect_tx(&full_c[st], kCodeBytes);
+        tma_load_2d(codes_ring + st * kCodeBytes, &tm_q, 64 * (4 * F + (n & 3)), W, &full_c[st]);
+    };
+
+    build_fp8_table(tab);
+    __syncthreads();  // the barriers are initialised before the first copy
+    griddep_wait();   // offsets, codes and exponents may come from the previous kernel
+    // the first copies need only the window, not the groups: issue them now
+    // so that they overlap the group set-up
+    if (tid == kThreads) {
+        issue_exps(0);
+        for (int32_t n = 0; n < kStages - 1 && n < my_tiles; n++)
+            issue_codes(n);
+    }
+    const int bad = load_groups(offs, G, M, off, base, warp_tot);  // ends with a CTA barrier
+    if (bad && blockIdx.x == 0 && tid == 0 && dev_status)
+        atomicOr(dev_status, 1);
+
     // block maxima of super-tile m: warp w0 takes the blocks w0, w0 + wstep, ...
     // of those meeting the window; each writes the shift-table rows of the
     // block's tokens in the window and, if the block starts in the window, the
@@ -683,30 +513,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
             }
         }
     };
-    auto issue_exps = [&](int32_t m) {  // one thread: super-tile m of this CTA
-        int32_t W, F;
-        super_xy(m, W, F);
-        const int be = m % kExps;
-        uint8_t *dst = exp_ring + be * kExpBytes;
-        mbar_arrive_expect_tx(&full_e[be], kExpBytes);
-#pragma unroll
-        for (int h = 0; h < 3; h++)
-            tma_load_2d(dst + h * kTok * kExpRowBytes, &tm_s, 16 * F, W + (h - 1) * kTok,
-                        &full_e[be]);
-    };
-    auto issue_codes = [&](int32_t n) {  // one thread: tile n of this CTA
-        int32_t W, F;
-        super_xy(n >> 2, W, F);
-        const int st = n % kStages;
-        mbar_arrive_expect_tx(&full_c[st], kCodeBytes);
-        tma_load_2d(codes_ring + st * kCodeBytes, &tm_q, 64 * (4 * F + (n & 3)), W, &full_c[st]);
-    };
-
-    // ---- super-tile 0: copies, then its maxima with every warp
-    if (tid == kThreads) {  // a light first burst: the first tile's data only
-        issue_exps(0);
-        issue_codes(0);
-    }
+    // ---- super-tile 0: its maxima with every warp
     const bool ok0 = !__syncthreads_or(!mbar_wait(&full_e[0], 0));
     if (ok0)
         maxima(0, wid, kThreads1p / 32);
@@ -714,12 +521,8 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     // with one exponent buffer the copy of super-tile 1 follows the first
     // maxima (with two it is issued in the loop below)
     const int32_t pre_e = kExps == 1 && ok0 && my_super > 1 ? 2 : 1;
-    if (tid == kThreads) {
-        for (int32_t n = 1; n < kStages - 1 && n < my_tiles; n++)
-            issue_codes(n);
-        if (pre_e == 2)
-            issue_exps(1);
-    }
+    if (tid == kThreads && pre_e == 2)
+        issue_exps(1);
 
     if (wid == kConvWarps) {
         // ================================================= producer warp

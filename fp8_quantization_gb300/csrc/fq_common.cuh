@@ -346,6 +346,11 @@ fq_status launch_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t M, 
 bool encode_tensor_map_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
                              uint64_t row_pitch, uint32_t box_inner, uint32_t box_rows,
                              bool promote_l2 = true);
+// The same for any element type and shared-memory swizzle (inner, box_inner
+// in elements; row_pitch in bytes).
+bool encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
+                          uint64_t inner, uint64_t rows, uint64_t row_pitch, uint32_t box_inner,
+                          uint32_t box_rows, CUtensorMapSwizzle swizzle, bool promote_l2);
 
 // Philox4x32-10 (Salmon et al., SC'11).
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1)

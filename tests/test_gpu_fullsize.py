@@ -331,7 +331,6 @@ def test_more_than_2_31_elements(fq):
     ry, rys = oracle.fp4_to_fp8_rows(rq, rs, 3)
     eq(rows_of(y), ry, "fp8 rows y")
     eq(rows_of(ys), rys, "fp8 rows ys")
-    del y, ys
     # transposed, one group: the 128-token windows ending at and after 2^31
     offs = np.array([0, M], dtype=np.int64)
     yT, yTs = cols_full(fq, q, s, offs, 3)
@@ -343,8 +342,11 @@ def test_more_than_2_31_elements(fq):
         eq(yT[:, t0:t0 + 128].contiguous(), ryT, f"window {wi} yT")
         eq(yTs[wi:wi + 1], ryTs[:1], f"window {wi} yTs")
     fused = fq.bf16_to_mxfp4_fp8(x, torch.from_numpy(offs).cuda(), 3)
-    assert torch.equal(fused[0], q) and torch.equal(fused[1], s) and torch.equal(fused[4], yT)
-    del q, s, yT, yTs, fused
+    for got, want, name in zip(fused, (q, s, y, ys, yT), ("q", "s", "y", "ys", "yT")):
+        assert torch.equal(got, want), f"one-call forward cast {name}"
+    nb = (M + 127) // 128
+    assert torch.equal(fused[5][:nb], yTs[:nb]), "one-call forward cast yT scales"
+    del q, s, y, ys, yT, yTs, fused
     torch.cuda.empty_cache()
 
     # NVFP4: the amax, 1x16 with RNE and SR, 2D with the transposed operand

@@ -282,12 +282,12 @@ def fused_input(M, K, seed):
 
 
 @pytest.mark.parametrize("case", sorted(COLS_CASES))
-@pytest.mark.parametrize("path", ["single_pass", "two_launch"])
-def test_bf16_to_mxfp4_fp8(fq, case, path):
+@pytest.mark.parametrize("kmod", ["k_mult_512", "k_not_mult_512"])
+def test_bf16_to_mxfp4_fp8(fq, case, kmod):
     """The one-call forward cast equals the oracle's MXFP4 -> FP8 rows and
     MXFP4 -> FP8 cols, byte for byte, with canaries on every output."""
     M, K, mk = COLS_CASES[case]
-    K = cols_k(K, path)
+    K = cols_k(K, "single_pass" if kmod == "k_mult_512" else "two_launch")
     offs = np.asarray(mk(M), dtype=np.int64)
     check_fused(fq, M, K, offs, (M + K) % 7, fused_input(M, K, seed=M + 3 * K))
 
@@ -298,6 +298,32 @@ def test_bf16_to_mxfp4_fp8_above_512_windows(fq):
     M, K = 66000, 1024
     offs = np.asarray(workloads.zipf_group_offsets(M, 32, 1.1, 13), dtype=np.int64)
     check_fused(fq, M, K, offs, 2, fused_input(M, K, seed=17))
+
+
+def test_bf16_to_mxfp4_fp8_malformed_offsets(fq):
+    """Malformed group offsets are clamped in the kernel, reported through
+    dev_status, and nothing is written outside the outputs."""
+    M, K = 700, 384
+    bits = fused_input(M, K, seed=23)
+    x = dev_bf16(bits)
+    for offs in ([0, 800], [5, 300, 200, 700], [0, -40, 700], [0, 100, 699], [10, 20, 700]):
+        offs = np.array(offs, dtype=np.int64)
+        G = offs.size - 1
+        cap = oracle.fp4_to_fp8_cols_scale_capacity(M, G)
+        outs = [canary_out(shape, dt) for shape, dt in (
+            ((M, K // 2), torch.uint8), ((M, K // 32), torch.uint8), ((M, K), torch.uint8),
+            ((M, K // 128), torch.float32), ((K, M), torch.uint8), ((cap, K), torch.float32))]
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        fq.bf16_to_mxfp4_fp8(x, torch.from_numpy(offs).cuda(), 0, *[o[1] for o in outs],
+                             dev_status=st)
+        for (raw, view), n in zip(outs, (M * K // 2, M * K // 32, M * K, M * K // 32, K * M,
+                                         cap * K * 4)):
+            check_canary(raw, n)
+        assert int(st.item()) == 1, offs
+        # the row outputs do not depend on the groups
+        rq, rs = oracle.mxfp4_quantize_rows(bits)
+        eq(outs[0][1], rq, "q")
+        eq(outs[1][1], rs, "s")
 
 
 def check_fused(fq, M, K, offs, k, bits):

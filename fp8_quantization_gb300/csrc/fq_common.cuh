@@ -213,16 +213,6 @@ __device__ __forceinline__ void build_fp8_table(uint8_t *tab /* [kTabRows * 8] *
     }
 }
 
-// Inverse of fp8_block_scale_bits: the aligned exponent S from the FP32 block
-// scale 2^(S - 127 - k) (0xFF for the NaN scale).
-__device__ __forceinline__ uint32_t fp8_block_scale_exponent(uint32_t bits, int k)
-{
-    if (bits == 0x7FC00000u)
-        return 0xFFu;
-    const int ex = (bits >> 23) ? static_cast<int>(bits >> 23) : (31 - __clz(bits)) - 22;
-    return static_cast<uint32_t>(ex + k);
-}
-
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialization may start while the previous kernel on the stream is still
 // running; it must read nothing that kernel writes, and write nothing,
@@ -312,6 +302,23 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
+}
+
+// Asynchronous 4-byte copy global -> shared (cp.async); with `src_bytes` 0
+// nothing is read and the 4 bytes are zero-filled.
+__device__ __forceinline__ void cp_async_4(void *dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
+                 : "memory");
+}
+
+// One arrival on `bar` once every cp.async this thread issued so far has
+// landed (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
 }
 
 // Barrier `id` over the first `count` threads of the CTA (a multiple of 32)

@@ -119,12 +119,12 @@ int64_t fp4_to_fp8_cols_scale_capacity(int64_t M, int32_t G);
 /* Largest group count accepted by fp4_to_fp8_cols. */
 #define FQ_COLS_MAX_GROUPS 1024
 
-/* Number of kernels fp4_to_fp8_cols enqueues for feature count K: 1 (a
- * single pass that also computes the block scales) when K % 512 == 0 and the
- * CUDA driver can encode tensor maps, else 2 (a block-scale pass, then the
- * conversion); 0 for a K the conversion rejects.  Host only: no kernel is
- * launched (for K % 512 == 0 it initialises the CUDA runtime on the current
- * device, as the conversion itself would). */
+/* Number of kernels fp4_to_fp8_cols enqueues for feature count K: 1 (one
+ * pass that also computes the block scales) when the CUDA driver can encode
+ * tensor maps; 0 for a K the conversion rejects, or without that driver
+ * support (the conversion then returns FQ_ERR_CUDA, cudaErrorNotSupported).
+ * Host only: no kernel is launched (for a valid K it initialises the CUDA
+ * runtime on the current device, as the conversion itself would). */
 int fp4_to_fp8_cols_launch_count(int64_t K);
 
 /*
@@ -170,8 +170,8 @@ fq_status fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t M, int64_t
  * and the transposed stage reads q and s back (kept in L2 where they fit).
  *   x : bf16 [M, K];  q, s, y, ys, yT, yT_scale, group_offsets, G, cap :
  *   as in the three calls.  Requires K % 128 == 0, 1 <= G <=
- *   FQ_COLS_MAX_GROUPS, 0 <= M < 2^31, k in [0, 6].  Enqueues
- *   1 + fp4_to_fp8_cols_launch_count(K) kernels.
+ *   FQ_COLS_MAX_GROUPS, 0 <= M < 2^31, k in [0, 6].  Enqueues two
+ *   kernels (the row kernel, then the transposed conversion).
  */
 fq_status bf16_to_mxfp4_fp8(const void *x, int64_t M, int64_t K, const int64_t *group_offsets,
                             int32_t G, int exp_offset_k, uint8_t *q, uint8_t *s, uint8_t *y,

@@ -201,20 +201,22 @@ COLS_CASES["g1_m_mult_16_k1536"] = (640, 1536, lambda M: np.array([0, M]))
 
 
 def cols_k(K, path):
-    """K of a case on one of the two paths: the single pass takes K % 512 == 0
-    (exponent rows a multiple of 16 bytes), the two-launch path the rest."""
-    if path == "single_pass":
+    """K of a case on one of the two exponent-row paths of the single pass:
+    K % 512 == 0 (rows of K/32 bytes are a multiple of 16 bytes: tensor
+    copies) or not (4-byte asynchronous copies, and a short last super-tile
+    of fewer than four 128-feature blocks)."""
+    if path == "k_mult_512":
         return (K + 511) // 512 * 512
     return K if K % 512 else K + 128
 
 
 @pytest.mark.parametrize("case", sorted(COLS_CASES))
 @pytest.mark.parametrize("k", [0, 6])
-@pytest.mark.parametrize("path", ["single_pass", "two_launch"])
+@pytest.mark.parametrize("path", ["k_mult_512", "k_not_mult_512"])
 def test_fp4_to_fp8_cols(fq, case, k, path):
     M, K, mk = COLS_CASES[case]
     K = cols_k(K, path)
-    assert fq.fp4_to_fp8_cols_launch_count(K) == (1 if path == "single_pass" else 2)
+    assert fq.fp4_to_fp8_cols_launch_count(K) == 1
     offs = np.asarray(mk(M), dtype=np.int64)
     q, s = rand_mx(M, K, seed=M * 7 + K + k, spread=16, nan_frac=0.002)
     run_cols(fq, q, s, offs, k)
@@ -234,6 +236,17 @@ def test_fp4_to_fp8_cols_launch_count_in_a_fresh_process(fq):
                          timeout=300)
     assert out.returncode == 0, out.stderr
     assert out.stdout.split() == ["1", "1"]
+
+
+@pytest.mark.parametrize("K", [128, 384, 640, 1920])
+def test_fp4_to_fp8_cols_short_super_tiles(fq, K):
+    """K % 512 != 0: every row's last super-tile has 1, 2 or 3 of its four
+    128-feature blocks (the others are empty slots), on both sides of the
+    walk-order switch (M = 70000: 547 windows), 32 Zipf groups, NaN scales."""
+    for M in (3000, 70000):
+        offs = np.asarray(workloads.zipf_group_offsets(M, 32, 1.1, K), dtype=np.int64)
+        q, s = rand_mx(M, K, seed=M + K, spread=16, nan_frac=0.001)
+        run_cols(fq, q, s, offs, 2)
 
 
 @pytest.mark.parametrize("M", [65536, 66000, 66001])
@@ -287,7 +300,7 @@ def test_bf16_to_mxfp4_fp8(fq, case, kmod):
     """The one-call forward cast equals the oracle's MXFP4 -> FP8 rows and
     MXFP4 -> FP8 cols, byte for byte, with canaries on every output."""
     M, K, mk = COLS_CASES[case]
-    K = cols_k(K, "single_pass" if kmod == "k_mult_512" else "two_launch")
+    K = cols_k(K, kmod)
     offs = np.asarray(mk(M), dtype=np.int64)
     check_fused(fq, M, K, offs, (M + K) % 7, fused_input(M, K, seed=M + 3 * K))
 

@@ -141,9 +141,12 @@ def hbm_peak():
 
 
 def file_sha(name: str) -> str:
-    """sha256[:16] of a kernel's source file followed by the shared header."""
+    """sha256[:16] of a kernel's source file followed by the headers it uses."""
     h = hashlib.sha256()
-    for part in (name, "fq_common.cuh"):
+    parts = [name, "fq_common.cuh"]
+    if name in ("fq_cols.cu", "fq_fused.cu"):
+        parts.append("fq_cols_common.cuh")
+    for part in parts:
         with open(os.path.join(ROOT, "fp8_quantization_gb300", "csrc", part), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

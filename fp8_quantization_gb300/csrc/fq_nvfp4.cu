@@ -107,6 +107,17 @@ __device__ __forceinline__ void addsub2(float &a0, float &a1, float &b0, float &
         : "+f"(a0), "+f"(a1), "+f"(b0), "+f"(b1));
 }
 
+// Butterfly stages h = 2, 4, 8 on pairs (j, j + 1), after stage h = 1.
+__device__ __forceinline__ void rht16_stages248(float z[16])
+{
+#pragma unroll
+    for (int h = 2; h < 16; h <<= 1)
+#pragma unroll
+        for (int j = 0; j < 16; j += 2)
+            if (!(j & h))
+                addsub2(z[j], z[j + 1], z[j + h], z[j + h + 1]);
+}
+
 // The butterflies, without the final factor 0.25 (z = H16 diag(d) x).
 __device__ __forceinline__ void rht16_z(const uint4 &a, const uint4 &b, const RhtFlip &f, float z[16])
 {
@@ -119,13 +130,41 @@ __device__ __forceinline__ void rht16_z(const uint4 &a, const uint4 &b, const Rh
         z[2 * i] = __fadd_rn(u, v);
         z[2 * i + 1] = __fsub_rn(u, v);
     }
-    // stages h = 2, 4, 8 on pairs (j, j + 1)
+    rht16_stages248(z);
+}
+
+// The same transform with the sign flips as bit 31 of one word per element,
+// folded into the BF16 -> binary32 conversions ((w << 16) + 2^31 flips bit
+// 31 as an exclusive or would).  The amax kernel takes these words as a
+// kernel argument, so they are read from the constant bank instead of being
+// held in registers (41.4 -> 40.4 us on 16384 x 7168; the quantizer with the
+// same change went from 48 to 68 registers and became slower).
+struct RhtFlipBits {
+    uint32_t lo[8], hi[8];  // element 2i / 2i+1 flips where bit 31 is set
+};
+
+inline RhtFlipBits rht_flip_bits(uint32_t sign_mask)
+{
+    RhtFlipBits f;
+    for (int i = 0; i < 8; i++) {
+        f.lo[i] = ((sign_mask >> (2 * i)) & 1u) << 31;
+        f.hi[i] = ((sign_mask >> (2 * i + 1)) & 1u) << 31;
+    }
+    return f;
+}
+
+__device__ __forceinline__ void rht16_z(const uint4 &a, const uint4 &b, const RhtFlipBits &f,
+                                        float z[16])
+{
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int h = 2; h < 16; h <<= 1)
-#pragma unroll
-        for (int j = 0; j < 16; j += 2)
-            if (!(j & h))
-                addsub2(z[j], z[j + 1], z[j + h], z[j + h + 1]);
+    for (int i = 0; i < 8; i++) {
+        const float u = __uint_as_float((w[i] << 16) + f.lo[i]);
+        const float v = __uint_as_float((w[i] & 0xFFFF0000u) ^ f.hi[i]);
+        z[2 * i] = __fadd_rn(u, v);
+        z[2 * i + 1] = __fsub_rn(u, v);
+    }
+    rht16_stages248(z);
 }
 
 __device__ __forceinline__ void rht16(const uint4 &a, const uint4 &b, const RhtFlip &f, float y[16])
@@ -139,13 +178,12 @@ __device__ __forceinline__ void rht16(const uint4 &a, const uint4 &b, const RhtF
 // max |y| over the transformed tensor: |y| bits ordered as unsigned integers
 // (NaN above infinity above every finite value), one atomicMax per CTA.
 __global__ void __launch_bounds__(kThreads) nvfp4_amax_rht_kernel(const uint16_t *__restrict__ x,
-                                                                  int64_t nblk, uint32_t sign_mask,
+                                                                  int64_t nblk, const RhtFlipBits f,
                                                                   uint32_t *__restrict__ out_bits)
 {
     __shared__ uint32_t red[kThreads / 32];
     griddep_wait();  // the previous kernel's outputs (PDL launch)
     griddep_launch_dependents();  // the next kernel may start its set-up
-    const RhtFlip f = rht_flip_words(sign_mask);
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
     uint32_t m = 0;
@@ -832,7 +870,7 @@ extern "C" fq_status nvfp4_amax_rht(const void *x, int64_t n, uint32_t sign_mask
     const int64_t work = (nblk + 2 * kThreads - 1) / (2 * kThreads);
     const int grid = persistent_grid(nvfp4_amax_rht_kernel, kThreads, 0, work);
     launch_pdl(nvfp4_amax_rht_kernel, dim3(grid), dim3(kThreads), 0, st,
-               static_cast<const uint16_t *>(x), nblk, sign_mask & 0xFFFFu,
+               static_cast<const uint16_t *>(x), nblk, rht_flip_bits(sign_mask & 0xFFFFu),
                reinterpret_cast<uint32_t *>(amax));
     return launch_status();
 }

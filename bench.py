@@ -976,6 +976,52 @@ def run_sweep_rows(m):
     return 0
 
 
+def run_ncu_calls(reps: int = 3):
+    """Every entry point of the DRAM-traffic record on the headline tensor
+    (16384 x 7168, 32 Zipf groups), each `reps` times with L2 cleaned before
+    each call, and nothing else: about 2 GB on the device and a few dozen
+    launches, a small case for an ncu capture of DRAM bytes per call."""
+    import torch
+    import numpy as np
+    import fp8_quantization_gb300 as fq
+    from fp8_quantization_gb300 import workloads
+    dev = torch.device("cuda", 0)
+    T = Timer(dev, 0)
+    M, K, G = M_ROWS, K_COLS, EXPERTS
+    bits = workloads.moe_dispatch(M, K, seed=0)
+    offs_np = workloads.zipf_group_offsets(M, G, 1.1, 0)
+    x = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+    del bits
+    offs = torch.from_numpy(offs_np).to(dev)
+    q, s = fq.mxfp4_quantize_rows(x)
+    amax = fq.nvfp4_amax(x)
+    ar = fq.nvfp4_amax_rht(x, 0x9E37)
+    hist = fq.amax_history(64, device=dev)
+    calls = [
+        lambda: fq.mxfp4_quantize_rows(x, q, s),
+        lambda: fq.fp4_to_fp8_rows(q, s, 0),
+        lambda: fq.fp4_to_fp8_cols(q, s, offs, 0),
+        lambda: fq.nvfp4_amax(x, amax),
+        lambda: fq.nvfp4_quantize(x, amax, use_sr=True, seed=1000, offset=0),
+        lambda: fq.nvfp4_quantize_2d(x, amax),
+        lambda: fq.nvfp4_amax_rht(x, 0x9E37, ar),
+        lambda: fq.nvfp4_quantize_rht(x, ar, 0x9E37, True, 4242, 0),
+        lambda: fq.fp8_quantize_1x128(x),
+        lambda: fq.fp8_quantize_128x128(x),
+        lambda: fq.mxfp4_dequantize_rows(q, s),
+        lambda: fq.nvfp4_quantize_2d_t(x, amax),
+        lambda: fq.nvfp4_quantize_delayed(x, hist, 0, True, 99, 0),
+        lambda: fq.bf16_to_mxfp4_fp8(x, offs, 0),
+    ]
+    for fn in calls:
+        for _ in range(reps):
+            T.flush()
+            fn()
+            torch.cuda.synchronize(dev)
+    print(json.dumps({"ncu_calls": len(calls), "reps": reps}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -986,7 +1032,12 @@ def main():
     ap.add_argument("--sweep-rows", type=int, default=0,
                     help="run the bandwidth-sweep chain at this many rows once (for an ncu "
                          "capture of one size) and exit")
+    ap.add_argument("--ncu-calls", action="store_true",
+                    help="run every entry point of the DRAM-traffic record three times on the "
+                         "headline tensor and exit (for an ncu capture of DRAM bytes per call)")
     args = ap.parse_args()
+    if args.ncu_calls:
+        return run_ncu_calls()
     if args.sweep_rows:
         return run_sweep_rows(args.sweep_rows)
     if args.warmup < 3:

@@ -70,6 +70,7 @@ KERNEL_SRC = {
     "nvfp4_quantize_rht": "fq_nvfp4.cu", "fp8_quantize_1x128": "fq_fp8.cu",
     "fp8_quantize_128x128": "fq_fp8.cu", "mxfp4_dequantize_rows": "fq_fp8.cu",
     "nvfp4_quantize_delayed": "fq_nvfp4.cu", "nvfp4_quantize_2d_t": "fq_nvfp4.cu",
+    "mxfp4_scales_mma_layout": "fq_mxfp4.cu",
 }
 FALLBACK_HBM_GBS = 6800.0
 TIMED_REGION_S = 1.5
@@ -679,6 +680,9 @@ def run_gpu(args):
     sbT = torch.empty((K // 16, M // 16), **u8)
     w2t_us = alone(lambda: fq.nvfp4_quantize_2d_t(x, out["amax"], out["q2"], out["sb2"], qT, sbT,
                                                   out["g2"]))
+    mma_n = fq.mxfp4_scales_mma_bytes(M, K)
+    s_mma = torch.empty((mma_n,), **u8)
+    mma_us = alone(lambda: fq.mxfp4_scales_mma_layout(out["s"], s_mma))
     next_rows = {
         "bf16_to_mxfp4_fp8": entry("bf16_to_mxfp4_fp8", fused_us, b_fused(M, K, nb_cols, G),
                                    1 + fq.fp4_to_fp8_cols_launch_count(K),
@@ -700,9 +704,11 @@ def run_gpu(args):
         "nvfp4_quantize_2d_t": entry("nvfp4_quantize_2d_t", w2t_us, b_2d_t(M, K), 1,
                                      without_transpose_alone_us=kernels["nvfp4_quantize_2d"][
                                          "alone"]["us"]),
+        "mxfp4_scales_mma_layout": entry("mxfp4_scales_mma_layout", mma_us, E // 32 + mma_n, 1,
+                                         l2_resident=E // 32 + mma_n <= l2_bytes),
         "reps": extra_reps, "timing": "alone, L2 flushed before every call",
     }
-    del fo, fy, fs1, fs2, deq, qT, sbT
+    del fo, fy, fs1, fs2, deq, qT, sbT, s_mma
 
     # ---------------------------------------------------------------- configs
     cfg_reps = max(3, min(args.steps, 50))
@@ -1012,6 +1018,7 @@ def run_ncu_calls(reps: int = 3):
         lambda: fq.nvfp4_quantize_2d_t(x, amax),
         lambda: fq.nvfp4_quantize_delayed(x, hist, 0, True, 99, 0),
         lambda: fq.bf16_to_mxfp4_fp8(x, offs, 0),
+        lambda: fq.mxfp4_scales_mma_layout(s),
     ]
     for fn in calls:
         for _ in range(reps):

@@ -55,6 +55,8 @@ SIGNATURES = {
                                       _vp, _vp, _vp, _vp]),
     "fp8_quantize_128x128": (_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
     "mxfp4_dequantize_rows": (_int, [_vp, _vp, _i64, _i64, _vp, _vp]),
+    "mxfp4_scales_mma_bytes": (_i64, [_i64, _i64]),
+    "mxfp4_scales_mma_layout": (_int, [_vp, _i64, _i64, _vp, _vp]),
     "nvfp4_quantize_rht": (_int, [_vp, _i64, _i64, _vp, ctypes.c_uint32, _int, _u64, _u64, _vp,
                                   _vp, _vp, _vp]),
 }
@@ -406,6 +408,28 @@ def mxfp4_dequantize_rows(q: torch.Tensor, s: torch.Tensor, out: torch.Tensor | 
     _need(out, torch.bfloat16, "out", numel=M * K)
     _on_device(q=q, s=s, out=out)
     _call("mxfp4_dequantize_rows", _p(q), _p(s), M, K, _p(out), _stream())
+    return out
+
+
+def mxfp4_scales_mma_bytes(M: int, K: int) -> int:
+    """Bytes of the block-scaled-MMA scale layout of an [M, K] MXFP4 tensor
+    (-1 for a rejected shape)."""
+    return int(abi().mxfp4_scales_mma_bytes(int(M), int(K)))
+
+
+def mxfp4_scales_mma_layout(s: torch.Tensor, out: torch.Tensor | None = None):
+    """MXFP4 scales uint8 [M, K/32] -> uint8 [mxfp4_scales_mma_bytes(M, K)]:
+    512-byte atoms of 128 rows x 4 scale columns for a block-scaled MMA
+    operand (layout in include/fq.h)."""
+    _need(s, torch.uint8, "s", 2)
+    M, K = s.shape[0], s.shape[1] * 32
+    n = mxfp4_scales_mma_bytes(M, K)
+    if n < 0:
+        raise ValueError(f"s of shape {tuple(s.shape)}: K = {K} must be a positive multiple of 128")
+    out = torch.empty((n,), dtype=torch.uint8, device=s.device) if out is None else out
+    _need(out, torch.uint8, "out", numel=n)
+    _on_device(s=s, out=out)
+    _call("mxfp4_scales_mma_layout", _p(s), M, K, _p(out), _stream())
     return out
 
 

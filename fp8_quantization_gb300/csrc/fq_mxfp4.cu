@@ -175,6 +175,40 @@ __global__ void __launch_bounds__(kThreads) fp4_to_fp8_rows_kernel(
     }
 }
 
+// ---------------------------------------------------------------- MMA scale layout
+
+// MXFP4 scales in the tiled layout that Blackwell block-scaled MMA operands
+// use: 512-byte atoms of 128 rows x 4 scale columns, atom (rb, cb) at byte
+// (rb * ncb + cb) * 512, and inside an atom the scale of row 32i + j, column
+// l at byte 16j + 4i + l.  One warp per atom: lane j gathers the four scale
+// words of rows j, j + 32, j + 64, j + 96 (4 columns = one aligned word of a
+// row, since K / 32 is a multiple of 4) and writes them as one 16-byte
+// piece, so the warp writes the atom's 512 bytes contiguously.  Rows past M
+// read as zero.
+__global__ void __launch_bounds__(kThreads) mxfp4_scales_mma_kernel(const uint8_t *__restrict__ s,
+                                                                    int64_t M, int64_t ncb,
+                                                                    int64_t natoms,
+                                                                    uint8_t *__restrict__ out)
+{
+    griddep_wait();  // the previous kernel's outputs (PDL launch)
+    griddep_launch_dependents();  // the next kernel may start its set-up
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t srow = 4 * ncb;  // scale bytes per row (K / 32)
+    for (int64_t atom = warp; atom < natoms; atom += nwarps) {
+        const int64_t rb = atom / ncb, cb = atom - rb * ncb;
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int64_t r = 128 * rb + 32 * i + lane;
+            w[i] = r < M ? __ldg(reinterpret_cast<const uint32_t *>(s + r * srow + 4 * cb)) : 0u;
+        }
+        __stcs(reinterpret_cast<uint4 *>(out + atom * 512 + 16 * lane),
+               make_uint4(w[0], w[1], w[2], w[3]));
+    }
+}
+
 }  // namespace fq
 
 using namespace fq;
@@ -239,5 +273,36 @@ extern "C" fq_status fp4_to_fp8_rows(const uint8_t *q, const uint8_t *s, int64_t
         persistent_grid(fp4_to_fp8_rows_kernel, kThreads, 0, (nfb + per_cta - 1) / per_cta);
     launch_pdl(fp4_to_fp8_rows_kernel, dim3(grid), dim3(kThreads), 0,
                static_cast<cudaStream_t>(stream), q, s, nfb, exp_offset_k, y, ys);
+    return launch_status();
+}
+
+extern "C" int64_t mxfp4_scales_mma_bytes(int64_t M, int64_t K)
+{
+    if (M < 0 || K <= 0 || K % 128 != 0 || M > INT64_MAX / 2 - 128)
+        return -1;
+    const int64_t nrb = (M + 127) / 128;
+    if (nrb > INT64_MAX / 512 / (K / 128))
+        return -1;
+    return nrb * (K / 128) * 512;
+}
+
+extern "C" fq_status mxfp4_scales_mma_layout(const uint8_t *s, int64_t M, int64_t K,
+                                             uint8_t *s_mma, void *stream)
+{
+    if (mxfp4_scales_mma_bytes(M, K) < 0)
+        return FQ_ERR_SHAPE;
+    if (M == 0)
+        return FQ_OK;
+    if (!s || !s_mma)
+        return FQ_ERR_NULL;
+    if (!aligned16(s) || !aligned16(s_mma))
+        return FQ_ERR_ALIGN;
+    const int64_t ncb = K / 128;
+    const int64_t natoms = ((M + 127) / 128) * ncb;
+    const int64_t per_cta = kThreads / 32;
+    const int grid = persistent_grid(mxfp4_scales_mma_kernel, kThreads, 0,
+                                     (natoms + per_cta - 1) / per_cta);
+    launch_pdl(mxfp4_scales_mma_kernel, dim3(grid), dim3(kThreads), 0,
+               static_cast<cudaStream_t>(stream), s, M, ncb, natoms, s_mma);
     return launch_status();
 }

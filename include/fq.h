@@ -210,6 +210,25 @@ fq_status mxfp4_dequantize_rows(const uint8_t *q, const uint8_t *s, int64_t M, i
                                 void *stream);
 
 /*
+ * MXFP4 scales re-laid for a block-scaled MMA operand ([MoE-FP4] 2.1 fixes
+ * the UE8M0 scale per 32-element block; the pages fix no layout for a GEMM
+ * to read it, so this is the tiled layout that Blackwell's block-scaled MMA
+ * operands use for their scale factors, as NVIDIA documents it for its
+ * block-scaled GEMMs).
+ *   s     : uint8 [M, K/32]  row-major scales, as mxfp4_quantize_rows writes them
+ *   s_mma : uint8, mxfp4_scales_mma_bytes(M, K) bytes (output): 512-byte atoms
+ *           of 128 rows x 4 scale columns; atom (rb, cb) starts at byte
+ *           (rb * (K/128) + cb) * 512; the scale of row 128 rb + 32 i + j,
+ *           column 4 cb + l sits at byte 16 j + 4 i + l of its atom; rows
+ *           from M up to the next multiple of 128 are 0.
+ * Requires K > 0, K % 128 == 0, M >= 0; s and s_mma 16-byte aligned.
+ * mxfp4_scales_mma_bytes returns -1 for a rejected shape.
+ */
+int64_t mxfp4_scales_mma_bytes(int64_t M, int64_t K);
+fq_status mxfp4_scales_mma_layout(const uint8_t *s, int64_t M, int64_t K, uint8_t *s_mma,
+                                  void *stream);
+
+/*
  * Per-tensor amax for NVFP4's FP32 tensor scale ([NVFP4] "Receta"):
  *   x      : bf16 [n]
  *   amax   : float in device memory (output) = max |x| (NaN if x holds NaN;

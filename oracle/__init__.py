@@ -99,6 +99,7 @@ def lib():
                                                                  ctypes.c_uint32, ctypes.c_int,
                                                                  u64, u64, vp, vp, vp]),
                 "oracle_mxfp4_dequantize_rows": (ctypes.c_int, [vp, vp, i64, i64, vp]),
+                "oracle_mxfp4_scales_mma_layout": (ctypes.c_int, [vp, i64, i64, vp]),
                 "oracle_bf16_rne_array": (None, [vp, i64, vp]),
                 "oracle_nvfp4_amax_rht": (ctypes.c_float, [vp, i64, ctypes.c_uint32]),
                 "oracle_nvfp4_quantize_rht": (ctypes.c_int, [vp, i64, i64, ctypes.c_float,
@@ -337,6 +338,18 @@ def mxfp4_dequantize_rows(q, s):
     rc = lib().oracle_mxfp4_dequantize_rows(_p(q), _p(s), M, K, _p(out))
     if rc:
         raise ValueError("oracle_mxfp4_dequantize_rows: bad arguments")
+    return out
+
+
+def mxfp4_scales_mma_layout(s, M: int, K: int):
+    """MXFP4 scales [M, K/32] in the tiled layout of a block-scaled MMA
+    operand: ceil(M/128) * K/128 atoms of 512 bytes (see the C oracle)."""
+    s = np.ascontiguousarray(s, dtype=np.uint8)
+    assert s.shape == (M, K // 32)
+    out = np.full(((M + 127) // 128) * (K // 128) * 512, 0xA5, dtype=np.uint8)
+    rc = lib().oracle_mxfp4_scales_mma_layout(_p(s), M, K, _p(out))
+    if rc:
+        raise ValueError("oracle_mxfp4_scales_mma_layout: bad arguments")
     return out
 
 

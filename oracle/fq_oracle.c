@@ -875,6 +875,32 @@ int oracle_mxfp4_dequantize_rows(const uint8_t *q, const uint8_t *s, int64_t M, 
     return ORACLE_OK;
 }
 
+/*
+ * MXFP4 scales in the tiled layout of a block-scaled MMA operand.  READING:
+ * the pages fix the UE8M0 scale per 32-element block ([MoE-FP4] 2.1) but no
+ * layout for a GEMM to read it; the layout taken is the one NVIDIA documents
+ * for the scale factors of its block-scaled GEMMs on Blackwell.  The [M, K/32]
+ * scale matrix, padded with zero rows to a multiple of 128 rows, is cut into
+ * 128 x 4 tiles; tile (rb, cb) is stored as 512 bytes at (rb * K/128 + cb) *
+ * 512; inside a tile, row 32 i + j and column l go to byte 16 j + 4 i + l.
+ */
+int oracle_mxfp4_scales_mma_layout(const uint8_t *s, int64_t M, int64_t K, uint8_t *out)
+{
+    if (M < 0 || K <= 0 || K % 128 != 0)
+        return ORACLE_EARG;
+    const int64_t ncol = K / 32, ncb = K / 128, nrb = (M + 127) / 128;
+    for (int64_t rb = 0; rb < nrb; rb++)
+        for (int64_t cb = 0; cb < ncb; cb++)
+            for (int i = 0; i < 4; i++)
+                for (int j = 0; j < 32; j++)
+                    for (int l = 0; l < 4; l++) {
+                        const int64_t r = 128 * rb + 32 * i + j, c = 4 * cb + l;
+                        out[(rb * ncb + cb) * 512 + 16 * j + 4 * i + l] =
+                            r < M ? s[r * ncol + c] : 0;
+                    }
+    return ORACLE_OK;
+}
+
 /* BF16 rounding of an array of doubles (exposed for the pins). */
 void oracle_bf16_rne_array(const double *v, int64_t n, uint16_t *out)
 {

@@ -36,7 +36,8 @@ def test_header_declares_the_entry_points():
               "bf16_to_mxfp4_fp8", "nvfp4_amax", "nvfp4_amax_rht", "nvfp4_quantize_rht",
               "fp8_quantize_1x128", "fp8_quantize_128x128", "mxfp4_dequantize_rows",
               "nvfp4_quantize_delayed", "nvfp4_quantize",
-              "nvfp4_quantize_2d", "fq_status_string", "fq_last_cuda_error", "fq_version"):
+              "nvfp4_quantize_2d", "mxfp4_scales_mma_bytes", "mxfp4_scales_mma_layout",
+              "fq_status_string", "fq_last_cuda_error", "fq_version"):
         assert n in names
 
 
@@ -120,6 +121,19 @@ def test_host_validation_fused(lib):
     assert f(P, 100, 128, P, 4, 0, P, P, None, P, P, P, 5, None, None) == NULL
     assert f(P, 100, 128, None, 4, 0, P, P, P, P, P, P, 5, None, None) == NULL
     assert f(PM, 100, 128, P, 4, 0, P, P, P, P, P, P, 5, None, None) == ALIGN
+
+
+def test_host_validation_mma_layout(lib):
+    n = lib.mxfp4_scales_mma_bytes
+    assert n(0, 128) == 0 and n(1, 128) == 512 and n(128, 128) == 512 and n(129, 256) == 2048
+    assert n(100, 7168) == 56 * 512
+    assert n(-1, 128) == -1 and n(4, 96) == -1 and n(4, 0) == -1 and n(4, 64) == -1
+    f = lib.mxfp4_scales_mma_layout
+    assert f(P, 4, 96, P, None) == SHAPE
+    assert f(P, -1, 128, P, None) == SHAPE
+    assert f(None, 0, 128, None, None) == OK          # empty: no-op
+    assert f(None, 4, 128, P, None) == NULL
+    assert f(P, 4, 128, PM, None) == ALIGN
 
 
 def test_host_validation_rht(lib):

@@ -70,9 +70,9 @@ class _CublasLt:
     """The few cuBLASLt calls of one block-scaled FP4 GEMM, through ctypes
     (enum values from cublasLt.h / cublas_api.h / library_types.h)."""
     OP_N, OP_T = 0, 1
-    COMPUTE_32F, R_32F, R_16BF, R_8F_E4M3 = 68, 0, 14, 28
+    COMPUTE_32F, R_32F, R_16BF, R_8F_E4M3, R_4F_E2M1 = 68, 0, 14, 28, 33
     TRANSA, TRANSB, A_SCALE_POINTER, B_SCALE_POINTER = 3, 4, 17, 18
-    A_SCALE_MODE, B_SCALE_MODE, SCALE_VEC32_UE8M0 = 31, 32, 2
+    A_SCALE_MODE, B_SCALE_MODE, SCALE_VEC16_UE4M3, SCALE_VEC32_UE8M0 = 31, 32, 1, 2
 
     def __init__(self):
         import ctypes
@@ -112,7 +112,7 @@ class _CublasLt:
                                                            c.c_size_t(c.sizeof(v))),
                    f"cublasLtMatmulDescSetAttribute({attr})")
 
-    def mx_gemm(self, a8, sa_mma, b8, sb_mma, M, N, K):
+    def mx_gemm(self, a8, sa_mma, b8, sb_mma, M, N, K, dtype=None, mode=None, alpha=1.0):
         """D [N, M] row-major (= M x N column-major) = A B^T with A = (a8, sa)
         [M, K] and B = (b8, sb) [N, K]: row-major E4M3 bytes, UE8M0 scales
         per 32 elements along K in the block-scaled MMA layout; fp32
@@ -123,17 +123,19 @@ class _CublasLt:
                                                      c.c_int(self.R_32F)), "cublasLtMatmulDescCreate")
         self.set_attr(desc, self.TRANSA, self.OP_T, c.c_int32)
         self.set_attr(desc, self.TRANSB, self.OP_N, c.c_int32)
-        self.set_attr(desc, self.A_SCALE_MODE, self.SCALE_VEC32_UE8M0, c.c_int32)
-        self.set_attr(desc, self.B_SCALE_MODE, self.SCALE_VEC32_UE8M0, c.c_int32)
+        dtype = self.R_8F_E4M3 if dtype is None else dtype
+        mode = self.SCALE_VEC32_UE8M0 if mode is None else mode
+        self.set_attr(desc, self.A_SCALE_MODE, mode, c.c_int32)
+        self.set_attr(desc, self.B_SCALE_MODE, mode, c.c_int32)
         self.set_attr(desc, self.A_SCALE_POINTER, sa_mma.data_ptr(), c.c_void_p)
         self.set_attr(desc, self.B_SCALE_POINTER, sb_mma.data_ptr(), c.c_void_p)
         # A: K x M column-major (row-major [M, K]), op T; B: K x N column-major, op N
-        la = self.layout(self.R_8F_E4M3, K, M, K)
-        lb = self.layout(self.R_8F_E4M3, K, N, K)
+        la = self.layout(dtype, K, M, K)
+        lb = self.layout(dtype, K, N, K)
         ld = self.layout(self.R_16BF, M, N, M)
         d = torch.zeros((N, M), dtype=torch.bfloat16, device="cuda")
         ws = torch.empty((64 << 20,), dtype=torch.uint8, device="cuda")
-        alpha, beta = c.c_float(1.0), c.c_float(0.0)
+        alpha, beta = c.c_float(alpha), c.c_float(0.0)
         st = self.lib.cublasLtMatmul(self.handle, desc, c.byref(alpha), c.c_void_p(a8.data_ptr()), la,
                                      c.c_void_p(b8.data_ptr()), lb, c.byref(beta),
                                      c.c_void_p(d.data_ptr()), ld, c.c_void_p(d.data_ptr()), ld, None,
@@ -187,3 +189,47 @@ def test_block_scaled_gemm_reads_the_layout(fq):
     assert st == 0
     werr = ((wrong.float() - ref).abs() / scale).max().item()
     assert werr > 0.1, werr
+
+
+def _nvfp4_operand(fq, rows, K, seed):
+    """An NVFP4 operand (round to nearest) and its decoded values: code x
+    E4M3 block scale x the FP32 per-tensor decode scale g."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((rows, K)).astype(np.float32)
+    x *= np.exp2(rng.integers(-4, 5, (rows, K // 16))).repeat(16, axis=1).astype(np.float32)
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)
+    xb = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+    amax = fq.nvfp4_amax(xb)
+    q, sb, g = fq.nvfp4_quantize(xb, amax)
+    mag = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], device="cuda")
+    codes = torch.stack([q & 0xF, q >> 4], dim=-1).reshape(rows, K).long()
+    v = mag[codes & 7] * torch.where(codes >= 8, -1.0, 1.0)
+    bscale = sb.view(torch.float8_e4m3fn).float().repeat_interleave(16, dim=1)
+    return q, sb, float(g.item()), v * bscale * float(g.item())
+
+
+def test_nvfp4_gemm_reads_codes_and_scales(fq):
+    """cuBLASLt's NVFP4 GEMM (E2M1 data, UE4M3 scales per 16 elements in the
+    same 128 x 4-tile layout, the per-tensor scales as alpha) on the 1x16
+    quantizer's codes and block scales equals the product of the decoded
+    operands: the nibble order, the scale bytes and the per-tensor scale mean
+    what the consumer reads."""
+    M, N, K = 256, 384, 1024
+    qa, sa, ga, da = _nvfp4_operand(fq, M, K, 3)
+    qb, sb, gb, db = _nvfp4_operand(fq, N, K, 4)
+    lt = _CublasLt()
+    # the layout is a byte permutation of a [rows, cols] scale matrix with
+    # cols % 4 == 0: the NVFP4 scales [rows, K/16] go through the same call
+    st, got = lt.mx_gemm(qa, fq.mxfp4_scales_mma_layout(sa), qb, fq.mxfp4_scales_mma_layout(sb),
+                         M, N, K, dtype=lt.R_4F_E2M1, mode=lt.SCALE_VEC16_UE4M3, alpha=ga * gb)
+    if st != 0:
+        pytest.skip(f"cuBLASLt NVFP4 GEMM unavailable here (status {st})")
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        ref = (da @ db.t()).t()
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    scale = ref.abs() + 1e-3 * ref.abs().max()
+    err = ((got.float() - ref).abs() / scale).max().item()
+    assert err < 2 ** -6, err

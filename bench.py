@@ -66,7 +66,8 @@ KERNEL_SRC = {
     "mxfp4_quantize_rows": "fq_mxfp4.cu", "fp4_to_fp8_rows": "fq_mxfp4.cu",
     "fp4_to_fp8_cols": "fq_cols.cu", "nvfp4_amax": "fq_nvfp4.cu",
     "nvfp4_quantize": "fq_nvfp4.cu", "nvfp4_quantize_2d": "fq_nvfp4.cu",
-    "bf16_to_mxfp4_fp8": "fq_fused.cu", "nvfp4_amax_rht": "fq_nvfp4.cu",
+    "bf16_to_mxfp4_fp8": "fq_fused.cu", "bf16_to_mxfp4_fp8_single_pass": "fq_fused.cu",
+    "nvfp4_amax_rht": "fq_nvfp4.cu",
     "nvfp4_quantize_rht": "fq_nvfp4.cu", "fp8_quantize_1x128": "fq_fp8.cu",
     "fp8_quantize_128x128": "fq_fp8.cu", "mxfp4_dequantize_rows": "fq_fp8.cu",
     "nvfp4_quantize_delayed": "fq_nvfp4.cu", "nvfp4_quantize_2d_t": "fq_nvfp4.cu",
@@ -653,6 +654,8 @@ def run_gpu(args):
     fo = {k: torch.empty_like(out[k]) for k in ("q", "s", "y", "ys", "yT", "yTs")}
     fused_us = alone(lambda: fq.bf16_to_mxfp4_fp8(x, offs, 0, fo["q"], fo["s"], fo["y"], fo["ys"],
                                                   fo["yT"], fo["yTs"]))
+    single_us = alone(lambda: fq.bf16_to_mxfp4_fp8_single_pass(x, offs, 0, fo["q"], fo["s"], fo["y"],
+                                                               fo["ys"], fo["yT"], fo["yTs"]))
     sep_us = sum(kernels[k]["alone"]["us"] for k in KERNELS[:3])
     rht_mask = 0x9E37
     ar = torch.empty((1,), **f32)
@@ -687,6 +690,8 @@ def run_gpu(args):
         "bf16_to_mxfp4_fp8": entry("bf16_to_mxfp4_fp8", fused_us, b_fused(M, K, nb_cols, G),
                                    1 + fq.fp4_to_fp8_cols_launch_count(K),
                                    separate_calls_alone_us=round(sep_us, 2)),
+        "bf16_to_mxfp4_fp8_single_pass": entry("bf16_to_mxfp4_fp8_single_pass", single_us,
+                                               b_fused(M, K, nb_cols, G), 1),
         "nvfp4_amax_rht": entry("nvfp4_amax_rht", amax_rht_us, 2 * E + 4, 2),
         "nvfp4_quantize_rht_sr": entry("nvfp4_quantize_rht", rht_us, b_nvfp4(M, K), 1,
                                        sign_mask=rht_mask),
@@ -1019,6 +1024,7 @@ def run_ncu_calls(reps: int = 3):
         lambda: fq.nvfp4_quantize_delayed(x, hist, 0, True, 99, 0),
         lambda: fq.bf16_to_mxfp4_fp8(x, offs, 0),
         lambda: fq.mxfp4_scales_mma_layout(s),
+        lambda: fq.bf16_to_mxfp4_fp8_single_pass(x, offs, 0),
     ]
     for fn in calls:
         for _ in range(reps):

@@ -45,6 +45,8 @@ SIGNATURES = {
     "fp4_to_fp8_cols": (_int, [_vp, _vp, _i64, _i64, _vp, _i32, _int, _vp, _vp, _i64, _vp, _vp]),
     "bf16_to_mxfp4_fp8": (_int, [_vp, _i64, _i64, _vp, _i32, _int, _vp, _vp, _vp, _vp, _vp, _vp,
                                  _i64, _vp, _vp]),
+    "bf16_to_mxfp4_fp8_single_pass": (_int, [_vp, _i64, _i64, _vp, _i32, _int, _vp, _vp, _vp, _vp,
+                                             _vp, _vp, _i64, _vp, _vp]),
     "nvfp4_amax": (_int, [_vp, _i64, _vp, _vp]),
     "nvfp4_quantize": (_int, [_vp, _i64, _i64, _vp, _int, _u64, _u64, _vp, _vp, _vp, _vp]),
     "nvfp4_quantize_2d": (_int, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
@@ -239,7 +241,21 @@ def bf16_to_mxfp4_fp8(x: torch.Tensor, group_offsets: torch.Tensor, exp_offset_k
                       dev_status: torch.Tensor | None = None):
     """BF16 [M, K] + int64 group offsets [G+1] (device) -> (q, s, y, ys, yT,
     yT_scale): the MXFP4 codes and scales, the FP8 rows and the transposed
-    FP8 columns, equal to the three separate calls."""
+    FP8 columns, equal to the three separate calls (two kernels)."""
+    return _forward_cast("bf16_to_mxfp4_fp8", x, group_offsets, exp_offset_k, q, s, y, ys, yT,
+                         yT_scale, dev_status)
+
+
+def bf16_to_mxfp4_fp8_single_pass(x: torch.Tensor, group_offsets: torch.Tensor,
+                                  exp_offset_k: int = 0, q=None, s=None, y=None, ys=None,
+                                  yT=None, yT_scale=None, dev_status: torch.Tensor | None = None):
+    """bf16_to_mxfp4_fp8 as one kernel that reads BF16 once and reads no
+    output back (slower on GB300)."""
+    return _forward_cast("bf16_to_mxfp4_fp8_single_pass", x, group_offsets, exp_offset_k, q, s, y,
+                         ys, yT, yT_scale, dev_status)
+
+
+def _forward_cast(entry, x, group_offsets, exp_offset_k, q, s, y, ys, yT, yT_scale, dev_status):
     _bf16_2d(x, "x")
     M, K = x.shape
     G = _groups(group_offsets)
@@ -264,7 +280,7 @@ def bf16_to_mxfp4_fp8(x: torch.Tensor, group_offsets: torch.Tensor, exp_offset_k
             raise ValueError("dev_status must hold one int32")
     _on_device(x=x, group_offsets=group_offsets, q=q, s=s, y=y, ys=ys, yT=yT, yT_scale=yT_scale,
                dev_status=dev_status)
-    _call("bf16_to_mxfp4_fp8", _p(x), M, K, _p(group_offsets), G, int(exp_offset_k), _p(q), _p(s),
+    _call(entry, _p(x), M, K, _p(group_offsets), G, int(exp_offset_k), _p(q), _p(s),
           _p(y), _p(ys), _p(yT), _p(yT_scale), int(yT_scale.shape[0]), _p(dev_status), _stream())
     return q, s, y, ys, yT, yT_scale
 

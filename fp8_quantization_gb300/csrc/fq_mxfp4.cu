@@ -180,32 +180,51 @@ __global__ void __launch_bounds__(kThreads) fp4_to_fp8_rows_kernel(
 // MXFP4 scales in the tiled layout that Blackwell block-scaled MMA operands
 // use: 512-byte atoms of 128 rows x 4 scale columns, atom (rb, cb) at byte
 // (rb * ncb + cb) * 512, and inside an atom the scale of row 32i + j, column
-// l at byte 16j + 4i + l.  One warp per atom: lane j gathers the four scale
-// words of rows j, j + 32, j + 64, j + 96 (4 columns = one aligned word of a
-// row, since K / 32 is a multiple of 4) and writes them as one 16-byte
-// piece, so the warp writes the atom's 512 bytes contiguously.  Rows past M
-// read as zero.
+// l at byte 16j + 4i + l.  A CTA takes one (128-row block, chunk of 16 atom
+// columns) unit at a time: each thread loads 8 words (half warps read 64
+// contiguous bytes of a row; rows past M and columns past the row's end read
+// as zero) into shared memory, and after a barrier each warp writes two whole
+// atoms, lane j the 16 bytes of rows j, j+32, j+64, j+96 (shared rows are
+// padded by one word, so those four reads are free of bank conflicts): one
+// 512-byte contiguous store per warp per atom.
+constexpr int kMmaRows = 128;    // rows of an atom
+constexpr int kMmaChunk = 16;    // atom columns (4-byte words of a row) per unit
+constexpr int kMmaRowWords = kMmaChunk + 1;
+
 __global__ void __launch_bounds__(kThreads) mxfp4_scales_mma_kernel(const uint8_t *__restrict__ s,
                                                                     int64_t M, int64_t ncb,
-                                                                    int64_t natoms,
+                                                                    int64_t nrb,
                                                                     uint8_t *__restrict__ out)
 {
+    __shared__ uint32_t rows[kMmaRows * kMmaRowWords];
     griddep_wait();  // the previous kernel's outputs (PDL launch)
     griddep_launch_dependents();  // the next kernel may start its set-up
-    const int lane = threadIdx.x & 31;
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const int64_t srow = 4 * ncb;  // scale bytes per row (K / 32)
-    for (int64_t atom = warp; atom < natoms; atom += nwarps) {
-        const int64_t rb = atom / ncb, cb = atom - rb * ncb;
-        uint32_t w[4];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const uint32_t *s32 = reinterpret_cast<const uint32_t *>(s);
+    const int64_t nch = (ncb + kMmaChunk - 1) / kMmaChunk;  // chunks per row block
+    const int w = tid & 15, i0 = tid >> 4;                  // word, first row of this thread
+    for (int64_t u = blockIdx.x; u < nrb * nch; u += gridDim.x) {
+        const int64_t rb = u / nch, c0 = (u - rb * nch) * kMmaChunk;
+        const bool col_ok = c0 + w < ncb;
+        uint32_t v[kMmaRows / 16];
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const int64_t r = 128 * rb + 32 * i + lane;
-            w[i] = r < M ? __ldg(reinterpret_cast<const uint32_t *>(s + r * srow + 4 * cb)) : 0u;
+        for (int k = 0; k < kMmaRows / 16; k++) {
+            const int64_t r = 128 * rb + i0 + 16 * k;
+            v[k] = r < M && col_ok ? __ldg(s32 + r * ncb + c0 + w) : 0u;  // ncb words per row
         }
-        __stcs(reinterpret_cast<uint4 *>(out + atom * 512 + 16 * lane),
-               make_uint4(w[0], w[1], w[2], w[3]));
+#pragma unroll
+        for (int k = 0; k < kMmaRows / 16; k++)
+            rows[(i0 + 16 * k) * kMmaRowWords + w] = v[k];
+        __syncthreads();
+        for (int c = wid; c < kMmaChunk && c0 + c < ncb; c += kThreads / 32) {
+            uint4 o;
+            o.x = rows[lane * kMmaRowWords + c];
+            o.y = rows[(lane + 32) * kMmaRowWords + c];
+            o.z = rows[(lane + 64) * kMmaRowWords + c];
+            o.w = rows[(lane + 96) * kMmaRowWords + c];
+            __stcs(reinterpret_cast<uint4 *>(out + (rb * ncb + c0 + c) * 512 + 16 * lane), o);
+        }
+        __syncthreads();  // the rows are read before the next unit lands
     }
 }
 
@@ -298,11 +317,10 @@ extern "C" fq_status mxfp4_scales_mma_layout(const uint8_t *s, int64_t M, int64_
     if (!aligned16(s) || !aligned16(s_mma))
         return FQ_ERR_ALIGN;
     const int64_t ncb = K / 128;
-    const int64_t natoms = ((M + 127) / 128) * ncb;
-    const int64_t per_cta = kThreads / 32;
+    const int64_t nrb = (M + 127) / 128;
     const int grid = persistent_grid(mxfp4_scales_mma_kernel, kThreads, 0,
-                                     (natoms + per_cta - 1) / per_cta);
+                                     nrb * ((ncb + kMmaChunk - 1) / kMmaChunk));
     launch_pdl(mxfp4_scales_mma_kernel, dim3(grid), dim3(kThreads), 0,
-               static_cast<cudaStream_t>(stream), s, M, ncb, natoms, s_mma);
+               static_cast<cudaStream_t>(stream), s, M, ncb, nrb, s_mma);
     return launch_status();
 }

@@ -179,6 +179,21 @@ fq_status bf16_to_mxfp4_fp8(const void *x, int64_t M, int64_t K, const int64_t *
                             int32_t *dev_status, void *stream);
 
 /*
+ * The same call as one kernel: the BF16 tensor is read once and every output
+ * is written once from registers and shared memory, q and s are not read
+ * back.  Same arguments, outputs (byte for byte) and requirements as
+ * bf16_to_mxfp4_fp8; *dev_status also gets bit 2 if a shared-memory copy did
+ * not land within the kernel's time limit.  Slower than bf16_to_mxfp4_fp8 on
+ * GB300.  Needs the driver's tensor-map encoder: without it the call returns
+ * FQ_ERR_CUDA with cudaErrorNotSupported as the CUDA error.
+ */
+fq_status bf16_to_mxfp4_fp8_single_pass(const void *x, int64_t M, int64_t K,
+                                        const int64_t *group_offsets, int32_t G, int exp_offset_k,
+                                        uint8_t *q, uint8_t *s, uint8_t *y, float *ys, uint8_t *yT,
+                                        float *yT_scale, int64_t cap, int32_t *dev_status,
+                                        void *stream);
+
+/*
  * BF16 -> FP8 E4M3 block quantization for the FP8 backward flow ([MoE-FP4]
  * 2.2: gradients stay in standard FP8; 2.1: the Hopper FP8 pipeline is E4M3
  * with 128-element blocks and FP32 block scales).  The pages give the format

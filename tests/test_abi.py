@@ -33,7 +33,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("mxfp4_quantize_rows", "fp4_to_fp8_rows", "fp4_to_fp8_cols",
               "fp4_to_fp8_cols_scale_capacity", "fp4_to_fp8_cols_launch_count",
-              "bf16_to_mxfp4_fp8", "nvfp4_amax", "nvfp4_amax_rht", "nvfp4_quantize_rht",
+              "bf16_to_mxfp4_fp8", "bf16_to_mxfp4_fp8_single_pass", "nvfp4_amax", "nvfp4_amax_rht", "nvfp4_quantize_rht",
               "fp8_quantize_1x128", "fp8_quantize_128x128", "mxfp4_dequantize_rows",
               "nvfp4_quantize_delayed", "nvfp4_quantize",
               "nvfp4_quantize_2d", "mxfp4_scales_mma_bytes", "mxfp4_scales_mma_layout",
@@ -109,8 +109,9 @@ def test_host_validation_rows_and_cols(lib):
     assert c(P, P, 0, 128, P, 4, 0, P, P, 4, None, None) == OK
 
 
-def test_host_validation_fused(lib):
-    f = lib.bf16_to_mxfp4_fp8
+@pytest.mark.parametrize("entry", ["bf16_to_mxfp4_fp8", "bf16_to_mxfp4_fp8_single_pass"])
+def test_host_validation_fused(lib, entry):
+    f = getattr(lib, entry)
     # x, M, K, offs, G, k, q, s, y, ys, yT, yTs, cap, status, stream
     assert f(P, 100, 96, P, 4, 0, P, P, P, P, P, P, 5, None, None) == SHAPE    # K % 128
     assert f(P, -1, 128, P, 4, 0, P, P, P, P, P, P, 5, None, None) == SHAPE

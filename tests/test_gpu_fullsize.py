@@ -80,6 +80,11 @@ def test_moe_dispatch_16384x7168_all_casts(fq):
     for got, ref, what in zip(fused[:5], (rq, rs, ry, rys, ryT), ("q", "s", "y", "ys", "yT")):
         eq(got, ref, "fused " + what)
     eq(fused[5][:nb], ryTs[:nb], "fused yT scales")
+    single = fq.bf16_to_mxfp4_fp8_single_pass(x, torch.from_numpy(offs).cuda(), 0)
+    for got, want in zip(single[:5], fused[:5]):
+        assert torch.equal(got, want), "single-pass forward cast"
+    assert torch.equal(single[5][:nb], fused[5][:nb]), "single-pass forward cast yT scales"
+    del single
     ra = oracle.nvfp4_amax(bits)
     assert amax.item() == float(ra)
     rq4, rsb4, rg4 = oracle.nvfp4_quantize(bits, ra, use_sr=True, seed=1000, offset=0)
@@ -161,6 +166,10 @@ def test_ragged_experts_65536x2048(fq, k):
     for got, ref, what in zip(fused[:5], (rq, rs, ry, rys, ryT), ("q", "s", "y", "ys", "yT")):
         eq(got, ref, "fused " + what)
     eq(fused[5][:nb], ryTs[:nb], "fused yT scales")
+    single = fq.bf16_to_mxfp4_fp8_single_pass(x, torch.from_numpy(offs).cuda(), k)
+    for got, want in zip(single[:5], fused[:5]):
+        assert torch.equal(got, want), "single-pass forward cast"
+    assert torch.equal(single[5][:nb], fused[5][:nb]), "single-pass forward cast yT scales"
 
 
 def test_nvfp4_activations_16384x14336(fq):
@@ -346,7 +355,12 @@ def test_more_than_2_31_elements(fq):
         assert torch.equal(got, want), f"one-call forward cast {name}"
     nb = (M + 127) // 128
     assert torch.equal(fused[5][:nb], yTs[:nb]), "one-call forward cast yT scales"
-    del q, s, y, ys, yT, yTs, fused
+    del fused
+    single = fq.bf16_to_mxfp4_fp8_single_pass(x, torch.from_numpy(offs).cuda(), 3)
+    for got, want, name in zip(single, (q, s, y, ys, yT), ("q", "s", "y", "ys", "yT")):
+        assert torch.equal(got, want), f"single-pass forward cast {name}"
+    assert torch.equal(single[5][:nb], yTs[:nb]), "single-pass forward cast yT scales"
+    del q, s, y, ys, yT, yTs, single
     torch.cuda.empty_cache()
 
     # NVFP4: the amax, 1x16 with RNE and SR, 2D with the transposed operand

@@ -294,26 +294,33 @@ def fused_input(M, K, seed):
     return workloads.bf16_bits(x)
 
 
+FORWARD_CASTS = ["bf16_to_mxfp4_fp8", "bf16_to_mxfp4_fp8_single_pass"]
+
+
+@pytest.mark.parametrize("entry", FORWARD_CASTS)
 @pytest.mark.parametrize("case", sorted(COLS_CASES))
 @pytest.mark.parametrize("kmod", ["k_mult_512", "k_not_mult_512"])
-def test_bf16_to_mxfp4_fp8(fq, case, kmod):
-    """The one-call forward cast equals the oracle's MXFP4 -> FP8 rows and
-    MXFP4 -> FP8 cols, byte for byte, with canaries on every output."""
+def test_bf16_to_mxfp4_fp8(fq, case, kmod, entry):
+    """The one-call forward cast (two kernels, or the single-pass kernel)
+    equals the oracle's MXFP4 -> FP8 rows and MXFP4 -> FP8 cols, byte for
+    byte, with canaries on every output."""
     M, K, mk = COLS_CASES[case]
     K = cols_k(K, kmod)
     offs = np.asarray(mk(M), dtype=np.int64)
-    check_fused(fq, M, K, offs, (M + K) % 7, fused_input(M, K, seed=M + 3 * K))
+    check_fused(fq, M, K, offs, (M + K) % 7, fused_input(M, K, seed=M + 3 * K), entry)
 
 
-def test_bf16_to_mxfp4_fp8_above_512_windows(fq):
+@pytest.mark.parametrize("entry", FORWARD_CASTS)
+def test_bf16_to_mxfp4_fp8_above_512_windows(fq, entry):
     """The one-call forward cast on 66000 tokens (516 windows: the transposed
     kernel's large-tensor configuration) x 1024 features, 32 Zipf groups."""
     M, K = 66000, 1024
     offs = np.asarray(workloads.zipf_group_offsets(M, 32, 1.1, 13), dtype=np.int64)
-    check_fused(fq, M, K, offs, 2, fused_input(M, K, seed=17))
+    check_fused(fq, M, K, offs, 2, fused_input(M, K, seed=17), entry)
 
 
-def test_bf16_to_mxfp4_fp8_malformed_offsets(fq):
+@pytest.mark.parametrize("entry", FORWARD_CASTS)
+def test_bf16_to_mxfp4_fp8_malformed_offsets(fq, entry):
     """Malformed group offsets are clamped in the kernel, reported through
     dev_status, and nothing is written outside the outputs."""
     M, K = 700, 384
@@ -327,8 +334,8 @@ def test_bf16_to_mxfp4_fp8_malformed_offsets(fq):
             ((M, K // 2), torch.uint8), ((M, K // 32), torch.uint8), ((M, K), torch.uint8),
             ((M, K // 128), torch.float32), ((K, M), torch.uint8), ((cap, K), torch.float32))]
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
-        fq.bf16_to_mxfp4_fp8(x, torch.from_numpy(offs).cuda(), 0, *[o[1] for o in outs],
-                             dev_status=st)
+        getattr(fq, entry)(x, torch.from_numpy(offs).cuda(), 0, *[o[1] for o in outs],
+                           dev_status=st)
         for (raw, view), n in zip(outs, (M * K // 2, M * K // 32, M * K, M * K // 32, K * M,
                                          cap * K * 4)):
             check_canary(raw, n)
@@ -339,7 +346,7 @@ def test_bf16_to_mxfp4_fp8_malformed_offsets(fq):
         eq(outs[1][1], rs, "s")
 
 
-def check_fused(fq, M, K, offs, k, bits):
+def check_fused(fq, M, K, offs, k, bits, entry="bf16_to_mxfp4_fp8"):
     G = offs.size - 1
     cap = oracle.fp4_to_fp8_cols_scale_capacity(M, G)
     qraw, q = canary_out((M, K // 2), torch.uint8)
@@ -350,7 +357,7 @@ def check_fused(fq, M, K, offs, k, bits):
     yTsraw = torch.full((K * cap * 4 + 64,), CANARY, dtype=torch.uint8, device="cuda")
     yTs = yTsraw[: K * cap * 4].view(torch.float32).view(cap, K)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    fq.bf16_to_mxfp4_fp8(dev_bf16(bits), torch.from_numpy(offs).cuda(), k, q, s, y, ys, yT, yTs, st)
+    getattr(fq, entry)(dev_bf16(bits), torch.from_numpy(offs).cuda(), k, q, s, y, ys, yT, yTs, st)
     for raw, n in ((qraw, M * K // 2), (sraw, M * K // 32), (yraw, M * K), (ysraw, M * K // 32),
                    (yTraw, K * M), (yTsraw, K * cap * 4)):
         check_canary(raw, n)

@@ -58,17 +58,22 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// Persistent grid: enough CTAs to fill every SM at the kernel's occupancy,
-// never more than there is work for.
+// Grid of `waves` times the CTAs that fill every SM at the kernel's
+// occupancy, never more than there is work for.  One wave is a persistent
+// grid.  For the grid-stride streaming kernels, two or four waves are faster
+// on GB300: each CTA then takes a smaller share, and SM slots are refilled as
+// CTAs finish.  With one wave, the warp schedulers favour an SM's oldest CTAs,
+// and its last-launched CTAs trail at the end with the SM part empty.
 template <typename Kernel>
-inline int persistent_grid(Kernel kernel, int threads, size_t smem, int64_t work_ctas)
+inline int persistent_grid(Kernel kernel, int threads, size_t smem, int64_t work_ctas,
+                           int waves = 1)
 {
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) !=
             cudaSuccess ||
         per_sm < 1)
         per_sm = 1;
-    int64_t g = static_cast<int64_t>(sm_count()) * per_sm;
+    int64_t g = static_cast<int64_t>(sm_count()) * per_sm * waves;
     if (work_ctas < g)
         g = work_ctas;
     return static_cast<int>(g < 1 ? 1 : g);

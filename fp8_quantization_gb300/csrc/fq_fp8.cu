@@ -255,7 +255,7 @@ extern "C" fq_status fp8_quantize_1x128(const void *x, int64_t M, int64_t K, uin
         return FQ_ERR_ALIGN;
     const int64_t nblk = M * (K / 128);
     const int64_t work = (nblk + 8 * (kThreads / 32) - 1) / (8 * (kThreads / 32));
-    const int grid = persistent_grid(fp8_quantize_1x128_kernel, kThreads, 0, work);
+    const int grid = persistent_grid(fp8_quantize_1x128_kernel, kThreads, 0, work, 4);
     launch_pdl(fp8_quantize_1x128_kernel, dim3(grid), dim3(kThreads), 0,
                static_cast<cudaStream_t>(stream), static_cast<const uint16_t *>(x), nblk, y, s);
     return launch_status();
@@ -275,7 +275,7 @@ extern "C" fq_status fp8_quantize_128x128(const void *w, int64_t N, int64_t K, u
     if (!aligned16(w) || !aligned16(y) || !aligned16(s))
         return FQ_ERR_ALIGN;
     const int64_t tiles = (N / 128) * (K / 128);
-    const int grid = persistent_grid(fp8_quantize_128x128_kernel, kThreads, 0, tiles);
+    const int grid = persistent_grid(fp8_quantize_128x128_kernel, kThreads, 0, tiles, 4);
     launch_pdl(fp8_quantize_128x128_kernel, dim3(grid), dim3(kThreads), 0,
                static_cast<cudaStream_t>(stream), static_cast<const uint16_t *>(w), N, K, y, s);
     return launch_status();
@@ -296,7 +296,7 @@ extern "C" fq_status mxfp4_dequantize_rows(const uint8_t *q, const uint8_t *s, i
         return FQ_ERR_ALIGN;
     const int64_t nw = M * (K / 8);
     const int64_t work = (nw + kDeqUnroll * kThreads - 1) / (kDeqUnroll * kThreads);
-    const int grid = persistent_grid(mxfp4_dequantize_rows_kernel, kThreads, 0, work);
+    const int grid = persistent_grid(mxfp4_dequantize_rows_kernel, kThreads, 0, work, 4);
     launch_pdl(mxfp4_dequantize_rows_kernel, dim3(grid), dim3(kThreads), 0,
                static_cast<cudaStream_t>(stream), q, s, nw, static_cast<uint16_t *>(x));
     return launch_status();

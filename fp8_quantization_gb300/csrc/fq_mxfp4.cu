@@ -240,11 +240,11 @@ fq_status launch_mxfp4_rows(const void *x, int64_t M, int64_t K, uint8_t *q, uin
     const int64_t nblk = M * (K / 32);
     const int64_t work = (nblk + 32 * (kThreads / 32) - 1) / (32 * (kThreads / 32));
     if (y) {
-        const int grid = persistent_grid(mxfp4_quantize_rows_kernel<true>, kThreads, 0, work);
+        const int grid = persistent_grid(mxfp4_quantize_rows_kernel<true>, kThreads, 0, work, 4);
         launch_pdl(mxfp4_quantize_rows_kernel<true>, dim3(grid), dim3(kThreads), 0, st,
                    static_cast<const uint16_t *>(x), nblk, q, s, k, y, ys);
     } else {
-        const int grid = persistent_grid(mxfp4_quantize_rows_kernel<false>, kThreads, 0, work);
+        const int grid = persistent_grid(mxfp4_quantize_rows_kernel<false>, kThreads, 0, work, 4);
         launch_pdl(mxfp4_quantize_rows_kernel<false>, dim3(grid), dim3(kThreads), 0, st,
                    static_cast<const uint16_t *>(x), nblk, q, s, 0, static_cast<uint8_t *>(nullptr),
                    static_cast<float *>(nullptr));
@@ -289,7 +289,7 @@ extern "C" fq_status fp4_to_fp8_rows(const uint8_t *q, const uint8_t *s, int64_t
     const int64_t nfb = M * (K / 128);
     const int64_t per_cta = 4 * kRowsUnroll * (kThreads / 32);
     const int grid =
-        persistent_grid(fp4_to_fp8_rows_kernel, kThreads, 0, (nfb + per_cta - 1) / per_cta);
+        persistent_grid(fp4_to_fp8_rows_kernel, kThreads, 0, (nfb + per_cta - 1) / per_cta, 4);
     launch_pdl(fp4_to_fp8_rows_kernel, dim3(grid), dim3(kThreads), 0,
                static_cast<cudaStream_t>(stream), q, s, nfb, exp_offset_k, y, ys);
     return launch_status();

@@ -800,7 +800,7 @@ extern "C" fq_status nvfp4_quantize(const void *x, int64_t M, int64_t K, const f
     const int64_t work = (nblk + kNvUnroll * kThreads - 1) / (kNvUnroll * kThreads);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto kern = use_sr ? nvfp4_quantize_kernel<true, false> : nvfp4_quantize_kernel<false, false>;
-    const int grid = persistent_grid(kern, kThreads, 0, work);
+    const int grid = persistent_grid(kern, kThreads, 0, work, 2);
     launch_pdl(kern, dim3(grid), dim3(kThreads), 0, st, static_cast<const uint16_t *>(x), nblk,
                amax, seed, offset, q, sb, g, static_cast<uint64_t *>(nullptr), 0, 0u);
     return launch_status();
@@ -821,7 +821,7 @@ extern "C" fq_status nvfp4_quantize_2d(const void *w, int64_t N, int64_t K, cons
         return FQ_ERR_ALIGN;
     const int64_t units = (N / 16) * ((K + 255) / 256);
     const int grid =
-        persistent_grid(nvfp4_quantize_2d_kernel, kThreads, 0, (units + 7) / 8);
+        persistent_grid(nvfp4_quantize_2d_kernel, kThreads, 0, (units + 7) / 8, 2);
     launch_pdl(nvfp4_quantize_2d_kernel, dim3(grid), dim3(kThreads), 0,
                static_cast<cudaStream_t>(stream), static_cast<const uint16_t *>(w), N, K, amax, q, sb,
                g);
@@ -844,7 +844,7 @@ extern "C" fq_status nvfp4_quantize_2d_t(const void *w, int64_t N, int64_t K, co
         !aligned16(sbT) || !aligned16(g))
         return FQ_ERR_ALIGN;
     const int64_t units = ((N / 16 + kT2Strips - 1) / kT2Strips) * ((K + 255) / 256);
-    const int grid = persistent_grid(nvfp4_quantize_2d_t_kernel, kThreads, 0, units);
+    const int grid = persistent_grid(nvfp4_quantize_2d_t_kernel, kThreads, 0, units, 2);
     launch_pdl(nvfp4_quantize_2d_t_kernel, dim3(grid), dim3(kThreads), 0,
                static_cast<cudaStream_t>(stream), static_cast<const uint16_t *>(w), N, K, amax, q,
                sb, qT, sbT, g);
@@ -898,11 +898,11 @@ extern "C" fq_status nvfp4_quantize_rht(const void *x, int64_t M, int64_t K, con
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint32_t mask = sign_mask & 0xFFFFu;
     if (use_sr) {
-        const int grid = persistent_grid(nvfp4_quantize_rht_kernel<true>, kThreads, 0, work);
+        const int grid = persistent_grid(nvfp4_quantize_rht_kernel<true>, kThreads, 0, work, 2);
         launch_pdl(nvfp4_quantize_rht_kernel<true>, dim3(grid), dim3(kThreads), 0, st,
                    static_cast<const uint16_t *>(x), nblk, amax, mask, seed, offset, q, sb, g);
     } else {
-        const int grid = persistent_grid(nvfp4_quantize_rht_kernel<false>, kThreads, 0, work);
+        const int grid = persistent_grid(nvfp4_quantize_rht_kernel<false>, kThreads, 0, work, 2);
         launch_pdl(nvfp4_quantize_rht_kernel<false>, dim3(grid), dim3(kThreads), 0, st,
                    static_cast<const uint16_t *>(x), nblk, amax, mask, seed, offset, q, sb, g);
     }

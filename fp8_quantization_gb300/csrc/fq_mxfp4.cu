@@ -297,10 +297,10 @@ extern "C" fq_status fp4_to_fp8_rows(const uint8_t *q, const uint8_t *s, int64_t
 
 extern "C" int64_t mxfp4_scales_mma_bytes(int64_t M, int64_t K)
 {
-    if (M < 0 || K <= 0 || K % 128 != 0 || M > INT64_MAX / 2 - 128)
+    if (M < 0 || K <= 0 || K % 128 != 0 || M > INT64_MAX - 127)
         return -1;
     const int64_t nrb = (M + 127) / 128;
-    if (nrb > INT64_MAX / 512 / (K / 128))
+    if (nrb > INT64_MAX / 512 / (K / 128))  // the byte count must fit in int64
         return -1;
     return nrb * (K / 128) * 512;
 }

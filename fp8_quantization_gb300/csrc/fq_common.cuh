@@ -309,25 +309,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
-// Bulk copy of `bytes` bytes (a multiple of 16; both addresses 16-byte
-// aligned) global -> shared, completing on `bar`.
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
-                                          uint64_t *bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// Orders the shared-memory reads this thread has seen complete (its own, and
-// its warp's after a __syncwarp) before its later copies into that memory.
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Asynchronous 4-byte copy global -> shared (cp.async); with `src_bytes` 0
 // nothing is read and the 4 bytes are zero-filled.
 __device__ __forceinline__ void cp_async_4(void *dst, const void *src, uint32_t src_bytes)

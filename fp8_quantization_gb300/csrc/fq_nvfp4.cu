@@ -565,202 +565,6 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_rht_kernel(
     }
 }
 
-// ---------------------------------------------------------------- 1x16, staged
-
-// The codes and scale byte of one 16-element block (two 16-byte words of
-// BF16), as in the kernels above; the transformed variant applies the sign
-// flips, the Hadamard butterflies and the factor 1/4 first.  `amax16` gets
-// the block's max |x| as BF16 bits (untransformed variant only).
-template <bool kSR, bool kRht>
-__device__ __forceinline__ uint2 nvfp4_block_codes(const uint4 &a, const uint4 &b,
-                                                   const TensorScales &ts, const float *rtab,
-                                                   const RhtFlip &f, uint32_t k0, uint32_t k1,
-                                                   uint64_t counter, uint32_t &sbyte,
-                                                   uint32_t &amax16)
-{
-    uint2 codes;
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (kSR)
-        w = philox4x32_10(make_uint4(static_cast<uint32_t>(counter),
-                                     static_cast<uint32_t>(counter >> 32), 0u, 0u),
-                          k0, k1);
-    if (kRht) {
-        float y[16];
-        rht16(a, b, f, y);
-        float m = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 16; j += 2)
-            m = absmax3f_nan(m, y[j], y[j + 1]);
-        const BlockScale bs = nvfp4_block_scale_f(m, ts.enc, rtab);
-        sbyte = bs.b;
-        codes.x = kSR ? encode8f_sr(y, bs.r, w.x, w.y) : encode8f_rne(y, bs.r);
-        codes.y = kSR ? encode8f_sr(y + 8, bs.r, w.z, w.w) : encode8f_rne(y + 8, bs.r);
-    } else {
-        uint32_t m = absmax_bf16x2(absmax_bf16x2(a.x & 0x7FFF7FFFu, a.y), a.z);
-        m = absmax_bf16x2(absmax_bf16x2(m, a.w), b.x);
-        m = absmax_bf16x2(absmax_bf16x2(m, b.y), b.z);
-        m = absmax_bf16x2(m, b.w);
-        amax16 = hmax_u16x2(m);
-        const BlockScale bs = nvfp4_block_scale(amax16, ts.enc, rtab);
-        sbyte = bs.b;
-        codes.x = kSR ? encode8_sr(a, bs.r, w.x, w.y) : encode8_rne(a, bs.r);
-        codes.y = kSR ? encode8_sr(b, bs.r, w.z, w.w) : encode8_rne(b, bs.r);
-    }
-    return codes;
-}
-
-// The 1x16 quantizers with the input staged in shared memory by bulk copies.
-// Each warp owns a ring of two stages.  A stage holds one chunk of 32 P
-// consecutive blocks; lane l takes blocks l, l + 32, ... of the chunk.  As
-// soon as the warp has read a chunk, lane 0 copies the warp's chunk after
-// next into that stage.  So a warp's next two chunks are always on their
-// way, however long its arithmetic takes.  In the register-loading kernels
-// above, a warp busy with Philox calls issues its next loads late; staged,
-// the stochastically rounded quantizer gains 50.9 -> 48.6 us on 16384 x 7168.
-// Round to nearest already runs at the copy bandwidth there; the staged
-// round trip through shared memory would cost it about 2 us.
-//
-// Every wait on a stage gives up after about two seconds.  The warp then
-// waits (bounded) for its copies still in flight, so that none lands after
-// the CTA has left, and sets *g_out to NaN.  g is never NaN otherwise (it is
-// A / 2688, or 1 when A is 0 or NaN), so a NaN g reports the failure.
-constexpr int kStagedWarps = 8;
-constexpr int kStagedDepth = 2;
-
-__host__ __device__ constexpr size_t staged_smem_bytes(int P)
-{
-    return static_cast<size_t>(kStagedWarps) * kStagedDepth * (32 * 32 * P) +
-           static_cast<size_t>(kStagedWarps) * kStagedDepth * sizeof(uint64_t);
-}
-
-template <bool kSR, bool kRht, bool kDelayed, int P>
-__global__ void __launch_bounds__(kStagedWarps * 32) nvfp4_quantize_staged_kernel(
-    const uint16_t *__restrict__ x, int64_t nblk, const float *__restrict__ amax,
-    uint32_t sign_mask, uint64_t seed, uint64_t offset, uint8_t *__restrict__ q,
-    uint8_t *__restrict__ sb, float *__restrict__ g_out, uint64_t *__restrict__ hist, int32_t W,
-    uint32_t t)
-{
-    static_assert(kStagedWarps * 32 == kThreads, "the window helpers reduce over kThreads");
-    constexpr int kChunk = 32 * P;                 // blocks per chunk
-    constexpr uint32_t kChunkBytes = kChunk * 32;  // 32 bytes of BF16 per block
-    extern __shared__ __align__(128) uint8_t stage_mem[];
-    __shared__ float rtab[128];
-    __shared__ uint32_t red[kStagedWarps];
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    uint8_t *ring = stage_mem + static_cast<size_t>(wid) * kStagedDepth * kChunkBytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(stage_mem + static_cast<size_t>(kStagedWarps) *
-                                                                  kStagedDepth * kChunkBytes) +
-                     wid * kStagedDepth;
-    if (lane == 0) {
-        for (int i = 0; i < kStagedDepth; i++)
-            mbar_init(&full[i], 1);
-        mbar_init_fence();
-    }
-    __syncwarp();
-    griddep_wait();  // the previous kernel's outputs (PDL launch)
-    griddep_launch_dependents();  // the next kernel may start its set-up
-
-    // chunk i of this warp is chunk gw + i tw of the tensor
-    const int64_t nch = (nblk + kChunk - 1) / kChunk;
-    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kStagedWarps + wid;
-    const int64_t tw = static_cast<int64_t>(gridDim.x) * kStagedWarps;
-    const int64_t my_n = gw < nch ? (nch - gw + tw - 1) / tw : 0;
-    auto issue = [&](int64_t i) {  // lane 0
-        const int64_t c = gw + i * tw;
-        const int64_t left = nblk - c * kChunk;
-        const uint32_t bytes = static_cast<uint32_t>(left < kChunk ? left : kChunk) * 32u;
-        uint64_t *bar = &full[i % kStagedDepth];
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_load(ring + (i % kStagedDepth) * kChunkBytes, x + c * (kChunk * 16), bytes, bar);
-    };
-    if (lane == 0)
-        for (int64_t i = 0; i < kStagedDepth && i < my_n; i++)
-            issue(i);
-
-    const TensorScales ts = kDelayed ? nvfp4_tensor_setup_from(window_estimate(hist, W, t, red), rtab)
-                                     : nvfp4_tensor_setup(amax, rtab);
-    if (blockIdx.x == 0 && threadIdx.x == 0)
-        *g_out = ts.g;
-    const RhtFlip f = rht_flip_words(sign_mask);
-    const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
-    const uint64_t c0 = offset >> 4;
-    uint32_t own = 0;  // max of this thread's block maxima (BF16 bits)
-    int64_t i = 0;
-    for (; i < my_n; i++) {
-        const int st = static_cast<int>(i % kStagedDepth);
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(&full[st], static_cast<uint32_t>(i / kStagedDepth) & 1u)))
-            break;
-        const uint4 *src = reinterpret_cast<const uint4 *>(ring + st * kChunkBytes);
-        uint4 v[P][2];
-#pragma unroll
-        for (int u = 0; u < P; u++) {
-            v[u][0] = src[2 * (lane + 32 * u)];
-            v[u][1] = src[2 * (lane + 32 * u) + 1];
-        }
-        __syncwarp();  // every lane has read the stage
-        if (lane == 0 && i + kStagedDepth < my_n) {
-            fence_proxy_async_smem();
-            issue(i + kStagedDepth);
-        }
-        const int64_t cb = (gw + i * tw) * kChunk;
-#pragma unroll
-        for (int u = 0; u < P; u++) {
-            const int64_t blk = cb + lane + 32 * u;
-            if (blk >= nblk)
-                break;
-            uint32_t sbyte, amax16 = 0;
-            const uint2 codes = nvfp4_block_codes<kSR, kRht>(
-                v[u][0], v[u][1], ts, rtab, f, k0, k1, c0 + static_cast<uint64_t>(blk), sbyte,
-                amax16);
-            if (kDelayed)
-                own = max(own, amax16);
-            __stcs(reinterpret_cast<uint2 *>(q + blk * 8), codes);
-            sb[blk] = static_cast<uint8_t>(sbyte);
-        }
-    }
-    if (i < my_n) {
-        for (int64_t j = i; j < my_n && j < i + kStagedDepth; j++)
-            mbar_wait(&full[j % kStagedDepth], static_cast<uint32_t>(j / kStagedDepth) & 1u);
-        if (lane == 0)
-            atomicExch(reinterpret_cast<unsigned int *>(g_out), 0x7FC00000u);
-    }
-    if (kDelayed) {
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1)
-            own = max(own, __shfl_xor_sync(0xffffffffu, own, d));
-        if (lane == 0)
-            red[wid] = own;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            uint32_t a = 0;
-            for (int w = 0; w < kStagedWarps; w++)
-                a = max(a, red[w]);
-            window_record(hist, W, t, a << 16);
-        }
-    }
-}
-
-template <bool kSR, bool kRht, bool kDelayed, int P>
-void launch_nvfp4_staged(const void *x, int64_t nblk, const float *amax, uint32_t sign_mask,
-                         uint64_t seed, uint64_t offset, uint8_t *q, uint8_t *sb, float *g,
-                         uint64_t *hist, int32_t W, uint32_t t, cudaStream_t st)
-{
-    auto kern = nvfp4_quantize_staged_kernel<kSR, kRht, kDelayed, P>;
-    constexpr size_t smem = staged_smem_bytes(P);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess ||
-        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-        return;  // reported by launch_status()
-    const int64_t nch = (nblk + 32 * P - 1) / (32 * P);
-    const int grid = persistent_grid(kern, kStagedWarps * 32, smem,
-                                     (nch + kStagedWarps - 1) / kStagedWarps);
-    launch_pdl(kern, dim3(grid), dim3(kStagedWarps * 32), smem, st,
-               static_cast<const uint16_t *>(x), nblk, amax, sign_mask, seed, offset, q, sb, g,
-               hist, W, t);
-}
-
 // ---------------------------------------------------------------- 16x16
 
 // One warp's share of the 2D quantization: the 16-row strip `strip` x 256
@@ -995,15 +799,10 @@ extern "C" fq_status nvfp4_quantize(const void *x, int64_t M, int64_t K, const f
     const int64_t nblk = M * (K / 16);
     const int64_t work = (nblk + kNvUnroll * kThreads - 1) / (kNvUnroll * kThreads);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (use_sr) {
-        launch_nvfp4_staged<true, false, false, 4>(x, nblk, amax, 0u, seed, offset, q, sb, g,
-                                                   nullptr, 0, 0u, st);
-    } else {
-        const int grid = persistent_grid(nvfp4_quantize_kernel<false, false>, kThreads, 0, work, 2);
-        launch_pdl(nvfp4_quantize_kernel<false, false>, dim3(grid), dim3(kThreads), 0, st,
-                   static_cast<const uint16_t *>(x), nblk, amax, seed, offset, q, sb, g,
-                   static_cast<uint64_t *>(nullptr), 0, 0u);
-    }
+    auto kern = use_sr ? nvfp4_quantize_kernel<true, false> : nvfp4_quantize_kernel<false, false>;
+    const int grid = persistent_grid(kern, kThreads, 0, work, 2);
+    launch_pdl(kern, dim3(grid), dim3(kThreads), 0, st, static_cast<const uint16_t *>(x), nblk,
+               amax, seed, offset, q, sb, g, static_cast<uint64_t *>(nullptr), 0, 0u);
     return launch_status();
 }
 
@@ -1103,8 +902,9 @@ extern "C" fq_status nvfp4_quantize_rht(const void *x, int64_t M, int64_t K, con
         launch_pdl(nvfp4_quantize_rht_kernel<true>, dim3(grid), dim3(kThreads), 0, st,
                    static_cast<const uint16_t *>(x), nblk, amax, mask, seed, offset, q, sb, g);
     } else {
-        launch_nvfp4_staged<false, true, false, 3>(x, nblk, amax, mask, seed, offset, q, sb, g,
-                                                   nullptr, 0, 0u, st);
+        const int grid = persistent_grid(nvfp4_quantize_rht_kernel<false>, kThreads, 0, work, 2);
+        launch_pdl(nvfp4_quantize_rht_kernel<false>, dim3(grid), dim3(kThreads), 0, st,
+                   static_cast<const uint16_t *>(x), nblk, amax, mask, seed, offset, q, sb, g);
     }
     return launch_status();
 }
@@ -1130,16 +930,10 @@ extern "C" fq_status nvfp4_quantize_delayed(const void *x, int64_t M, int64_t K,
         return FQ_ERR_ALIGN;
     const int64_t nblk = M * (K / 16);
     const int64_t work = (nblk + kNvUnroll * kThreads - 1) / (kNvUnroll * kThreads);
-    if (use_sr) {
-        launch_nvfp4_staged<true, false, true, 4>(x, nblk, nullptr, 0u, seed, offset, q, sb, g,
-                                                  amax_history, window, step,
-                                                  static_cast<cudaStream_t>(stream));
-    } else {
-        const int grid = persistent_grid(nvfp4_quantize_kernel<false, true>, kThreads, 0, work);
-        launch_pdl(nvfp4_quantize_kernel<false, true>, dim3(grid), dim3(kThreads), 0,
-                   static_cast<cudaStream_t>(stream), static_cast<const uint16_t *>(x), nblk,
-                   static_cast<const float *>(nullptr), seed, offset, q, sb, g, amax_history,
-                   window, step);
-    }
+    auto kern = use_sr ? nvfp4_quantize_kernel<true, true> : nvfp4_quantize_kernel<false, true>;
+    const int grid = persistent_grid(kern, kThreads, 0, work);
+    launch_pdl(kern, dim3(grid), dim3(kThreads), 0, static_cast<cudaStream_t>(stream),
+               static_cast<const uint16_t *>(x), nblk, static_cast<const float *>(nullptr), seed,
+               offset, q, sb, g, amax_history, window, step);
     return launch_status();
 }

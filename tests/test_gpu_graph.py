@@ -24,7 +24,7 @@ def fq():
     return m
 
 
-def _outputs(fq, x, offs, hist, step):
+def _outputs(fq, x, offs, hist, step, nb):
     """All calls on x into fresh outputs (also the capture body)."""
     q, s = fq.mxfp4_quantize_rows(x)
     y, ys = fq.fp4_to_fp8_rows(q, s, 0)
@@ -42,23 +42,34 @@ def _outputs(fq, x, offs, hist, step):
     w = fq.nvfp4_quantize_2d_t(x, amax)
     dl = fq.nvfp4_quantize_delayed(x, hist, step, True, 7, 0)
     mma = fq.mxfp4_scales_mma_layout(s)
-    return [q, s, y, ys, yT, yTs, amax, q4, sb4, g4, q2, sb2, g2, *fused, *single, ar, qr, sbr,
-            gr, *f1, *f2, deq, *w, *dl, mma]
+    # rows of the transposed scales past the last (nb-th) block are not written
+    fused, single = list(fused), list(single)
+    fused[5], single[5] = fused[5][:nb], single[5][:nb]
+    return [q, s, y, ys, yT, yTs[:nb], amax, q4, sb4, g4, q2, sb2, g2, *fused, *single, ar, qr,
+            sbr, gr, *f1, *f2, deq, *w, *dl, mma]
+
+
+def _blocks(offs_np):
+    """128-token blocks of the groups (the rows of the transposed scales in use)."""
+    counts = np.diff(offs_np)
+    return int(((counts + 127) // 128).sum())
 
 
 def test_calls_replay_in_a_cuda_graph(fq):
     M, K, G = 2048, 1024, 8
-    offs = torch.from_numpy(workloads.zipf_group_offsets(M, G, 1.1, 5)).cuda()
+    offs_np = workloads.zipf_group_offsets(M, G, 1.1, 5)
+    offs = torch.from_numpy(offs_np).cuda()
+    nb = _blocks(offs_np)
     inputs = [workloads.moe_dispatch(M, K, seed=s) for s in (1, 2)]
     x = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
     x.copy_(torch.from_numpy(inputs[0].view(np.int16)).view(torch.bfloat16))
     hist_g = fq.amax_history(8, device="cuda")
-    _outputs(fq, x, offs, fq.amax_history(8, device="cuda"), 0)  # lazy set-up outside capture
+    _outputs(fq, x, offs, fq.amax_history(8, device="cuda"), 0, nb)  # lazy set-up outside capture
     torch.cuda.synchronize()
 
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        captured = _outputs(fq, x, offs, hist_g, 0)
+        captured = _outputs(fq, x, offs, hist_g, 0, nb)
     torch.cuda.synchronize()
 
     hist_d = fq.amax_history(8, device="cuda")
@@ -68,7 +79,7 @@ def test_calls_replay_in_a_cuda_graph(fq):
         graph.replay()
         torch.cuda.synchronize()
         xd = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
-        direct = _outputs(fq, xd, offs, hist_d, 0)
+        direct = _outputs(fq, xd, offs, hist_d, 0, nb)
         torch.cuda.synchronize()
         assert len(direct) == len(captured)
         for i, (a, b) in enumerate(zip(captured, direct)):

@@ -68,7 +68,8 @@ KERNEL_SRC = {
     "nvfp4_quantize": "fq_nvfp4.cu", "nvfp4_quantize_2d": "fq_nvfp4.cu",
     "bf16_to_mxfp4_fp8": "fq_fused.cu", "bf16_to_mxfp4_fp8_single_pass": "fq_fused.cu",
     "nvfp4_amax_rht": "fq_nvfp4.cu",
-    "nvfp4_quantize_rht": "fq_nvfp4.cu", "fp8_quantize_1x128": "fq_fp8.cu",
+    "nvfp4_quantize_rht": "fq_nvfp4.cu", "nvfp4_quantize_rht_rne": "fq_nvfp4.cu",
+    "fp8_quantize_1x128": "fq_fp8.cu",
     "fp8_quantize_128x128": "fq_fp8.cu", "mxfp4_dequantize_rows": "fq_fp8.cu",
     "nvfp4_quantize_delayed": "fq_nvfp4.cu", "nvfp4_quantize_2d_t": "fq_nvfp4.cu",
     "mxfp4_scales_mma_layout": "fq_mxfp4.cu",
@@ -643,10 +644,10 @@ def run_gpu(args):
     extra_reps = max(3, min(args.steps, 200))
     E = M * K
 
-    def entry(call, us, nb, launches, **kw):
+    def entry(call, us, nb, launches, traffic_key=None, **kw):
         gbs, fr = frac(nb, us)
         return {"call": call, "us": round(us, 2), "bytes": nb, "GB/s": gbs, "frac": fr,
-                "launches_per_call": launches, "traffic": ncu_traffic(call), **kw}
+                "launches_per_call": launches, "traffic": ncu_traffic(traffic_key or call), **kw}
 
     def alone(fn):
         return max_over_ranks(T.alone_us(fn, extra_reps), dev)
@@ -696,7 +697,7 @@ def run_gpu(args):
         "nvfp4_quantize_rht_sr": entry("nvfp4_quantize_rht", rht_us, b_nvfp4(M, K), 1,
                                        sign_mask=rht_mask),
         "nvfp4_quantize_rht_rne": entry("nvfp4_quantize_rht", rht_rne_us, b_nvfp4(M, K), 1,
-                                        sign_mask=rht_mask),
+                                        traffic_key="nvfp4_quantize_rht_rne", sign_mask=rht_mask),
         "fp8_quantize_1x128": entry("fp8_quantize_1x128", fp8_1x128_us, 3 * E + 4 * (E // 128), 1),
         "fp8_quantize_128x128": entry("fp8_quantize_128x128", fp8_128_us,
                                       3 * E + 4 * (E // 16384), 1),
@@ -1017,6 +1018,7 @@ def run_ncu_calls(reps: int = 3):
         lambda: fq.nvfp4_quantize_2d(x, amax),
         lambda: fq.nvfp4_amax_rht(x, 0x9E37, ar),
         lambda: fq.nvfp4_quantize_rht(x, ar, 0x9E37, True, 4242, 0),
+        lambda: fq.nvfp4_quantize_rht(x, ar, 0x9E37, False, 0, 0),
         lambda: fq.fp8_quantize_1x128(x),
         lambda: fq.fp8_quantize_128x128(x),
         lambda: fq.mxfp4_dequantize_rows(q, s),

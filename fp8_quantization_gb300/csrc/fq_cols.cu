@@ -12,8 +12,9 @@
 // with tensor-memory-access copies into shared memory (described at the
 // kernel).  When a token's row of exponents (K/32 bytes) is a multiple of 16
 // bytes (K % 512 == 0) the exponent rows come by tensor copy; otherwise by
-// 4-byte asynchronous copies, and the last super-tile of a row of
-// 128-feature blocks may be short.
+// tensor copies of four-row groups (M % 4 == 0) or by 4-byte asynchronous
+// copies, and the last super-tile of a row of 128-feature blocks may be
+// short.
 #include "fq_cols_common.cuh"
 
 namespace fq {
@@ -109,19 +110,41 @@ constexpr int kExpBytes = 3 * kTok * kExpRowBytes;
 constexpr int kSmemAlign = 128;  // tensor-copy destinations
 static_assert(kCodeBytes % kSmemAlign == 0 && kExpBytes % kSmemAlign == 0, "aligned buffers");
 
+// How a super-tile's exponent rows (tokens W-128 .. W+255, the 16 bytes of
+// its 16 MX columns from each) reach shared memory:
+//  * kExpRows (K % 512 == 0): three tensor copies of 128 rows x 16 bytes.
+//  * kExpQuads (K % 512 != 0, M % 4 == 0): a row of 4 nfeat exponent bytes is
+//    then not a multiple of 16 bytes, which a tensor map's row pitch must
+//    be, but a group of four rows is.  The exponents are viewed as M/4 rows
+//    of 16 nfeat bytes.  Row j of a group starts 4 nfeat j bytes into it, so
+//    its slice [16F, 16F + 16) lies in the 32 bytes from the 16-byte
+//    boundary 16F + floor16(4 nfeat j), at offset 4 nfeat j mod 16.  One
+//    tensor copy per j brings those 32 bytes of the super-tile's 96 groups:
+//    buffer [j][group][32 bytes].  Bytes past a row's end belong to the next
+//    row (or read as zero); they fall in the columns of a short super-tile's
+//    missing feature blocks, whose maxima are never used.
+//  * kExpAsync (otherwise): 4-byte asynchronous copies of each row's slice.
+constexpr int kExpAsync = 0;
+constexpr int kExpRows = 1;
+constexpr int kExpQuads = 2;
+constexpr int kQuadRows = 3 * kTok / 4;  // four-row groups of a super-tile
+constexpr int exp_buf_bytes(int mode) { return mode == kExpQuads ? 4 * kQuadRows * 32 : kExpBytes; }
+static_assert(exp_buf_bytes(kExpQuads) % kSmemAlign == 0, "aligned buffers");
+
 // Two configurations of the single pass (code stages x exponent buffers):
 // kStages x kExps = 4 x 2 up to kWinFastMax windows, 2 x 1 beyond (measured:
 // at 131072 x 7168 the 2 x 1 kernel is 6 % faster, at 16384 x 7168 7 %
 // slower).  Per shift-row buffer: the shift-table rows of every token of a
 // super-tile (uint4: one byte per MX column).
-inline size_t cols1_dyn_bytes(int32_t G, int stages, int exps)
+inline size_t cols1_dyn_bytes(int32_t G, int stages, int exps, int exp_mode)
 {
     return kSmemAlign + static_cast<size_t>(stages) * kCodeBytes +
-           static_cast<size_t>(exps) * kExpBytes + static_cast<size_t>(kExpBufs) * kTok * sizeof(uint4) +
+           static_cast<size_t>(exps) * exp_buf_bytes(exp_mode) +
+           static_cast<size_t>(kExpBufs) * kTok * sizeof(uint4) +
            kTileWords * sizeof(uint32_t) + static_cast<size_t>(G + 1) * 2 * sizeof(int32_t);
 }
 
-template <bool kAligned16, int kStages, int kExps, bool kExpTma>
+template <bool kAligned16, int kStages, int kExps, int kExpMode>
 __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
     const uint8_t *__restrict__ s, int32_t M, int32_t nfeat, const int64_t *__restrict__ offs,
@@ -139,7 +162,8 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     uint8_t *codes_ring = dyn_raw + ((kSmemAlign - (smem_u32(dyn_raw) & (kSmemAlign - 1))) &
                                      (kSmemAlign - 1));
     uint8_t *exp_ring = codes_ring + kStages * kCodeBytes;
-    uint4 *Uring = reinterpret_cast<uint4 *>(exp_ring + kExps * kExpBytes);  // [kExpBufs][kTok]
+    constexpr int kExpBuf = exp_buf_bytes(kExpMode);
+    uint4 *Uring = reinterpret_cast<uint4 *>(exp_ring + kExps * kExpBuf);  // [kExpBufs][kTok]
     uint32_t *tile = reinterpret_cast<uint32_t *>(Uring + kExpBufs * kTok);    // [kTileWords]
     int32_t *off = reinterpret_cast<int32_t *>(tile + kTileWords);             // [G + 1]
     int32_t *base = off + G + 1;                                              // [G + 1]
@@ -160,7 +184,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
             mbar_init(&empty_c[i], kConvWarps);
         }
         for (int i = 0; i < kExps; i++)
-            mbar_init(&full_e[i], kExpTma ? 1 : 32);
+            mbar_init(&full_e[i], kExpMode == kExpAsync ? 32 : 1);
         for (int i = 0; i < kExpBufs; i++) {
             mbar_init(&sready[i], 1);
             mbar_init(&empty_e[i], kConvWarps);
@@ -173,22 +197,31 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
         F = wfast ? sg / nwin : sg % nquad;
     };
     // exponent rows of super-tile m (tokens W-128 .. W+255, 16 bytes each;
-    // rows outside the tensor and columns past the last feature block read as
-    // zero), called by the whole producer warp: one tensor copy per 128 rows
-    // when a row of exponents is a multiple of 16 bytes, else 4-byte
-    // asynchronous copies, 12 rows per lane, tracked by the same barrier
+    // rows outside the tensor read as zero), called by the whole producer
+    // warp in the three modes described above; the asynchronous copies (12
+    // rows per lane, columns past the last feature block read as zero) are
+    // tracked by the same barrier
     auto issue_exps = [&](int32_t m) {
         int32_t W, F;
         super_xy(m, W, F);
         const int be = m % kExps;
-        uint8_t *dst = exp_ring + be * kExpBytes;
-        if (kExpTma) {
+        uint8_t *dst = exp_ring + be * kExpBuf;
+        if (kExpMode == kExpRows) {
             if (lane == 0) {
-                mbar_arrive_expect_tx(&full_e[be], kExpBytes);
+                mbar_arrive_expect_tx(&full_e[be], kExpBuf);
 #pragma unroll
                 for (int h = 0; h < 3; h++)
                     tma_load_2d(dst + h * kTok * kExpRowBytes, &tm_s, 16 * F,
                                 W + (h - 1) * kTok, &full_e[be]);
+            }
+        } else if (kExpMode == kExpQuads) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full_e[be], kExpBuf);
+#pragma unroll
+                for (int j = 0; j < 4; j++)
+                    tma_load_2d(dst + j * kQuadRows * 32, &tm_s,
+                                16 * F + ((j * static_cast<int32_t>(srow)) & ~15),
+                                (W - kTok) / 4, &full_e[be]);
             }
         } else {
             // lanes 4r' .. 4r'+3 copy the four words of one row: eight rows
@@ -243,7 +276,16 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     auto maxima = [&](int32_t m, int w0, int wstep) {
         int32_t W, F;
         super_xy(m, W, F);
-        const uint4 *ex = reinterpret_cast<const uint4 *>(exp_ring + (m % kExps) * kExpBytes);
+        const uint8_t *eb = exp_ring + (m % kExps) * kExpBuf;
+        // exponent slice of token W - 128 + r
+        auto exp_row = [&](int32_t r) -> uint4 {
+            if (kExpMode != kExpQuads)
+                return reinterpret_cast<const uint4 *>(eb)[r];
+            const int j = r & 3;
+            const uint32_t *p = reinterpret_cast<const uint32_t *>(
+                eb + j * kQuadRows * 32 + (r >> 2) * 32 + ((j * static_cast<int32_t>(srow)) & 15));
+            return make_uint4(p[0], p[1], p[2], p[3]);
+        };
         uint4 *U_of = Uring + (m % kExpBufs) * kTok;
         const int32_t We = min(W + kTok, M);
         const int gW = warp_find_last_le(off, G, W);
@@ -262,7 +304,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
             for (int u = 0; u < 4; u++) {
                 const int32_t t = bs + lane + 32 * u;
                 if (t < be) {
-                    const uint4 v = ex[t - W + kTok];
+                    const uint4 v = exp_row(t - W + kTok);
                     m4.x = bytemax4(m4.x, v.x);
                     m4.y = bytemax4(m4.y, v.y);
                     m4.z = bytemax4(m4.z, v.z);
@@ -277,7 +319,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
             };
             const uint4 S = make_uint4(wmax(m4.x), wmax(m4.y), wmax(m4.z), wmax(m4.w));
             for (int32_t t = max(bs, W) + lane; t < min(be, We); t += 32) {
-                const uint4 e = ex[t - W + kTok];
+                const uint4 e = exp_row(t - W + kTok);
                 U_of[t - W] = make_uint4(shift_rows4(S.x, e.x, k), shift_rows4(S.y, e.y, k),
                                          shift_rows4(S.z, e.z, k), shift_rows4(S.w, e.w, k));
             }
@@ -492,43 +534,63 @@ extern "C" int fp4_to_fp8_cols_launch_count(int64_t K)
     return single_pass_ok(K) ? 1 : 0;
 }
 
+namespace {
+using Cols1Kernel = void (*)(const CUtensorMap, const CUtensorMap, const uint8_t *, int32_t,
+                             int32_t, const int64_t *, int32_t, int, uint8_t *, float *,
+                             int32_t *);
+
+template <int kStages, int kExps, int kExpMode>
+Cols1Kernel pick_cols1(bool aligned16)
+{
+    return aligned16 ? fp4_to_fp8_cols_1pass_kernel<true, kStages, kExps, kExpMode>
+                     : fp4_to_fp8_cols_1pass_kernel<false, kStages, kExps, kExpMode>;
+}
+}  // namespace
+
 fq_status fq::launch_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t M, int64_t K,
                                      const int64_t *group_offsets, int32_t G, int exp_offset_k,
                                      uint8_t *yT, float *yT_scale, int64_t cap,
                                      int32_t *dev_status, cudaStream_t st)
 {
-    // single pass; the exponent rows come by tensor copy when a row of K/32
-    // bytes is a multiple of 16 bytes, else by 4-byte asynchronous copies
+    // single pass; the exponent rows come in one of the three modes
+    // described at kExpRows
     CUtensorMap tm_q, tm_s;
-    const bool exp_tma = K % 512 == 0;
-    if (encode_tensor_map_2d_u8(&tm_q, q, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(M),
-                                static_cast<uint64_t>(K / 2), 64, kTok, false) &&
-        // a super-tile reads 16 of each exponent row's K/32 bytes; the rest of
-        // the 128-byte line belongs to super-tiles a whole pass of windows
-        // later, so whole-line promotion would fetch it again from DRAM once
-        // the tensor outgrows L2
-        (!exp_tma ||
-         encode_tensor_map_2d_u8(&tm_s, s, static_cast<uint64_t>(K / 32), static_cast<uint64_t>(M),
-                                 static_cast<uint64_t>(K / 32), kExpRowBytes, kTok, false))) {
-        if (!exp_tma)
-            tm_s = tm_q;  // not read
+    const int mode = K % 512 == 0 ? kExpRows : (M % 4 == 0 ? kExpQuads : kExpAsync);
+    bool maps = encode_tensor_map_2d_u8(&tm_q, q, static_cast<uint64_t>(K / 2),
+                                        static_cast<uint64_t>(M), static_cast<uint64_t>(K / 2), 64,
+                                        kTok, false);
+    // a super-tile reads 16 (or 32) of each exponent row's bytes; the rest of
+    // the 128-byte line belongs to super-tiles a whole pass of windows later,
+    // so whole-line promotion would fetch it again from DRAM once the tensor
+    // outgrows L2
+    if (maps && mode == kExpRows)
+        maps = encode_tensor_map_2d_u8(&tm_s, s, static_cast<uint64_t>(K / 32),
+                                       static_cast<uint64_t>(M), static_cast<uint64_t>(K / 32),
+                                       kExpRowBytes, kTok, false);
+    else if (maps && mode == kExpQuads)
+        maps = encode_tensor_map_2d_u8(&tm_s, s, static_cast<uint64_t>(K / 8),
+                                       static_cast<uint64_t>(M / 4), static_cast<uint64_t>(K / 8),
+                                       32, kQuadRows, false);
+    else
+        tm_s = tm_q;  // not read
+    if (maps) {
+        // four code stages and two exponent buffers up to kWinFastMax
+        // windows, two and one beyond; the four-row groups fill twice the
+        // exponent buffer, so they keep one (and three CTAs per SM)
         const bool large = (M + kTok - 1) / kTok > kWinFastMax;
-        const size_t dyn = large ? cols1_dyn_bytes(G, 2, 1) : cols1_dyn_bytes(G, 4, 2);
         const bool a16 = M % 16 == 0;
-        using Kern = void (*)(const CUtensorMap, const CUtensorMap, const uint8_t *, int32_t,
-                              int32_t, const int64_t *, int32_t, int, uint8_t *, float *,
-                              int32_t *);
-        Kern kern;
+        const int stages = large ? 2 : 4;
+        const int exps = large || mode == kExpQuads ? 1 : 2;
+        const size_t dyn = cols1_dyn_bytes(G, stages, exps, mode);
+        Cols1Kernel kern;
         if (large)
-            kern = exp_tma ? (a16 ? fp4_to_fp8_cols_1pass_kernel<true, 2, 1, true>
-                                  : fp4_to_fp8_cols_1pass_kernel<false, 2, 1, true>)
-                           : (a16 ? fp4_to_fp8_cols_1pass_kernel<true, 2, 1, false>
-                                  : fp4_to_fp8_cols_1pass_kernel<false, 2, 1, false>);
+            kern = mode == kExpRows    ? pick_cols1<2, 1, kExpRows>(a16)
+                   : mode == kExpQuads ? pick_cols1<2, 1, kExpQuads>(a16)
+                                       : pick_cols1<2, 1, kExpAsync>(a16);
         else
-            kern = exp_tma ? (a16 ? fp4_to_fp8_cols_1pass_kernel<true, 4, 2, true>
-                                  : fp4_to_fp8_cols_1pass_kernel<false, 4, 2, true>)
-                           : (a16 ? fp4_to_fp8_cols_1pass_kernel<true, 4, 2, false>
-                                  : fp4_to_fp8_cols_1pass_kernel<false, 4, 2, false>);
+            kern = mode == kExpRows    ? pick_cols1<4, 2, kExpRows>(a16)
+                   : mode == kExpQuads ? pick_cols1<4, 1, kExpQuads>(a16)
+                                       : pick_cols1<4, 2, kExpAsync>(a16);
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(dyn)) != cudaSuccess ||
             cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,

@@ -201,10 +201,11 @@ COLS_CASES["g1_m_mult_16_k1536"] = (640, 1536, lambda M: np.array([0, M]))
 
 
 def cols_k(K, path):
-    """K of a case on one of the two exponent-row paths of the single pass:
+    """K of a case on one of the exponent-row paths of the single pass:
     K % 512 == 0 (rows of K/32 bytes are a multiple of 16 bytes: tensor
-    copies) or not (4-byte asynchronous copies, and a short last super-tile
-    of fewer than four 128-feature blocks)."""
+    copies of rows) or not (tensor copies of four-row groups when M % 4 == 0,
+    else 4-byte asynchronous copies; and a short last super-tile of fewer
+    than four 128-feature blocks)."""
     if path == "k_mult_512":
         return (K + 511) // 512 * 512
     return K if K % 512 else K + 128
@@ -250,13 +251,14 @@ def test_fp4_to_fp8_cols_short_super_tiles(fq, K):
 
 
 @pytest.mark.parametrize("M", [65536, 66000, 66001])
-def test_fp4_to_fp8_cols_walk_orders(fq, M):
+@pytest.mark.parametrize("K", [1024, 1152])
+def test_fp4_to_fp8_cols_walk_orders(fq, M, K):
     """Every output of the single pass on either side of the switch between
     its two configurations: up to 512 128-token windows the super-tiles
-    (window x 512 features) are walked window fastest with 4 code stages and 2
-    exponent buffers, beyond that feature quad fastest with 2 and 1 (M % 16
-    != 0 included).  Two feature quads, 32 Zipf groups, NaN scales."""
-    K = 1024
+    (window x 512 features) are walked window fastest with 4 code stages,
+    beyond that feature quad fastest with 2 (M % 16 != 0 included); K = 1152
+    takes the four-row exponent groups (M % 4 == 0) or the asynchronous
+    copies, with a short last super-tile.  32 Zipf groups, NaN scales."""
     assert fq.fp4_to_fp8_cols_launch_count(K) == 1
     offs = np.asarray(workloads.zipf_group_offsets(M, 32, 1.1, 11), dtype=np.int64)
     q, s = rand_mx(M, K, seed=M + 5, spread=16, nan_frac=0.0005)

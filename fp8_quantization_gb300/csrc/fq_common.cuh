@@ -380,6 +380,12 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
     return c;
 }
 
+// Requests the line holding p into L2 (no registers held, nothing returned).
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint4 ld_nc_v4(const void *p)
 {
     return __ldg(reinterpret_cast<const uint4 *>(p));

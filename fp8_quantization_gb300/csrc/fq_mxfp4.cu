@@ -36,18 +36,26 @@ __global__ void __launch_bounds__(kThreads) mxfp4_quantize_rows_kernel(
 {
     __shared__ __align__(16) uint8_t tab[kRows8 ? kTabRows * 8 : 8];
     uint64_t keep = 0, stream = 0;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t ntiles = (nblk + 31) >> 5;
+    griddep_wait();  // the previous kernel's outputs (PDL launch)
     if (kRows8) {
+        // the warp's first tile is requested into L2 before the shift table
+        // is built, as in the FP8 row kernel
+        if (warp < ntiles)
+            for (int i = 0; i < 4; i++) {
+                const int64_t blk = (warp << 5) + (lane >> 2) + 8 * i;
+                if (blk < nblk)
+                    prefetch_l2(x + blk * 32 + (lane & 3) * 8);
+            }
         build_fp8_table(tab);
         __syncthreads();
         keep = l2_evict_last();
         stream = l2_evict_first();
     }
-    griddep_wait();  // the previous kernel's outputs (PDL launch)
     griddep_launch_dependents();  // the next kernel may start its set-up
-    const int lane = threadIdx.x & 31;
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const int64_t ntiles = (nblk + 31) >> 5;
 
     for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
         const int64_t blk0 = tile << 5;
@@ -124,8 +132,6 @@ __global__ void __launch_bounds__(kThreads) fp4_to_fp8_rows_kernel(
     uint8_t *__restrict__ y, float *__restrict__ ys)
 {
     __shared__ __align__(16) uint8_t tab[kTabRows * 8];
-    build_fp8_table(tab);
-    __syncthreads();
     griddep_wait();  // the previous kernel's outputs (PDL launch)
     griddep_launch_dependents();  // the next kernel may start its set-up
 
@@ -134,6 +140,24 @@ __global__ void __launch_bounds__(kThreads) fp4_to_fp8_rows_kernel(
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t ntiles = (nfb + 4 * kRowsUnroll - 1) / (4 * kRowsUnroll);
+    // the warp's first tile is requested into L2 before the shift table is
+    // built, so that its DRAM latency runs under the table and the barrier
+    // (16384 x 7168: 30.8 -> 30.2 us alone, 71.7 -> 70.5 us after the row
+    // quantizer; building the table before the programmatic-launch wait
+    // instead overlaps it with the previous kernel but leaves the first
+    // loads behind it)
+    if (warp < ntiles && part == 0) {
+        const int64_t fb0 = warp * (4 * kRowsUnroll);
+        for (int i = 0; i < kRowsUnroll; i++) {
+            const int64_t fb = fb0 + 4 * i + (lane >> 3);
+            if (fb < nfb) {
+                prefetch_l2(q + fb * 64);
+                prefetch_l2(s + fb * 4);
+            }
+        }
+    }
+    build_fp8_table(tab);
+    __syncthreads();
 
     for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
         const int64_t fb0 = tile * (4 * kRowsUnroll);

@@ -396,17 +396,6 @@ __device__ __forceinline__ uint32_t encode8f_sr(const float *y, float r, uint32_
     return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
-// The first grid-stride iteration's data of a thread, requested into L2
-// before the per-tensor set-up (the amax load, the division, the scale table
-// and a CTA barrier) so that its DRAM latency runs under the set-up instead
-// of after it; the prefetch holds no registers.  On 16384 x 7168, alone:
-// 16x16 49.2 -> 47.8 us, 1x16 SR 50.3 -> 50.1 us; neutral or slower for the
-// Hadamard and transposed-operand kernels, which do not issue it.
-__device__ __forceinline__ void prefetch_l2(const void *p)
-{
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 // ---------------------------------------------------------------- 1x16
 
 // One lane per 16-element block (32 bytes of input, 8 bytes of codes), four
@@ -430,7 +419,13 @@ __global__ void __launch_bounds__(kThreads, kDelayed ? 4 : 0) nvfp4_quantize_ker
     __shared__ uint32_t red[kThreads / 32];
     griddep_wait();  // the previous kernel's outputs (PDL launch)
     griddep_launch_dependents();  // the next kernel may start its set-up
-    if (!kDelayed) {  // with the history set-up instead the prefetch was slower (53.1 -> 53.6 us)
+    // the first grid-stride iteration's blocks are requested into L2 before
+    // the per-tensor set-up (the amax load, the division, the scale table and
+    // a CTA barrier), so that their DRAM latency runs under it (16384 x 7168
+    // alone: 1x16 SR 50.3 -> 50.0 us, 16x16 49.2 -> 48.0 us; neutral or
+    // slower for the delayed, Hadamard and transposed-operand kernels, which
+    // do not issue it)
+    if (!kDelayed) {
         const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
         const int64_t n = static_cast<int64_t>(gridDim.x) * blockDim.x;
 #pragma unroll
@@ -639,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 2) nvfp4_quantize_2d_kernel(
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t ncg = (K + 255) >> 8;  // 256-column groups
     const int64_t nunits = (N >> 4) * ncg;
-    if (warp < nunits) {  // the warp's first strip
+    if (warp < nunits) {  // the warp's first strip, requested as in the 1x16 kernel
         const int64_t strip = warp / ncg;
         const int64_t col = ((warp - strip * ncg) << 8) + 8 * lane;
         if (col < K)

@@ -91,7 +91,8 @@ __device__ __forceinline__ void write_tile(const uint32_t *tile, uint8_t *__rest
 //    MX column) and, for a block whose first token lies in the window,
 //    writes the block's FP32 scales of the super-tile's 512 features (2 KB,
 //    contiguous in the block-major scale rows).  The first super-tile's
-//    maxima are computed by all nine warps at once.
+//    maxima are computed by all nine warps at once, one (block, 4-column
+//    word) item per warp.
 //  * The eight converting warps wait for a tile's codes (and, on a
 //    super-tile's first tile, for its maxima), convert each (token, MX
 //    column) unit into the FP8 tile through its shift-table row once every
@@ -256,13 +257,22 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     build_fp8_table(tab);
     __syncthreads();  // the barriers are initialised before the first copy
     griddep_wait();   // offsets, codes and exponents may come from the previous kernel
-    // the first exponent copy needs only the window, not the groups: issue
-    // it now so that it overlaps the group set-up.  The first code copies
-    // follow once it has landed, so that it does not queue behind the whole
-    // grid's code copies (their flight then overlaps the first maxima:
-    // 16384 x 7168 38.0 -> 37.4 us, 16384 x 7040 38.6 -> 37.7 us)
-    if (wid == kConvWarps)
+    // the first exponent copy and the first code copies need only the
+    // window, not the groups: issue them now so that they overlap the group
+    // set-up and the first maxima.  Median timer stamps from the first CTA's
+    // entry, 16384 x 7168: the wait returns at 1.1 us, the groups are in
+    // shared memory at 2.1 us (one warp for up to 63 groups; 2.9 us with
+    // CTA-wide scans), the first maxima are done at 3.5 us (split over all
+    // warps; 4.5 us with one warp per block) and the first tile is written
+    // at 5.3 us (6.4 us).  The code copies are then already in flight (they
+    // used to follow the exponent copy's landing).  65536 x 2048: 41.2 ->
+    // 40.5 us; one-call forward cast: 97.4 -> 96.5 us.
+    if (wid == kConvWarps) {
         issue_exps(0);
+        if (lane == 0)
+            for (int32_t n = 0; n < kStages - 1 && n < my_tiles; n++)
+                issue_codes(n);
+    }
     const int bad = load_groups(offs, G, M, off, base, warp_tot);  // ends with a CTA barrier
     if (bad && blockIdx.x == 0 && tid == 0 && dev_status)
         atomicOr(dev_status, 1);
@@ -339,13 +349,61 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
             }
         }
     };
+    // the first super-tile's maxima with every warp: one work item per
+    // (block, 4-column word), so that the few blocks meeting the window are
+    // spread over all nine warps
+    auto maxima_split = [&](int32_t m, int w0, int wstep) {
+        int32_t W, F;
+        super_xy(m, W, F);
+        const uint8_t *eb = exp_ring + (m % kExps) * kExpBuf;
+        auto exp_word = [&](int32_t r, int cw) -> uint32_t {
+            if (kExpMode != kExpQuads)
+                return reinterpret_cast<const uint32_t *>(eb)[4 * r + cw];
+            const int j = r & 3;
+            const uint32_t *p = reinterpret_cast<const uint32_t *>(
+                eb + j * kQuadRows * 32 + (r >> 2) * 32 + ((j * static_cast<int32_t>(srow)) & 15));
+            return p[cw];
+        };
+        uint32_t *U32 = reinterpret_cast<uint32_t *>(Uring + (m % kExpBufs) * kTok);
+        const int32_t We = min(W + kTok, M);
+        const int gW = warp_find_last_le(off, G, W);
+        const int32_t blkW = base[gW] + ((W - off[gW]) >> 7);
+        const int gL = warp_find_last_le(off, G, We - 1);
+        const int32_t nbw = base[gL] + ((We - 1 - off[gL]) >> 7) - blkW + 1;  // <= 128
+        int g = gW;
+        for (int32_t it = w0; it < 4 * nbw; it += wstep) {
+            const int32_t b = blkW + (it >> 2);
+            const int cw = it & 3;
+            while (base[g + 1] <= b)  // group of block b (skips empty groups)
+                g++;
+            const int32_t bs = off[g] + ((b - base[g]) << 7);
+            const int32_t be = min(bs + kTok, off[g + 1]);
+            uint32_t mx = 0;
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const int32_t t = bs + lane + 32 * u;
+                if (t < be)
+                    mx = bytemax4(mx, exp_word(t - W + kTok, cw));
+            }
+            const uint32_t S = __reduce_max_sync(0xffffffffu, mx & 0xFFu) |
+                               (__reduce_max_sync(0xffffffffu, (mx >> 8) & 0xFFu) << 8) |
+                               (__reduce_max_sync(0xffffffffu, (mx >> 16) & 0xFFu) << 16) |
+                               (__reduce_max_sync(0xffffffffu, mx >> 24) << 24);
+            for (int32_t t = max(bs, W) + lane; t < min(be, We); t += 32)
+                U32[4 * (t - W) + cw] = shift_rows4(S, exp_word(t - W + kTok, cw), k);
+            if (bs >= W && 4 * F + cw < nfeat) {
+                // features 512 F + 128 cw + 4 lane .. + 3: MX column 4 cw + lane / 8
+                float *dst = yTs + static_cast<int64_t>(b) * (128 * static_cast<int64_t>(nfeat)) +
+                             512 * static_cast<int64_t>(F) + 128 * cw + 4 * lane;
+                const uint32_t v = fp8_block_scale_bits((S >> (8 * (lane >> 3))) & 0xFFu, k);
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(v, v, v, v);
+            }
+        }
+    };
     // ---- super-tile 0: its maxima with every warp
     const bool ok0 = !__syncthreads_or(!mbar_wait(&full_e[0], 0));
-    if (ok0 && wid == kConvWarps && lane == 0)
-        for (int32_t n = 0; n < kStages - 1 && n < my_tiles; n++)
-            issue_codes(n);
     if (ok0)
-        maxima(0, wid, kThreads1p / 32);
+        maxima_split(0, wid, kThreads1p / 32);
     __syncthreads();  // every warp is done with exponent buffer 0
     // with one exponent buffer the copy of super-tile 1 follows the first
     // maxima (with two it is issued in the loop below)
@@ -356,7 +414,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     if (wid == kConvWarps) {
         // ================================================= producer warp
         bool ok = ok0;
-        int32_t issued_c = ok0 ? min(kStages - 1, my_tiles) : 0, issued_e = pre_e;  // copies issued
+        int32_t issued_c = min(kStages - 1, my_tiles), issued_e = pre_e;  // copies issued
         int32_t waited_e = ok0 ? 1 : 0;  // exponent copies waited for
         if (ok0 && lane == 0)
             mbar_arrive(&sready[0]);

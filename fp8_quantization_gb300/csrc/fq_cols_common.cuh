@@ -107,36 +107,57 @@ __device__ inline int load_groups(const int64_t *__restrict__ offs, int32_t G, i
                            int32_t *base, int32_t *warp_tot)
 {
     const int tid = threadIdx.x;
-    if (G < 32) {
-        // one warp: clamp, max-scan and sum-scan with shuffles (G + 1 <= 32)
+    if (G < 64) {
+        // one warp, entries 2l and 2l + 1 in lane l (G + 1 <= 64): clamp,
+        // max-scan and sum-scan with shuffles, no CTA barrier but the last
         int bad = 0;
         if (tid < 32) {
             const int lane = tid;
-            int64_t o = lane <= G ? offs[lane] : M;
-            const int64_t prev = lane >= 1 && lane <= G ? offs[lane - 1] : 0;
-            const int64_t c = o < 0 ? 0 : (o > M ? M : o);
-            bad = lane <= G && (c != o || (lane == 0 && o != 0) || (lane == G && o != M) ||
-                                (lane > 0 && o < prev));
-            int32_t v = static_cast<int32_t>(c);
+            const int i0 = 2 * lane, i1 = i0 + 1;
+            const int64_t o0 = i0 <= G ? offs[i0] : M;
+            const int64_t o1 = i1 <= G ? offs[i1] : M;
+            const int64_t p0 = __shfl_up_sync(0xffffffffu, o1, 1);  // offs[i0 - 1] for lane >= 1
+            const int64_t c0 = o0 < 0 ? 0 : (o0 > M ? M : o0);
+            const int64_t c1 = o1 < 0 ? 0 : (o1 > M ? M : o1);
+            bad = (i0 <= G && (c0 != o0 || (i0 == 0 && o0 != 0) || (i0 == G && o0 != M) ||
+                               (i0 > 0 && o0 < p0))) ||
+                  (i1 <= G && (c1 != o1 || (i1 == G && o1 != M) || o1 < o0));
+            const int32_t m1 = static_cast<int32_t>(c0 > c1 ? c0 : c1);
+            int32_t incl = m1;
             for (int d = 1; d < 32; d <<= 1) {
-                const int32_t u = __shfl_up_sync(0xffffffffu, v, d);
+                const int32_t u = __shfl_up_sync(0xffffffffu, incl, d);
                 if (lane >= d)
-                    v = max(v, u);
+                    incl = max(incl, u);
             }
+            int32_t excl = __shfl_up_sync(0xffffffffu, incl, 1);
             if (lane == 0)
-                v = 0;
-            if (lane == G)
-                v = M;
-            const int32_t below = __shfl_up_sync(0xffffffffu, v, 1);
-            int32_t nb = lane >= 1 && lane <= G ? (v - below + kTok - 1) / kTok : 0;
+                excl = 0;
+            int32_t v0 = max(excl, static_cast<int32_t>(c0)), v1 = max(excl, m1);
+            if (i0 == 0)
+                v0 = 0;
+            if (i0 == G)
+                v0 = M;
+            if (i1 == G)
+                v1 = M;
+            const int32_t vprev = __shfl_up_sync(0xffffffffu, v1, 1);  // entry i0 - 1
+            const int32_t nb0 = i0 >= 1 && i0 <= G ? (v0 - vprev + kTok - 1) / kTok : 0;
+            const int32_t nb1 = i1 <= G ? (v1 - v0 + kTok - 1) / kTok : 0;
+            int32_t sincl = nb0 + nb1;
             for (int d = 1; d < 32; d <<= 1) {
-                const int32_t u = __shfl_up_sync(0xffffffffu, nb, d);
+                const int32_t u = __shfl_up_sync(0xffffffffu, sincl, d);
                 if (lane >= d)
-                    nb += u;
+                    sincl += u;
             }
-            if (lane <= G) {
-                off[lane] = v;
-                base[lane] = nb;
+            int32_t sexcl = __shfl_up_sync(0xffffffffu, sincl, 1);
+            if (lane == 0)
+                sexcl = 0;
+            if (i0 <= G) {
+                off[i0] = v0;
+                base[i0] = sexcl + nb0;
+            }
+            if (i1 <= G) {
+                off[i1] = v1;
+                base[i1] = sexcl + nb0 + nb1;
             }
             bad = __any_sync(0xffffffffu, bad);
         }

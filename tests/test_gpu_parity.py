@@ -192,6 +192,9 @@ COLS_CASES = {
     "m_not_mult_4": (1001, 128, lambda M: workloads.random_group_offsets(M, 9, seed=5)),
     "small_m": (3, 128, lambda M: np.array([0, 1, 3])),
     "many_groups": (2000, 128, lambda M: workloads.random_group_offsets(M, 1024, seed=6)),
+    # 63 and 64 groups: the last count of the one-warp group set-up, the first of the CTA-wide one
+    "groups_63": (3000, 256, lambda M: workloads.random_group_offsets(M, 63, seed=7)),
+    "groups_64": (3000, 128, lambda M: workloads.random_group_offsets(M, 64, seed=8)),
     "one_token_groups": (200, 128, lambda M: np.arange(M + 1)),
 }
 
@@ -274,6 +277,23 @@ def test_fp4_to_fp8_cols_malformed_offsets(fq, K):
     for offs in ([0, 800], [5, 300, 200, 700], [0, -40, 700], [0, 100, 699], [10, 20, 700]):
         _, _, st = run_cols(fq, q, s, np.array(offs, dtype=np.int64), 0, check=False)
         assert st == 1, offs
+    # 40 groups (two offsets per lane of the one-warp set-up): a decrease at
+    # an odd and at an even index, a negative and a too-large offset inside,
+    # a last offset short of M; 80 groups for the CTA-wide set-up
+    good = np.linspace(0, M, 41).astype(np.int64)
+    for i, v in ((17, good[16] - 1), (18, good[17] - 1), (33, -3), (20, M + 5), (40, M - 1)):
+        offs = good.copy()
+        offs[i] = v
+        _, _, st = run_cols(fq, q, s, offs, 0, check=False)
+        assert st == 1, (i, v)
+    good80 = np.linspace(0, M, 81).astype(np.int64)
+    for i, v in ((41, good80[40] - 1), (80, M + 1)):
+        offs = good80.copy()
+        offs[i] = v
+        _, _, st = run_cols(fq, q, s, offs, 0, check=False)
+        assert st == 1, (i, v)
+    _, _, st = run_cols(fq, q, s, good, 0)
+    assert st == 0
 
 
 # ------------------------------------------------------------------ fused MXFP4 forward cast

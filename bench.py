@@ -25,9 +25,10 @@ the events, which sit at the two ends of every pass.
 `configs`: every configuration of the workload definition -- the 256 x 512
 outlier tensor, the MoE-dispatch tensor, the 65536 x 2048 ragged experts, the
 NVFP4 activations (16384 x 14336 Student-t(4)) and weights (14336 x 4096
-N(0, 0.02)), the 1K-262144 row bandwidth sweep at 7168, and a hidden size
+N(0, 0.02)), the 1K-262144 row bandwidth sweep at 7168, a hidden size
 that is a multiple of 128 but not of 512 (the transposed conversion's
-two-launch path) -- each call timed inside its configuration's chain (an
+exponent rows by four-row groups), and the same with a token count that is
+not a multiple of 16 -- each call timed inside its configuration's chain (an
 event between every two calls) and alone (L2 flushed before the call).
 
 `error_stats`: the oracle's numbers about the formats on each
@@ -833,8 +834,11 @@ def run_gpu(args):
              b_cols(m, Ks, (m + 127) // 128, 1))])
     del xs, qs, ss, ys_, yss, yTflat, yTsflat
 
-    # a hidden size that is a multiple of 128 but not of 512: the transposed
-    # conversion's two-launch path, MoE-dispatch recipe, 32 Zipf experts
+    # a hidden size that is a multiple of 128 but not of 512 (the transposed
+    # conversion's exponent rows by four-row groups), MoE-dispatch recipe, 32
+    # Zipf experts; then the same with a token count that is not a multiple
+    # of 16 (output rows of yT not 16-byte aligned, the last M % 4 exponent
+    # rows patched)
     Mt, Kt = 16384, TWO_LAUNCH_K
     xt = to_dev(workloads.moe_dispatch(Mt, Kt, seed=0))
     offt = torch.from_numpy(offs_np).to(dev)
@@ -848,6 +852,19 @@ def run_gpu(args):
                                                                   ot["yT"], ot["yTs"]),
                     b_cols(Mt, Kt, nb_cols, 32))])
     del xt, offt, ot
+    Mu = 16389
+    offs_u = workloads.zipf_group_offsets(Mu, EXPERTS, 1.1, 0)
+    xu = to_dev(workloads.moe_dispatch(Mu, Kt, seed=0))
+    offu = torch.from_numpy(offs_u).to(dev)
+    ou = mx_outputs(Mu, Kt, 32)
+    run_config(f"moe_dispatch {Mu}x{Kt} (M % 16 != 0, K % 512 != 0)",
+               "N(0,1) x row lognormal(0,1), 32 Zipf(1.1) experts", [
+                   ("mxfp4_quantize_rows", lambda: fq.mxfp4_quantize_rows(xu, ou["q"], ou["s"]),
+                    b_mxfp4(Mu, Kt)),
+                   ("fp4_to_fp8_cols", lambda: fq.fp4_to_fp8_cols(ou["q"], ou["s"], offu, 0,
+                                                                  ou["yT"], ou["yTs"]),
+                    b_cols(Mu, Kt, col_blocks(offs_u), 32))])
+    del xu, offu, ou
     torch.cuda.empty_cache()
     # the bar: every call on a tensor of at least 4x L2 at >= 75 % alone
     big = [(n, lab, c["alone_frac"]) for n, cf in configs.items() for lab, c in cf["calls"].items()

@@ -12,9 +12,9 @@
 // with tensor-memory-access copies into shared memory (described at the
 // kernel).  When a token's row of exponents (K/32 bytes) is a multiple of 16
 // bytes (K % 512 == 0) the exponent rows come by tensor copy; otherwise by
-// tensor copies of four-row groups (M % 4 == 0) or by 4-byte asynchronous
-// copies, and the last super-tile of a row of 128-feature blocks may be
-// short.
+// tensor copies of four-row groups (M >= 4; the last M % 4 rows patched in
+// shared memory) or by 4-byte asynchronous copies (M < 4), and the last
+// super-tile of a row of 128-feature blocks may be short.
 #include "fq_cols_common.cuh"
 
 namespace fq {
@@ -22,9 +22,110 @@ namespace fq {
 constexpr int kTileSlots = tile_slots(kTok / 4);  // 1254
 constexpr int kTileWords = kTileSlots * 4;
 
+// Word i (0..3, not a compile-time constant) of y, without indexing a
+// register array.
+__device__ __forceinline__ uint32_t word_sel(const uint32_t y[4], int i)
+{
+    return (i & 2) ? ((i & 1) ? y[3] : y[2]) : ((i & 1) ? y[1] : y[0]);
+}
+
+// Bytes [s, s + 16) of the 32 bytes p ++ x (p first), 0 < s < 16.
+__device__ __forceinline__ void bytes_at(const uint32_t p[4], const uint32_t x[4], int s,
+                                         uint32_t y[4])
+{
+    const uint32_t z[8] = {p[0], p[1], p[2], p[3], x[0], x[1], x[2], x[3]};
+    const int w0 = s >> 2;
+    uint32_t zs[5];
+#pragma unroll
+    for (int j = 0; j < 5; j++)
+        zs[j] = (w0 & 2) ? ((w0 & 1) ? z[3 + j] : z[2 + j]) : ((w0 & 1) ? z[1 + j] : z[j]);
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        y[i] = __funnelshift_r(zs[i], zs[i + 1], 8 * (s & 3));
+}
+
+// Bytes [lo, hi) of the 16-byte block y to blk + lo .. blk + hi - 1 (blk
+// 16-byte aligned), as aligned pieces of 8, 4, 2 and 1 bytes.
+__device__ __forceinline__ void store_block_range(uint8_t *blk, const uint32_t y[4], int lo,
+                                                  int hi)
+{
+    if (hi == 16) {
+        // a suffix [lo, 16): the pieces are the set bits of 16 - lo, smallest first
+#pragma unroll
+        for (int sz = 1; sz <= 8; sz <<= 1) {
+            if (lo & sz) {
+                const uint32_t w = word_sel(y, lo >> 2);
+                if (sz == 8)
+                    __stcs(reinterpret_cast<uint2 *>(blk + lo), make_uint2(w, word_sel(y, (lo >> 2) + 1)));
+                else if (sz == 4)
+                    __stcs(reinterpret_cast<unsigned int *>(blk + lo), w);
+                else if (sz == 2)
+                    __stcs(reinterpret_cast<unsigned short *>(blk + lo),
+                           static_cast<unsigned short>(w >> (8 * (lo & 2))));
+                else
+                    blk[lo] = static_cast<uint8_t>(w >> (8 * (lo & 3)));
+                lo += sz;
+            }
+        }
+        return;
+    }
+    if (lo == 0) {
+        // a prefix [0, hi): the pieces are the set bits of hi, largest first
+#pragma unroll
+        for (int sz = 8; sz >= 1; sz >>= 1) {
+            if (hi & sz) {
+                const int o = hi & ~(2 * sz - 1);
+                const uint32_t w = word_sel(y, o >> 2);
+                if (sz == 8)
+                    __stcs(reinterpret_cast<uint2 *>(blk + o), make_uint2(w, word_sel(y, (o >> 2) + 1)));
+                else if (sz == 4)
+                    __stcs(reinterpret_cast<unsigned int *>(blk + o), w);
+                else if (sz == 2)
+                    __stcs(reinterpret_cast<unsigned short *>(blk + o),
+                           static_cast<unsigned short>(w >> (8 * (o & 2))));
+                else
+                    blk[o] = static_cast<uint8_t>(w >> (8 * (o & 3)));
+            }
+        }
+        return;
+    }
+    int o = lo;
+    while (o < hi) {
+        const uint32_t w = word_sel(y, o >> 2);
+        if (!(o & 7) && o + 8 <= hi) {
+            __stcs(reinterpret_cast<uint2 *>(blk + o), make_uint2(w, word_sel(y, (o >> 2) + 1)));
+            o += 8;
+        } else if (!(o & 3) && o + 4 <= hi) {
+            __stcs(reinterpret_cast<unsigned int *>(blk + o), w);
+            o += 4;
+        } else if (!(o & 1) && o + 2 <= hi) {
+            __stcs(reinterpret_cast<unsigned short *>(blk + o),
+                   static_cast<unsigned short>(w >> (8 * (o & 2))));
+            o += 2;
+        } else {
+            blk[o] = static_cast<uint8_t>(w >> (8 * (o & 3)));
+            o += 1;
+        }
+    }
+}
+
 // Write-out of a converted tile (window W, feature block f): warp w handles
 // feature words 4w..4w+3 (m_out), lane%8 tokens 16c..16c+15 (c_out); each
-// 16-byte store of a quarter warp fills one 128-byte output line.
+// 16-byte store of a quarter warp fills one 128-byte output line.  When the
+// output rows are not 16-byte aligned (M % 16 != 0), a row's segment of the
+// window starts a = (row start) mod 16 bytes past a 16-byte boundary:
+//  * M % 4 == 0 (a = 0, 4, 8 or 12, the same for every chunk of the row):
+//    each lane stores its chunk as one 16-byte, two 8-byte or four 4-byte
+//    pieces;
+//  * otherwise lane c writes the aligned block that holds the last a bytes
+//    of chunk c - 1 (taken from the lane below with a shuffle) and the first
+//    16 - a bytes of its own chunk, lane 7 also the block after the segment;
+//    the two partial blocks at the segment's ends (shared with the
+//    neighbouring windows) are written as aligned pieces of 8, 4, 2 and 1
+//    bytes.
+// Byte-by-byte stores (the earlier path for both) made M % 16 != 0 about ten
+// times slower: 16385 x 7040 ran 399 us, now 81 us (16384: 38 us); 16392 x
+// 7168 401 -> 45 us.  Called by whole warps.
 template <bool kAligned16>
 __device__ __forceinline__ void write_tile(const uint32_t *tile, uint8_t *__restrict__ yT,
                                            int32_t M, int32_t W, int32_t f, int m_out, int c_out)
@@ -38,7 +139,64 @@ __device__ __forceinline__ void write_tile(const uint32_t *tile, uint8_t *__rest
     }
     const int32_t t0 = W + 16 * c_out;
     uint8_t *p = yT + (static_cast<int64_t>(f) * 128 + 4 * m_out) * M + t0;
-    if (kAligned16 && W + kTok <= M) {
+    if (!kAligned16 && (M & 3) == 0) {
+        // rows 4-byte aligned: each lane stores its own chunk in aligned
+        // pieces of its row's alignment (16, 8 or 4 bytes); the window's
+        // token count is a multiple of 4
+        const int n = min(kTok, M - W);
+#pragma unroll
+        for (int rr = 0; rr < 4; rr++) {
+            const int a = static_cast<int>(reinterpret_cast<uintptr_t>(p) & 15);
+            const int m = min(16, n - 16 * c_out);  // bytes of the chunk in the window
+            if (m == 16 && a == 0) {
+                __stcs(reinterpret_cast<uint4 *>(p),
+                       make_uint4(rows[rr][0], rows[rr][1], rows[rr][2], rows[rr][3]));
+            } else if (m == 16 && (a & 7) == 0) {
+                __stcs(reinterpret_cast<uint2 *>(p), make_uint2(rows[rr][0], rows[rr][1]));
+                __stcs(reinterpret_cast<uint2 *>(p + 8), make_uint2(rows[rr][2], rows[rr][3]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    if (4 * i < m)
+                        __stcs(reinterpret_cast<unsigned int *>(p + 4 * i), rows[rr][i]);
+            }
+            p += M;
+        }
+    } else if (!kAligned16) {
+        const int n = min(kTok, M - W);  // tokens of the window
+        uint8_t *seg = yT + (static_cast<int64_t>(f) * 128 + 4 * m_out) * M + W;
+#pragma unroll
+        for (int rr = 0; rr < 4; rr++) {
+            const int a = static_cast<int>(reinterpret_cast<uintptr_t>(seg) & 15);
+            uint8_t *base = seg - a;  // 16-byte aligned
+            uint32_t prev[4], y[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+                prev[i] = __shfl_up_sync(0xffffffffu, rows[rr][i], 1, 8);
+            if (a == 0) {
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    y[i] = rows[rr][i];
+            } else {
+                bytes_at(prev, rows[rr], 16 - a, y);
+            }
+            // block c_out holds the segment's bytes [16 c - a, 16 c - a + 16)
+            const int b0 = 16 * c_out - a;
+            const int lo = max(0, b0), hi = min(n, b0 + 16);
+            if (hi - lo == 16)
+                __stcs(reinterpret_cast<uint4 *>(base + 16 * c_out),
+                       make_uint4(y[0], y[1], y[2], y[3]));
+            else if (lo < hi)
+                store_block_range(base + 16 * c_out, y, lo - b0, hi - b0);
+            if (c_out == 7 && a != 0 && 128 - a < n) {
+                // the block after: the segment's bytes [128 - a, n)
+                uint32_t y8[4];
+                bytes_at(rows[rr], rows[rr], 16 - a, y8);
+                store_block_range(base + 128, y8, 0, n - (128 - a));
+            }
+            seg += M;
+        }
+    } else if (W + kTok <= M) {
 #pragma unroll
         for (int rr = 0; rr < 4; rr++) {
             __stcs(reinterpret_cast<uint4 *>(p),  // evict-first: yT is not re-read
@@ -49,7 +207,7 @@ __device__ __forceinline__ void write_tile(const uint32_t *tile, uint8_t *__rest
         const int32_t We = min(W + kTok, M);
 #pragma unroll
         for (int rr = 0; rr < 4; rr++) {
-            if (kAligned16 && t0 + 16 <= We) {
+            if (t0 + 16 <= We) {
                 __stcs(reinterpret_cast<uint4 *>(p),
                        make_uint4(rows[rr][0], rows[rr][1], rows[rr][2], rows[rr][3]));
             } else {
@@ -114,17 +272,20 @@ static_assert(kCodeBytes % kSmemAlign == 0 && kExpBytes % kSmemAlign == 0, "alig
 // How a super-tile's exponent rows (tokens W-128 .. W+255, the 16 bytes of
 // its 16 MX columns from each) reach shared memory:
 //  * kExpRows (K % 512 == 0): three tensor copies of 128 rows x 16 bytes.
-//  * kExpQuads (K % 512 != 0, M % 4 == 0): a row of 4 nfeat exponent bytes is
+//  * kExpQuads (K % 512 != 0, M >= 4): a row of 4 nfeat exponent bytes is
 //    then not a multiple of 16 bytes, which a tensor map's row pitch must
-//    be, but a group of four rows is.  The exponents are viewed as M/4 rows
-//    of 16 nfeat bytes.  Row j of a group starts 4 nfeat j bytes into it, so
-//    its slice [16F, 16F + 16) lies in the 32 bytes from the 16-byte
-//    boundary 16F + floor16(4 nfeat j), at offset 4 nfeat j mod 16.  One
-//    tensor copy per j brings those 32 bytes of the super-tile's 96 groups:
-//    buffer [j][group][32 bytes].  Bytes past a row's end belong to the next
-//    row (or read as zero); they fall in the columns of a short super-tile's
-//    missing feature blocks, whose maxima are never used.
-//  * kExpAsync (otherwise): 4-byte asynchronous copies of each row's slice.
+//    be, but a group of four rows is.  The exponents are viewed as
+//    floor(M/4) rows of 16 nfeat bytes.  Row j of a group starts 4 nfeat j
+//    bytes into it, so its slice [16F, 16F + 16) lies in the 32 bytes from
+//    the 16-byte boundary 16F + floor16(4 nfeat j), at offset 4 nfeat j mod
+//    16.  One tensor copy per j brings those 32 bytes of the super-tile's 96
+//    groups: buffer [j][group][32 bytes].  Bytes past a row's end belong to
+//    the next row (or read as zero); they fall in the columns of a short
+//    super-tile's missing feature blocks, whose maxima are never used.  When
+//    M % 4 != 0 the last M % 4 tokens lie past the view's rows (read as
+//    zero); once a copy that reaches them has landed, the producer warp
+//    writes their slices into the buffer with 4-byte loads (patch_tail).
+//  * kExpAsync (M < 4): 4-byte asynchronous copies of each row's slice.
 constexpr int kExpAsync = 0;
 constexpr int kExpRows = 1;
 constexpr int kExpQuads = 2;
@@ -252,6 +413,35 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
         } else {
             mbar_arrive(&full_c[st]);
         }
+    };
+
+    // four-row groups with M % 4 != 0: the slices of the last M % 4 tokens,
+    // which the tensor copies read as zero, written into super-tile m's
+    // landed exponent buffer by the calling warp (lane 4i + w: word w of
+    // tail token i; words past the row's end are left alone), then ordered
+    // before the tensor copies that later refill the buffer
+    const int32_t Mq = M & ~3;  // tokens the four-row view covers
+    auto patch_tail = [&](int32_t m) {
+        int32_t W, F;
+        super_xy(m, W, F);
+        const int ti = lane >> 2, w = lane & 3;
+        const int32_t t = Mq + ti;
+        const int32_t r = t - W + kTok;  // row of the super-tile's exponent rows
+        if (ti < 3 && t < M && w < min(4, nfeat - 4 * F) && r >= 0 && r < 3 * kTok) {
+            const int j = r & 3;
+            uint32_t *dst = reinterpret_cast<uint32_t *>(
+                exp_ring + (m % kExps) * kExpBuf + j * kQuadRows * 32 + (r >> 2) * 32 +
+                ((j * static_cast<int32_t>(srow)) & 15));
+            dst[w] = *reinterpret_cast<const uint32_t *>(s + static_cast<int64_t>(t) * srow +
+                                                         16 * F + 4 * w);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    };
+    // does super-tile m's exponent copy reach the tokens past the view?
+    auto reaches_tail = [&](int32_t m) {
+        int32_t W, F;
+        super_xy(m, W, F);
+        return kExpMode == kExpQuads && Mq != M && W + 2 * kTok > Mq;
     };
 
     build_fp8_table(tab);
@@ -402,6 +592,11 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     };
     // ---- super-tile 0: its maxima with every warp
     const bool ok0 = !__syncthreads_or(!mbar_wait(&full_e[0], 0));
+    if (ok0 && reaches_tail(0)) {
+        if (wid == kConvWarps)
+            patch_tail(0);
+        __syncthreads();
+    }
     if (ok0)
         maxima_split(0, wid, kThreads1p / 32);
     __syncthreads();  // every warp is done with exponent buffer 0
@@ -468,6 +663,10 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
                     if (!ok)
                         break;
                     waited_e = m + 1;
+                    if (reaches_tail(m)) {
+                        patch_tail(m);
+                        __syncwarp();
+                    }
                     maxima(m, 0, 1);
                     __syncwarp();
                     if (lane == 0)
@@ -615,7 +814,7 @@ fq_status fq::launch_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
     // single pass; the exponent rows come in one of the three modes
     // described at kExpRows
     CUtensorMap tm_q, tm_s;
-    const int mode = K % 512 == 0 ? kExpRows : (M % 4 == 0 ? kExpQuads : kExpAsync);
+    const int mode = K % 512 == 0 ? kExpRows : (M >= 4 ? kExpQuads : kExpAsync);
     bool maps = encode_tensor_map_2d_u8(&tm_q, q, static_cast<uint64_t>(K / 2),
                                         static_cast<uint64_t>(M), static_cast<uint64_t>(K / 2), 64,
                                         kTok, false);

@@ -195,6 +195,11 @@ COLS_CASES = {
     # 63 and 64 groups: the last count of the one-warp group set-up, the first of the CTA-wide one
     "groups_63": (3000, 256, lambda M: workloads.random_group_offsets(M, 63, seed=7)),
     "groups_64": (3000, 128, lambda M: workloads.random_group_offsets(M, 64, seed=8)),
+    # M % 4 = 2 and 3: with K % 512 != 0 the last tokens' exponent rows are
+    # patched into the four-row groups in shared memory (the last group
+    # below lies wholly in those tokens)
+    "tail_2": (1026, 384, lambda M: workloads.random_group_offsets(M, 7, seed=9)),
+    "tail_3_last_group": (1003, 256, lambda M: np.array([0, 500, 1000, 1003])),
     "one_token_groups": (200, 128, lambda M: np.arange(M + 1)),
 }
 
@@ -206,9 +211,10 @@ COLS_CASES["g1_m_mult_16_k1536"] = (640, 1536, lambda M: np.array([0, M]))
 def cols_k(K, path):
     """K of a case on one of the exponent-row paths of the single pass:
     K % 512 == 0 (rows of K/32 bytes are a multiple of 16 bytes: tensor
-    copies of rows) or not (tensor copies of four-row groups when M % 4 == 0,
-    else 4-byte asynchronous copies; and a short last super-tile of fewer
-    than four 128-feature blocks)."""
+    copies of rows) or not (tensor copies of four-row groups when M >= 4,
+    the last M % 4 rows patched in shared memory, else 4-byte asynchronous
+    copies; and a short last super-tile of fewer than four 128-feature
+    blocks)."""
     if path == "k_mult_512":
         return (K + 511) // 512 * 512
     return K if K % 512 else K + 128
@@ -246,22 +252,24 @@ def test_fp4_to_fp8_cols_launch_count_in_a_fresh_process(fq):
 def test_fp4_to_fp8_cols_short_super_tiles(fq, K):
     """K % 512 != 0: every row's last super-tile has 1, 2 or 3 of its four
     128-feature blocks (the others are empty slots), on both sides of the
-    walk-order switch (M = 70000: 547 windows), 32 Zipf groups, NaN scales."""
-    for M in (3000, 70000):
+    walk-order switch (M = 70000: 547 windows), 32 Zipf groups, NaN scales;
+    M % 4 != 0 patches the last rows of the four-row exponent groups."""
+    for M in (3000, 3003, 70000, 70002):
         offs = np.asarray(workloads.zipf_group_offsets(M, 32, 1.1, K), dtype=np.int64)
         q, s = rand_mx(M, K, seed=M + K, spread=16, nan_frac=0.001)
         run_cols(fq, q, s, offs, 2)
 
 
-@pytest.mark.parametrize("M", [65536, 66000, 66001])
+@pytest.mark.parametrize("M", [65536, 66000, 66001, 66003])
 @pytest.mark.parametrize("K", [1024, 1152])
 def test_fp4_to_fp8_cols_walk_orders(fq, M, K):
     """Every output of the single pass on either side of the switch between
     its two configurations: up to 512 128-token windows the super-tiles
     (window x 512 features) are walked window fastest with 4 code stages,
     beyond that feature quad fastest with 2 (M % 16 != 0 included); K = 1152
-    takes the four-row exponent groups (M % 4 == 0) or the asynchronous
-    copies, with a short last super-tile.  32 Zipf groups, NaN scales."""
+    takes the four-row exponent groups (the last M % 4 rows patched in
+    shared memory), with a short last super-tile.  32 Zipf groups, NaN
+    scales."""
     assert fq.fp4_to_fp8_cols_launch_count(K) == 1
     offs = np.asarray(workloads.zipf_group_offsets(M, 32, 1.1, 11), dtype=np.int64)
     q, s = rand_mx(M, K, seed=M + 5, spread=16, nan_frac=0.0005)

@@ -19,8 +19,14 @@
 
 namespace fq {
 
-constexpr int kTileSlots = tile_slots(kTok / 4);  // 1254
-constexpr int kTileWords = kTileSlots * 4;
+// Output-row alignment of an instance: the rows of yT start on 16-byte
+// boundaries (M % 16 == 0), on 4-byte boundaries (M % 4 == 0), or anywhere.
+// Tile geometry: the instances for the first two convert the window's 128
+// tokens; the last ("extended" tiles) also the next window's first 16
+// tokens, so that every row segment they write starts on a 16-byte boundary
+// (see write_tile).
+__host__ __device__ constexpr int code_rows(bool ext) { return ext ? kTok + 16 : kTok; }
+constexpr int tile_words(bool ext) { return tile_slots(code_rows(ext) / 4) * 4; }
 
 // Word i (0..3, not a compile-time constant) of y, without indexing a
 // register array.
@@ -112,21 +118,21 @@ __device__ __forceinline__ void store_block_range(uint8_t *blk, const uint32_t y
 // Write-out of a converted tile (window W, feature block f): warp w handles
 // feature words 4w..4w+3 (m_out), lane%8 tokens 16c..16c+15 (c_out); each
 // 16-byte store of a quarter warp fills one 128-byte output line.  When the
-// output rows are not 16-byte aligned (M % 16 != 0), a row's segment of the
-// window starts a = (row start) mod 16 bytes past a 16-byte boundary:
-//  * M % 4 == 0 (a = 0, 4, 8 or 12, the same for every chunk of the row):
-//    each lane stores its chunk as one 16-byte, two 8-byte or four 4-byte
-//    pieces;
-//  * otherwise lane c writes the aligned block that holds the last a bytes
-//    of chunk c - 1 (taken from the lane below with a shuffle) and the first
-//    16 - a bytes of its own chunk, lane 7 also the block after the segment;
-//    the two partial blocks at the segment's ends (shared with the
-//    neighbouring windows) are written as aligned pieces of 8, 4, 2 and 1
-//    bytes.
-// Byte-by-byte stores (the earlier path for both) made M % 16 != 0 about ten
-// times slower: 16385 x 7040 ran 399 us, now 81 us (16384: 38 us); 16392 x
-// 7168 401 -> 45 us.  Called by whole warps.
-template <bool kAligned16>
+// output rows are not 16-byte aligned (M % 16 != 0):
+//  * M % 4 == 0: a row's chunks all start a = 4, 8 or 12 bytes past a
+//    16-byte boundary (or on it), and each lane stores its chunk as two
+//    8-byte or four 4-byte pieces;
+//  * otherwise the tile holds the next window's first 16 tokens too, and
+//    each row's segment is shifted to start on a 16-byte boundary, so that
+//    it is still written as whole aligned 16-byte blocks (pieces only at the
+//    tensor's two ends).
+// Earlier designs for such M (16384 x 7040 takes 37 us): single-byte stores,
+// 16385 x 7040 in 399 us and 16392 x 7168 in 401 us; then for M % 4 != 0
+// aligned blocks between shuffled chunks with 1-8-byte pieces at both ends
+// of every row segment, 16385 x 7040 in 82 us (the pieces alone cost 27 us:
+// five times the L2 write requests of the aligned case); the extended tiles
+// take 56 us.  For M % 4 == 0 the pieces take 45 us and extended tiles 51.
+template <int kAlign>
 __device__ __forceinline__ void write_tile(const uint32_t *tile, uint8_t *__restrict__ yT,
                                            int32_t M, int32_t W, int32_t f, int m_out, int c_out)
 {
@@ -139,7 +145,7 @@ __device__ __forceinline__ void write_tile(const uint32_t *tile, uint8_t *__rest
     }
     const int32_t t0 = W + 16 * c_out;
     uint8_t *p = yT + (static_cast<int64_t>(f) * 128 + 4 * m_out) * M + t0;
-    if (!kAligned16 && (M & 3) == 0) {
+    if (kAlign == 4) {
         // rows 4-byte aligned: each lane stores its own chunk in aligned
         // pieces of its row's alignment (16, 8 or 4 bytes); the window's
         // token count is a multiple of 4
@@ -162,37 +168,47 @@ __device__ __forceinline__ void write_tile(const uint32_t *tile, uint8_t *__rest
             }
             p += M;
         }
-    } else if (!kAligned16) {
-        const int n = min(kTok, M - W);  // tokens of the window
+    } else if (kAlign == 1) {
+        // row k of yT starts a = (k M + W) mod 16 bytes past a 16-byte
+        // boundary: this window writes its tokens from sft = (16 - a) mod 16
+        // on as eight aligned 16-byte blocks, the last of which reaches sft
+        // tokens into the next window (converted in the same tile, chunk 8);
+        // the previous window wrote tokens W .. W + sft - 1 the same way.
+        // Block c holds tile tokens sft + 16 c .. + 15: bytes sft .. 15 of
+        // chunk c and 0 .. sft - 1 of chunk c + 1.
+        uint32_t nx[4][4];
+#pragma unroll
+        for (int qq = 0; qq < 4; qq++) {
+            const uint4 v =
+                *reinterpret_cast<const uint4 *>(tile + 4 * slot_index(4 * c_out + 4 + qq, m_out));
+            transpose4x4(v, nx[0][qq], nx[1][qq], nx[2][qq], nx[3][qq]);
+        }
+        const int32_t left = M - W;  // tokens from W to the end of the tensor
         uint8_t *seg = yT + (static_cast<int64_t>(f) * 128 + 4 * m_out) * M + W;
 #pragma unroll
         for (int rr = 0; rr < 4; rr++) {
             const int a = static_cast<int>(reinterpret_cast<uintptr_t>(seg) & 15);
-            uint8_t *base = seg - a;  // 16-byte aligned
-            uint32_t prev[4], y[4];
-#pragma unroll
-            for (int i = 0; i < 4; i++)
-                prev[i] = __shfl_up_sync(0xffffffffu, rows[rr][i], 1, 8);
-            if (a == 0) {
+            const int sft = (16 - a) & 15;
+            uint32_t y[4];
+            if (sft == 0) {
 #pragma unroll
                 for (int i = 0; i < 4; i++)
                     y[i] = rows[rr][i];
             } else {
-                bytes_at(prev, rows[rr], 16 - a, y);
+                bytes_at(rows[rr], nx[rr], sft, y);
             }
-            // block c_out holds the segment's bytes [16 c - a, 16 c - a + 16)
-            const int b0 = 16 * c_out - a;
-            const int lo = max(0, b0), hi = min(n, b0 + 16);
-            if (hi - lo == 16)
-                __stcs(reinterpret_cast<uint4 *>(base + 16 * c_out),
-                       make_uint4(y[0], y[1], y[2], y[3]));
-            else if (lo < hi)
-                store_block_range(base + 16 * c_out, y, lo - b0, hi - b0);
-            if (c_out == 7 && a != 0 && 128 - a < n) {
-                // the block after: the segment's bytes [128 - a, n)
-                uint32_t y8[4];
-                bytes_at(rows[rr], rows[rr], 16 - a, y8);
-                store_block_range(base + 128, y8, 0, n - (128 - a));
+            const int t_blk = sft + 16 * c_out;  // the block's first token, from W
+            const int len = min(16, left - t_blk);
+            if (len >= 16)
+                __stcs(reinterpret_cast<uint4 *>(seg + t_blk), make_uint4(y[0], y[1], y[2], y[3]));
+            else if (len > 0)
+                store_block_range(seg + t_blk, y, 0, len);
+            if (W == 0 && c_out == 0 && sft != 0) {
+                // the row's first tokens 0 .. sft - 1: bytes a .. 15 of the
+                // aligned block before the first
+                uint32_t yh[4];
+                bytes_at(rows[rr], rows[rr], 16 - a, yh);
+                store_block_range(seg - a, yh, a, a + min(sft, left));
             }
             seg += M;
         }
@@ -263,15 +279,19 @@ constexpr int32_t kWinFastMax = 512;  // windows walked fastest up to this many
 constexpr int kExpBufs = 2;     // shift-row buffers (super-tiles in flight)
 constexpr int kConvWarps = kThreads / 32;
 constexpr int kThreads1p = kThreads + 32;
-constexpr int kCodeBytes = kTok * 64;
 constexpr int kExpRowBytes = 16;
-constexpr int kExpBytes = 3 * kTok * kExpRowBytes;
 constexpr int kSmemAlign = 128;  // tensor-copy destinations
-static_assert(kCodeBytes % kSmemAlign == 0 && kExpBytes % kSmemAlign == 0, "aligned buffers");
+// exponent rows of a super-tile: tokens W - 128 .. W - 128 + exp_rows - 1, in
+// 128-row copies; the blocks of the tile's tokens reach 127 tokens beyond
+// its last (W + 255, or W + 271 with the next window's first 16 tokens)
+constexpr int exp_rows(bool ext) { return (ext ? 4 : 3) * kTok; }
+static_assert((kTok + 16) * 64 % kSmemAlign == 0, "aligned code stages");
 
-// How a super-tile's exponent rows (tokens W-128 .. W+255, the 16 bytes of
-// its 16 MX columns from each) reach shared memory:
-//  * kExpRows (K % 512 == 0): three tensor copies of 128 rows x 16 bytes.
+// How a super-tile's exponent rows (tokens W-128 .. W+255, or W+383 when
+// the tile takes 16 more tokens; the 16 bytes of its 16 MX columns from
+// each) reach shared memory:
+//  * kExpRows (K % 512 == 0): three (four) tensor copies of 128 rows x 16
+//    bytes.
 //  * kExpQuads (K % 512 != 0, M >= 4): a row of 4 nfeat exponent bytes is
 //    then not a multiple of 16 bytes, which a tensor map's row pitch must
 //    be, but a group of four rows is.  The exponents are viewed as
@@ -279,7 +299,7 @@ static_assert(kCodeBytes % kSmemAlign == 0 && kExpBytes % kSmemAlign == 0, "alig
 //    bytes into it, so its slice [16F, 16F + 16) lies in the 32 bytes from
 //    the 16-byte boundary 16F + floor16(4 nfeat j), at offset 4 nfeat j mod
 //    16.  One tensor copy per j brings those 32 bytes of the super-tile's 96
-//    groups: buffer [j][group][32 bytes].  Bytes past a row's end belong to
+//    (128) groups: buffer [j][group][32 bytes].  Bytes past a row's end belong to
 //    the next row (or read as zero); they fall in the columns of a short
 //    super-tile's missing feature blocks, whose maxima are never used.  When
 //    M % 4 != 0 the last M % 4 tokens lie past the view's rows (read as
@@ -289,24 +309,31 @@ static_assert(kCodeBytes % kSmemAlign == 0 && kExpBytes % kSmemAlign == 0, "alig
 constexpr int kExpAsync = 0;
 constexpr int kExpRows = 1;
 constexpr int kExpQuads = 2;
-constexpr int kQuadRows = 3 * kTok / 4;  // four-row groups of a super-tile
-constexpr int exp_buf_bytes(int mode) { return mode == kExpQuads ? 4 * kQuadRows * 32 : kExpBytes; }
-static_assert(exp_buf_bytes(kExpQuads) % kSmemAlign == 0, "aligned buffers");
+constexpr int quad_rows(bool ext) { return exp_rows(ext) / 4; }  // four-row groups of a super-tile
+constexpr int exp_buf_bytes(int mode, bool ext)
+{
+    return mode == kExpQuads ? 4 * quad_rows(ext) * 32 : exp_rows(ext) * kExpRowBytes;
+}
+static_assert(exp_buf_bytes(kExpQuads, true) % kSmemAlign == 0 &&
+                  exp_buf_bytes(kExpQuads, false) % kSmemAlign == 0 &&
+                  exp_buf_bytes(kExpRows, true) % kSmemAlign == 0 &&
+                  exp_buf_bytes(kExpRows, false) % kSmemAlign == 0,
+              "aligned buffers");
 
 // Two configurations of the single pass (code stages x exponent buffers):
 // kStages x kExps = 4 x 2 up to kWinFastMax windows, 2 x 1 beyond (measured:
 // at 131072 x 7168 the 2 x 1 kernel is 6 % faster, at 16384 x 7168 7 %
 // slower).  Per shift-row buffer: the shift-table rows of every token of a
 // super-tile (uint4: one byte per MX column).
-inline size_t cols1_dyn_bytes(int32_t G, int stages, int exps, int exp_mode)
+inline size_t cols1_dyn_bytes(int32_t G, int stages, int exps, int exp_mode, bool ext)
 {
-    return kSmemAlign + static_cast<size_t>(stages) * kCodeBytes +
-           static_cast<size_t>(exps) * exp_buf_bytes(exp_mode) +
-           static_cast<size_t>(kExpBufs) * kTok * sizeof(uint4) +
-           kTileWords * sizeof(uint32_t) + static_cast<size_t>(G + 1) * 2 * sizeof(int32_t);
+    return kSmemAlign + static_cast<size_t>(stages) * code_rows(ext) * 64 +
+           static_cast<size_t>(exps) * exp_buf_bytes(exp_mode, ext) +
+           static_cast<size_t>(kExpBufs) * code_rows(ext) * sizeof(uint4) +
+           tile_words(ext) * sizeof(uint32_t) + static_cast<size_t>(G + 1) * 2 * sizeof(int32_t);
 }
 
-template <bool kAligned16, int kStages, int kExps, int kExpMode>
+template <int kAlign, int kStages, int kExps, int kExpMode>
 __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
     const uint8_t *__restrict__ s, int32_t M, int32_t nfeat, const int64_t *__restrict__ offs,
@@ -323,11 +350,16 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     extern __shared__ __align__(16) uint8_t dyn_raw[];
     uint8_t *codes_ring = dyn_raw + ((kSmemAlign - (smem_u32(dyn_raw) & (kSmemAlign - 1))) &
                                      (kSmemAlign - 1));
+    constexpr bool kExt = kAlign == 1;             // extended tiles
+    constexpr int kRows = code_rows(kExt);         // tokens of a tile
+    constexpr int kCodeBytes = kRows * 64;
+    constexpr int kExpN = exp_rows(kExt);
+    constexpr int kQuadRows = quad_rows(kExt);
     uint8_t *exp_ring = codes_ring + kStages * kCodeBytes;
-    constexpr int kExpBuf = exp_buf_bytes(kExpMode);
-    uint4 *Uring = reinterpret_cast<uint4 *>(exp_ring + kExps * kExpBuf);  // [kExpBufs][kTok]
-    uint32_t *tile = reinterpret_cast<uint32_t *>(Uring + kExpBufs * kTok);    // [kTileWords]
-    int32_t *off = reinterpret_cast<int32_t *>(tile + kTileWords);             // [G + 1]
+    constexpr int kExpBuf = exp_buf_bytes(kExpMode, kExt);
+    uint4 *Uring = reinterpret_cast<uint4 *>(exp_ring + kExps * kExpBuf);  // [kExpBufs][kRows]
+    uint32_t *tile = reinterpret_cast<uint32_t *>(Uring + kExpBufs * kRows);  // [tile_words]
+    int32_t *off = reinterpret_cast<int32_t *>(tile + tile_words(kExt));  // [G + 1]
     int32_t *base = off + G + 1;                                              // [G + 1]
 
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -372,7 +404,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
             if (lane == 0) {
                 mbar_arrive_expect_tx(&full_e[be], kExpBuf);
 #pragma unroll
-                for (int h = 0; h < 3; h++)
+                for (int h = 0; h < kExpN / kTok; h++)
                     tma_load_2d(dst + h * kTok * kExpRowBytes, &tm_s, 16 * F,
                                 W + (h - 1) * kTok, &full_e[be]);
             }
@@ -390,7 +422,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
             // (16 contiguous bytes each) per warp instruction
             const int nw = min(4, nfeat - 4 * F);  // exponent words of the super-tile
             const int w = lane & 3;
-            for (int r = lane >> 2; r < 3 * kTok; r += 8) {
+            for (int r = lane >> 2; r < kExpN; r += 8) {
                 const int32_t t = W - kTok + r;
                 const bool rd = t >= 0 && t < M && w < nw;
                 const uint8_t *src = rd ? s + static_cast<int64_t>(t) * srow + 16 * F + 4 * w : s;
@@ -427,7 +459,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
         const int ti = lane >> 2, w = lane & 3;
         const int32_t t = Mq + ti;
         const int32_t r = t - W + kTok;  // row of the super-tile's exponent rows
-        if (ti < 3 && t < M && w < min(4, nfeat - 4 * F) && r >= 0 && r < 3 * kTok) {
+        if (ti < 3 && t < M && w < min(4, nfeat - 4 * F) && r >= 0 && r < kExpN) {
             const int j = r & 3;
             uint32_t *dst = reinterpret_cast<uint32_t *>(
                 exp_ring + (m % kExps) * kExpBuf + j * kQuadRows * 32 + (r >> 2) * 32 +
@@ -441,7 +473,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     auto reaches_tail = [&](int32_t m) {
         int32_t W, F;
         super_xy(m, W, F);
-        return kExpMode == kExpQuads && Mq != M && W + 2 * kTok > Mq;
+        return kExpMode == kExpQuads && Mq != M && W - kTok + kExpN > Mq;
     };
 
     build_fp8_table(tab);
@@ -485,19 +517,19 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
                 eb + j * kQuadRows * 32 + (r >> 2) * 32 + ((j * static_cast<int32_t>(srow)) & 15));
             return make_uint4(p[0], p[1], p[2], p[3]);
         };
-        uint4 *U_of = Uring + (m % kExpBufs) * kTok;
-        const int32_t We = min(W + kTok, M);
+        uint4 *U_of = Uring + (m % kExpBufs) * kRows;
+        const int32_t We = min(W + kRows, M);  // the tile's tokens end
         const int gW = warp_find_last_le(off, G, W);
         const int32_t blkW = base[gW] + ((W - off[gW]) >> 7);
         const int gL = warp_find_last_le(off, G, We - 1);
-        const int32_t nbw = base[gL] + ((We - 1 - off[gL]) >> 7) - blkW + 1;  // <= 128
+        const int32_t nbw = base[gL] + ((We - 1 - off[gL]) >> 7) - blkW + 1;  // <= kRows
         int g = gW;
         for (int32_t jb = w0; jb < nbw; jb += wstep) {
             const int32_t b = blkW + jb;
             while (base[g + 1] <= b)  // group of block b (skips empty groups)
                 g++;
             const int32_t bs = off[g] + ((b - base[g]) << 7);
-            const int32_t be = min(bs + kTok, off[g + 1]);  // W-127 <= bs, be <= W+255
+            const int32_t be = min(bs + kTok, off[g + 1]);  // W-127 <= bs, be <= We+127
             uint4 m4 = make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int u = 0; u < 4; u++) {
@@ -522,7 +554,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
                 U_of[t - W] = make_uint4(shift_rows4(S.x, e.x, k), shift_rows4(S.y, e.y, k),
                                          shift_rows4(S.z, e.z, k), shift_rows4(S.w, e.w, k));
             }
-            if (bs >= W) {
+            if (bs >= W && (!kExt || bs < W + kTok)) {  // the block starts in the window
                 // feature 512F + x, x = 4 lane + 128 c4 .. + 3: MX column x / 32
                 const uint32_t Sw[4] = {S.x, S.y, S.z, S.w};
                 uint4 *dst = reinterpret_cast<uint4 *>(
@@ -554,12 +586,12 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
                 eb + j * kQuadRows * 32 + (r >> 2) * 32 + ((j * static_cast<int32_t>(srow)) & 15));
             return p[cw];
         };
-        uint32_t *U32 = reinterpret_cast<uint32_t *>(Uring + (m % kExpBufs) * kTok);
-        const int32_t We = min(W + kTok, M);
+        uint32_t *U32 = reinterpret_cast<uint32_t *>(Uring + (m % kExpBufs) * kRows);
+        const int32_t We = min(W + kRows, M);
         const int gW = warp_find_last_le(off, G, W);
         const int32_t blkW = base[gW] + ((W - off[gW]) >> 7);
         const int gL = warp_find_last_le(off, G, We - 1);
-        const int32_t nbw = base[gL] + ((We - 1 - off[gL]) >> 7) - blkW + 1;  // <= 128
+        const int32_t nbw = base[gL] + ((We - 1 - off[gL]) >> 7) - blkW + 1;  // <= kRows
         int g = gW;
         for (int32_t it = w0; it < 4 * nbw; it += wstep) {
             const int32_t b = blkW + (it >> 2);
@@ -581,7 +613,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
                                (__reduce_max_sync(0xffffffffu, mx >> 24) << 24);
             for (int32_t t = max(bs, W) + lane; t < min(be, We); t += 32)
                 U32[4 * (t - W) + cw] = shift_rows4(S, exp_word(t - W + kTok, cw), k);
-            if (bs >= W && 4 * F + cw < nfeat) {
+            if (bs >= W && (!kExt || bs < W + kTok) && 4 * F + cw < nfeat) {
                 // features 512 F + 128 cw + 4 lane .. + 3: MX column 4 cw + lane / 8
                 float *dst = yTs + static_cast<int64_t>(b) * (128 * static_cast<int64_t>(nfeat)) +
                              512 * static_cast<int64_t>(F) + 128 * cw + 4 * lane;
@@ -700,7 +732,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
     if (!ok0)
         return;  // the producer, which reached no refill, reports it
     const int j = tid & 3;     // MX column of both units
-    const int tl0 = tid >> 2;  // token of unit 0 (unit 1: tl0 + 64)
+    const int tl0 = tid >> 2;  // token of unit 0 (unit h: tl0 + 64 h, below kRows)
     const int m_out = 4 * wid + (lane >> 3);
     const int c_out = lane & 7;
     const int32_t sg0 = blockIdx.x;  // first super-tile
@@ -718,11 +750,11 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
         const bool real = f < nfeat;  // not the empty slot of a short super-tile
         if (ok && real) {
             const uint4 *codes = reinterpret_cast<const uint4 *>(codes_ring + st * kCodeBytes);
-            const uint32_t *U_w = reinterpret_cast<const uint32_t *>(Uring + bf * kTok);
+            const uint32_t *U_w = reinterpret_cast<const uint32_t *>(Uring + bf * kRows);
 #pragma unroll
-            for (int h = 0; h < 2; h++) {
+            for (int h = 0; h < (kRows + 63) / 64; h++) {
                 const int tl = tl0 + 64 * h;
-                if (W + tl < M)
+                if ((!kExt || tl < kRows) && W + tl < M)
                     convert_unit_row(tile, tab, tl, j, codes[tl * 4 + j],
                                      (U_w[tl * 4 + i] >> (8 * j)) & 0xFFu);
             }
@@ -741,7 +773,7 @@ __global__ void __launch_bounds__(kThreads1p, 3) fp4_to_fp8_cols_1pass_kernel(
             break;
         }
         if (real)
-            write_tile<kAligned16>(tile, yT, M, W, f, m_out, c_out);
+            write_tile<kAlign>(tile, yT, M, W, f, m_out, c_out);
 
         if (++st == kStages) {
             st = 0;
@@ -798,11 +830,34 @@ using Cols1Kernel = void (*)(const CUtensorMap, const CUtensorMap, const uint8_t
                              int32_t, const int64_t *, int32_t, int, uint8_t *, float *,
                              int32_t *);
 
-template <int kStages, int kExps, int kExpMode>
-Cols1Kernel pick_cols1(bool aligned16)
+// The instances: beyond kWinFastMax windows two code stages and one
+// exponent buffer (the exponents then come by rows or four-row groups: M
+// >= 4); up to it by exponent mode and output-row alignment.  The extended
+// tiles (kAlign 1) keep three CTAs per SM with one exponent buffer, and three
+// code stages with the four-row groups (two for M < 4).
+template <int kAlign>
+Cols1Kernel pick_cols1_large(int mode)
 {
-    return aligned16 ? fp4_to_fp8_cols_1pass_kernel<true, kStages, kExps, kExpMode>
-                     : fp4_to_fp8_cols_1pass_kernel<false, kStages, kExps, kExpMode>;
+    return mode == kExpRows ? fp4_to_fp8_cols_1pass_kernel<kAlign, 2, 1, kExpRows>
+                            : fp4_to_fp8_cols_1pass_kernel<kAlign, 2, 1, kExpQuads>;
+}
+
+Cols1Kernel pick_cols1_small(int align, int mode, int &stages, int &exps)
+{
+    if (align != 1) {  // M >= 4: no asynchronous exponent copies
+        stages = 4;
+        exps = mode == kExpQuads ? 1 : 2;
+        if (align == 16)
+            return mode == kExpRows ? fp4_to_fp8_cols_1pass_kernel<16, 4, 2, kExpRows>
+                                    : fp4_to_fp8_cols_1pass_kernel<16, 4, 1, kExpQuads>;
+        return mode == kExpRows ? fp4_to_fp8_cols_1pass_kernel<4, 4, 2, kExpRows>
+                                : fp4_to_fp8_cols_1pass_kernel<4, 4, 1, kExpQuads>;
+    }
+    exps = 1;
+    stages = mode == kExpRows ? 4 : (mode == kExpQuads ? 3 : 2);
+    return mode == kExpRows    ? fp4_to_fp8_cols_1pass_kernel<1, 4, 1, kExpRows>
+           : mode == kExpQuads ? fp4_to_fp8_cols_1pass_kernel<1, 3, 1, kExpQuads>
+                               : fp4_to_fp8_cols_1pass_kernel<1, 2, 1, kExpAsync>;
 }
 }  // namespace
 
@@ -815,9 +870,11 @@ fq_status fq::launch_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
     // described at kExpRows
     CUtensorMap tm_q, tm_s;
     const int mode = K % 512 == 0 ? kExpRows : (M >= 4 ? kExpQuads : kExpAsync);
+    const int align = M % 16 == 0 ? 16 : (M % 4 == 0 ? 4 : 1);  // of the rows of yT
+    const bool ext = align == 1;
     bool maps = encode_tensor_map_2d_u8(&tm_q, q, static_cast<uint64_t>(K / 2),
                                         static_cast<uint64_t>(M), static_cast<uint64_t>(K / 2), 64,
-                                        kTok, false);
+                                        code_rows(ext), false);
     // a super-tile reads 16 (or 32) of each exponent row's bytes; the rest of
     // the 128-byte line belongs to super-tiles a whole pass of windows later,
     // so whole-line promotion would fetch it again from DRAM once the tensor
@@ -829,7 +886,7 @@ fq_status fq::launch_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
     else if (maps && mode == kExpQuads)
         maps = encode_tensor_map_2d_u8(&tm_s, s, static_cast<uint64_t>(K / 8),
                                        static_cast<uint64_t>(M / 4), static_cast<uint64_t>(K / 8),
-                                       32, kQuadRows, false);
+                                       32, quad_rows(ext), false);
     else
         tm_s = tm_q;  // not read
     if (maps) {
@@ -837,19 +894,13 @@ fq_status fq::launch_fp4_to_fp8_cols(const uint8_t *q, const uint8_t *s, int64_t
         // windows, two and one beyond; the four-row groups fill twice the
         // exponent buffer, so they keep one (and three CTAs per SM)
         const bool large = (M + kTok - 1) / kTok > kWinFastMax;
-        const bool a16 = M % 16 == 0;
-        const int stages = large ? 2 : 4;
-        const int exps = large || mode == kExpQuads ? 1 : 2;
-        const size_t dyn = cols1_dyn_bytes(G, stages, exps, mode);
-        Cols1Kernel kern;
-        if (large)
-            kern = mode == kExpRows    ? pick_cols1<2, 1, kExpRows>(a16)
-                   : mode == kExpQuads ? pick_cols1<2, 1, kExpQuads>(a16)
-                                       : pick_cols1<2, 1, kExpAsync>(a16);
-        else
-            kern = mode == kExpRows    ? pick_cols1<4, 2, kExpRows>(a16)
-                   : mode == kExpQuads ? pick_cols1<4, 1, kExpQuads>(a16)
-                                       : pick_cols1<4, 2, kExpAsync>(a16);
+        int stages = 2, exps = 1;
+        const Cols1Kernel kern =
+            large ? (align == 16  ? pick_cols1_large<16>(mode)
+                     : align == 4 ? pick_cols1_large<4>(mode)
+                                  : pick_cols1_large<1>(mode))
+                  : pick_cols1_small(align, mode, stages, exps);
+        const size_t dyn = cols1_dyn_bytes(G, stages, exps, mode, ext);
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(dyn)) != cudaSuccess ||
             cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,

@@ -1005,6 +1005,31 @@ def run_sweep_rows(m):
     return 0
 
 
+def run_ncu_cols(m: int, k: int, reps: int = 3):
+    """The transposed conversion alone on the MoE-dispatch recipe at m x k
+    (32 Zipf groups), `reps` calls with L2 cleaned before each, after one
+    MXFP4 row quantization that makes its input: a small case for an ncu
+    capture of one instance of the kernel (any m, such as one that is not a
+    multiple of 16)."""
+    import torch
+    import numpy as np
+    import fp8_quantization_gb300 as fq
+    from fp8_quantization_gb300 import workloads
+    dev = torch.device("cuda", 0)
+    T = Timer(dev, 0)
+    bits = workloads.moe_dispatch(m, k, seed=0)
+    offs = torch.from_numpy(workloads.zipf_group_offsets(m, EXPERTS, 1.1, 0)).to(dev)
+    x = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+    q, s = fq.mxfp4_quantize_rows(x)
+    yT, yTs = fq.fp4_to_fp8_cols(q, s, offs, 0)
+    for _ in range(reps):
+        T.flush()
+        fq.fp4_to_fp8_cols(q, s, offs, 0, yT, yTs)
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"ncu_cols": [m, k], "reps": reps}), flush=True)
+    return 0
+
+
 def run_ncu_calls(reps: int = 3):
     """Every entry point of the DRAM-traffic record on the headline tensor
     (16384 x 7168, 32 Zipf groups), each `reps` times with L2 cleaned before
@@ -1067,9 +1092,15 @@ def main():
     ap.add_argument("--ncu-calls", action="store_true",
                     help="run every entry point of the DRAM-traffic record three times on the "
                          "headline tensor and exit (for an ncu capture of DRAM bytes per call)")
+    ap.add_argument("--ncu-cols", type=int, nargs=2, metavar=("M", "K"), default=None,
+                    help="run the transposed conversion alone on the MoE-dispatch recipe at "
+                         "M x K (32 groups) four times and exit (for an ncu capture of one "
+                         "instance)")
     args = ap.parse_args()
     if args.ncu_calls:
         return run_ncu_calls()
+    if args.ncu_cols:
+        return run_ncu_cols(*args.ncu_cols)
     if args.sweep_rows:
         return run_sweep_rows(args.sweep_rows)
     if args.warmup < 3:

@@ -185,6 +185,93 @@ __device__ inline int load_groups(const int64_t *__restrict__ offs, int32_t G, i
     return bad;
 }
 
+// Word i (0..3, not a compile-time constant) of y, without indexing a
+// register array.
+__device__ __forceinline__ uint32_t word_sel(const uint32_t y[4], int i)
+{
+    return (i & 2) ? ((i & 1) ? y[3] : y[2]) : ((i & 1) ? y[1] : y[0]);
+}
+
+// Bytes [s, s + 16) of the 32 bytes p ++ x (p first), 0 < s < 16.
+__device__ __forceinline__ void bytes_at(const uint32_t p[4], const uint32_t x[4], int s,
+                                         uint32_t y[4])
+{
+    const uint32_t z[8] = {p[0], p[1], p[2], p[3], x[0], x[1], x[2], x[3]};
+    const int w0 = s >> 2;
+    uint32_t zs[5];
+#pragma unroll
+    for (int j = 0; j < 5; j++)
+        zs[j] = (w0 & 2) ? ((w0 & 1) ? z[3 + j] : z[2 + j]) : ((w0 & 1) ? z[1 + j] : z[j]);
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        y[i] = __funnelshift_r(zs[i], zs[i + 1], 8 * (s & 3));
+}
+
+// Bytes [lo, hi) of the 16-byte block y to blk + lo .. blk + hi - 1 (blk
+// 16-byte aligned), as aligned pieces of 8, 4, 2 and 1 bytes.
+__device__ __forceinline__ void store_block_range(uint8_t *blk, const uint32_t y[4], int lo,
+                                                  int hi)
+{
+    if (hi == 16) {
+        // a suffix [lo, 16): the pieces are the set bits of 16 - lo, smallest first
+#pragma unroll
+        for (int sz = 1; sz <= 8; sz <<= 1) {
+            if (lo & sz) {
+                const uint32_t w = word_sel(y, lo >> 2);
+                if (sz == 8)
+                    __stcs(reinterpret_cast<uint2 *>(blk + lo), make_uint2(w, word_sel(y, (lo >> 2) + 1)));
+                else if (sz == 4)
+                    __stcs(reinterpret_cast<unsigned int *>(blk + lo), w);
+                else if (sz == 2)
+                    __stcs(reinterpret_cast<unsigned short *>(blk + lo),
+                           static_cast<unsigned short>(w >> (8 * (lo & 2))));
+                else
+                    blk[lo] = static_cast<uint8_t>(w >> (8 * (lo & 3)));
+                lo += sz;
+            }
+        }
+        return;
+    }
+    if (lo == 0) {
+        // a prefix [0, hi): the pieces are the set bits of hi, largest first
+#pragma unroll
+        for (int sz = 8; sz >= 1; sz >>= 1) {
+            if (hi & sz) {
+                const int o = hi & ~(2 * sz - 1);
+                const uint32_t w = word_sel(y, o >> 2);
+                if (sz == 8)
+                    __stcs(reinterpret_cast<uint2 *>(blk + o), make_uint2(w, word_sel(y, (o >> 2) + 1)));
+                else if (sz == 4)
+                    __stcs(reinterpret_cast<unsigned int *>(blk + o), w);
+                else if (sz == 2)
+                    __stcs(reinterpret_cast<unsigned short *>(blk + o),
+                           static_cast<unsigned short>(w >> (8 * (o & 2))));
+                else
+                    blk[o] = static_cast<uint8_t>(w >> (8 * (o & 3)));
+            }
+        }
+        return;
+    }
+    int o = lo;
+    while (o < hi) {
+        const uint32_t w = word_sel(y, o >> 2);
+        if (!(o & 7) && o + 8 <= hi) {
+            __stcs(reinterpret_cast<uint2 *>(blk + o), make_uint2(w, word_sel(y, (o >> 2) + 1)));
+            o += 8;
+        } else if (!(o & 3) && o + 4 <= hi) {
+            __stcs(reinterpret_cast<unsigned int *>(blk + o), w);
+            o += 4;
+        } else if (!(o & 1) && o + 2 <= hi) {
+            __stcs(reinterpret_cast<unsigned short *>(blk + o),
+                   static_cast<unsigned short>(w >> (8 * (o & 2))));
+            o += 2;
+        } else {
+            blk[o] = static_cast<uint8_t>(w >> (8 * (o & 3)));
+            o += 1;
+        }
+    }
+}
+
 // 4x4 byte transpose: in = four words (rows), out[r] = byte r of each word.
 __device__ __forceinline__ void transpose4x4(uint4 v, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                              uint32_t &r3)

@@ -147,15 +147,70 @@ __device__ __forceinline__ void write_block_tile(const uint32_t *tile, uint8_t *
     const int m_out = 4 * wid + (lane >> 3), c_out = lane & 7;
     uint8_t *const base = yT + (t0 - a);
     if (!kAligned16) {
-        for (int i = c_out; i < nch; i += 8) {
-            const int lo = 16 * i, hi = min(n - 16 * i, 16);
+        // rows of yT not 16-byte aligned (a = 0: the tile's token columns are
+        // the unit's tokens).  Row k's segment starts a_k = (its start) mod 16
+        // bytes past a 16-byte boundary, so its aligned blocks start at token
+        // sft = (16 - a_k) mod 16 and every 16 tokens after: lane c writes
+        // block c when it is whole (bytes sft .. 15 of chunk c and 0 .. sft - 1
+        // of chunk c + 1); the partial blocks at the segment's two ends are
+        // written below, one thread per row and end.  (Single-byte stores
+        // made M % 16 != 0 about three times slower than M % 16 == 0.)
+        uint32_t cur[4][4], nx[4][4];
 #pragma unroll
-            for (int rr = 0; rr < 4; rr++) {
-                uint32_t w[4];
-                tile_row16(tile, i, m_out, rr, w);
-                uint8_t *p = base + (feat0 + 4 * m_out + rr) * static_cast<int64_t>(M) + lo;
-                for (int bb = 0; bb < hi; bb++)
-                    p[bb] = static_cast<uint8_t>(word_at(w, bb >> 2) >> (8 * (bb & 3)));
+        for (int qq = 0; qq < 4; qq++) {
+            const uint4 v =
+                *reinterpret_cast<const uint4 *>(tile + 4 * slot_index(4 * c_out + qq, m_out));
+            transpose4x4(v, cur[0][qq], cur[1][qq], cur[2][qq], cur[3][qq]);
+            const uint4 u =
+                *reinterpret_cast<const uint4 *>(tile + 4 * slot_index(4 * c_out + 4 + qq, m_out));
+            transpose4x4(u, nx[0][qq], nx[1][qq], nx[2][qq], nx[3][qq]);
+        }
+        uint8_t *seg = yT + (feat0 + 4 * m_out) * static_cast<int64_t>(M) + t0;
+#pragma unroll
+        for (int rr = 0; rr < 4; rr++) {
+            const int ar = static_cast<int>(reinterpret_cast<uintptr_t>(seg) & 15);
+            const int sft = (16 - ar) & 15;
+            const int t_blk = sft + 16 * c_out;
+            if (t_blk + 16 <= n) {
+                uint32_t y[4];
+                if (sft == 0) {
+#pragma unroll
+                    for (int i = 0; i < 4; i++)
+                        y[i] = cur[rr][i];
+                } else {
+                    bytes_at(cur[rr], nx[rr], sft, y);
+                }
+                __stcs(reinterpret_cast<uint4 *>(seg + t_blk), make_uint4(y[0], y[1], y[2], y[3]));
+            }
+            seg += M;
+        }
+        // the partial blocks: thread tid & 127 owns row tid & 127, threads
+        // below 128 its head (tokens 0 .. sft - 1), the others its tail
+        const int kr = tid & (kTok - 1);
+        uint8_t *row = yT + (feat0 + kr) * static_cast<int64_t>(M) + t0;
+        const int ar = static_cast<int>(reinterpret_cast<uintptr_t>(row) & 15);
+        const int sft = (16 - ar) & 15;
+        const int full = n >= sft ? (n - sft) >> 4 : 0;  // whole blocks
+        uint32_t w0[4], w1[4], y[4];
+        if (tid < kTok) {
+            if (sft > 0) {
+                tile_row16(tile, 0, kr >> 2, kr & 3, w0);
+                bytes_at(w0, w0, 16 - ar, y);  // y[ar + i] = token i
+                store_block_range(row - ar, y, ar, ar + min(sft, n));
+            }
+        } else {
+            const int tt = sft + 16 * full;  // the tail block's first token
+            if (n > sft && tt < n) {
+                tile_row16(tile, full, kr >> 2, kr & 3, w0);
+                if (sft == 0) {
+#pragma unroll
+                    for (int i = 0; i < 4; i++)
+                        y[i] = w0[i];
+                } else {
+                    tile_row16(tile, full + 1, kr >> 2, kr & 3, w1);
+                    bytes_at(w0, w1, sft, y);
+                }
+                store_block_range(row + tt, y, 0, n - tt);
             }
         }
         return;
